@@ -1,0 +1,535 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 small-batch decode hot path.
+
+One "step" is one pass of every hot-path operation of a Kimi-K3-shaped decode layer,
+at every decode batch B in {1,2,4,8,16,32,64}, on synthetic bf16 inputs:
+
+    input projection   Y = X . W^T            K=7168  -> N=8192       (batch switch)
+    output projection  Y = X . W^T + R        K=16384 -> N=7168       (split-K + residual)
+    L2 prefetch        shared-expert gate/up weights, side stream, during the front end
+    MoE front end      router 384 + latent 512 rows in one product, softmax, top-8
+    MoE experts        384 routed experts (gate/up 2x2048x7168, down 7168x2048) grouped
+                       GEMV + shared expert of the same shape on a side stream + combine
+
+`value` is the whole step's algorithmic HBM bytes (weights read once + activations in
+and out, using the actual number of distinct experts each batch routes to) divided by
+the device time of the step, replayed as one CUDA graph: GB/s. Every weight tensor is
+re-read only after more than 3x the L2 size of other weight traffic, so every read is
+cold. `sweep` gives the same figures per operation and batch (CUDA graph of R calls
+over a rotating pool of weight copies >= 3x L2). `e2e` runs the step eagerly through
+the public API with the step's activations copied from pinned host memory and its
+outputs copied back inside the timed region. `cpu_baseline` times the fp64 oracle on a
+bounded sample of the same step on the host cores.
+
+Multi-GPU: the path has no exchange step on one GPU, so N ranks run N independent
+replicas (weak scaling); the step time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "achieved HBM GB/s (fraction of GB300 roofline) and µs/call per decode batch 1–64"
+BATCHES = [1, 2, 4, 8, 16, 32, 64]
+H, N_IN, K_O, E, L, I, TOPK = 7168, 8192, 16384, 384, 512, 2048, 8
+PREFETCH_BYTES = 24 << 20
+WORKLOAD = ("Kimi-K3-shaped decode layer hot path, B in {1,2,4,8,16,32,64}: input projection "
+            "7168->8192 (batch-size kernel switch), output projection 16384->7168 + residual, "
+            "MoE front end 7168->384 router + 512 latent with softmax/top-8, 384 routed experts "
+            "(gate/up 2x2048x7168, down 7168x2048) + shared expert on a side stream, "
+            "L2 prefetch of the shared expert's weights")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--batches", default=",".join(map(str, BATCHES)))
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target host time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------ byte accounting --
+
+def bytes_linear(B, N, K, residual):
+    return N * K * 2 + B * K * 2 + B * N * 2 + (B * N * 2 if residual else 0)
+
+
+def bytes_front(B):
+    return (E + L) * H * 2 + B * H * 2 + B * L * 2 + B * TOPK * 8
+
+
+def bytes_experts(B, U):
+    per_expert = 3 * I * H * 2
+    return (U + 1) * per_expert + 2 * B * H * 2 + B * TOPK * 8
+
+
+# ------------------------------------------------------------------- clocks ----
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------- workload ----
+
+class Workload:
+    """All tensors of the step on one GPU, plus the per-call launch counts."""
+
+    def __init__(self, torch, ssd, inputs, dev, batches, seed=0):
+        self.torch, self.ssd, self.dev, self.batches = torch, ssd, dev, batches
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.l2 = l2
+        bf = torch.bfloat16
+        W_in = inputs.weight(N_IN, H, dev, seed, "w_in")
+        W_o = inputs.weight(H, K_O, dev, seed, "w_o")
+        W_cat = inputs.weight(E + L, H, dev, seed, "w_cat")
+        # rotating copies for the per-operation sweep: >= 3x L2 per pool
+        def pool(w):
+            n = max(1, math.ceil(3 * l2 / (w.numel() * 2)))
+            return [w] + [w.clone() for _ in range(n - 1)]
+        self.W_in, self.W_o, self.W_cat = pool(W_in), pool(W_o), pool(W_cat)
+        self.Wgu, self.Wd = inputs.expert_bank(E, H, I, dev, seed, "bank")
+        self.Wgs, self.Wds = inputs.shared_expert(H, I, dev, seed, "bank_shared")
+        self.side = torch.cuda.Stream(device=dev)
+        self.fork = torch.cuda.Event()
+        self.t = {}
+        for B in batches:
+            d = {}
+            d["x_in"] = inputs.activations(B, H, dev, seed, "x_in")
+            d["x_o"] = inputs.activations(B, K_O, dev, seed, "x_o")
+            d["r_o"] = inputs.residual(B, H, dev, seed, "r_o")
+            d["x_moe"] = [inputs.activations(B, H, dev, seed + v, "x_moe") for v in range(3)]
+            d["y_in"] = torch.empty(B, N_IN, dtype=bf, device=dev)
+            d["y_o"] = torch.empty(B, H, dtype=bf, device=dev)
+            d["lat"] = [torch.empty(B, L, dtype=bf, device=dev) for _ in range(3)]
+            d["idx"] = [torch.empty(B, TOPK, dtype=torch.int32, device=dev) for _ in range(3)]
+            d["w"] = [torch.empty(B, TOPK, dtype=torch.float32, device=dev) for _ in range(3)]
+            d["rm"] = [torch.empty(ssd.moe_route_map_ints(B, E, TOPK), dtype=torch.int32, device=dev)
+                       for _ in range(3)]
+            d["y_moe"] = torch.empty(B, H, dtype=bf, device=dev)
+            d["ws_in"] = ssd.workspace(ssd.dec_linear_workspace_bytes(B, N_IN, H), dev)
+            d["ws_o"] = ssd.workspace(ssd.dec_linear_workspace_bytes(B, H, K_O), dev)
+            d["ws_f"] = ssd.workspace(ssd.moe_front_workspace_bytes(B, E, L, H), dev)
+            d["ws_e"] = ssd.workspace(ssd.moe_experts_workspace_bytes(B, E, TOPK, H, I), dev)
+            self.t[B] = d
+        self.launches = 0
+        torch.cuda.synchronize()
+
+    # -- operations (each adds the kernels it launches to self.launches) --
+    def op_in(self, B, rot=0):
+        d = self.t[B]
+        self.ssd.dec_linear(d["x_in"], self.W_in[rot % len(self.W_in)], None, d["y_in"], d["ws_in"])
+        self.launches += 1
+
+    def op_o(self, B, rot=0):
+        d = self.t[B]
+        self.ssd.dec_linear(d["x_o"], self.W_o[rot % len(self.W_o)], d["r_o"], d["y_o"], d["ws_o"])
+        self.launches += 1
+
+    def op_front(self, B, rot=0, v=0, prefetch=True):
+        torch, ssd, d = self.torch, self.ssd, self.t[B]
+        if prefetch:
+            main = torch.cuda.current_stream()
+            self.fork.record(main)
+            self.side.wait_event(self.fork)
+            ssd.l2_prefetch(self.Wgs, nbytes=PREFETCH_BYTES, max_ctas=8, stream=self.side)
+            self.launches += 1
+        ssd.moe_front(d["x_moe"][v], self.W_cat[rot % len(self.W_cat)], E, L, TOPK, d["lat"][v],
+                      d["idx"][v], d["w"][v], d["ws_f"], route_map=d["rm"][v])
+        self.launches += 1
+
+    def op_experts(self, B, v=0):
+        d = self.t[B]
+        self.ssd.moe_experts(d["x_moe"][v], d["idx"][v], d["w"][v], d["rm"][v], self.Wgu, self.Wd,
+                             self.Wgs, self.Wds, d["y_moe"], d["ws_e"], side_stream=self.side)
+        self.launches += 6  # gather, shared gate/up + down, routed gate/up + down, combine
+
+    def step(self):
+        for B in self.batches:
+            self.op_in(B)
+            self.op_o(B)
+            self.op_front(B)
+            self.op_experts(B)
+
+    def used_experts(self, B, v=0):
+        rm = self.t[B]["rm"][v]
+        P = B * TOPK
+        return int(rm[2 * E + 1 + 2 * P].item())
+
+    def step_bytes(self):
+        tot = 0
+        for B in self.batches:
+            tot += bytes_linear(B, N_IN, H, False) + bytes_linear(B, H, K_O, True)
+            tot += bytes_front(B) + bytes_experts(B, self.used_experts(B))
+        return tot
+
+
+def capture(torch, fn):
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()  # one eager pass on the capture stream (function attributes, lazy init)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph(torch, g, reps):
+    st = torch.cuda.current_stream()
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        g.replay()
+        b.record(st)
+        b.synchronize()
+        ts.append(a.elapsed_time(b) * 1e3)  # us
+    return ts
+
+
+# -------------------------------------------------------------- CPU baseline ----
+
+def cpu_sample_fn(batches, seed=0):
+    """A bounded slice of the step for the fp64 oracle: per batch, 64 rows of the input
+    projection, 32 rows of the output projection, the whole front end, and the full
+    expert layer (8 routed + shared) for one token. Returns (run(), bytes)."""
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(seed)
+
+    def bf(shape, std):
+        v = (rng.standard_normal(shape) * std).astype(np.float32)
+        return (v.view(np.uint32) >> 16).astype(np.uint16)
+
+    w_in = bf((64, H), 0.02)
+    w_o = bf((32, K_O), 0.02)
+    w_cat = bf((E + L, H), 0.02)
+    w_gu = [bf((2 * I, H), 0.02) for _ in range(TOPK + 1)]
+    w_d = [bf((H, I), 0.02) for _ in range(TOPK + 1)]
+    xs = {B: (bf((B, H), 1.0), bf((B, K_O), 1.0), bf((B, 32), 1.0)) for B in batches}
+    nbytes = 0
+    for B in batches:
+        nbytes += bytes_linear(B, 64, H, False) + bytes_linear(B, 32, K_O, True)
+        nbytes += bytes_front(B) + (TOPK + 1) * 3 * I * H * 2 + 2 * H * 2
+
+    def run():
+        for B in batches:
+            x, xo, r = xs[B]
+            oracle.linear(x, w_in)
+            oracle.linear(xo, w_o, r)
+            f = oracle.moe_front(x, w_cat, E, L, TOPK)
+            yp = np.empty((1, TOPK, H))
+            for j in range(TOPK):
+                _, yp[0, j] = oracle.expert_mlp(x[0], w_gu[j], w_d[j])
+            _, s = oracle.expert_mlp(x[0], w_gu[TOPK], w_d[TOPK])
+            oracle.combine(f["w"][:1], yp, s[None, :])
+
+    return run, nbytes
+
+
+SAMPLE_DESC = ("per batch B in {%s}: 64 rows of the input projection, 32 rows of the output "
+               "projection (+residual), the whole MoE front end, and one token through 8 routed "
+               "experts + the shared expert; fp64 C oracle, OpenMP over output rows")
+
+
+def cpu_baseline(batches, target_s):
+    import oracle
+    run, nbytes = cpu_sample_fn(batches)
+    t0 = time.perf_counter()
+    run()
+    one = time.perf_counter() - t0
+    reps = max(1, int(target_s / max(one, 1e-3)) - 1)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        run()
+    dt = (time.perf_counter() - t0) / reps
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds_per_sample": dt,
+            "sample": SAMPLE_DESC % ",".join(map(str, batches))}
+
+
+# ------------------------------------------------------------------- main ----
+
+def dist_setup(torch):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def max_over_ranks(torch, world, x, dev):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(torch, world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    batches = [int(b) for b in args.batches.split(",")]
+    run, nbytes = cpu_sample_fn(batches)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = (time.perf_counter() - t0) / args.steps
+    v = nbytes / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "batches": batches,
+                       "sample": "bounded host sample of the step (see cpu_baseline.sample)"},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": oracle.num_threads(),
+                             "kind": "oracle",
+                             "sample": SAMPLE_DESC % ",".join(map(str, batches))},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    import torch
+    world, rank, local = dist_setup(torch)
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    import split_switched_decode_gb300 as ssd
+    from split_switched_decode_gb300 import inputs
+    ssd.build()
+    batches = [int(b) for b in args.batches.split(",")]
+    wl = Workload(torch, ssd, inputs, dev, batches)
+
+    # routing of every X set (fixed inputs -> fixed routing -> fixed bytes)
+    for B in batches:
+        for v in range(3):
+            wl.op_front(B, v=v, prefetch=False)
+    torch.cuda.synchronize()
+
+    # ---- per-operation sweep: graphs of R calls over rotating weight copies
+    sweep = {}
+    R_SMALL = 12
+    for B in batches:
+        row = {}
+        for name, fn, nb in (
+                ("input_projection", lambda B=B: [wl.op_in(B, r) for r in range(R_SMALL)],
+                 bytes_linear(B, N_IN, H, False)),
+                ("output_projection", lambda B=B: [wl.op_o(B, r) for r in range(R_SMALL)],
+                 bytes_linear(B, H, K_O, True)),
+                ("moe_front", lambda B=B: [wl.op_front(B, r, v=0, prefetch=False)
+                                           for r in range(R_SMALL)], bytes_front(B))):
+            g = capture(torch, fn)
+            ts = time_graph(torch, g, 7)
+            us = statistics.median(ts) / R_SMALL
+            row[name] = {"us_per_call": us, "GBps": nb / us / 1e3,
+                         "variant": ssd.dec_variant_name(ssd.dec_last_variant())}
+            del g
+        us_e = []
+        nb_e = 0
+        g = capture(torch, lambda B=B: [wl.op_experts(B, v) for v in range(3)])
+        ts = time_graph(torch, g, 5)
+        nb_e = sum(bytes_experts(B, wl.used_experts(B, v)) for v in range(3)) / 3
+        us = statistics.median(ts) / 3
+        row["moe_experts"] = {"us_per_call": us, "GBps": nb_e / us / 1e3,
+                              "distinct_experts": [wl.used_experts(B, v) for v in range(3)]}
+        del g
+        sweep[str(B)] = row
+    torch.cuda.synchronize()
+
+    # ---- the step as one CUDA graph
+    launches0 = wl.launches
+    g_step = capture(torch, wl.step)
+    per_step_launches = (wl.launches - launches0) // 2
+    step_bytes = wl.step_bytes()
+    for _ in range(args.warmup):
+        g_step.replay()
+    torch.cuda.synchronize()
+    clk = ClockSampler(local)
+    clk.start()
+    barrier(torch, world)
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    for _ in range(args.steps):
+        g_step.replay()
+    b.record(st)
+    torch.cuda.synchronize()
+    barrier(torch, world)
+    clocks = clk.stop()
+    ms = a.elapsed_time(b) / args.steps
+    ms = max_over_ranks(torch, world, ms, dev)
+    value = step_bytes * world / (ms * 1e-3) / 1e9
+    assert ssd.dec_sync_status() == ssd.DEC_OK
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        host_in = {B: {k: wl.t[B][k].cpu().pin_memory() for k in ("x_in", "x_o", "r_o")}
+                   for B in batches}
+        for B in batches:
+            host_in[B]["x_moe"] = wl.t[B]["x_moe"][0].cpu().pin_memory()
+        host_out = {B: {k: torch.empty(wl.t[B][k].shape, dtype=wl.t[B][k].dtype).pin_memory()
+                        for k in ("y_in", "y_o", "y_moe")} for B in batches}
+        h2d = sum(t.numel() * t.element_size() for d in host_in.values() for t in d.values())
+        d2h = sum(t.numel() * t.element_size() for d in host_out.values() for t in d.values())
+
+        def e2e_step():
+            for B in batches:
+                d, hi, ho = wl.t[B], host_in[B], host_out[B]
+                d["x_in"].copy_(hi["x_in"], non_blocking=True)
+                d["x_o"].copy_(hi["x_o"], non_blocking=True)
+                d["r_o"].copy_(hi["r_o"], non_blocking=True)
+                d["x_moe"][0].copy_(hi["x_moe"], non_blocking=True)
+                wl.op_in(B)
+                wl.op_o(B)
+                wl.op_front(B)
+                wl.op_experts(B)
+                ho["y_in"].copy_(d["y_in"], non_blocking=True)
+                ho["y_o"].copy_(d["y_o"], non_blocking=True)
+                ho["y_moe"].copy_(d["y_moe"], non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ea.record(st)
+        for _ in range(args.steps):
+            e2e_step()
+        eb.record(st)
+        torch.cuda.synchronize()
+        ems = max_over_ranks(torch, world, ea.elapsed_time(eb) / args.steps, dev)
+        e2e = {"value": step_bytes * world / (ems * 1e-3) / 1e9, "unit": "GB/s",
+               "ms_per_step": ems, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "path": "eager public-API calls, pinned host inputs/outputs copied every step"}
+
+    # ---- roofline of the dominant operation (routed + shared expert GEMV at the largest B)
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except OSError:
+        pass
+    peak = peaks.get("hbm_gbs")
+    peak_src = "measured" if peak else "fallback"
+    peak = peak or 6800.0
+    Bmax = str(max(batches))
+    dom = sweep[Bmax]["moe_experts"]
+    roofline = {"bound": "hbm", "kernel": f"moe_experts grouped expert GEMV, B={Bmax}",
+                "achieved": dom["GBps"], "peak": peak, "peak_source": peak_src, "unit": "GB/s",
+                "frac": dom["GBps"] / peak, "traffic": None}
+    for Bk, row in sweep.items():
+        for op in row.values():
+            op["frac"] = op["GBps"] / peak
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        cpu = cpu_baseline(batches, args.cpu_seconds)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": WORKLOAD, "batches": batches, "step_bytes": step_bytes,
+                           "l2": "cold: every weight tensor is re-read only after >3x L2 of "
+                                 "other weight traffic (step), rotating copies >=3x L2 (sweep)",
+                           "timing": "CUDA graph replay, CUDA events on the replay stream",
+                           "parallelism": f"replicas x{world}"},
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": per_step_launches * args.steps, "clocks": clocks,
+                "sweep": sweep}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

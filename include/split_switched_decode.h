@@ -1,0 +1,246 @@
+/*
+ * split_switched_decode.h -- C ABI of the small-batch decode hot path for one NVIDIA
+ * GB300 (sm_103a): the decode projection with a batch-size kernel switch, the MoE
+ * front end (router scores + latent projection as one product, then softmax/top-k),
+ * the routed-expert grouped GEMV with the shared expert on a side stream, and an L2
+ * prefetch kernel.
+ *
+ * The method is the one described in "Hyper Optimizing Kimi K3 in vLLM: Moving Fast
+ * and Responsibly" (vLLM blog), Part 1, sections 1-4. Each entry point below cites
+ * the section that describes the operation.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Types. dec_bf16 is the raw 16-bit pattern of an IEEE bfloat16. Matrices are
+ *    row-major with the last dimension contiguous. Weights W[N,K] use the nn.Linear
+ *    layout, so Y = X . W^T.
+ *  - Memory. Every pointer is DEVICE memory owned by the caller. The library never
+ *    allocates or frees memory. Where a call needs scratch memory it takes a caller
+ *    workspace whose size comes from the matching *_workspace_bytes() query; the
+ *    workspace must be zero-filled once before its first use (cudaMemset), every
+ *    completed call leaves it ready for the next, and one workspace must not be used
+ *    by two calls that can run at the same time.
+ *  - Alignment. X, W, Wcat, Wgu, Wd and every workspace must be 16-byte aligned; K and
+ *    every other reduction length must be a multiple of 8 (rows are then 16-byte
+ *    multiples). Other pointers need their natural alignment.
+ *  - Streams. Every call is asynchronous on the stream(s) it is given (NULL = legacy
+ *    default stream) and never synchronises the host.
+ *  - Errors. Arguments are checked on the host before anything is launched; a failed
+ *    check returns a status and launches nothing. DEC_ERR_UNSUPPORTED_SHAPE means
+ *    "outside the validated envelope: use your standard path". A failed launch returns
+ *    DEC_ERR_CUDA. Every wait inside a kernel is bounded in time; a wait that runs out
+ *    makes the kernel stop early and sets a device status word that dec_sync_status()
+ *    reports (DEC_ERR_TIMEOUT). No kernel traps.
+ *  - Batch. Decode batch B is 1..64.
+ */
+#ifndef SPLIT_SWITCHED_DECODE_H
+#define SPLIT_SWITCHED_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DEC_API __attribute__((visibility("default")))
+#else
+#define DEC_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t dec_bf16;
+/* Same object as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *dec_stream_t;
+
+typedef enum {
+    DEC_OK = 0,
+    DEC_ERR_INVALID_ARG = 1,         /* null pointer, non-positive size, bad option   */
+    DEC_ERR_UNSUPPORTED_SHAPE = 2,   /* outside the envelope: use the standard path   */
+    DEC_ERR_MISALIGNED = 3,          /* pointer or length breaks the alignment rules  */
+    DEC_ERR_WORKSPACE_TOO_SMALL = 4, /* ws_bytes below the *_workspace_bytes() value  */
+    DEC_ERR_CUDA = 5,                /* a CUDA runtime call or launch failed          */
+    DEC_ERR_TIMEOUT = 6              /* a bounded device wait ran out (see above)     */
+} dec_status;
+
+/* Kernel variants that dec_linear can pick ("different batch sizes need different
+ * kernel choices", Part 1 / 1. Tune shapes for the workload). */
+typedef enum {
+    DEC_VARIANT_NONE = -1,
+    DEC_VARIANT_TINY = 0,        /* tiny-matrix GEMV, B <= 2, CUDA cores              */
+    DEC_VARIANT_SPLITK = 1,      /* split-K, TMA-staged weight tiles, CUDA cores     */
+    DEC_VARIANT_SPLITK_TC = 2    /* split-K, TMA-staged tiles, tcgen05 tensor cores  */
+} dec_variant;
+
+/* ------------------------------------------------------------ diagnostics ---- */
+
+/* Static English text for a status code (never NULL). */
+DEC_API const char *dec_status_string(int status);
+/* Static name of a variant ("tiny", "splitk", "splitk_tc", "none"). */
+DEC_API const char *dec_variant_name(int variant);
+/* Variant launched by the most recent successful projection call on this host
+ * thread (dec_gemv, dec_splitk_gemm, dec_linear, moe_front), or DEC_VARIANT_NONE. */
+DEC_API int dec_last_variant(void);
+/* Library ABI version: 100 * major + minor. */
+DEC_API int dec_version(void);
+
+/* Force the variant dec_linear picks on this process: DEC_VARIANT_NONE restores the
+ * batch-size switch. A forced variant that cannot run the shape makes dec_linear
+ * return DEC_ERR_UNSUPPORTED_SHAPE. Used to test every variant at every batch size.
+ * The environment variable DEC_FORCE_VARIANT (tiny|splitk|splitk_tc) sets the
+ * initial value. Returns DEC_ERR_INVALID_ARG for an unknown value. */
+DEC_API dec_status dec_set_force_variant(int variant);
+
+/* Host-side fault injection for tests: the next `count` launches of this process
+ * fail before reaching the GPU and return DEC_ERR_CUDA. 0 disables. */
+DEC_API dec_status dec_set_fault_inject(int count);
+
+/* Time limit of every bounded device wait, in nanoseconds (default 2e9).
+ * Values below 1e6 are rejected with DEC_ERR_INVALID_ARG. */
+DEC_API dec_status dec_set_wait_limit_ns(uint64_t ns);
+
+/* Synchronise `s`, then read and clear the current device's status word.
+ * Returns DEC_ERR_TIMEOUT if any kernel since the last read gave up on a wait,
+ * DEC_ERR_INVALID_ARG if moe_experts found an expert index out of range or repeated
+ * within a token (its output is then undefined), DEC_ERR_CUDA if the stream reports
+ * an error, DEC_OK otherwise. */
+DEC_API dec_status dec_sync_status(dec_stream_t s);
+
+/* Self-test of the bounded-wait path: launches one kernel on `s` that waits on an
+ * mbarrier nothing ever arrives at, with a limit of `limit_ns` nanoseconds
+ * (1e6 .. 1e10). The kernel gives up, records the timeout and returns; the caller
+ * then sees DEC_ERR_TIMEOUT from dec_sync_status(). Nothing faults or traps. */
+DEC_API dec_status dec_debug_wait_timeout(uint64_t limit_ns, dec_stream_t s);
+
+/* ------------------------------------------------------ decode projection ---- */
+
+/*
+ * Tiny-matrix projection for decode batches of 1 and 2
+ * ("Part 1 / 1. Tune shapes for the workload": specialised small-matrix kernels at
+ * batch sizes 1-2), with the optional residual add of the output projection
+ * ("Part 1 / 2. Overlap computation and communication", single-GPU part):
+ *
+ *     Y[b,n] = bf16( sum_k X[b,k] * W[n,k]  (+ R[b,n]) ),  fp32 accumulation,
+ *                                                           one round to nearest even
+ *
+ * X [B,K], W [N,K], R [B,N] or NULL, Y [B,N]. B in {1,2}; N >= 1; K >= 8, K % 8 == 0.
+ * Streams W once with 128-bit loads; no workspace. Y may not alias X, W or R.
+ */
+DEC_API dec_status dec_gemv(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 *R, dec_bf16 *Y,
+                    int B, int N, int K, dec_stream_t s);
+
+/*
+ * Split-K projection for larger decode batches ("Part 1 / 1. Tune shapes for the
+ * workload": split-K kernels that divide the matrix multiplication across more GPU
+ * workers), same result as dec_gemv for any B in 1..64.
+ *
+ * W is cut into 128-row tiles and 64-wide k-blocks. The (tile, k-block) sequence is
+ * divided into contiguous ranges, one per CTA ("worker"); partial sums of a tile
+ * produced by several workers go to the workspace and the last worker to finish the
+ * tile adds them in worker order (fixed order: bit-identical results for a fixed
+ * split), adds R and rounds once.
+ *
+ *   split_k == 0 : one worker per SM, ranges of equal length (stream-K style).
+ *   split_k == S : every tile split into S equal k-ranges (S <= k-blocks per tile).
+ * use_tc: 0 = CUDA-core tiles, 1 = tcgen05 tensor-core tiles (W rows are the MMA M
+ * dimension, the batch is the MMA N dimension, accumulator in tensor memory).
+ */
+DEC_API size_t dec_splitk_workspace_bytes(int B, int N, int K, int split_k);
+DEC_API dec_status dec_splitk_gemm(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 *R,
+                           dec_bf16 *Y, int B, int N, int K, int split_k, int use_tc,
+                           void *ws, size_t ws_bytes, dec_stream_t s);
+
+/*
+ * The batch-size switch: picks dec_gemv for B <= 2, the split-K tiles on CUDA cores
+ * for small B and on tensor cores from a threshold batch upward, then runs it.
+ * dec_linear_workspace_bytes() covers whichever variant the switch can pick.
+ */
+DEC_API size_t dec_linear_workspace_bytes(int B, int N, int K);
+DEC_API dec_status dec_linear(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 *R, dec_bf16 *Y,
+                      int B, int N, int K, void *ws, size_t ws_bytes, dec_stream_t s);
+
+/* ------------------------------------------------------------ MoE front ------- */
+
+/*
+ * Route-map layout (int32), written by moe_front when route_map is given and read by
+ * moe_experts. With P = B*topk:
+ *   [0, E)              counts[e]   tokens routed to expert e
+ *   [E, 2E+1)           offsets[e]  exclusive prefix sum of counts; offsets[E] = P
+ *   [2E+1, 2E+1+P)      pairs[i]    entries b*topk+j sorted by (expert, b)
+ *   [2E+1+P, 2E+1+2P)   pos[b*topk+j] position of that entry in pairs
+ *   [2E+1+2P]           num_used    number of experts with counts > 0
+ *   [2E+2+2P, 3E+2+2P)  used[u]     those experts, ascending
+ */
+DEC_API size_t moe_route_map_ints(int B, int E, int topk);
+
+/*
+ * MoE front end ("Part 1 / 3. Improve MoE scheduling and overlap": the router scores
+ * and the latent input projection combined into one matrix multiplication), followed
+ * by the routing the pages leave implicit, read as: softmax over the E raw router
+ * logits; the topk experts with the largest logits (fp32), ties to the lower expert
+ * index, listed by descending logit; weights renormalised over the chosen experts.
+ *
+ *     Z = X . Wcat^T          Wcat [E+L, K]: router rows first, then latent rows
+ *     latent[b,:] = bf16(Z[b, E:E+L])
+ *     topk_idx[b,:], topk_w[b,:]  as above;  probs[b,e] = softmax(Z[b,0:E])_e
+ *
+ * X [B,K]; latent [B,L] (NULL allowed when L == 0); topk_idx int32 [B,topk];
+ * topk_w fp32 [B,topk]; probs_opt fp32 [B,E] or NULL; route_map_opt int32
+ * [moe_route_map_ints(B,E,topk)] or NULL. E in 1..512, topk in 1..min(E,16), L >= 0.
+ * One launch: the last CTA to finish the product does the routing.
+ */
+DEC_API size_t moe_front_workspace_bytes(int B, int E, int L, int K);
+DEC_API dec_status moe_front(const dec_bf16 *X, const dec_bf16 *Wcat, int B, int K, int E, int L,
+                     int topk, dec_bf16 *latent, int32_t *topk_idx, float *topk_w,
+                     float *probs_opt, int32_t *route_map_opt, void *ws, size_t ws_bytes,
+                     dec_stream_t s);
+
+/* --------------------------------------------------------------- experts ------ */
+
+/*
+ * Routed experts as a grouped GEMV plus the shared expert on a side stream
+ * ("Part 1 / 3. Improve MoE scheduling and overlap": the shared expert runs on a
+ * separate stream and overlaps the routed-expert computation; the schedule limits
+ * the GPU resources each operation uses):
+ *
+ *     for each token b and rank j, e = topk_idx[b,j]:
+ *        g = X[b] . Wgu[e, 0:I]^T,   u = X[b] . Wgu[e, I:2I]^T
+ *        A = bf16(silu(g) * u),      silu(t) = t / (1 + exp(-t))
+ *        Yp[b,j] = A . Wd[e]^T       (fp32)
+ *     S[b] = the same MLP with Wgu_shared / Wd_shared (when given)
+ *     Y[b] = bf16( sum_j topk_w[b,j] * Yp[b,j]  +  S[b] )   (j ascending, fp32)
+ *
+ * X [B,H]; topk_idx int32 [B,topk]; topk_w fp32 [B,topk]; route_map from moe_front or
+ * NULL (then rebuilt on `main`); Wgu [E,2I,H]; Wd [E,H,I]; Wgu_shared [2I,H] and
+ * Wd_shared [H,I], both NULL for no shared expert; Y [B,H].
+ * Each used expert's weights are read once for all of its tokens.
+ * The shared expert runs on `side` with at most side_max_ctas CTAs (0 = chosen from
+ * the expected weight bytes); the routed experts use the remaining SMs on `main`.
+ * `side` may equal `main` (then no overlap). The call records events so that `main`
+ * waits for `side` before the combine; on return all work is ordered after `main`.
+ * H % 128 == 0, I % 64 == 0, topk <= 16, E <= 512.
+ */
+DEC_API size_t moe_experts_workspace_bytes(int B, int E, int topk, int H, int I);
+DEC_API dec_status moe_experts(const dec_bf16 *X, const int32_t *topk_idx, const float *topk_w,
+                       const int32_t *route_map, const dec_bf16 *Wgu, const dec_bf16 *Wd,
+                       int E, const dec_bf16 *Wgu_shared, const dec_bf16 *Wd_shared, int B,
+                       int H, int I, int topk, dec_bf16 *Y, void *ws, size_t ws_bytes,
+                       dec_stream_t main_stream, dec_stream_t side_stream, int side_max_ctas);
+
+/* ------------------------------------------------------------ L2 prefetch ----- */
+
+/*
+ * Pull the byte range [p, p+bytes) toward L2 on stream `s` with at most max_ctas
+ * CTAs (0 = 8) and write nothing ("Part 1 / 4. Prefetching upcoming weights into
+ * cache": a dedicated side-stream kernel raises the cache hit rate of the next
+ * operation's weights during phases that cannot use the full memory bandwidth).
+ * p must be 16-byte aligned; bytes is rounded down to a multiple of 16.
+ * Results of other calls never depend on it.
+ */
+DEC_API dec_status l2_prefetch(const void *p, size_t bytes, int max_ctas, dec_stream_t s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPLIT_SWITCHED_DECODE_H */

@@ -1,0 +1,645 @@
+// api.cu -- host side of the C ABI declared in include/split_switched_decode.h:
+// argument checks, the batch-size kernel switch, workspace planning, TMA descriptor
+// encoding, side-stream scheduling of the shared expert, and error reporting.
+#include <atomic>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/split_switched_decode.h"
+#include "common.cuh"
+#include "internal.h"
+
+using namespace ssd;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kAlign = 256;
+
+// Device status word: set by a kernel whose bounded wait ran out.
+__device__ unsigned g_dec_status_word;
+
+std::atomic<int> g_force_variant{-2};  // -2: not read from the environment yet
+std::atomic<int> g_fault_inject{0};
+std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+thread_local int t_last_variant = DEC_VARIANT_NONE;
+
+struct DeviceInfo {
+  std::once_flag once;
+  int num_sms = 0;
+  unsigned *status = nullptr;
+  cudaError_t err = cudaSuccess;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+std::once_flag g_encode_once;
+EncodeTiledFn g_encode = nullptr;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Current device's info; nullptr (and *err set) when no device is usable.
+DeviceInfo *device_info(cudaError_t *err) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *err = (e != cudaSuccess) ? e : cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  DeviceInfo &d = g_dev[dev];
+  std::call_once(d.once, [&]() {
+    d.err = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (d.err == cudaSuccess)
+      d.err = cudaGetSymbolAddress(reinterpret_cast<void **>(&d.status), g_dec_status_word);
+  });
+  if (d.err != cudaSuccess) {
+    *err = d.err;
+    return nullptr;
+  }
+  return &d;
+}
+
+int current_num_sms() {
+  cudaError_t e;
+  DeviceInfo *d = device_info(&e);
+  return d ? d->num_sms : 0;
+}
+
+bool encoder_ready() {
+  std::call_once(g_encode_once, []() {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+// 2-D bf16 tensor [rows, inner] (inner contiguous), 128-byte swizzled boxes of
+// 64 x box_rows elements.
+bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows,
+              uint32_t box_rows) {
+  if (!encoder_ready()) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(TILE_K), box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int force_variant() {
+  int v = g_force_variant.load();
+  if (v == -2) {
+    int init = DEC_VARIANT_NONE;
+    if (const char *s = std::getenv("DEC_FORCE_VARIANT")) {
+      if (!std::strcmp(s, "tiny")) init = DEC_VARIANT_TINY;
+      else if (!std::strcmp(s, "splitk")) init = DEC_VARIANT_SPLITK;
+      else if (!std::strcmp(s, "splitk_tc")) init = DEC_VARIANT_SPLITK_TC;
+    }
+    int expected = -2;
+    g_force_variant.compare_exchange_strong(expected, init);
+    v = g_force_variant.load();
+  }
+  return v;
+}
+
+// Host-side fault injection: true when this launch must be reported as failed.
+bool consume_fault() {
+  int n = g_fault_inject.load();
+  while (n > 0) {
+    if (g_fault_inject.compare_exchange_weak(n, n - 1)) return true;
+  }
+  return false;
+}
+
+dec_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DEC_OK : DEC_ERR_CUDA; }
+
+// ------------------------------------------------------------ split-K planning --
+
+struct SplitPlan {
+  int T, KB, G, maxc;
+  size_t partial_bytes, counter_bytes, total;
+};
+
+// Workers: split_k == 0 -> one per SM (at most T*KB); S > 0 -> T*S (classic split-K).
+bool plan_splitk(int B, int N, int K, int split_k, int num_sms, SplitPlan *pl) {
+  pl->T = ceil_div(N, TILE_N);
+  pl->KB = ceil_div(K, TILE_K);
+  const int64_t iters = static_cast<int64_t>(pl->T) * pl->KB;
+  if (split_k == 0) {
+    pl->G = static_cast<int>(iters < num_sms ? iters : num_sms);
+  } else {
+    if (split_k > pl->KB) return false;
+    const int64_t g = static_cast<int64_t>(pl->T) * split_k;
+    if (g > (1 << 20)) return false;
+    pl->G = static_cast<int>(g);
+  }
+  if (pl->G < 1) return false;
+  pl->maxc = engine_maxc_for(B);
+  pl->partial_bytes = align_up(static_cast<size_t>(2) * pl->G * 128 * pl->maxc * sizeof(float));
+  pl->counter_bytes = align_up(static_cast<size_t>(pl->T) * sizeof(int));
+  pl->total = pl->partial_bytes + pl->counter_bytes;
+  return true;
+}
+
+void fill_engine_common(EngineParams &p, const SplitPlan &pl, int mode, int N, int K, int B,
+                        void *ws, const DeviceInfo *d) {
+  std::memset(&p, 0, sizeof p);
+  p.mode = mode;
+  p.N = N;
+  p.K = K;
+  p.T = pl.T;
+  p.KB = pl.KB;
+  p.G = pl.G;
+  p.B = B;
+  p.slot_cols = pl.maxc;
+  p.partials = static_cast<float *>(ws);
+  p.counters = reinterpret_cast<int *>(static_cast<char *>(ws) + pl.partial_bytes);
+  p.status = d->status;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+}
+
+dec_status check_linear_args(const dec_bf16 *X, const dec_bf16 *W, dec_bf16 *Y, int B, int N,
+                             int K) {
+  if (!X || !W || !Y) return DEC_ERR_INVALID_ARG;
+  if (B < 1 || N < 1 || K < 1) return DEC_ERR_INVALID_ARG;
+  if (B > MAX_B) return DEC_ERR_UNSUPPORTED_SHAPE;
+  if (K % 8 != 0) return DEC_ERR_MISALIGNED;
+  if (!aligned16(X) || !aligned16(W)) return DEC_ERR_MISALIGNED;
+  if (static_cast<int64_t>(N) * K > (int64_t(1) << 40)) return DEC_ERR_UNSUPPORTED_SHAPE;
+  return DEC_OK;
+}
+
+dec_status run_splitk(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 *R, dec_bf16 *Y,
+                      int B, int N, int K, int split_k, int use_tc, void *ws, size_t ws_bytes,
+                      cudaStream_t s) {
+  cudaError_t ce;
+  DeviceInfo *d = device_info(&ce);
+  if (!d) return DEC_ERR_CUDA;
+  SplitPlan pl;
+  if (!plan_splitk(B, N, K, split_k, d->num_sms, &pl)) return DEC_ERR_UNSUPPORTED_SHAPE;
+  if (!ws) return DEC_ERR_INVALID_ARG;
+  if (!aligned16(ws)) return DEC_ERR_MISALIGNED;
+  if (ws_bytes < pl.total) return DEC_ERR_WORKSPACE_TOO_SMALL;
+  CUtensorMap wmap, xmap;
+  if (!make_map(&wmap, W, K, N, WBOX_ROWS) || !make_map(&xmap, X, K, B, XBOX_ROWS))
+    return DEC_ERR_CUDA;
+  EngineParams p;
+  fill_engine_common(p, pl, MODE_LINEAR, N, K, B, ws, d);
+  p.Y = Y;
+  p.R = R;
+  if (consume_fault()) return DEC_ERR_CUDA;
+  ce = use_tc ? launch_engine_tc(pl.maxc, wmap, xmap, p, s)
+              : launch_engine_cc(pl.maxc, wmap, xmap, p, s);
+  if (ce == cudaErrorNotSupported) return DEC_ERR_UNSUPPORTED_SHAPE;
+  if (ce != cudaSuccess) return DEC_ERR_CUDA;
+  t_last_variant = use_tc ? DEC_VARIANT_SPLITK_TC : DEC_VARIANT_SPLITK;
+  return DEC_OK;
+}
+
+// The batch-size switch: the B at and above which tensor-core tiles are used.
+int tc_min_batch() {
+  if (const char *s = std::getenv("DEC_TC_MIN_B")) {
+    int v = std::atoi(s);
+    if (v >= 1) return v;
+  }
+  return 1 << 30;  // tensor-core tiles not yet enabled by default
+}
+
+// ------------------------------------------------------------- MoE planning --
+
+struct FrontPlan {
+  SplitPlan sk;
+  size_t done_off, logits_off, total;
+};
+
+bool plan_front(int B, int E, int L, int K, int num_sms, FrontPlan *fp) {
+  if (!plan_splitk(B, E + L, K, 0, num_sms, &fp->sk)) return false;
+  fp->done_off = fp->sk.total;
+  fp->logits_off = fp->done_off + kAlign;
+  fp->total = fp->logits_off + align_up(static_cast<size_t>(B) * E * sizeof(float));
+  return true;
+}
+
+struct ExpertsPlan {
+  int maxc, Tg, Td, KBg, KBd;
+  size_t rm_off, xg_off, a_off, yp_off, as_off, s_off;
+  size_t main_part_off, main_cnt_off, side_part_off, side_cnt_off, total;
+};
+
+bool plan_experts(int B, int E, int topk, int H, int I, int num_sms, ExpertsPlan *ep) {
+  const size_t P = static_cast<size_t>(B) * topk;
+  ep->maxc = engine_maxc_for(B);
+  ep->Tg = I / 64;
+  ep->Td = H / TILE_N;
+  ep->KBg = ceil_div(H, TILE_K);
+  ep->KBd = ceil_div(I, TILE_K);
+  size_t o = 0;
+  ep->rm_off = o;
+  o += align_up(moe_route_map_ints(B, E, topk) * sizeof(int32_t));
+  ep->xg_off = o;
+  o += align_up(P * H * 2);
+  ep->a_off = o;
+  o += align_up(P * I * 2);
+  ep->yp_off = o;
+  o += align_up(P * H * sizeof(float));
+  ep->as_off = o;
+  o += align_up(static_cast<size_t>(B) * I * 2);
+  ep->s_off = o;
+  o += align_up(static_cast<size_t>(B) * H * sizeof(float));
+  const size_t part = align_up(static_cast<size_t>(2) * num_sms * 128 * ep->maxc * sizeof(float));
+  const int tmax = ep->Tg > ep->Td ? ep->Tg : ep->Td;
+  ep->main_part_off = o;
+  o += part;
+  ep->main_cnt_off = o;
+  o += align_up(static_cast<size_t>(E) * tmax * sizeof(int));
+  ep->side_part_off = o;
+  o += part;
+  ep->side_cnt_off = o;
+  o += align_up(static_cast<size_t>(tmax) * sizeof(int));
+  ep->total = o;
+  return true;
+}
+
+// Two events per (host thread, device) for the main/side fork and join.
+struct StreamEvents {
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+thread_local StreamEvents t_events[kMaxDevices];
+
+dec_status get_events(StreamEvents **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DEC_ERR_CUDA;
+  StreamEvents &ev = t_events[dev];
+  if (!ev.fork) {
+    if (cudaEventCreateWithFlags(&ev.fork, cudaEventDisableTiming) != cudaSuccess)
+      return DEC_ERR_CUDA;
+    if (cudaEventCreateWithFlags(&ev.join, cudaEventDisableTiming) != cudaSuccess)
+      return DEC_ERR_CUDA;
+  }
+  *out = &ev;
+  return DEC_OK;
+}
+
+}  // namespace
+
+// =================================================================== C ABI ====
+
+extern "C" {
+
+const char *dec_status_string(int status) {
+  switch (status) {
+    case DEC_OK: return "ok";
+    case DEC_ERR_INVALID_ARG: return "invalid argument";
+    case DEC_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (use the standard path)";
+    case DEC_ERR_MISALIGNED: return "misaligned pointer or length";
+    case DEC_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case DEC_ERR_CUDA: return "CUDA error";
+    case DEC_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+const char *dec_variant_name(int variant) {
+  switch (variant) {
+    case DEC_VARIANT_TINY: return "tiny";
+    case DEC_VARIANT_SPLITK: return "splitk";
+    case DEC_VARIANT_SPLITK_TC: return "splitk_tc";
+    default: return "none";
+  }
+}
+
+int dec_last_variant(void) { return t_last_variant; }
+
+int dec_version(void) { return 100; }
+
+dec_status dec_set_force_variant(int variant) {
+  if (variant < DEC_VARIANT_NONE || variant > DEC_VARIANT_SPLITK_TC) return DEC_ERR_INVALID_ARG;
+  g_force_variant.store(variant);
+  return DEC_OK;
+}
+
+dec_status dec_set_fault_inject(int count) {
+  if (count < 0) return DEC_ERR_INVALID_ARG;
+  g_fault_inject.store(count);
+  return DEC_OK;
+}
+
+dec_status dec_set_wait_limit_ns(uint64_t ns) {
+  if (ns < 1000000ull) return DEC_ERR_INVALID_ARG;
+  g_wait_limit_ns.store(ns);
+  return DEC_OK;
+}
+
+dec_status dec_sync_status(dec_stream_t s) {
+  cudaError_t ce;
+  DeviceInfo *d = device_info(&ce);
+  if (!d) return DEC_ERR_CUDA;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(s)) != cudaSuccess) return DEC_ERR_CUDA;
+  unsigned word = 0, zero = 0;
+  if (cudaMemcpy(&word, d->status, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return DEC_ERR_CUDA;
+  if (word != 0 && cudaMemcpy(d->status, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+    return DEC_ERR_CUDA;
+  if (word & ST_TIMEOUT) return DEC_ERR_TIMEOUT;
+  if (word & ST_BAD_ROUTING) return DEC_ERR_INVALID_ARG;
+  return DEC_OK;
+}
+
+dec_status dec_debug_wait_timeout(uint64_t limit_ns, dec_stream_t s) {
+  if (limit_ns < 1000000ull || limit_ns > 10000000000ull) return DEC_ERR_INVALID_ARG;
+  cudaError_t ce;
+  DeviceInfo *d = device_info(&ce);
+  if (!d) return DEC_ERR_CUDA;
+  return cuda_status(launch_wait_selftest(d->status, limit_ns, reinterpret_cast<cudaStream_t>(s)));
+}
+
+// ------------------------------------------------------------- projection ----
+
+dec_status dec_gemv(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 *R, dec_bf16 *Y, int B,
+                    int N, int K, dec_stream_t s) {
+  dec_status st = check_linear_args(X, W, Y, B, N, K);
+  if (st != DEC_OK) return st;
+  if (B > 2) return DEC_ERR_UNSUPPORTED_SHAPE;
+  cudaError_t ce;
+  DeviceInfo *d = device_info(&ce);
+  if (!d) return DEC_ERR_CUDA;
+  if (consume_fault()) return DEC_ERR_CUDA;
+  ce = launch_gemv_tiny(X, W, R, Y, B, N, K, d->num_sms, reinterpret_cast<cudaStream_t>(s));
+  if (ce != cudaSuccess) return DEC_ERR_CUDA;
+  t_last_variant = DEC_VARIANT_TINY;
+  return DEC_OK;
+}
+
+size_t dec_splitk_workspace_bytes(int B, int N, int K, int split_k) {
+  if (B < 1 || B > MAX_B || N < 1 || K < 1 || split_k < 0) return 0;
+  SplitPlan pl;
+  const int sms = current_num_sms();
+  if (sms <= 0 || !plan_splitk(B, N, K, split_k, sms, &pl)) return 0;
+  return pl.total;
+}
+
+dec_status dec_splitk_gemm(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 *R, dec_bf16 *Y,
+                           int B, int N, int K, int split_k, int use_tc, void *ws,
+                           size_t ws_bytes, dec_stream_t s) {
+  dec_status st = check_linear_args(X, W, Y, B, N, K);
+  if (st != DEC_OK) return st;
+  if (split_k < 0 || (use_tc != 0 && use_tc != 1)) return DEC_ERR_INVALID_ARG;
+  return run_splitk(X, W, R, Y, B, N, K, split_k, use_tc, ws, ws_bytes,
+                    reinterpret_cast<cudaStream_t>(s));
+}
+
+size_t dec_linear_workspace_bytes(int B, int N, int K) {
+  return dec_splitk_workspace_bytes(B, N, K, 0);
+}
+
+dec_status dec_linear(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 *R, dec_bf16 *Y, int B,
+                      int N, int K, void *ws, size_t ws_bytes, dec_stream_t s) {
+  dec_status st = check_linear_args(X, W, Y, B, N, K);
+  if (st != DEC_OK) return st;
+  int v = force_variant();
+  if (v == DEC_VARIANT_NONE)
+    v = (B <= 2) ? DEC_VARIANT_TINY
+                 : (B >= tc_min_batch() ? DEC_VARIANT_SPLITK_TC : DEC_VARIANT_SPLITK);
+  if (v == DEC_VARIANT_TINY) return dec_gemv(X, W, R, Y, B, N, K, s);
+  return run_splitk(X, W, R, Y, B, N, K, 0, v == DEC_VARIANT_SPLITK_TC ? 1 : 0, ws, ws_bytes,
+                    reinterpret_cast<cudaStream_t>(s));
+}
+
+// ------------------------------------------------------------------- MoE ----
+
+size_t moe_route_map_ints(int B, int E, int topk) {
+  if (B < 1 || E < 1 || topk < 1) return 0;
+  return static_cast<size_t>(3) * E + 2 + static_cast<size_t>(2) * B * topk;
+}
+
+size_t moe_front_workspace_bytes(int B, int E, int L, int K) {
+  if (B < 1 || B > MAX_B || E < 1 || E > MAX_E || L < 0 || K < 1) return 0;
+  const int sms = current_num_sms();
+  FrontPlan fp;
+  if (sms <= 0 || !plan_front(B, E, L, K, sms, &fp)) return 0;
+  return fp.total;
+}
+
+dec_status moe_front(const dec_bf16 *X, const dec_bf16 *Wcat, int B, int K, int E, int L,
+                     int topk, dec_bf16 *latent, int32_t *topk_idx, float *topk_w,
+                     float *probs_opt, int32_t *route_map_opt, void *ws, size_t ws_bytes,
+                     dec_stream_t s) {
+  if (!X || !Wcat || !topk_idx || !topk_w || !ws) return DEC_ERR_INVALID_ARG;
+  if (L > 0 && !latent) return DEC_ERR_INVALID_ARG;
+  if (B < 1 || K < 1 || E < 1 || L < 0 || topk < 1) return DEC_ERR_INVALID_ARG;
+  if (B > MAX_B || E > MAX_E || topk > MAX_TOPK || topk > E) return DEC_ERR_UNSUPPORTED_SHAPE;
+  if (K % 8 != 0 || !aligned16(X) || !aligned16(Wcat) || !aligned16(ws)) return DEC_ERR_MISALIGNED;
+  cudaError_t ce;
+  DeviceInfo *d = device_info(&ce);
+  if (!d) return DEC_ERR_CUDA;
+  FrontPlan fp;
+  if (!plan_front(B, E, L, K, d->num_sms, &fp)) return DEC_ERR_UNSUPPORTED_SHAPE;
+  if (ws_bytes < fp.total) return DEC_ERR_WORKSPACE_TOO_SMALL;
+  CUtensorMap wmap, xmap;
+  if (!make_map(&wmap, Wcat, K, E + L, WBOX_ROWS) || !make_map(&xmap, X, K, B, XBOX_ROWS))
+    return DEC_ERR_CUDA;
+  EngineParams p;
+  fill_engine_common(p, fp.sk, MODE_FRONT, E + L, K, B, ws, d);
+  char *wsb = static_cast<char *>(ws);
+  p.done_counter = reinterpret_cast<int *>(wsb + fp.done_off);
+  p.logits = reinterpret_cast<float *>(wsb + fp.logits_off);
+  p.E = E;
+  p.L = L;
+  p.topk = topk;
+  p.latent = latent;
+  p.topk_idx = topk_idx;
+  p.topk_w = topk_w;
+  p.probs = probs_opt;
+  p.route_map_out = route_map_opt;
+  if (consume_fault()) return DEC_ERR_CUDA;
+  int v = force_variant();
+  const bool tc = (v == DEC_VARIANT_SPLITK_TC) || (v == DEC_VARIANT_NONE && B >= tc_min_batch());
+  ce = tc ? launch_engine_tc(fp.sk.maxc, wmap, xmap, p, reinterpret_cast<cudaStream_t>(s))
+          : launch_engine_cc(fp.sk.maxc, wmap, xmap, p, reinterpret_cast<cudaStream_t>(s));
+  if (ce == cudaErrorNotSupported) return DEC_ERR_UNSUPPORTED_SHAPE;
+  if (ce != cudaSuccess) return DEC_ERR_CUDA;
+  t_last_variant = tc ? DEC_VARIANT_SPLITK_TC : DEC_VARIANT_SPLITK;
+  return DEC_OK;
+}
+
+size_t moe_experts_workspace_bytes(int B, int E, int topk, int H, int I) {
+  if (B < 1 || B > MAX_B || E < 1 || E > MAX_E || topk < 1 || topk > MAX_TOPK || H < 1 || I < 1)
+    return 0;
+  const int sms = current_num_sms();
+  ExpertsPlan ep;
+  if (sms <= 0 || !plan_experts(B, E, topk, H, I, sms, &ep)) return 0;
+  return ep.total;
+}
+
+dec_status moe_experts(const dec_bf16 *X, const int32_t *topk_idx, const float *topk_w,
+                       const int32_t *route_map, const dec_bf16 *Wgu, const dec_bf16 *Wd, int E,
+                       const dec_bf16 *Wgu_shared, const dec_bf16 *Wd_shared, int B, int H,
+                       int I, int topk, dec_bf16 *Y, void *ws, size_t ws_bytes,
+                       dec_stream_t main_stream, dec_stream_t side_stream, int side_max_ctas) {
+  if (!X || !topk_idx || !topk_w || !Wgu || !Wd || !Y || !ws) return DEC_ERR_INVALID_ARG;
+  if ((Wgu_shared == nullptr) != (Wd_shared == nullptr)) return DEC_ERR_INVALID_ARG;
+  if (B < 1 || E < 1 || H < 1 || I < 1 || topk < 1 || side_max_ctas < 0)
+    return DEC_ERR_INVALID_ARG;
+  if (B > MAX_B || E > MAX_E || topk > MAX_TOPK || topk > E) return DEC_ERR_UNSUPPORTED_SHAPE;
+  if (H % TILE_N != 0 || I % 64 != 0) return DEC_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(X) || !aligned16(Wgu) || !aligned16(Wd) || !aligned16(ws) ||
+      (Wgu_shared && (!aligned16(Wgu_shared) || !aligned16(Wd_shared))) || !aligned16(Y) ||
+      (reinterpret_cast<uintptr_t>(topk_w) & 3u) || (reinterpret_cast<uintptr_t>(topk_idx) & 3u))
+    return DEC_ERR_MISALIGNED;
+  cudaError_t ce;
+  DeviceInfo *d = device_info(&ce);
+  if (!d) return DEC_ERR_CUDA;
+  ExpertsPlan ep;
+  if (!plan_experts(B, E, topk, H, I, d->num_sms, &ep)) return DEC_ERR_UNSUPPORTED_SHAPE;
+  if (ws_bytes < ep.total) return DEC_ERR_WORKSPACE_TOO_SMALL;
+  StreamEvents *ev = nullptr;
+  dec_status st = get_events(&ev);
+  if (st != DEC_OK) return st;
+
+  cudaStream_t ms = reinterpret_cast<cudaStream_t>(main_stream);
+  cudaStream_t ss = reinterpret_cast<cudaStream_t>(side_stream);
+  const bool shared = (Wgu_shared != nullptr);
+  const bool overlap = shared && (ss != ms);
+  const int P = B * topk;
+  char *wsb = static_cast<char *>(ws);
+  int32_t *rm = route_map ? const_cast<int32_t *>(route_map)
+                          : reinterpret_cast<int32_t *>(wsb + ep.rm_off);
+  uint16_t *Xg = reinterpret_cast<uint16_t *>(wsb + ep.xg_off);
+  uint16_t *A = reinterpret_cast<uint16_t *>(wsb + ep.a_off);
+  float *Yp = reinterpret_cast<float *>(wsb + ep.yp_off);
+  uint16_t *As = reinterpret_cast<uint16_t *>(wsb + ep.as_off);
+  float *S = reinterpret_cast<float *>(wsb + ep.s_off);
+
+  // CTA split between the routed experts (main) and the shared expert (side): in
+  // proportion to the weight bytes each reads, using the expected number of distinct
+  // experts for this batch, unless the caller caps the side.
+  int g_side = 0;
+  if (overlap) {
+    if (side_max_ctas > 0) {
+      g_side = side_max_ctas;
+    } else {
+      double miss = 1.0;
+      for (int b = 0; b < B; ++b) miss *= 1.0 - static_cast<double>(topk) / E;
+      const double u_exp = E * (1.0 - miss);
+      g_side = static_cast<int>(d->num_sms / (1.0 + u_exp) + 0.5);
+    }
+    if (g_side < 1) g_side = 1;
+    if (g_side > d->num_sms / 2) g_side = d->num_sms / 2;
+  }
+  const int g_main = d->num_sms - g_side;
+
+  CUtensorMap m_wgu, m_wd, m_xg, m_a;
+  if (!make_map(&m_wgu, Wgu, H, static_cast<uint64_t>(E) * 2 * I, WBOX_ROWS) ||
+      !make_map(&m_wd, Wd, I, static_cast<uint64_t>(E) * H, WBOX_ROWS) ||
+      !make_map(&m_xg, Xg, H, P, XBOX_ROWS) || !make_map(&m_a, A, I, P, XBOX_ROWS))
+    return DEC_ERR_CUDA;
+  CUtensorMap m_wgus, m_wds, m_x, m_as;
+  if (shared && (!make_map(&m_wgus, Wgu_shared, H, 2 * I, WBOX_ROWS) ||
+                 !make_map(&m_wds, Wd_shared, I, H, WBOX_ROWS) ||
+                 !make_map(&m_x, X, H, B, XBOX_ROWS) || !make_map(&m_as, As, I, B, XBOX_ROWS)))
+    return DEC_ERR_CUDA;
+
+  if (consume_fault()) return DEC_ERR_CUDA;
+
+  auto engine = [&](const CUtensorMap &wm, const CUtensorMap &xm, EngineParams &p,
+                    cudaStream_t st_) -> cudaError_t {
+    return launch_engine_cc(p.slot_cols, wm, xm, p, st_);
+  };
+  auto base = [&](EngineParams &p, int mode, int N, int K, int T, int KB, int G, int grouped,
+                  size_t part_off, size_t cnt_off) {
+    std::memset(&p, 0, sizeof p);
+    p.mode = mode;
+    p.N = N;
+    p.K = K;
+    p.T = T;
+    p.KB = KB;
+    p.G = G;
+    p.grouped = grouped;
+    p.B = B;
+    p.slot_cols = ep.maxc;
+    p.E = E;
+    p.P = P;
+    p.route_map = rm;
+    p.partials = reinterpret_cast<float *>(wsb + part_off);
+    p.counters = reinterpret_cast<int *>(wsb + cnt_off);
+    p.status = d->status;
+    p.wait_limit_ns = g_wait_limit_ns.load();
+  };
+
+  // ---- shared expert, side stream (or main when no second stream was given)
+  if (shared) {
+    cudaStream_t sst = overlap ? ss : ms;
+    const int gs = overlap ? g_side : d->num_sms;
+    if (overlap) {
+      if ((ce = cudaEventRecord(ev->fork, ms)) != cudaSuccess) return DEC_ERR_CUDA;
+      if ((ce = cudaStreamWaitEvent(ss, ev->fork, 0)) != cudaSuccess) return DEC_ERR_CUDA;
+    }
+    EngineParams p;
+    base(p, MODE_GATEUP, I, H, ep.Tg, ep.KBg, gs < ep.Tg * ep.KBg ? gs : ep.Tg * ep.KBg, 0,
+         overlap ? ep.side_part_off : ep.main_part_off, overlap ? ep.side_cnt_off : ep.main_cnt_off);
+    p.w_group_rows = 2 * I;
+    p.up_row_off = I;
+    p.A = As;
+    if ((ce = engine(m_wgus, m_x, p, sst)) != cudaSuccess) return DEC_ERR_CUDA;
+    base(p, MODE_DOWN, H, I, ep.Td, ep.KBd, gs < ep.Td * ep.KBd ? gs : ep.Td * ep.KBd, 0,
+         overlap ? ep.side_part_off : ep.main_part_off, overlap ? ep.side_cnt_off : ep.main_cnt_off);
+    p.w_group_rows = H;
+    p.Yp = S;
+    if ((ce = engine(m_wds, m_as, p, sst)) != cudaSuccess) return DEC_ERR_CUDA;
+    if (overlap && (ce = cudaEventRecord(ev->join, ss)) != cudaSuccess) return DEC_ERR_CUDA;
+  }
+
+  // ---- routed experts, main stream
+  if (!route_map) {
+    if ((ce = launch_route_map_rebuild(topk_idx, B, topk, E, rm, d->status, ms)) != cudaSuccess)
+      return DEC_ERR_CUDA;
+  }
+  if ((ce = launch_gather_rows(X, rm, B, topk, E, H, Xg, ms)) != cudaSuccess) return DEC_ERR_CUDA;
+  {
+    EngineParams p;
+    // G <= T*KB keeps every worker range non-empty even with a single used expert
+    const int gg = g_main < ep.Tg * ep.KBg ? g_main : ep.Tg * ep.KBg;
+    const int gd = g_main < ep.Td * ep.KBd ? g_main : ep.Td * ep.KBd;
+    base(p, MODE_GATEUP, I, H, ep.Tg, ep.KBg, gg, 1, ep.main_part_off, ep.main_cnt_off);
+    p.w_group_rows = 2 * I;
+    p.up_row_off = I;
+    p.A = A;
+    if ((ce = engine(m_wgu, m_xg, p, ms)) != cudaSuccess) return DEC_ERR_CUDA;
+    base(p, MODE_DOWN, H, I, ep.Td, ep.KBd, gd, 1, ep.main_part_off, ep.main_cnt_off);
+    p.w_group_rows = H;
+    p.Yp = Yp;
+    if ((ce = engine(m_wd, m_a, p, ms)) != cudaSuccess) return DEC_ERR_CUDA;
+  }
+  if (overlap && (ce = cudaStreamWaitEvent(ms, ev->join, 0)) != cudaSuccess) return DEC_ERR_CUDA;
+  if ((ce = launch_combine(topk_w, rm, Yp, shared ? S : nullptr, B, topk, E, H, Y, ms)) !=
+      cudaSuccess)
+    return DEC_ERR_CUDA;
+  return DEC_OK;
+}
+
+// ------------------------------------------------------------- L2 prefetch ----
+
+dec_status l2_prefetch(const void *p, size_t bytes, int max_ctas, dec_stream_t s) {
+  if (!p || max_ctas < 0) return DEC_ERR_INVALID_ARG;
+  if (!aligned16(p)) return DEC_ERR_MISALIGNED;
+  bytes &= ~static_cast<size_t>(15);
+  if (bytes == 0) return DEC_OK;
+  if (consume_fault()) return DEC_ERR_CUDA;
+  const int ctas = max_ctas == 0 ? 8 : max_ctas;
+  return cuda_status(launch_l2_prefetch(p, bytes, ctas, reinterpret_cast<cudaStream_t>(s)));
+}
+
+}  // extern "C"

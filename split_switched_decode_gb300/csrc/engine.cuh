@@ -1,0 +1,213 @@
+// engine.cuh -- schedule, deterministic split-K reduction and epilogues shared by the
+// CUDA-core (engine_cc.cu) and tensor-core (engine_tc.cu) split-K kernels.
+//
+// "Hyper Optimizing Kimi K3 in vLLM", Part 1 / 1 "Tune shapes for the workload": at
+// larger batches the projections use split-K kernels that divide the matrix
+// multiplication across more GPU workers.
+//
+// Work decomposition. A launch covers `groups` independent products that share N and
+// K (one for a projection, one per used expert for the grouped expert GEMV). Each
+// product is cut into T output tiles of 128 weight rows and KB k-blocks of 64. The
+// flattened sequence of (group, tile, k-block) iterations is divided into G contiguous
+// ranges of equal length (+-1), one per CTA ("worker"): every SM streams the same
+// number of weight bytes, whatever N, K and the number of groups are. A worker walks
+// its range in "segments", one per tile it touches. A segment covering a whole tile
+// ends in the epilogue directly; otherwise the worker stores its partial tile in its
+// workspace slot and bumps the tile's arrival counter, and the worker that arrives
+// last adds the partials of all contributors in worker order (fixed order, so the
+// result is bit-identical run to run for a fixed G), runs the epilogue and resets the
+// counter to zero for the next launch. Nobody waits on another CTA.
+#pragma once
+
+#include "common.cuh"
+#include "internal.h"
+#include "routing.cuh"
+
+namespace ssd {
+
+__device__ __forceinline__ int64_t sk_start(int64_t total, int G, int w) {
+  return static_cast<int64_t>(w) * total / G;
+}
+
+// Worker whose range holds iteration i (requires G <= total: no empty ranges).
+__device__ __forceinline__ int sk_worker_of(int64_t total, int G, int64_t i) {
+  return static_cast<int>(((i + 1) * static_cast<int64_t>(G) - 1) / total);
+}
+
+__device__ __forceinline__ int rm_num_used(const EngineParams &p) {
+  return min(max(p.route_map[2 * p.E + 1 + 2 * p.P], 0), p.E);
+}
+
+struct SegInfo {
+  int gt;      // global tile id (group * T + tile)
+  int t;       // tile within its group
+  int kb0;     // first k-block of the segment
+  int kb1;     // one past the last k-block
+  int ncols;   // activation rows (batch columns) of the group
+  int xrow0;   // first activation row of the group
+  int wrow0;   // W row of tile rows 0..63
+  int wrow1;   // W row of tile rows 64..127
+  bool full;   // the segment covers the whole tile
+};
+
+__device__ __forceinline__ void seg_info(const EngineParams &p, int64_t it, int64_t end,
+                                         SegInfo &s) {
+  s.gt = static_cast<int>(it / p.KB);
+  s.kb0 = static_cast<int>(it - static_cast<int64_t>(s.gt) * p.KB);
+  const int64_t tend = static_cast<int64_t>(s.gt + 1) * p.KB;
+  const int64_t se = end < tend ? end : tend;
+  s.kb1 = s.kb0 + static_cast<int>(se - it);
+  const int g = s.gt / p.T;
+  s.t = s.gt - g * p.T;
+  int wbase;
+  if (p.grouped) {
+    // the route map comes from moe_front or the validating rebuild kernel; the clamps
+    // only keep a corrupted map from steering loads or stores out of their buffers
+    const int32_t *rm = p.route_map;
+    const int e = min(max(rm[2 * p.E + 2 + 2 * p.P + g], 0), p.E - 1);
+    s.xrow0 = min(max(rm[p.E + e], 0), p.P);
+    s.ncols = min(max(rm[e], 0), min(p.slot_cols, p.P - s.xrow0));
+    wbase = e * p.w_group_rows;
+  } else {
+    s.ncols = p.B;
+    s.xrow0 = 0;
+    wbase = 0;
+  }
+  if (p.mode == MODE_GATEUP) {
+    s.wrow0 = wbase + s.t * 64;                 // gate rows
+    s.wrow1 = wbase + p.up_row_off + s.t * 64;  // matching up rows
+  } else {
+    s.wrow0 = wbase + s.t * 128;
+    s.wrow1 = s.wrow0 + 64;
+  }
+  s.full = (s.kb0 == 0 && s.kb1 == p.KB);
+}
+
+// Split-K reduction of one tile, run by the 128 threads that hold the segment's values
+// (thread r holds row r, columns 0..ncols-1 in v). Returns true when v holds the final
+// tile values on return (whole-tile segment, or this worker arrived last).
+template <int MAXC>
+__device__ __forceinline__ bool reduce_tile(const EngineParams &p, const SegInfo &s, int64_t total, int w,
+                            int64_t begin, int r, float (&v)[MAXC], int bar_id,
+                            volatile int *flags) {
+  if (s.full) return true;
+  const int64_t tb = static_cast<int64_t>(s.gt) * p.KB;
+  const int which_me = (begin >= tb) ? 0 : 1;
+  const size_t slot_floats = static_cast<size_t>(128) * p.slot_cols;
+  float *slot = p.partials + static_cast<size_t>(w * 2 + which_me) * slot_floats;
+#pragma unroll
+  for (int j = 0; j < MAXC; ++j)
+    if (j < s.ncols) slot[j * 128 + r] = v[j];
+  __threadfence();
+  named_bar_sync(bar_id, 128);
+  const int first = sk_worker_of(total, p.G, tb);
+  const int last = sk_worker_of(total, p.G, tb + p.KB - 1);
+  if (r == 0) {
+    const int old = atomicAdd(&p.counters[s.gt], 1);
+    flags[1] = (old == last - first) ? 1 : 0;
+  }
+  named_bar_sync(bar_id, 128);
+  if (!flags[1]) return false;
+  __threadfence();
+  float t[MAXC];
+#pragma unroll
+  for (int j = 0; j < MAXC; ++j) t[j] = 0.f;
+  for (int wk = first; wk <= last; ++wk) {
+    if (wk == w) {
+#pragma unroll
+      for (int j = 0; j < MAXC; ++j) t[j] += v[j];
+    } else {
+      const int which = (sk_start(total, p.G, wk) >= tb) ? 0 : 1;
+      const float *sl = p.partials + static_cast<size_t>(wk * 2 + which) * slot_floats;
+#pragma unroll
+      for (int j = 0; j < MAXC; ++j)
+        if (j < s.ncols) t[j] += __ldcg(sl + j * 128 + r);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < MAXC; ++j) v[j] = t[j];
+  if (r == 0) p.counters[s.gt] = 0;
+  return true;
+}
+
+// Epilogue of one finished tile, run by the same 128 threads. `scratch` holds at least
+// 64 * MAXC floats and is free on entry.
+template <int MAXC>
+__device__ __forceinline__ void epilogue_rows(const EngineParams &p, const SegInfo &s, int r, float (&v)[MAXC],
+                              float *scratch, int bar_id, volatile int *flags) {
+  if (p.mode == MODE_LINEAR) {
+    const int n = s.t * 128 + r;
+    if (n < p.N) {
+#pragma unroll
+      for (int j = 0; j < MAXC; ++j) {
+        if (j < s.ncols) {
+          float y = v[j];
+          if (p.R != nullptr) y += bf16_to_f32(p.R[static_cast<size_t>(j) * p.N + n]);
+          p.Y[static_cast<size_t>(j) * p.N + n] = f32_to_bf16_rn(y);
+        }
+      }
+    }
+  } else if (p.mode == MODE_FRONT) {
+    const int n = s.t * 128 + r;
+#pragma unroll
+    for (int j = 0; j < MAXC; ++j) {
+      if (j < s.ncols) {
+        if (n < p.E)
+          p.logits[static_cast<size_t>(j) * p.E + n] = v[j];
+        else if (n < p.E + p.L)
+          p.latent[static_cast<size_t>(j) * p.L + (n - p.E)] = f32_to_bf16_rn(v[j]);
+      }
+    }
+    __threadfence();
+    named_bar_sync(bar_id, 128);
+    if (r == 0) {
+      const int old = atomicAdd(p.done_counter, 1);
+      if (old == p.T - 1) flags[2] = 1;  // this CTA finished the last tile: it routes
+    }
+  } else if (p.mode == MODE_GATEUP) {
+    named_bar_sync(bar_id, 128);
+    if (r >= 64) {
+#pragma unroll
+      for (int j = 0; j < MAXC; ++j)
+        if (j < s.ncols) scratch[j * 64 + (r - 64)] = v[j];
+    }
+    named_bar_sync(bar_id, 128);
+    if (r < 64) {
+      const int i = s.t * 64 + r;
+#pragma unroll
+      for (int j = 0; j < MAXC; ++j) {
+        if (j < s.ncols) {
+          const float g = v[j];
+          const float u = scratch[j * 64 + r];
+          const float a = g / (1.f + expf(-g)) * u;
+          p.A[static_cast<size_t>(s.xrow0 + j) * p.N + i] = f32_to_bf16_rn(a);
+        }
+      }
+    }
+  } else {  // MODE_DOWN
+    const int n = s.t * 128 + r;
+    if (n < p.N) {
+#pragma unroll
+      for (int j = 0; j < MAXC; ++j)
+        if (j < s.ncols) p.Yp[static_cast<size_t>(s.xrow0 + j) * p.N + n] = v[j];
+    }
+  }
+}
+
+// Routing tail of MODE_FRONT, run by the 8 warps (256 threads, named barrier 1) of the
+// CTA that finished the last tile. `work` is free shared memory of >= 16 KB.
+__device__ __forceinline__ void front_route_tail(const EngineParams &p, uint8_t *work,
+                                                 int warp) {
+  __threadfence();
+  int32_t *sidx = reinterpret_cast<int32_t *>(work);
+  unsigned long long *smask = reinterpret_cast<unsigned long long *>(work + 4 * MAX_B * MAX_TOPK);
+  int *soff = reinterpret_cast<int *>(work + 4 * MAX_B * MAX_TOPK + 8 * MAX_E);
+  route_tokens_warp(p.logits, p.B, p.E, p.topk, p.topk_idx, p.topk_w, p.probs, sidx, warp, 8);
+  if (p.route_map_out != nullptr) {
+    named_bar_sync(1, 256);
+    build_route_map(sidx, p.B, p.topk, p.E, p.route_map_out, smask, soff, 256, 1);
+  }
+  if (threadIdx.x == 0) *p.done_counter = 0;
+}
+
+}  // namespace ssd

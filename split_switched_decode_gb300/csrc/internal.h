@@ -1,0 +1,78 @@
+// internal.h -- interface between the library's translation units (not installed).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace ssd {
+
+// Parameters of one launch of the split-K engine (see engine.cuh). Passed by value.
+struct EngineParams {
+  int mode;          // EngineMode
+  int N;             // epilogue output width: LINEAR/FRONT rows of W, GATEUP I, DOWN H
+  int K;             // reduction length
+  int T;             // tiles per group
+  int KB;            // 64-wide k-blocks per tile
+  int G;             // workers (== gridDim.x), G <= T*KB
+  int grouped;       // 0: one group of B columns; 1: groups = used experts of a route map
+  int B;             // columns of the single group
+  int w_group_rows;  // W rows per group in the weight bank (grouped)
+  int up_row_off;    // GATEUP: row offset of the up half inside a group (= I)
+  int slot_cols;     // columns per partial slot (slot = 128 * slot_cols floats)
+  int E;             // experts (grouped route map, FRONT router rows)
+  int P;             // B * topk (grouped route map)
+  const int32_t *route_map;  // grouped: counts | offsets | pairs | pos | num_used | used
+  // MODE_LINEAR
+  uint16_t *Y;
+  const uint16_t *R;
+  // MODE_FRONT
+  float *logits;     // [B,E] fp32
+  uint16_t *latent;  // [B,L] bf16
+  int L;
+  int topk;
+  int32_t *topk_idx;
+  float *topk_w;
+  float *probs;
+  int32_t *route_map_out;
+  int *done_counter;
+  // MODE_GATEUP / MODE_DOWN: output row = group's first activation row + column
+  uint16_t *A;  // [rows, N] bf16
+  float *Yp;    // [rows, N] fp32
+  // split-K reduction
+  float *partials;  // [2*G][128*slot_cols]
+  int *counters;    // one per (group, tile), zero between launches
+  // error reporting
+  unsigned *status;
+  uint64_t wait_limit_ns;
+};
+
+// ------------------------------------------------------------- engine_cc.cu --
+int engine_maxc_for(int ncols);                 // 2, 4, 8, 16, 32 or 64
+size_t engine_cc_smem_bytes(int maxc);
+cudaError_t launch_engine_cc(int maxc, const CUtensorMap &wmap, const CUtensorMap &xmap,
+                             const EngineParams &p, cudaStream_t s);
+
+// ------------------------------------------------------------- engine_tc.cu --
+size_t engine_tc_smem_bytes(int maxc);
+cudaError_t launch_engine_tc(int maxc, const CUtensorMap &wmap, const CUtensorMap &xmap,
+                             const EngineParams &p, cudaStream_t s);
+
+// ------------------------------------------------------------- gemv_tiny.cu --
+int gemv_tiny_grid(int N, int num_sms);
+cudaError_t launch_gemv_tiny(const uint16_t *X, const uint16_t *W, const uint16_t *R,
+                             uint16_t *Y, int B, int N, int K, int num_sms, cudaStream_t s);
+
+// --------------------------------------------------------------- moe_aux.cu --
+cudaError_t launch_route_map_rebuild(const int32_t *topk_idx, int B, int topk, int E,
+                                     int32_t *route_map, unsigned *status, cudaStream_t s);
+cudaError_t launch_gather_rows(const uint16_t *X, const int32_t *route_map, int B, int topk,
+                               int E, int K, uint16_t *Xg, cudaStream_t s);
+cudaError_t launch_combine(const float *topk_w, const int32_t *route_map, const float *Yp,
+                           const float *S, int B, int topk, int E, int H, uint16_t *Y,
+                           cudaStream_t s);
+cudaError_t launch_l2_prefetch(const void *p, size_t bytes, int ctas, cudaStream_t s);
+cudaError_t launch_wait_selftest(unsigned *status, uint64_t limit_ns, cudaStream_t s);
+
+}  // namespace ssd

@@ -1,0 +1,165 @@
+// moe_aux.cu -- small kernels around the grouped expert GEMV, the L2 prefetch kernel
+// and the bounded-wait self-test.
+#include "common.cuh"
+#include "internal.h"
+#include "routing.cuh"
+
+namespace ssd {
+
+namespace {
+
+// Rebuild the route map from topk_idx when the caller did not keep moe_front's.
+// Caller indices are validated first (0 <= e < E, distinct within a token); any
+// violation yields an empty map (no used expert, zeros elsewhere) and ST_BAD_ROUTING.
+__global__ void __launch_bounds__(256) route_map_kernel(const int32_t *topk_idx, int B, int topk,
+                                                        int E, int32_t *rm, unsigned *status) {
+  __shared__ int32_t sidx[MAX_B * MAX_TOPK];
+  __shared__ unsigned long long smask[MAX_E];
+  __shared__ int soff[MAX_E];
+  __shared__ int bad;
+  if (threadIdx.x == 0) bad = 0;
+  __syncthreads();
+  for (int q = threadIdx.x; q < B * topk; q += 256) {
+    const int e = topk_idx[q];
+    sidx[q] = e;
+    if (e < 0 || e >= E) bad = 1;
+  }
+  __syncthreads();
+  for (int b = threadIdx.x; b < B; b += 256)
+    for (int i = 0; i < topk; ++i)
+      for (int j = i + 1; j < topk; ++j)
+        if (sidx[b * topk + i] == sidx[b * topk + j]) bad = 1;
+  __syncthreads();
+  if (bad) {
+    const int n = 3 * E + 2 + 2 * B * topk;
+    for (int i = threadIdx.x; i < n; i += 256) rm[i] = 0;
+    if (threadIdx.x == 0) atomicOr(status, ST_BAD_ROUTING);
+    return;
+  }
+  build_route_map(sidx, B, topk, E, rm, smask, soff, 256, 1);
+}
+
+// Xg[q, :] = X[pairs[q] / topk, :] -- the activation rows of every (token, slot) entry
+// in expert order, so each expert's rows are contiguous for the TMA tile loads.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t *X, const int32_t *rm,
+                                                          int B, int topk, int E, int K,
+                                                          uint16_t *Xg) {
+  const int P = B * topk;
+  const int32_t *pairs = rm + 2 * E + 1;
+  const int chunks = K / 8;  // 16-byte chunks per row
+  const int64_t n = static_cast<int64_t>(P) * chunks;
+  for (int64_t i = blockIdx.x * 256ll + threadIdx.x; i < n; i += gridDim.x * 256ll) {
+    const int q = static_cast<int>(i / chunks);
+    const int c = static_cast<int>(i - static_cast<int64_t>(q) * chunks);
+    const int b = min(max(pairs[q] / topk, 0), B - 1);
+    const uint4 v = reinterpret_cast<const uint4 *>(X + static_cast<size_t>(b) * K)[c];
+    reinterpret_cast<uint4 *>(Xg + static_cast<size_t>(q) * K)[c] = v;
+  }
+}
+
+// Y[b,h] = bf16( sum_{j ascending} w[b,j] * Yp[pos[b,j], h]  (+ S[b,h]) ), fp32.
+__global__ void __launch_bounds__(256) combine_kernel(const float *topk_w, const int32_t *rm,
+                                                      const float *Yp, const float *S, int B,
+                                                      int topk, int E, int H, uint16_t *Y) {
+  const int P = B * topk;
+  const int32_t *pos = rm + 2 * E + 1 + P;
+  const int H4 = H / 4;
+  const int64_t n = static_cast<int64_t>(B) * H4;
+  for (int64_t i = blockIdx.x * 256ll + threadIdx.x; i < n; i += gridDim.x * 256ll) {
+    const int b = static_cast<int>(i / H4);
+    const int h4 = static_cast<int>(i - static_cast<int64_t>(b) * H4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < topk; ++j) {
+      const float wj = topk_w[b * topk + j];
+      const int at = min(max(pos[b * topk + j], 0), P - 1);
+      const float4 y = reinterpret_cast<const float4 *>(Yp + static_cast<size_t>(at) * H)[h4];
+      acc.x = fmaf(wj, y.x, acc.x);
+      acc.y = fmaf(wj, y.y, acc.y);
+      acc.z = fmaf(wj, y.z, acc.z);
+      acc.w = fmaf(wj, y.w, acc.w);
+    }
+    if (S != nullptr) {
+      const float4 sv = reinterpret_cast<const float4 *>(S + static_cast<size_t>(b) * H)[h4];
+      acc.x += sv.x;
+      acc.y += sv.y;
+      acc.z += sv.z;
+      acc.w += sv.w;
+    }
+    uint2 o;
+    o.x = static_cast<uint32_t>(f32_to_bf16_rn(acc.x)) |
+          (static_cast<uint32_t>(f32_to_bf16_rn(acc.y)) << 16);
+    o.y = static_cast<uint32_t>(f32_to_bf16_rn(acc.z)) |
+          (static_cast<uint32_t>(f32_to_bf16_rn(acc.w)) << 16);
+    reinterpret_cast<uint2 *>(Y + static_cast<size_t>(b) * H)[h4] = o;
+  }
+}
+
+// Each thread issues bulk L2 prefetches of PF_CHUNK bytes over the range; nothing is
+// written and nothing waits: the copies into L2 proceed after the kernel retires.
+constexpr uint32_t PF_CHUNK = 32768;
+
+__global__ void __launch_bounds__(128) l2_prefetch_kernel(const uint8_t *p, size_t bytes) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x * PF_CHUNK;
+  for (size_t off = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) * PF_CHUNK;
+       off < bytes; off += stride) {
+    const size_t left = bytes - off;
+    const uint32_t n = left < PF_CHUNK ? static_cast<uint32_t>(left) : PF_CHUNK;
+    prefetch_l2_bulk(p + off, n);
+  }
+}
+
+// Waits on an mbarrier that nothing arrives at; must give up after limit_ns.
+__global__ void wait_selftest_kernel(unsigned *status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  (void)mbar_wait_bounded(&bar, 0u, status, &abort_flag, limit_ns);
+}
+
+}  // namespace
+
+cudaError_t launch_route_map_rebuild(const int32_t *topk_idx, int B, int topk, int E,
+                                     int32_t *route_map, unsigned *status, cudaStream_t s) {
+  route_map_kernel<<<1, 256, 0, s>>>(topk_idx, B, topk, E, route_map, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const uint16_t *X, const int32_t *route_map, int B, int topk,
+                               int E, int K, uint16_t *Xg, cudaStream_t s) {
+  const int64_t n = static_cast<int64_t>(B) * topk * (K / 8);
+  int grid = static_cast<int>((n + 255) / 256);
+  if (grid > 1024) grid = 1024;
+  gather_rows_kernel<<<grid, 256, 0, s>>>(X, route_map, B, topk, E, K, Xg);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const float *topk_w, const int32_t *route_map, const float *Yp,
+                           const float *S, int B, int topk, int E, int H, uint16_t *Y,
+                           cudaStream_t s) {
+  const int64_t n = static_cast<int64_t>(B) * (H / 4);
+  int grid = static_cast<int>((n + 255) / 256);
+  if (grid > 1024) grid = 1024;
+  combine_kernel<<<grid, 256, 0, s>>>(topk_w, route_map, Yp, S, B, topk, E, H, Y);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_l2_prefetch(const void *p, size_t bytes, int ctas, cudaStream_t s) {
+  const size_t per_cta = static_cast<size_t>(128) * PF_CHUNK;
+  size_t need = (bytes + per_cta - 1) / per_cta;
+  int grid = static_cast<int>(need < static_cast<size_t>(ctas) ? need : static_cast<size_t>(ctas));
+  if (grid < 1) grid = 1;
+  l2_prefetch_kernel<<<grid, 128, 0, s>>>(static_cast<const uint8_t *>(p), bytes);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(unsigned *status, uint64_t limit_ns, cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace ssd

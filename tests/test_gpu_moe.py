@@ -1,0 +1,303 @@
+"""GPU parity of the MoE front end, the routed experts + shared expert, and the L2
+prefetch ("Hyper Optimizing Kimi K3 in vLLM", Part 1 / 3 and / 4) against the fp64
+oracle, through the C ABI. Expert indices must match bit for bit; floats within the
+tolerance of gpu_common."""
+import numpy as np
+import pytest
+
+from gpu_common import assert_close, to_f64, topk_gap
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import oracle
+    import split_switched_decode_gb300 as ssd
+    ssd.build()
+    oracle.build()
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    ssd.dec_set_force_variant(ssd.VARIANT_NONE)
+    return torch, ssd, oracle, dev
+
+
+def _run_front(env, X, Wc, E, L, k, probs=True, route_map=True):
+    torch, ssd, oracle, dev = env
+    B = X.shape[0]
+    lat = torch.empty(B, L, dtype=torch.bfloat16, device=dev) if L else None
+    idx = torch.full((B, k), -1, dtype=torch.int32, device=dev)
+    w = torch.empty(B, k, dtype=torch.float32, device=dev)
+    pr = torch.empty(B, E, dtype=torch.float32, device=dev) if probs else None
+    rm = torch.full((ssd.moe_route_map_ints(B, E, k),), -7, dtype=torch.int32, device=dev) if route_map else None
+    ws = ssd.workspace(ssd.moe_front_workspace_bytes(B, E, L, X.shape[1]), dev)
+    ssd.moe_front(X, Wc, E, L, k, lat, idx, w, ws, probs=pr, route_map=rm)
+    torch.cuda.synchronize()
+    return lat, idx, w, pr, rm
+
+
+def _check_front(env, X, Wc, E, L, k, what):
+    torch, ssd, oracle, dev = env
+    from split_switched_decode_gb300 import inputs
+    lat, idx, w, pr, rm = _run_front(env, X, Wc, E, L, k)
+    ref = oracle.moe_front(inputs.bits(X), inputs.bits(Wc), E, L, k)
+    gi = idx.cpu().numpy()
+    if not np.array_equal(gi, ref["idx"]):
+        bad = np.where((gi != ref["idx"]).any(1))[0]
+        gaps = [topk_gap(ref["logits"][b], k) for b in bad]
+        raise AssertionError(f"{what}: top-k differs for tokens {bad.tolist()} "
+                             f"(oracle near-tie gaps {gaps})")
+    assert_close(w.cpu().numpy(), ref["w"], f"{what} weights")
+    assert_close(pr.cpu().numpy(), ref["probs"], f"{what} probs")
+    if L:
+        assert_close(to_f64(oracle, lat), oracle.bf16_to_f64(ref["latent"]), f"{what} latent")
+    m = oracle.route_map(ref["idx"], E)
+    r = rm.cpu().numpy()
+    B, P = X.shape[0], X.shape[0] * k
+    assert np.array_equal(r[:E], m["counts"])
+    assert np.array_equal(r[E:2 * E + 1], m["offsets"])
+    assert np.array_equal(r[2 * E + 1:2 * E + 1 + P], m["pairs"])
+    assert np.array_equal(r[2 * E + 1 + P:2 * E + 1 + 2 * P], m["pos"])
+    assert r[2 * E + 1 + 2 * P] == m["num_used"]
+    assert np.array_equal(r[2 * E + 2 + 2 * P:2 * E + 2 + 2 * P + m["num_used"]], m["used"])
+    return ref
+
+
+@pytest.mark.parametrize("B", [1, 8, 64])
+def test_moe_front_full_size(env, B):
+    """X[B,7168] x Wcat[384+512,7168], softmax over 384, top-8, renormalised."""
+    torch, ssd, oracle, dev = env
+    from split_switched_decode_gb300 import inputs
+    E, L, K, k = 384, 512, 7168, 8
+    X = inputs.activations(B, K, dev, 0, "front_x")
+    Wc = inputs.weight(E + L, K, dev, 0, "front_w")
+    _check_front(env, X, Wc, E, L, k, f"front B={B}")
+
+
+@pytest.mark.parametrize("B,E,L,K,k", [(1, 40, 24, 200, 3), (5, 130, 0, 456, 16),
+                                       (33, 512, 8, 64, 1), (64, 16, 100, 1032, 16),
+                                       (2, 1, 0, 8, 1)])
+def test_moe_front_ragged_shapes(env, B, E, L, K, k):
+    torch, ssd, oracle, dev = env
+    from split_switched_decode_gb300 import inputs
+    X = inputs.activations(B, K, dev, 1, "fx")
+    Wc = inputs.randn_bf16((E + L, K), 0.2, dev, 1, "fw", E, L, K)
+    _check_front(env, X, Wc, E, L, k, f"front B={B} E={E} L={L} K={K} k={k}")
+
+
+def test_moe_front_ties_go_to_lower_index(env):
+    """Duplicate router rows in one tile give bit-identical fp32 logits: lower index first.
+    All-zero router rows give equal logits: experts 0..k-1, weights 1/k, probs 1/E."""
+    torch, ssd, oracle, dev = env
+    from split_switched_decode_gb300 import inputs
+    B, E, L, K, k = 4, 64, 16, 512, 4
+    X = inputs.activations(B, K, dev, 2, "tx")
+    Wc = inputs.weight(E + L, K, dev, 2, "tw")
+    big = inputs.randn_bf16((K,), 0.5, dev, 2, "big")
+    Wc[9] = big
+    Wc[40] = big          # same tile (rows 0..127): identical accumulation order
+    Wc[20] = -big
+    Wc[33] = -big
+    lat, idx, w, pr, rm = _run_front(env, X, Wc, E, L, k)
+    ref = oracle.moe_front(inputs.bits(X), inputs.bits(Wc), E, L, k)
+    assert np.array_equal(idx.cpu().numpy(), ref["idx"])
+    for b in range(B):
+        row = idx[b].tolist()
+        pair = (9, 40) if 9 in row[:2] else (20, 33)
+        assert row[:2] == list(pair), row
+    Wz = Wc.clone()
+    Wz[:E] = 0
+    lat, idx, w, pr, rm = _run_front(env, X, Wz, E, L, k)
+    assert np.array_equal(idx.cpu().numpy(), np.tile(np.arange(k), (B, 1)))
+    assert torch.all(w == 1.0 / k) and torch.all(pr == 1.0 / E)
+
+
+def test_moe_front_optional_outputs(env):
+    torch, ssd, oracle, dev = env
+    from split_switched_decode_gb300 import inputs
+    B, E, L, K, k = 3, 96, 32, 256, 6
+    X = inputs.activations(B, K, dev, 3, "ox")
+    Wc = inputs.weight(E + L, K, dev, 3, "ow")
+    lat, idx, w, pr, rm = _run_front(env, X, Wc, E, L, k, probs=False, route_map=False)
+    ref = oracle.moe_front(inputs.bits(X), inputs.bits(Wc), E, L, k)
+    assert np.array_equal(idx.cpu().numpy(), ref["idx"])
+    assert_close(w.cpu().numpy(), ref["w"], "weights without optional outputs")
+
+
+# ------------------------------------------------------------------ experts ----
+
+def _routing(B, E, k, seed):
+    rng = np.random.default_rng(seed)
+    idx = np.stack([rng.choice(E, k, replace=False) for _ in range(B)]).astype(np.int32)
+    w = rng.random((B, k)).astype(np.float32) + 0.05
+    w /= w.sum(1, keepdims=True)
+    return idx, w.astype(np.float32)
+
+
+def _run_experts(env, X, idx, w, Wgu, Wd, Wgs, Wds, rm=None, side=True, side_ctas=0):
+    torch, ssd, oracle, dev = env
+    B, H = X.shape
+    E, twoI, _ = Wgu.shape
+    k = idx.shape[1]
+    Y = torch.empty(B, H, dtype=torch.bfloat16, device=dev)
+    ws = ssd.workspace(ssd.moe_experts_workspace_bytes(B, E, k, H, twoI // 2), dev)
+    ss = torch.cuda.Stream(device=dev) if side else None
+    ssd.moe_experts(X, idx, w, rm, Wgu, Wd, Wgs, Wds, Y, ws, side_stream=ss, side_max_ctas=side_ctas)
+    torch.cuda.synchronize()
+    assert ssd.dec_sync_status() == ssd.DEC_OK
+    return Y
+
+
+@pytest.mark.parametrize("B,k", [(1, 8), (4, 2), (17, 8), (64, 8), (64, 1)])
+@pytest.mark.parametrize("shared,side", [(True, True), (True, False), (False, False)])
+def test_moe_experts_small_bank(env, B, k, shared, side):
+    torch, ssd, oracle, dev = env
+    from split_switched_decode_gb300 import inputs
+    E, H, I = 16, 256, 128
+    Wgu, Wd = inputs.expert_bank(E, H, I, dev, 4)
+    Wgs, Wds = inputs.shared_expert(H, I, dev, 4) if shared else (None, None)
+    X = inputs.activations(B, H, dev, 4, "ex")
+    idx_np, w_np = _routing(B, E, k, 40 + B)
+    idx = torch.from_numpy(idx_np).to(dev)
+    w = torch.from_numpy(w_np).to(dev)
+    Y = _run_experts(env, X, idx, w, Wgu, Wd, Wgs, Wds, side=side)
+    y_ref, _ = oracle.moe_experts(inputs.bits(X), idx_np, w_np.astype(np.float64),
+                                  inputs.bits(Wgu), inputs.bits(Wd),
+                                  None if Wgs is None else inputs.bits(Wgs),
+                                  None if Wds is None else inputs.bits(Wds))
+    assert_close(to_f64(oracle, Y), y_ref, f"experts B={B} k={k} shared={shared} side={side}")
+
+
+def test_moe_experts_every_token_on_one_expert(env):
+    """64 tokens on one expert: the widest grouped tile (4 activation boxes)."""
+    torch, ssd, oracle, dev = env
+    from split_switched_decode_gb300 import inputs
+    E, H, I, B = 6, 384, 192, 64
+    Wgu, Wd = inputs.expert_bank(E, H, I, dev, 5)
+    X = inputs.activations(B, H, dev, 5, "one")
+    idx_np = np.tile(np.array([[3, 1]], np.int32), (B, 1))
+    w_np = np.tile(np.array([[0.75, 0.25]], np.float32), (B, 1))
+    Y = _run_experts(env, X, torch.from_numpy(idx_np).to(dev), torch.from_numpy(w_np).to(dev),
+                     Wgu, Wd, None, None, side=False)
+    y_ref, _ = oracle.moe_experts(inputs.bits(X), idx_np, w_np.astype(np.float64),
+                                  inputs.bits(Wgu), inputs.bits(Wd))
+    assert_close(to_f64(oracle, Y), y_ref, "one expert for all tokens")
+
+
+def test_route_map_from_front_equals_rebuilt(env):
+    torch, ssd, oracle, dev = env
+    from split_switched_decode_gb300 import inputs
+    B, E, L, K, k, I = 12, 32, 0, 256, 4, 64
+    X = inputs.activations(B, K, dev, 6, "rx")
+    Wc = inputs.weight(E, K, dev, 6, "rw")
+    _, idx, w, _, rm = _run_front(env, X, Wc, E, L, k)
+    Wgu, Wd = inputs.expert_bank(E, K, I, dev, 6)
+    Y1 = _run_experts(env, X, idx, w, Wgu, Wd, None, None, rm=rm, side=False)
+    Y2 = _run_experts(env, X, idx, w, Wgu, Wd, None, None, rm=None, side=False)
+    assert torch.equal(Y1, Y2)
+
+
+def test_side_cta_cap_changes_schedule_not_result(env):
+    torch, ssd, oracle, dev = env
+    from split_switched_decode_gb300 import inputs
+    E, H, I, B, k = 8, 256, 128, 6, 2
+    Wgu, Wd = inputs.expert_bank(E, H, I, dev, 7)
+    Wgs, Wds = inputs.shared_expert(H, I, dev, 7)
+    X = inputs.activations(B, H, dev, 7, "cap")
+    idx_np, w_np = _routing(B, E, k, 7)
+    idx, w = torch.from_numpy(idx_np).to(dev), torch.from_numpy(w_np).to(dev)
+    y_ref, _ = oracle.moe_experts(inputs.bits(X), idx_np, w_np.astype(np.float64),
+                                  inputs.bits(Wgu), inputs.bits(Wd), inputs.bits(Wgs),
+                                  inputs.bits(Wds))
+    for cap in (1, 3, 40):
+        Y = _run_experts(env, X, idx, w, Wgu, Wd, Wgs, Wds, side=True, side_ctas=cap)
+        assert_close(to_f64(oracle, Y), y_ref, f"side cap {cap}")
+
+
+@pytest.fixture(scope="module")
+def big_layer(env):
+    """The synthetic MoE decode layer: 384 experts (gate/up 2x2048x7168, down 7168x2048)
+    plus a shared expert of the same shape and the 384+512-row front end (~34 GB)."""
+    torch, ssd, oracle, dev = env
+    from split_switched_decode_gb300 import inputs
+    E, H, I, L = 384, 7168, 2048, 512
+    Wgu, Wd = inputs.expert_bank(E, H, I, dev, 0, "bank")
+    Wgs, Wds = inputs.shared_expert(H, I, dev, 0, "bank_shared")
+    Wc = inputs.weight(E + L, H, dev, 0, "front_w")
+    yield dict(Wgu=Wgu, Wd=Wd, Wgs=Wgs, Wds=Wds, Wc=Wc, E=E, H=H, I=I, L=L)
+    del Wgu, Wd
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("B", [1, 64])
+def test_moe_layer_full_size(env, big_layer, B):
+    """Front end -> routed experts + shared expert (side stream) on the full-size layer;
+    sampled tokens checked against the oracle with their experts copied to the host."""
+    torch, ssd, oracle, dev = env
+    from split_switched_decode_gb300 import inputs
+    g = big_layer
+    E, H, I, L, k = g["E"], g["H"], g["I"], g["L"], 8
+    X = inputs.activations(B, H, dev, 0, "layer_x")
+    _, idx, w, _, rm = _run_front(env, X, g["Wc"], E, L, k)
+    Y = _run_experts(env, X, idx, w, g["Wgu"], g["Wd"], g["Wgs"], g["Wds"], rm=rm, side=True)
+    idx_np, w_np = idx.cpu().numpy(), w.cpu().numpy().astype(np.float64)
+    Yf = to_f64(oracle, Y)
+    xb = inputs.bits(X)
+    gs, ds = inputs.bits(g["Wgs"]), inputs.bits(g["Wds"])
+    tokens = [0] if B == 1 else [0, 37, B - 1]
+    y_ref = np.empty((len(tokens), H))
+    for t, b in enumerate(tokens):
+        yp = np.empty((1, k, H))
+        for j in range(k):
+            e = int(idx_np[b, j])
+            _, yp[0, j] = oracle.expert_mlp(xb[b], inputs.bits(g["Wgu"][e]), inputs.bits(g["Wd"][e]))
+        _, s = oracle.expert_mlp(xb[b], gs, ds)
+        y_ref[t] = oracle.combine(w_np[b:b + 1], yp, s[None, :])[0][0]
+    assert_close(Yf[tokens], y_ref, f"MoE layer B={B}")
+
+
+def test_l2_prefetch_does_not_change_results(env):
+    torch, ssd, oracle, dev = env
+    from split_switched_decode_gb300 import inputs
+    B, N, K = 4, 2048, 2048
+    X = inputs.activations(B, K, dev, 8)
+    W = inputs.weight(N, K, dev, 8)
+    Y1 = torch.empty(B, N, dtype=torch.bfloat16, device=dev)
+    Y2 = torch.empty_like(Y1)
+    ws = ssd.workspace(ssd.dec_linear_workspace_bytes(B, N, K), dev)
+    ssd.dec_linear(X, W, None, Y1, ws)
+    side = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(side):
+        ssd.l2_prefetch(W, max_ctas=4, stream=side)
+    ssd.l2_prefetch(W)  # also on the main stream, any byte count
+    ssd.l2_prefetch(W, nbytes=W.numel() * 2 - 40)
+    torch.cuda.synchronize()
+    ssd.dec_linear(X, W, None, Y2, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(Y1, Y2)
+
+
+def test_invalid_routing_is_reported_not_faulted(env):
+    """An out-of-range or repeated expert index passed without a route map is caught by
+    the rebuild kernel: empty map, DEC_ERR_INVALID_ARG from dec_sync_status."""
+    torch, ssd, oracle, dev = env
+    from split_switched_decode_gb300 import inputs
+    E, H, I, B = 8, 256, 64, 3
+    Wgu, Wd = inputs.expert_bank(E, H, I, dev, 9)
+    X = inputs.activations(B, H, dev, 9, "bad")
+    w = torch.full((B, 2), 0.5, dtype=torch.float32, device=dev)
+    Y = torch.empty(B, H, dtype=torch.bfloat16, device=dev)
+    ws = ssd.workspace(ssd.moe_experts_workspace_bytes(B, E, 2, H, I), dev)
+    for bad in ([[0, 1], [2, 8], [3, 4]], [[0, 1], [5, 5], [3, 4]], [[-1, 1], [2, 3], [3, 4]]):
+        idx = torch.tensor(bad, dtype=torch.int32, device=dev)
+        ssd.moe_experts(X, idx, w, None, Wgu, Wd, None, None, Y, ws)
+        assert ssd.dec_sync_status() == ssd.DEC_ERR_INVALID_ARG
+    idx = torch.tensor([[0, 1], [2, 7], [3, 4]], dtype=torch.int32, device=dev)
+    ssd.moe_experts(X, idx, w, None, Wgu, Wd, None, None, Y, ws)
+    assert ssd.dec_sync_status() == ssd.DEC_OK
+    y_ref, _ = oracle.moe_experts(inputs.bits(X), idx.cpu().numpy(), w.cpu().numpy().astype(np.float64),
+                                  inputs.bits(Wgu), inputs.bits(Wd))
+    assert_close(to_f64(oracle, Y), y_ref, "valid routing after invalid ones")
