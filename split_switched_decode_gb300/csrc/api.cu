@@ -554,9 +554,13 @@ dec_status moe_experts(const dec_bf16 *X, const int32_t *topk_idx, const float *
 
   if (consume_fault()) return DEC_ERR_CUDA;
 
+  // tensor-core tiles for the expert GEMVs from the same batch threshold as dec_linear
+  const int fv = force_variant();
+  const bool tc = (fv == DEC_VARIANT_SPLITK_TC) || (fv == DEC_VARIANT_NONE && B >= tc_min_batch());
   auto engine = [&](const CUtensorMap &wm, const CUtensorMap &xm, EngineParams &p,
                     cudaStream_t st_) -> cudaError_t {
-    return launch_engine_cc(p.slot_cols, wm, xm, p, st_);
+    return tc ? launch_engine_tc(p.slot_cols, wm, xm, p, st_)
+              : launch_engine_cc(p.slot_cols, wm, xm, p, st_);
   };
   auto base = [&](EngineParams &p, int mode, int N, int K, int T, int KB, int G, int grouped,
                   size_t part_off, size_t cnt_off) {

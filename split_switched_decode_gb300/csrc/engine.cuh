@@ -194,20 +194,23 @@ __device__ __forceinline__ void epilogue_rows(const EngineParams &p, const SegIn
   }
 }
 
-// Routing tail of MODE_FRONT, run by the 8 warps (256 threads, named barrier 1) of the
-// CTA that finished the last tile. `work` is free shared memory of >= 16 KB.
-__device__ __forceinline__ void front_route_tail(const EngineParams &p, uint8_t *work,
-                                                 int warp) {
+// Routing tail of MODE_FRONT, run by `nwarps` warps (wid = 0..nwarps-1, named barrier
+// bar_id over nwarps*32 threads) of the CTA that finished the last tile. `work` is free
+// shared memory of >= 10 KB. `leader` marks the one thread that resets the counter.
+__device__ __forceinline__ void front_route_tail(const EngineParams &p, uint8_t *work, int wid,
+                                                 int nwarps, int bar_id, bool leader) {
   __threadfence();
   int32_t *sidx = reinterpret_cast<int32_t *>(work);
   unsigned long long *smask = reinterpret_cast<unsigned long long *>(work + 4 * MAX_B * MAX_TOPK);
   int *soff = reinterpret_cast<int *>(work + 4 * MAX_B * MAX_TOPK + 8 * MAX_E);
-  route_tokens_warp(p.logits, p.B, p.E, p.topk, p.topk_idx, p.topk_w, p.probs, sidx, warp, 8);
+  route_tokens_warp(p.logits, p.B, p.E, p.topk, p.topk_idx, p.topk_w, p.probs, sidx, wid,
+                    nwarps);
   if (p.route_map_out != nullptr) {
-    named_bar_sync(1, 256);
-    build_route_map(sidx, p.B, p.topk, p.E, p.route_map_out, smask, soff, 256, 1);
+    named_bar_sync(bar_id, nwarps * 32);
+    build_route_map(sidx, p.B, p.topk, p.E, p.route_map_out, smask, soff, nwarps * 32, bar_id,
+                    wid * 32 + (threadIdx.x & 31));
   }
-  if (threadIdx.x == 0) *p.done_counter = 0;
+  if (leader) *p.done_counter = 0;
 }
 
 }  // namespace ssd

@@ -1,13 +1,333 @@
-// engine_tc.cu -- split-K engine with tcgen05 tensor-core tiles (not built yet).
+// engine_tc.cu -- split-K engine with tcgen05 tensor-core tiles ("swap-AB").
+//
+// Same schedule, TMA staging, reduction and epilogues as engine_cc.cu (engine.cuh);
+// only the multiply differs. The weight tile is the MMA A operand (M = 128 rows) and
+// the activation rows are the B operand (N = 16 x boxes = 16..64 columns), both
+// K-major with the 128-byte swizzle exactly as TMA wrote them, so no data is
+// rearranged in shared memory. One CTA per SM, warp-specialised:
+//
+//   warp 0     TMA producer (lane 0): weight + activation boxes into an 8-deep ring
+//   warp 1     tensor-memory owner and MMA issuer (lane 0): 4 x tcgen05.mma
+//              (M128 x N x K16) per 64-wide k-block into an fp32 accumulator in
+//              tensor memory; tcgen05.commit frees the stage when those MMAs finish
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator (warp w reads lanes
+//              32*(w%4)..+31 = tile rows), then the split-K reduction and epilogue
+//
+// The accumulator is double-buffered (2 x 64 columns) so the epilogue of one segment
+// overlaps the MMAs of the next. The tensor cores keep the multiply off the CUDA
+// cores, which would bound the CUDA-core tiles from about 8 batch columns upward.
+#include <atomic>
+
 #include "engine.cuh"
 
 namespace ssd {
 
-size_t engine_tc_smem_bytes(int) { return 0; }
+namespace {
 
-cudaError_t launch_engine_tc(int, const CUtensorMap &, const CUtensorMap &,
-                             const EngineParams &, cudaStream_t) {
-  return cudaErrorNotSupported;
+constexpr int TC_THREADS = 192;  // 6 warps
+constexpr int TC_SMEM_LIMIT = 232448;
+constexpr uint32_t TMEM_COLS = 128;  // two accumulators of up to 64 fp32 columns
+
+template <int MAXC>
+struct TCConfig {
+  static constexpr int NC = MAXC < 16 ? 16 : MAXC;  // accumulator columns read back
+  static constexpr int NXB = NC / 16;
+  static constexpr int STAGE_BYTES = 16384 + NXB * 2048;
+  static constexpr int SCRATCH_BYTES = 64 * MAXC * 4;  // gate/up pairing
+  static constexpr int TAIL = 256;
+  static constexpr int BUDGET = TC_SMEM_LIMIT - 1024 - TAIL;
+  static constexpr int FIT = (BUDGET - SCRATCH_BYTES) / STAGE_BYTES;
+  static constexpr int STAGES = FIT > 8 ? 8 : FIT;
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + SCRATCH_BYTES + TAIL;
+  static_assert(STAGES >= 4, "pipeline too shallow");
+  static_assert(STAGES * STAGE_BYTES >= 4 * MAX_B * MAX_TOPK + 12 * MAX_E, "routing space");
+};
+
+// ------------------------------------------------------------ tcgen05 PTX ----
+
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate; one thread issues.
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on `bar` when every MMA this thread issued so far has completed.
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+// 16 consecutive fp32 columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand stored with the 128-byte
+// swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart (stride byte offset),
+// leading byte offset unused for this layout, descriptor version 1, layout 2 (128B).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(1) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both K-major,
+// M = 128, N = n (multiple of 16, 16..256).
+__device__ __forceinline__ uint32_t idesc_bf16(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(128 >> 4) << 24);
+}
+
+template <int MAXC>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    engine_tc_kernel(const __grid_constant__ CUtensorMap wmap,
+                     const __grid_constant__ CUtensorMap xmap, const EngineParams p) {
+  using C = TCConfig<MAXC>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t *stage_mem = smem;
+  float *scratch = reinterpret_cast<float *>(smem + C::STAGES * C::STAGE_BYTES);
+  uint8_t *tail = smem + C::STAGES * C::STAGE_BYTES + C::SCRATCH_BYTES;
+  uint64_t *full = reinterpret_cast<uint64_t *>(tail);
+  uint64_t *empty = full + C::STAGES;
+  uint64_t *acc_full = empty + C::STAGES;   // [2]
+  uint64_t *acc_empty = acc_full + 2;       // [2]
+  uint64_t *drain = acc_empty + 2;          // [1]
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *flags = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int w = blockIdx.x;
+  const int ngroups = p.grouped ? rm_num_used(p) : 1;
+  const int64_t total = static_cast<int64_t>(ngroups) * p.T * p.KB;
+  const int64_t begin = sk_start(total, p.G, w);
+  const int64_t end = sk_start(total, p.G, w + 1);
+
+  if (tid == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    mbar_init(drain, 1);
+    flags[0] = 0;
+    flags[1] = 0;
+    flags[2] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      prefetch_tensormap(&wmap);
+      prefetch_tensormap(&xmap);
+      const uint64_t pol = policy_evict_first();
+      uint32_t q = 0;
+      bool ok = true;
+      for (int64_t it = begin; it < end && ok;) {
+        SegInfo s;
+        seg_info(p, it, end, s);
+        const int nxb = s.ncols > 16 ? (s.ncols + 15) >> 4 : 1;
+        const uint32_t bytes = 16384u + static_cast<uint32_t>(nxb) * 2048u;
+        for (int kb = s.kb0; kb < s.kb1; ++kb, ++q) {
+          const int st = static_cast<int>(q % C::STAGES);
+          const uint32_t par = ((q / C::STAGES) & 1u) ^ 1u;
+          if (!mbar_wait_bounded(&empty[st], par, p.status, flags, p.wait_limit_ns)) {
+            ok = false;
+            break;
+          }
+          uint8_t *dst = stage_mem + st * C::STAGE_BYTES;
+          mbar_arrive_expect_tx(&full[st], bytes);
+          tma_load_2d_evict_first(dst, &wmap, &full[st], kb * TILE_K, s.wrow0, pol);
+          tma_load_2d_evict_first(dst + 8192, &wmap, &full[st], kb * TILE_K, s.wrow1, pol);
+          for (int i = 0; i < nxb; ++i)
+            tma_load_2d(dst + 16384 + i * 2048, &xmap, &full[st], kb * TILE_K,
+                        s.xrow0 + XBOX_ROWS * i);
+        }
+        it += s.kb1 - s.kb0;
+      }
+      if (flags[0]) {
+        const uint32_t q0 = q > C::STAGES ? q - C::STAGES : 0u;
+        for (uint32_t qq = q0; qq < q; ++qq)
+          (void)mbar_wait_drain(&full[qq % C::STAGES], (qq / C::STAGES) & 1u, 10000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      uint32_t q = 0, seg = 0;
+      bool ok = true;
+      for (int64_t it = begin; it < end && ok; ++seg) {
+        SegInfo s;
+        seg_info(p, it, end, s);
+        const int nxb = s.ncols > 16 ? (s.ncols + 15) >> 4 : 1;
+        const uint32_t idesc = idesc_bf16(16 * nxb);
+        const uint32_t buf = seg & 1u;
+        if (!mbar_wait_bounded(&acc_empty[buf], ((seg >> 1) & 1u) ^ 1u, p.status, flags,
+                               p.wait_limit_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * 64u;
+        for (int kb = s.kb0; kb < s.kb1; ++kb, ++q) {
+          const int st = static_cast<int>(q % C::STAGES);
+          if (!mbar_wait_bounded(&full[st], (q / C::STAGES) & 1u, p.status, flags,
+                                 p.wait_limit_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(stage_mem + st * C::STAGE_BYTES);
+          const uint64_t adesc = sw128_desc(a_addr);
+          const uint64_t bdesc = sw128_desc(a_addr + 16384u);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)  // K = 16 per MMA: +32 bytes along the swizzled row
+            tc_mma(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc,
+                   (kb > s.kb0 || kk > 0) ? 1u : 0u);
+          tc_commit(&empty[st]);  // the stage is free once these MMAs have read it
+        }
+        if (!ok) break;
+        tc_commit(&acc_full[buf]);  // accumulator ready for the epilogue
+        it += s.kb1 - s.kb0;
+      }
+      if (flags[0]) {  // let every MMA issued so far finish before the memory is freed
+        tc_commit(drain);
+        (void)mbar_wait_drain(drain, 0u, 10000000ull);
+      }
+    }
+  } else {
+    // --------------------------------------------------------------- epilogue
+    const int r = 32 * (warp & 3) + lane;  // tile row == tensor-memory lane
+    uint32_t seg = 0;
+    for (int64_t it = begin; it < end; ++seg) {
+      SegInfo s;
+      seg_info(p, it, end, s);
+      const uint32_t buf = seg & 1u;
+      (void)mbar_wait_bounded(&acc_full[buf], (seg >> 1) & 1u, p.status, flags, p.wait_limit_ns);
+      named_bar_sync(2, 128);
+      if (flags[0]) break;  // uniform across the 128 epilogue threads after the barrier
+      tc_fence_after();
+      float v[C::NC];
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + buf * 64u;
+#pragma unroll
+      for (int c = 0; c < C::NC / 16; ++c) tmem_ld16(taddr + 16u * c, v + 16 * c);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      float acc[MAXC];
+#pragma unroll
+      for (int j = 0; j < MAXC; ++j) acc[j] = v[j];
+      if (reduce_tile<MAXC>(p, s, total, w, begin, r, acc, 2, flags))
+        epilogue_rows<MAXC>(p, s, r, acc, scratch, 2, flags);
+      it += s.kb1 - s.kb0;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (p.mode == MODE_FRONT && flags[2] && !flags[0] && warp >= 2)
+    front_route_tail(p, stage_mem, warp - 2, 4, 3, tid == 64);
+  if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+template <int MAXC>
+cudaError_t launch_t(const CUtensorMap &wmap, const CUtensorMap &xmap, const EngineParams &p,
+                     cudaStream_t s) {
+  using C = TCConfig<MAXC>;
+  static std::atomic<uint64_t> attr_set{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(attr_set.load() & bit)) {
+    e = cudaFuncSetAttribute(engine_tc_kernel<MAXC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set.fetch_or(bit);
+  }
+  engine_tc_kernel<MAXC><<<p.G, TC_THREADS, C::SMEM, s>>>(wmap, xmap, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t engine_tc_smem_bytes(int maxc) {
+  switch (maxc) {
+    case 2: return TCConfig<2>::SMEM;
+    case 4: return TCConfig<4>::SMEM;
+    case 8: return TCConfig<8>::SMEM;
+    case 16: return TCConfig<16>::SMEM;
+    case 32: return TCConfig<32>::SMEM;
+    default: return TCConfig<64>::SMEM;
+  }
+}
+
+cudaError_t launch_engine_tc(int maxc, const CUtensorMap &wmap, const CUtensorMap &xmap,
+                             const EngineParams &p, cudaStream_t s) {
+  switch (maxc) {
+    case 2: return launch_t<2>(wmap, xmap, p, s);
+    case 4: return launch_t<4>(wmap, xmap, p, s);
+    case 8: return launch_t<8>(wmap, xmap, p, s);
+    case 16: return launch_t<16>(wmap, xmap, p, s);
+    case 32: return launch_t<32>(wmap, xmap, p, s);
+    case 64: return launch_t<64>(wmap, xmap, p, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace ssd

@@ -36,7 +36,7 @@ __global__ void __launch_bounds__(256) route_map_kernel(const int32_t *topk_idx,
     if (threadIdx.x == 0) atomicOr(status, ST_BAD_ROUTING);
     return;
   }
-  build_route_map(sidx, B, topk, E, rm, smask, soff, 256, 1);
+  build_route_map(sidx, B, topk, E, rm, smask, soff, 256, 1, threadIdx.x);
 }
 
 // Xg[q, :] = X[pairs[q] / topk, :] -- the activation rows of every (token, slot) entry

@@ -92,13 +92,13 @@ __device__ __noinline__ static void route_tokens_warp(const float *logits, int B
 }
 
 // Counting sort of the routing into the route-map layout of the public header, run by
-// `nthreads` threads of one CTA (a multiple of 32, >= 32) that synchronise on named
-// barrier `bar_id`. sidx: shared [B*topk] expert ids; smask: shared uint64 [E];
-// soff: shared int [E]. Requires B <= 64 (one bit per token).
-__device__ __noinline__ static void build_route_map(const int32_t *sidx, int B, int topk, int E, int32_t *rm,
-                                unsigned long long *smask, int *soff, int nthreads,
-                                int bar_id) {
-  const int tid = threadIdx.x;
+// `nthreads` threads of one CTA (a multiple of 32, >= 32; `tid` = 0..nthreads-1, whole
+// warps) that synchronise on named barrier `bar_id`. sidx: shared [B*topk] expert ids;
+// smask: shared uint64 [E]; soff: shared int [E]. Requires B <= 64 (one bit per token).
+__device__ __noinline__ static void build_route_map(const int32_t *sidx, int B, int topk, int E,
+                                                    int32_t *rm, unsigned long long *smask,
+                                                    int *soff, int nthreads, int bar_id,
+                                                    int tid) {
   const int P = B * topk;
   int32_t *counts = rm;
   int32_t *offsets = rm + E;

@@ -93,7 +93,7 @@ def test_moe_front_ties_go_to_lower_index(env):
     All-zero router rows give equal logits: experts 0..k-1, weights 1/k, probs 1/E."""
     torch, ssd, oracle, dev = env
     from split_switched_decode_gb300 import inputs
-    B, E, L, K, k = 4, 64, 16, 512, 4
+    B, E, L, K, k = 16, 64, 16, 512, 4
     X = inputs.activations(B, K, dev, 2, "tx")
     Wc = inputs.weight(E + L, K, dev, 2, "tw")
     big = inputs.randn_bf16((K,), 0.5, dev, 2, "big")
@@ -104,10 +104,14 @@ def test_moe_front_ties_go_to_lower_index(env):
     lat, idx, w, pr, rm = _run_front(env, X, Wc, E, L, k)
     ref = oracle.moe_front(inputs.bits(X), inputs.bits(Wc), E, L, k)
     assert np.array_equal(idx.cpu().numpy(), ref["idx"])
+    tied = 0
     for b in range(B):
-        row = idx[b].tolist()
-        pair = (9, 40) if 9 in row[:2] else (20, 33)
-        assert row[:2] == list(pair), row
+        top2 = sorted(ref["idx"][b, :2].tolist())
+        if top2 in ([9, 40], [20, 33]):  # the planted pair leads this token: a real tie
+            tied += 1
+            assert idx[b, :2].tolist() == top2, idx[b].tolist()
+            assert w[b, 0].item() == w[b, 1].item()
+    assert tied >= B // 2
     Wz = Wc.clone()
     Wz[:E] = 0
     lat, idx, w, pr, rm = _run_front(env, X, Wz, E, L, k)
