@@ -151,6 +151,24 @@ DEC_API dec_status dec_splitk_gemm(const dec_bf16 *X, const dec_bf16 *W, const d
                            void *ws, size_t ws_bytes, dec_stream_t s);
 
 /*
+ * dec_splitk_gemm without a workspace, for callers that cannot allocate device memory
+ * (for example a plugin running inside another runtime that owns the GPU memory pool,
+ * or a serving loop whose memory is frozen after warm-up). The paper has no counterpart:
+ * it is an addition of this library. Same result and arguments as dec_splitk_gemm with
+ * split_k = 0; the scratch lives in a fixed 16 MiB device array inside the library
+ * (held on every GPU that loads it until the process exits), so a shape whose split-K
+ * scratch would exceed 16 MiB is rejected with DEC_ERR_WORKSPACE_TOO_SMALL. The first
+ * call on a device looks up the array's address: make it before any stream capture.
+ * Every call on a device shares the one array (its counters are cleared at the start
+ * of each call): two calls that can overlap on that GPU race, so issue them on one
+ * stream or otherwise serialise them. No cudaMalloc, cudaFree or allocating library
+ * routine is called.
+ */
+DEC_API dec_status dec_splitk_gemm_noalloc(const dec_bf16 *X, const dec_bf16 *W,
+                                           const dec_bf16 *R, dec_bf16 *Y, int B, int N, int K,
+                                           int use_tc, dec_stream_t s);
+
+/*
  * The batch-size switch: picks dec_gemv for B <= 2, the split-K tiles on CUDA cores
  * for small B and on tensor cores from a threshold batch upward, then runs it.
  * dec_linear_workspace_bytes() covers whichever variant the switch can pick.

@@ -36,7 +36,7 @@ EXPORTS = [
     "dec_sync_status", "dec_debug_wait_timeout", "dec_gemv", "dec_splitk_workspace_bytes",
     "dec_splitk_gemm", "dec_linear_workspace_bytes", "dec_linear", "moe_route_map_ints",
     "moe_front_workspace_bytes", "moe_front", "moe_experts_workspace_bytes", "moe_experts",
-    "l2_prefetch",
+    "l2_prefetch", "dec_splitk_gemm_noalloc",
 ]
 
 _lib = None
@@ -86,6 +86,7 @@ def _load():
         "moe_experts_workspace_bytes": (S, [I, I, I, I, I]),
         "moe_experts": (I, [P, P, P, P, P, P, I, P, P, I, I, I, I, P, P, S, P, P, I]),
         "l2_prefetch": (I, [P, S, I, P]),
+        "dec_splitk_gemm_noalloc": (I, [P, P, P, P, I, I, I, I, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -185,6 +186,17 @@ def dec_splitk_gemm(X, W, R, Y, ws, split_k=0, use_tc=0, stream=None):
     _check(_load().dec_splitk_gemm(_ptr(X), _ptr(W), _ptr(R), _ptr(Y), B, N, K, split_k, use_tc,
                                    _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
            "dec_splitk_gemm")
+
+
+def dec_splitk_gemm_noalloc(X, W, R, Y, use_tc=0, stream=None):
+    """dec_splitk_gemm for callers that cannot allocate: the scratch is a fixed 16 MiB
+    array inside the library; calls on one GPU must not overlap."""
+    for t, n in ((X, "X"), (W, "W"), (R, "R"), (Y, "Y")):
+        _bf16(t, n)
+    B, K = X.shape
+    N = W.shape[0]
+    _check(_load().dec_splitk_gemm_noalloc(_ptr(X), _ptr(W), _ptr(R), _ptr(Y), B, N, K, use_tc,
+                                           _stream(stream)), "dec_splitk_gemm_noalloc")
 
 
 def dec_linear_workspace_bytes(B, N, K) -> int:

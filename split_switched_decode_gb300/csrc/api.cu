@@ -647,3 +647,70 @@ dec_status l2_prefetch(const void *p, size_t bytes, int max_ctas, dec_stream_t s
 }
 
 }  // extern "C"
+
+// ======================================================= no-allocation variant ====
+//
+// Some callers cannot hand this library a workspace: code running inside a host
+// program that owns the GPU memory pool and forbids allocation after start-up (a
+// plugin inside another inference runtime, a serving loop whose memory was frozen
+// after warm-up), or code that must not call cudaMalloc at all. dec_splitk_gemm_noalloc
+// gives them the split-K projection with its scratch (per-worker partial tiles and
+// per-tile arrival counters) in the fixed device array below, which every GPU that
+// loads this library keeps until the process exits.
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB per device
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct NoAllocDevice {
+  std::once_flag once;
+  void *scratch = nullptr;  // device address of g_noalloc_scratch on this device
+  cudaError_t err = cudaSuccess;
+};
+NoAllocDevice g_noalloc_dev[kMaxDevices];
+
+}  // namespace
+
+extern "C" dec_status dec_splitk_gemm_noalloc(const dec_bf16 *X, const dec_bf16 *W,
+                                              const dec_bf16 *R, dec_bf16 *Y, int B, int N,
+                                              int K, int use_tc, dec_stream_t s) {
+  dec_status st = check_linear_args(X, W, Y, B, N, K);
+  if (st != DEC_OK) return st;
+  if (use_tc != 0 && use_tc != 1) return DEC_ERR_INVALID_ARG;
+  cudaError_t ce;
+  DeviceInfo *d = device_info(&ce);
+  if (!d) return DEC_ERR_CUDA;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DEC_ERR_CUDA;
+  // First call on this device (which is current here): look up the array's device
+  // address. The name g_noalloc_scratch is only a host-side stand-in.
+  NoAllocDevice &nd = g_noalloc_dev[dev];
+  std::call_once(nd.once, [&]() {
+    nd.err = cudaGetSymbolAddress(&nd.scratch, g_noalloc_scratch);
+  });
+  if (nd.err != cudaSuccess || nd.scratch == nullptr) return DEC_ERR_CUDA;
+  SplitPlan pl;
+  if (!plan_splitk(B, N, K, 0, d->num_sms, &pl)) return DEC_ERR_UNSUPPORTED_SHAPE;
+  if (pl.total > kNoAllocScratchBytes) return DEC_ERR_WORKSPACE_TOO_SMALL;
+  CUtensorMap wmap, xmap;
+  if (!make_map(&wmap, W, K, N, WBOX_ROWS) || !make_map(&xmap, X, K, B, XBOX_ROWS))
+    return DEC_ERR_CUDA;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
+  // The array keeps whatever the previous call left; the arrival counters must start
+  // at zero, so clear them (the partial tiles are always written before being read).
+  if (cudaMemsetAsync(static_cast<char *>(nd.scratch) + pl.partial_bytes, 0, pl.counter_bytes,
+                      cs) != cudaSuccess)
+    return DEC_ERR_CUDA;
+  EngineParams p;
+  fill_engine_common(p, pl, MODE_LINEAR, N, K, B, nd.scratch, d);
+  p.Y = Y;
+  p.R = R;
+  if (consume_fault()) return DEC_ERR_CUDA;
+  ce = use_tc ? launch_engine_tc(pl.maxc, wmap, xmap, p, cs)
+              : launch_engine_cc(pl.maxc, wmap, xmap, p, cs);
+  if (ce == cudaErrorNotSupported) return DEC_ERR_UNSUPPORTED_SHAPE;
+  if (ce != cudaSuccess) return DEC_ERR_CUDA;
+  t_last_variant = use_tc ? DEC_VARIANT_SPLITK_TC : DEC_VARIANT_SPLITK;
+  return DEC_OK;
+}
