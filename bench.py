@@ -61,6 +61,13 @@ def parse_args():
                     help="target host time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ops", default="in,o,front,experts",
+                    help="operations of the sweep (profiling subsets: in,o,front,experts)")
+    ap.add_argument("--sweep-only", action="store_true",
+                    help="only the per-operation sweep (for profiler captures)")
+    ap.add_argument("--num-experts", type=int, default=E,
+                    help="routed experts in the bank (smaller for profiler captures)")
+    ap.add_argument("--reps", type=int, default=7, help="graph replays per sweep entry")
     return ap.parse_args()
 
 
@@ -70,8 +77,8 @@ def bytes_linear(B, N, K, residual):
     return N * K * 2 + B * K * 2 + B * N * 2 + (B * N * 2 if residual else 0)
 
 
-def bytes_front(B):
-    return (E + L) * H * 2 + B * H * 2 + B * L * 2 + B * TOPK * 8
+def bytes_front(B, n_experts=E):
+    return (n_experts + L) * H * 2 + B * H * 2 + B * L * 2 + B * TOPK * 8
 
 
 def bytes_experts(B, U):
@@ -134,20 +141,22 @@ class ClockSampler:
 class Workload:
     """All tensors of the step on one GPU, plus the per-call launch counts."""
 
-    def __init__(self, torch, ssd, inputs, dev, batches, seed=0):
+    def __init__(self, torch, ssd, inputs, dev, batches, seed=0, num_experts=E, experts=True):
         self.torch, self.ssd, self.dev, self.batches = torch, ssd, dev, batches
+        self.E = num_experts
         l2 = torch.cuda.get_device_properties(dev).L2_cache_size
         self.l2 = l2
         bf = torch.bfloat16
         W_in = inputs.weight(N_IN, H, dev, seed, "w_in")
         W_o = inputs.weight(H, K_O, dev, seed, "w_o")
-        W_cat = inputs.weight(E + L, H, dev, seed, "w_cat")
+        W_cat = inputs.weight(num_experts + L, H, dev, seed, "w_cat")
         # rotating copies for the per-operation sweep: >= 3x L2 per pool
         def pool(w):
             n = max(1, math.ceil(3 * l2 / (w.numel() * 2)))
             return [w] + [w.clone() for _ in range(n - 1)]
         self.W_in, self.W_o, self.W_cat = pool(W_in), pool(W_o), pool(W_cat)
-        self.Wgu, self.Wd = inputs.expert_bank(E, H, I, dev, seed, "bank")
+        if experts:
+            self.Wgu, self.Wd = inputs.expert_bank(num_experts, H, I, dev, seed, "bank")
         self.Wgs, self.Wds = inputs.shared_expert(H, I, dev, seed, "bank_shared")
         self.side = torch.cuda.Stream(device=dev)
         self.fork = torch.cuda.Event()
@@ -163,13 +172,13 @@ class Workload:
             d["lat"] = [torch.empty(B, L, dtype=bf, device=dev) for _ in range(3)]
             d["idx"] = [torch.empty(B, TOPK, dtype=torch.int32, device=dev) for _ in range(3)]
             d["w"] = [torch.empty(B, TOPK, dtype=torch.float32, device=dev) for _ in range(3)]
-            d["rm"] = [torch.empty(ssd.moe_route_map_ints(B, E, TOPK), dtype=torch.int32, device=dev)
-                       for _ in range(3)]
+            d["rm"] = [torch.empty(ssd.moe_route_map_ints(B, self.E, TOPK), dtype=torch.int32,
+                                   device=dev) for _ in range(3)]
             d["y_moe"] = torch.empty(B, H, dtype=bf, device=dev)
             d["ws_in"] = ssd.workspace(ssd.dec_linear_workspace_bytes(B, N_IN, H), dev)
             d["ws_o"] = ssd.workspace(ssd.dec_linear_workspace_bytes(B, H, K_O), dev)
-            d["ws_f"] = ssd.workspace(ssd.moe_front_workspace_bytes(B, E, L, H), dev)
-            d["ws_e"] = ssd.workspace(ssd.moe_experts_workspace_bytes(B, E, TOPK, H, I), dev)
+            d["ws_f"] = ssd.workspace(ssd.moe_front_workspace_bytes(B, self.E, L, H), dev)
+            d["ws_e"] = ssd.workspace(ssd.moe_experts_workspace_bytes(B, self.E, TOPK, H, I), dev)
             self.t[B] = d
         self.launches = 0
         torch.cuda.synchronize()
@@ -193,7 +202,7 @@ class Workload:
             self.side.wait_event(self.fork)
             ssd.l2_prefetch(self.Wgs, nbytes=PREFETCH_BYTES, max_ctas=8, stream=self.side)
             self.launches += 1
-        ssd.moe_front(d["x_moe"][v], self.W_cat[rot % len(self.W_cat)], E, L, TOPK, d["lat"][v],
+        ssd.moe_front(d["x_moe"][v], self.W_cat[rot % len(self.W_cat)], self.E, L, TOPK, d["lat"][v],
                       d["idx"][v], d["w"][v], d["ws_f"], route_map=d["rm"][v])
         self.launches += 1
 
@@ -213,13 +222,13 @@ class Workload:
     def used_experts(self, B, v=0):
         rm = self.t[B]["rm"][v]
         P = B * TOPK
-        return int(rm[2 * E + 1 + 2 * P].item())
+        return int(rm[2 * self.E + 1 + 2 * P].item())
 
     def step_bytes(self):
         tot = 0
         for B in self.batches:
             tot += bytes_linear(B, N_IN, H, False) + bytes_linear(B, H, K_O, True)
-            tot += bytes_front(B) + bytes_experts(B, self.used_experts(B))
+            tot += bytes_front(B, self.E) + bytes_experts(B, self.used_experts(B))
         return tot
 
 
@@ -381,7 +390,11 @@ def main():
     from split_switched_decode_gb300 import inputs
     ssd.build()
     batches = [int(b) for b in args.batches.split(",")]
-    wl = Workload(torch, ssd, inputs, dev, batches)
+    ops = set(args.ops.split(","))
+    if not args.sweep_only:
+        ops = {"in", "o", "front", "experts"}
+    wl = Workload(torch, ssd, inputs, dev, batches, num_experts=args.num_experts,
+                  experts="experts" in ops)
 
     # routing of every X set (fixed inputs -> fixed routing -> fixed bytes)
     for B in batches:
@@ -394,30 +407,37 @@ def main():
     R_SMALL = 12
     for B in batches:
         row = {}
-        for name, fn, nb in (
-                ("input_projection", lambda B=B: [wl.op_in(B, r) for r in range(R_SMALL)],
+        for key, name, fn, nb in (
+                ("in", "input_projection", lambda B=B: [wl.op_in(B, r) for r in range(R_SMALL)],
                  bytes_linear(B, N_IN, H, False)),
-                ("output_projection", lambda B=B: [wl.op_o(B, r) for r in range(R_SMALL)],
+                ("o", "output_projection", lambda B=B: [wl.op_o(B, r) for r in range(R_SMALL)],
                  bytes_linear(B, H, K_O, True)),
-                ("moe_front", lambda B=B: [wl.op_front(B, r, v=0, prefetch=False)
-                                           for r in range(R_SMALL)], bytes_front(B))):
+                ("front", "moe_front", lambda B=B: [wl.op_front(B, r, v=0, prefetch=False)
+                                                    for r in range(R_SMALL)],
+                 bytes_front(B, wl.E))):
+            if key not in ops:
+                continue
             g = capture(torch, fn)
-            ts = time_graph(torch, g, 7)
+            ts = time_graph(torch, g, args.reps)
             us = statistics.median(ts) / R_SMALL
             row[name] = {"us_per_call": us, "GBps": nb / us / 1e3,
                          "variant": ssd.dec_variant_name(ssd.dec_last_variant())}
             del g
-        us_e = []
-        nb_e = 0
-        g = capture(torch, lambda B=B: [wl.op_experts(B, v) for v in range(3)])
-        ts = time_graph(torch, g, 5)
-        nb_e = sum(bytes_experts(B, wl.used_experts(B, v)) for v in range(3)) / 3
-        us = statistics.median(ts) / 3
-        row["moe_experts"] = {"us_per_call": us, "GBps": nb_e / us / 1e3,
-                              "distinct_experts": [wl.used_experts(B, v) for v in range(3)]}
-        del g
+        if "experts" in ops:
+            g = capture(torch, lambda B=B: [wl.op_experts(B, v) for v in range(3)])
+            ts = time_graph(torch, g, max(3, args.reps - 2))
+            nb_e = sum(bytes_experts(B, wl.used_experts(B, v)) for v in range(3)) / 3
+            us = statistics.median(ts) / 3
+            row["moe_experts"] = {"us_per_call": us, "GBps": nb_e / us / 1e3,
+                                  "distinct_experts": [wl.used_experts(B, v) for v in range(3)]}
+            del g
         sweep[str(B)] = row
     torch.cuda.synchronize()
+    if args.sweep_only:
+        if rank == 0:
+            print(json.dumps({"sweep_only": True, "batches": batches, "ops": sorted(ops),
+                              "num_experts": wl.E, "sweep": sweep}), flush=True)
+        return 0
 
     # ---- the step as one CUDA graph
     launches0 = wl.launches

@@ -109,19 +109,33 @@ __device__ __forceinline__ bool reduce_tile(const EngineParams &p, const SegInfo
   named_bar_sync(bar_id, 128);
   if (!flags[1]) return false;
   __threadfence();
+  // Add the contributors' partials in worker order. Only the first contributor can
+  // have started before this tile (its slot 1); every later one began inside it (slot
+  // 0). Loads of RD contributors are issued before their adds so they overlap.
+  constexpr int RD = MAXC >= 16 ? 1 : 16 / MAXC;
+  const int which_first = (sk_start(total, p.G, first) >= tb) ? 0 : 1;
   float t[MAXC];
 #pragma unroll
   for (int j = 0; j < MAXC; ++j) t[j] = 0.f;
-  for (int wk = first; wk <= last; ++wk) {
-    if (wk == w) {
+  for (int wk0 = first; wk0 <= last; wk0 += RD) {
+    float tmp[RD][MAXC];
 #pragma unroll
-      for (int j = 0; j < MAXC; ++j) t[j] += v[j];
-    } else {
-      const int which = (sk_start(total, p.G, wk) >= tb) ? 0 : 1;
+    for (int d = 0; d < RD; ++d) {
+      const int wk = wk0 + d;
+      const int which = (wk == first) ? which_first : 0;
       const float *sl = p.partials + static_cast<size_t>(wk * 2 + which) * slot_floats;
+      const bool other = (wk <= last) && (wk != w);
 #pragma unroll
       for (int j = 0; j < MAXC; ++j)
-        if (j < s.ncols) t[j] += __ldcg(sl + j * 128 + r);
+        tmp[d][j] = (other && j < s.ncols) ? __ldcg(sl + j * 128 + r) : 0.f;
+    }
+#pragma unroll
+    for (int d = 0; d < RD; ++d) {
+      const int wk = wk0 + d;
+      if (wk <= last) {
+#pragma unroll
+        for (int j = 0; j < MAXC; ++j) t[j] += (wk == w) ? v[j] : tmp[d][j];
+      }
     }
   }
 #pragma unroll

@@ -181,8 +181,8 @@ __global__ void __launch_bounds__(CC_THREADS, 1)
     }
   }
   __syncthreads();
-  if (p.mode == MODE_FRONT && flags[2] && !flags[0] && warp < 8)
-    front_route_tail(p, stage_mem, warp, 8, 1, tid == 0);
+  if (p.mode == MODE_FRONT && flags[2] && !flags[0])  // every warp of the CTA routes
+    front_route_tail(p, stage_mem, warp, CC_THREADS / 32, 1, tid == 0);
 }
 
 // The shared-memory opt-in is a per-device function attribute: set it on the first

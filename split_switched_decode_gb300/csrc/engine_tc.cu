@@ -280,8 +280,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (p.mode == MODE_FRONT && flags[2] && !flags[0] && warp >= 2)
-    front_route_tail(p, stage_mem, warp - 2, 4, 3, tid == 64);
+  if (p.mode == MODE_FRONT && flags[2] && !flags[0])  // every warp of the CTA routes
+    front_route_tail(p, stage_mem, warp, TC_THREADS / 32, 3, tid == 0);
   if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
 }
 

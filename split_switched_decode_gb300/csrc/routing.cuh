@@ -53,27 +53,39 @@ __device__ __noinline__ static void route_tokens_warp(const float *logits, int B
       }
     }
 
-    // top-k: k rounds of a warp-wide arg-max on (logit desc, index asc)
+    // top-k: k rounds of a warp-wide arg-max on (logit desc, index asc). Each lane
+    // caches the best of its own remaining logits; only the lane that wins a round
+    // rescans.
+    uint32_t key[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) key[i] = f32_order_key(v[i]);
     uint32_t taken = 0;
-    int my_e = 0;
-    float my_v = 0.f;
-    for (int j = 0; j < topk; ++j) {
-      int bi = -1;
-      uint32_t bk = 0;
+    int bi = -1;
+    uint32_t bk = 0;
+    auto rescan = [&]() {
+      bi = -1;
+      bk = 0;
 #pragma unroll
       for (int i = 0; i < VPL; ++i) {
         const bool ok = (lane + 32 * i < E) && !((taken >> i) & 1u);
-        const uint32_t key = f32_order_key(v[i]);
-        if (ok && (bi < 0 || key > bk)) {  // strict: lower index (smaller i) wins ties
+        if (ok && (bi < 0 || key[i] > bk)) {  // strict: lower index (smaller i) wins ties
           bi = i;
-          bk = key;
+          bk = key[i];
         }
       }
+    };
+    rescan();
+    int my_e = 0;
+    float my_v = 0.f;
+    for (int j = 0; j < topk; ++j) {
       const uint32_t kmax = __reduce_max_sync(FULL, bi >= 0 ? bk : 0u);
       const uint32_t cand =
           (bi >= 0 && bk == kmax) ? static_cast<uint32_t>(lane + 32 * bi) : 0xFFFFFFFFu;
       const uint32_t win = __reduce_min_sync(FULL, cand);
-      if (lane == static_cast<int>(win & 31u)) taken |= 1u << (win >> 5);
+      if (lane == static_cast<int>(win & 31u)) {
+        taken |= 1u << (win >> 5);
+        rescan();
+      }
       if (lane == j) {
         my_e = static_cast<int>(win);
         my_v = order_key_to_f32(kmax);
