@@ -2,6 +2,7 @@
 // argument checks, the batch-size kernel switch, workspace planning, TMA descriptor
 // encoding, side-stream scheduling of the shared expert, and error reporting.
 #include <atomic>
+#include <cmath>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -11,6 +12,16 @@
 #include "internal.h"
 
 using namespace ssd;
+
+namespace ssd {
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char *s = std::getenv("DEC_PDL");
+    return !(s && s[0] == '0');
+  }();
+  return on;
+}
+}  // namespace ssd
 
 namespace {
 
@@ -535,7 +546,10 @@ dec_status moe_experts(const dec_bf16 *X, const int32_t *topk_idx, const float *
       double miss = 1.0;
       for (int b = 0; b < B; ++b) miss *= 1.0 - static_cast<double>(topk) / E;
       const double u_exp = E * (1.0 - miss);
-      g_side = static_cast<int>(d->num_sms / (1.0 + u_exp) + 0.5);
+      // a fair bandwidth share is num_sms/(U+1) SMs; round up with 25% slack so the
+      // shared expert (88 MB at the Kimi shape) never becomes the critical path
+      g_side = static_cast<int>(std::ceil(1.25 * d->num_sms / (1.0 + u_exp)));
+      if (g_side < 2) g_side = 2;
     }
     if (g_side < 1) g_side = 1;
     if (g_side > d->num_sms / 2) g_side = d->num_sms / 2;

@@ -151,6 +151,20 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void *addr, uint32_t byte
                : "memory");
 }
 
+// ------------------------------------------------ programmatic dependent launch ----
+// griddep_wait: block until the previous kernel of the stream has completed and its
+// writes are visible (a no-op when the launch was not programmatic). Everything that
+// reads an activation, a route map or the workspace, or writes any output, comes after
+// it; only static weights may be loaded before it. The "memory" clobber keeps the
+// compiler from hoisting ordinary loads above the wait.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Let the next kernel of the stream be scheduled as SMs free up.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------ named barriers ----
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {

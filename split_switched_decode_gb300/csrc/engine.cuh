@@ -83,6 +83,73 @@ __device__ __forceinline__ void seg_info(const EngineParams &p, int64_t it, int6
   s.full = (s.kb0 == 0 && s.kb1 == p.KB);
 }
 
+// Activation boxes (16 rows each) a segment needs: at least one.
+__device__ __forceinline__ int seg_xboxes(const SegInfo &s) {
+  return s.ncols > 16 ? (s.ncols + 15) >> 4 : 1;
+}
+
+// TMA producer of both engines, run by one thread. The weight boxes of the first
+// STAGES k-blocks do not depend on the previous kernel of the stream, so for a
+// projection they are issued before griddep_wait (programmatic dependent launch); the
+// activation boxes, and everything of a grouped launch (which reads the route map),
+// only after it.
+template <int STAGES, int STAGE_BYTES>
+__device__ __forceinline__ void engine_produce(const EngineParams &p, const CUtensorMap *wmap,
+                                               const CUtensorMap *xmap, uint8_t *stage_mem,
+                                               uint64_t *full, uint64_t *empty,
+                                               volatile int *flags, int64_t begin, int64_t end) {
+  prefetch_tensormap(wmap);
+  prefetch_tensormap(xmap);
+  const uint64_t pol = policy_evict_first();
+  uint32_t pre = 0;
+  if (!p.grouped) {
+    for (int64_t it = begin; it < end && pre < STAGES;) {
+      SegInfo s;
+      seg_info(p, it, end, s);
+      const uint32_t bytes = 16384u + static_cast<uint32_t>(seg_xboxes(s)) * 2048u;
+      for (int kb = s.kb0; kb < s.kb1 && pre < STAGES; ++kb, ++pre) {
+        uint8_t *dst = stage_mem + pre * STAGE_BYTES;
+        mbar_arrive_expect_tx(&full[pre], bytes);  // first use of the stage: it is empty
+        tma_load_2d_evict_first(dst, wmap, &full[pre], kb * TILE_K, s.wrow0, pol);
+        tma_load_2d_evict_first(dst + 8192, wmap, &full[pre], kb * TILE_K, s.wrow1, pol);
+      }
+      it += s.kb1 - s.kb0;
+    }
+  }
+  griddep_wait();
+  uint32_t q = 0;
+  bool ok = true;
+  for (int64_t it = begin; it < end && ok;) {
+    SegInfo s;
+    seg_info(p, it, end, s);
+    const int nxb = seg_xboxes(s);
+    const uint32_t bytes = 16384u + static_cast<uint32_t>(nxb) * 2048u;
+    for (int kb = s.kb0; kb < s.kb1; ++kb, ++q) {
+      const int st = static_cast<int>(q % STAGES);
+      uint8_t *dst = stage_mem + st * STAGE_BYTES;
+      if (q >= pre) {
+        const uint32_t par = ((q / STAGES) & 1u) ^ 1u;
+        if (!mbar_wait_bounded(&empty[st], par, p.status, flags, p.wait_limit_ns)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[st], bytes);
+        tma_load_2d_evict_first(dst, wmap, &full[st], kb * TILE_K, s.wrow0, pol);
+        tma_load_2d_evict_first(dst + 8192, wmap, &full[st], kb * TILE_K, s.wrow1, pol);
+      }
+      for (int i = 0; i < nxb; ++i)
+        tma_load_2d(dst + 16384 + i * 2048, xmap, &full[st], kb * TILE_K, s.xrow0 + XBOX_ROWS * i);
+    }
+    it += s.kb1 - s.kb0;
+  }
+  if (flags[0]) {
+    // after a time-out: let this CTA's copies still in flight land before it exits
+    const uint32_t q0 = q > STAGES ? q - STAGES : 0u;
+    for (uint32_t qq = q0; qq < q; ++qq)
+      (void)mbar_wait_drain(&full[qq % STAGES], (qq / STAGES) & 1u, 10000000ull);
+  }
+}
+
 // Split-K reduction of one tile, run by the 128 threads that hold the segment's values
 // (thread r holds row r, columns 0..ncols-1 in v). Returns true when v holds the final
 // tile values on return (whole-tile segment, or this worker arrived last).

@@ -90,6 +90,7 @@ __global__ void __launch_bounds__(CC_THREADS, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int w = blockIdx.x;
+  if (p.grouped) griddep_wait();  // the route map comes from the previous kernel
   const int ngroups = p.grouped ? rm_num_used(p) : 1;
   const int64_t total = static_cast<int64_t>(ngroups) * p.T * p.KB;
   const int64_t begin = sk_start(total, p.G, w);
@@ -107,45 +108,18 @@ __global__ void __launch_bounds__(CC_THREADS, 1)
   }
   __syncthreads();
 
+  griddep_launch_dependents();
+
   if (warp == 8) {
     // ---------------------------------------------------------------- producer
-    if (lane == 0) {
-      prefetch_tensormap(&wmap);
-      prefetch_tensormap(&xmap);
-      const uint64_t pol = policy_evict_first();
-      uint32_t q = 0;
-      bool ok = true;
-      for (int64_t it = begin; it < end && ok;) {
-        SegInfo s;
-        seg_info(p, it, end, s);
-        const int nxb = (s.ncols + 15) >> 4;
-        const uint32_t bytes = 16384u + static_cast<uint32_t>(nxb) * 2048u;
-        for (int kb = s.kb0; kb < s.kb1; ++kb, ++q) {
-          const int st = static_cast<int>(q % C::STAGES);
-          const uint32_t par = ((q / C::STAGES) & 1u) ^ 1u;
-          if (!mbar_wait_bounded(&empty[st], par, p.status, flags, p.wait_limit_ns)) {
-            ok = false;
-            break;
-          }
-          uint8_t *dst = stage_mem + st * C::STAGE_BYTES;
-          mbar_arrive_expect_tx(&full[st], bytes);
-          tma_load_2d_evict_first(dst, &wmap, &full[st], kb * TILE_K, s.wrow0, pol);
-          tma_load_2d_evict_first(dst + 8192, &wmap, &full[st], kb * TILE_K, s.wrow1, pol);
-          for (int i = 0; i < nxb; ++i)
-            tma_load_2d(dst + 16384 + i * 2048, &xmap, &full[st], kb * TILE_K,
-                        s.xrow0 + XBOX_ROWS * i);
-        }
-        it += s.kb1 - s.kb0;
-      }
-      if (flags[0]) {
-        // after a time-out: let this CTA's copies still in flight land before exit
-        const uint32_t q0 = q > C::STAGES ? q - C::STAGES : 0u;
-        for (uint32_t qq = q0; qq < q; ++qq)
-          (void)mbar_wait_drain(&full[qq % C::STAGES], (qq / C::STAGES) & 1u, 10000000ull);
-      }
-    }
+    if (lane == 0)
+      engine_produce<C::STAGES, C::STAGE_BYTES>(p, &wmap, &xmap, stage_mem, full, empty, flags,
+                                                begin, end);
+    else
+      griddep_wait();
   } else {
     // --------------------------------------------------------------- consumers
+    griddep_wait();
     const int r = tid & 127, h = tid >> 7;
     uint32_t q = 0;
     for (int64_t it = begin; it < end;) {
@@ -202,8 +176,7 @@ cudaError_t launch_t(const CUtensorMap &wmap, const CUtensorMap &xmap, const Eng
     if (e != cudaSuccess) return e;
     attr_set.fetch_or(bit);
   }
-  engine_cc_kernel<MAXC><<<p.G, CC_THREADS, C::SMEM, s>>>(wmap, xmap, p);
-  return cudaGetLastError();
+  return launch_pdl(engine_cc_kernel<MAXC>, dim3(p.G), dim3(CC_THREADS), C::SMEM, s, wmap, xmap, p);
 }
 
 }  // namespace

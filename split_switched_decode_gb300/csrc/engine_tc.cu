@@ -139,6 +139,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int w = blockIdx.x;
+  if (p.grouped) griddep_wait();  // the route map comes from the previous kernel
   const int ngroups = p.grouped ? rm_num_used(p) : 1;
   const int64_t total = static_cast<int64_t>(ngroups) * p.T * p.KB;
   const int64_t begin = sk_start(total, p.G, w);
@@ -168,52 +169,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
+  griddep_launch_dependents();
+
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
-    if (lane == 0) {
-      prefetch_tensormap(&wmap);
-      prefetch_tensormap(&xmap);
-      const uint64_t pol = policy_evict_first();
-      uint32_t q = 0;
-      bool ok = true;
-      for (int64_t it = begin; it < end && ok;) {
-        SegInfo s;
-        seg_info(p, it, end, s);
-        const int nxb = s.ncols > 16 ? (s.ncols + 15) >> 4 : 1;
-        const uint32_t bytes = 16384u + static_cast<uint32_t>(nxb) * 2048u;
-        for (int kb = s.kb0; kb < s.kb1; ++kb, ++q) {
-          const int st = static_cast<int>(q % C::STAGES);
-          const uint32_t par = ((q / C::STAGES) & 1u) ^ 1u;
-          if (!mbar_wait_bounded(&empty[st], par, p.status, flags, p.wait_limit_ns)) {
-            ok = false;
-            break;
-          }
-          uint8_t *dst = stage_mem + st * C::STAGE_BYTES;
-          mbar_arrive_expect_tx(&full[st], bytes);
-          tma_load_2d_evict_first(dst, &wmap, &full[st], kb * TILE_K, s.wrow0, pol);
-          tma_load_2d_evict_first(dst + 8192, &wmap, &full[st], kb * TILE_K, s.wrow1, pol);
-          for (int i = 0; i < nxb; ++i)
-            tma_load_2d(dst + 16384 + i * 2048, &xmap, &full[st], kb * TILE_K,
-                        s.xrow0 + XBOX_ROWS * i);
-        }
-        it += s.kb1 - s.kb0;
-      }
-      if (flags[0]) {
-        const uint32_t q0 = q > C::STAGES ? q - C::STAGES : 0u;
-        for (uint32_t qq = q0; qq < q; ++qq)
-          (void)mbar_wait_drain(&full[qq % C::STAGES], (qq / C::STAGES) & 1u, 10000000ull);
-      }
-    }
+    if (lane == 0)
+      engine_produce<C::STAGES, C::STAGE_BYTES>(p, &wmap, &xmap, stage_mem, full, empty, flags,
+                                                begin, end);
+    else
+      griddep_wait();
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
+    griddep_wait();
     if (lane == 0) {
       uint32_t q = 0, seg = 0;
       bool ok = true;
       for (int64_t it = begin; it < end && ok; ++seg) {
         SegInfo s;
         seg_info(p, it, end, s);
-        const int nxb = s.ncols > 16 ? (s.ncols + 15) >> 4 : 1;
-        const uint32_t idesc = idesc_bf16(16 * nxb);
+        const uint32_t idesc = idesc_bf16(16 * seg_xboxes(s));
         const uint32_t buf = seg & 1u;
         if (!mbar_wait_bounded(&acc_empty[buf], ((seg >> 1) & 1u) ^ 1u, p.status, flags,
                                p.wait_limit_ns)) {
@@ -250,6 +224,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
   } else {
     // --------------------------------------------------------------- epilogue
+    griddep_wait();
     const int r = 32 * (warp & 3) + lane;  // tile row == tensor-memory lane
     uint32_t seg = 0;
     for (int64_t it = begin; it < end; ++seg) {
@@ -300,8 +275,7 @@ cudaError_t launch_t(const CUtensorMap &wmap, const CUtensorMap &xmap, const Eng
     if (e != cudaSuccess) return e;
     attr_set.fetch_or(bit);
   }
-  engine_tc_kernel<MAXC><<<p.G, TC_THREADS, C::SMEM, s>>>(wmap, xmap, p);
-  return cudaGetLastError();
+  return launch_pdl(engine_tc_kernel<MAXC>, dim3(p.G), dim3(TC_THREADS), C::SMEM, s, wmap, xmap, p);
 }
 
 }  // namespace

@@ -13,7 +13,10 @@
 // them with the matching activation chunks (coherent loads, L1-resident), and keeps
 // NB x 4 fp32 partial sums in registers. A warp reduces them with shuffles; the P
 // piece sums of a row are added in piece order from shared memory. The result does
-// not depend on launch timing: every sum has a fixed order.
+// not depend on launch timing: every sum has a fixed order. Under programmatic
+// dependent launch the first weight loads are issued before griddepcontrol.wait and
+// every activation load after it (asm volatile loads with a memory clobber, so the
+// compiler cannot hoist them above the wait).
 #include "common.cuh"
 #include "internal.h"
 
@@ -67,6 +70,8 @@ __global__ void __launch_bounds__(TINY_THREADS, 2)
   const uint8_t *Wb = reinterpret_cast<const uint8_t *>(W);
   const uint8_t *Xb = reinterpret_cast<const uint8_t *>(X);
   const size_t row_bytes = static_cast<size_t>(K) * 2;
+  griddep_launch_dependents();
+  bool waited = false;  // the first weight loads go out before the dependency wait
 
   for (int rl = slot; rl < nrows; rl += S * TINY_RG) {
     float acc[TINY_RG][NB];
@@ -89,6 +94,10 @@ __global__ void __launch_bounds__(TINY_THREADS, 2)
           else
             wv[g][u] = make_uint4(0u, 0u, 0u, 0u);
         }
+      }
+      if (!waited) {  // activations are written by the previous kernel of the stream
+        griddep_wait();
+        waited = true;
       }
 #pragma unroll
       for (int u = 0; u < TINY_JU; ++u) {
@@ -116,6 +125,7 @@ __global__ void __launch_bounds__(TINY_THREADS, 2)
       }
     }
   }
+  griddep_wait();  // before the residual read and the output write
   __syncthreads();
   for (int i = threadIdx.x; i < nrows * NB; i += TINY_THREADS) {
     const int row = i / NB, b = i - row * NB;
@@ -151,10 +161,10 @@ cudaError_t launch_gemv_tiny(const uint16_t *X, const uint16_t *W, const uint16_
   const int rows = (N + G - 1) / G;
   const size_t smem = static_cast<size_t>(rows) * P * B * sizeof(float);
   if (B == 1)
-    gemv_tiny_kernel<1><<<G, TINY_THREADS, smem, s>>>(X, W, R, Y, N, K, P);
-  else
-    gemv_tiny_kernel<2><<<G, TINY_THREADS, smem, s>>>(X, W, R, Y, N, K, P);
-  return cudaGetLastError();
+    return launch_pdl(gemv_tiny_kernel<1>, dim3(G), dim3(TINY_THREADS), smem, s, X, W, R, Y, N, K,
+                      P);
+  return launch_pdl(gemv_tiny_kernel<2>, dim3(G), dim3(TINY_THREADS), smem, s, X, W, R, Y, N, K,
+                    P);
 }
 
 }  // namespace ssd

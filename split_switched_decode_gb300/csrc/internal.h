@@ -48,6 +48,29 @@ struct EngineParams {
   uint64_t wait_limit_ns;
 };
 
+// ------------------------------------------------------------------ launch --
+// Programmatic dependent launch on or off for this process (DEC_PDL=0 turns it off).
+bool pdl_enabled();
+
+// cudaLaunchKernelEx with programmatic stream serialisation when enabled, so the kernel
+// may start (and load weights) while the previous kernel of the stream finishes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 // ------------------------------------------------------------- engine_cc.cu --
 int engine_maxc_for(int ncols);                 // 2, 4, 8, 16, 32 or 64
 size_t engine_cc_smem_bytes(int maxc);

@@ -13,6 +13,8 @@ namespace {
 // violation yields an empty map (no used expert, zeros elsewhere) and ST_BAD_ROUTING.
 __global__ void __launch_bounds__(256) route_map_kernel(const int32_t *topk_idx, int B, int topk,
                                                         int E, int32_t *rm, unsigned *status) {
+  griddep_wait();
+  griddep_launch_dependents();
   __shared__ int32_t sidx[MAX_B * MAX_TOPK];
   __shared__ unsigned long long smask[MAX_E];
   __shared__ int soff[MAX_E];
@@ -44,6 +46,8 @@ __global__ void __launch_bounds__(256) route_map_kernel(const int32_t *topk_idx,
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t *X, const int32_t *rm,
                                                           int B, int topk, int E, int K,
                                                           uint16_t *Xg) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int P = B * topk;
   const int32_t *pairs = rm + 2 * E + 1;
   const int chunks = K / 8;  // 16-byte chunks per row
@@ -61,6 +65,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t *X, con
 __global__ void __launch_bounds__(256) combine_kernel(const float *topk_w, const int32_t *rm,
                                                       const float *Yp, const float *S, int B,
                                                       int topk, int E, int H, uint16_t *Y) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int P = B * topk;
   const int32_t *pos = rm + 2 * E + 1 + P;
   const int H4 = H / 4;
@@ -125,8 +131,8 @@ __global__ void wait_selftest_kernel(unsigned *status, uint64_t limit_ns) {
 
 cudaError_t launch_route_map_rebuild(const int32_t *topk_idx, int B, int topk, int E,
                                      int32_t *route_map, unsigned *status, cudaStream_t s) {
-  route_map_kernel<<<1, 256, 0, s>>>(topk_idx, B, topk, E, route_map, status);
-  return cudaGetLastError();
+  return launch_pdl(route_map_kernel, dim3(1), dim3(256), 0, s, topk_idx, B, topk, E, route_map,
+                    status);
 }
 
 cudaError_t launch_gather_rows(const uint16_t *X, const int32_t *route_map, int B, int topk,
@@ -134,8 +140,8 @@ cudaError_t launch_gather_rows(const uint16_t *X, const int32_t *route_map, int 
   const int64_t n = static_cast<int64_t>(B) * topk * (K / 8);
   int grid = static_cast<int>((n + 255) / 256);
   if (grid > 1024) grid = 1024;
-  gather_rows_kernel<<<grid, 256, 0, s>>>(X, route_map, B, topk, E, K, Xg);
-  return cudaGetLastError();
+  return launch_pdl(gather_rows_kernel, dim3(grid), dim3(256), 0, s, X, route_map, B, topk, E, K,
+                    Xg);
 }
 
 cudaError_t launch_combine(const float *topk_w, const int32_t *route_map, const float *Yp,
@@ -144,8 +150,8 @@ cudaError_t launch_combine(const float *topk_w, const int32_t *route_map, const 
   const int64_t n = static_cast<int64_t>(B) * (H / 4);
   int grid = static_cast<int>((n + 255) / 256);
   if (grid > 1024) grid = 1024;
-  combine_kernel<<<grid, 256, 0, s>>>(topk_w, route_map, Yp, S, B, topk, E, H, Y);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3(grid), dim3(256), 0, s, topk_w, route_map, Yp, S, B, topk,
+                    E, H, Y);
 }
 
 cudaError_t launch_l2_prefetch(const void *p, size_t bytes, int ctas, cudaStream_t s) {
