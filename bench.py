@@ -68,6 +68,10 @@ def parse_args():
     ap.add_argument("--num-experts", type=int, default=E,
                     help="routed experts in the bank (smaller for profiler captures)")
     ap.add_argument("--reps", type=int, default=7, help="graph replays per sweep entry")
+    ap.add_argument("--step-only", action="store_true",
+                    help="only the step graph (no sweep, e2e or CPU baseline), for profiler captures")
+    ap.add_argument("--no-prefetch", action="store_true",
+                    help="leave out the L2 prefetch of the shared expert's weights")
     return ap.parse_args()
 
 
@@ -181,6 +185,7 @@ class Workload:
             d["ws_e"] = ssd.workspace(ssd.moe_experts_workspace_bytes(B, self.E, TOPK, H, I), dev)
             self.t[B] = d
         self.launches = 0
+        self.prefetch = True
         torch.cuda.synchronize()
 
     # -- operations (each adds the kernels it launches to self.launches) --
@@ -216,7 +221,7 @@ class Workload:
         for B in self.batches:
             self.op_in(B)
             self.op_o(B)
-            self.op_front(B)
+            self.op_front(B, prefetch=self.prefetch)
             self.op_experts(B)
 
     def used_experts(self, B, v=0):
@@ -395,6 +400,7 @@ def main():
         ops = {"in", "o", "front", "experts"}
     wl = Workload(torch, ssd, inputs, dev, batches, num_experts=args.num_experts,
                   experts="experts" in ops)
+    wl.prefetch = not args.no_prefetch
 
     # routing of every X set (fixed inputs -> fixed routing -> fixed bytes)
     for B in batches:
@@ -405,7 +411,7 @@ def main():
     # ---- per-operation sweep: graphs of R calls over rotating weight copies
     sweep = {}
     R_SMALL = 12
-    for B in batches:
+    for B in ([] if args.step_only else batches):
         row = {}
         for key, name, fn, nb in (
                 ("in", "input_projection", lambda B=B: [wl.op_in(B, r) for r in range(R_SMALL)],
@@ -464,6 +470,12 @@ def main():
     ms = max_over_ranks(torch, world, ms, dev)
     value = step_bytes * world / (ms * 1e-3) / 1e9
     assert ssd.dec_sync_status() == ssd.DEC_OK
+    if args.step_only:
+        if rank == 0:
+            print(json.dumps({"step_only": True, "value": value, "unit": "GB/s", "ms_per_step": ms,
+                              "batches": batches, "num_experts": wl.E,
+                              "l2_prefetch": wl.prefetch}), flush=True)
+        return 0
 
     # ---- end to end through the public API with host buffers
     e2e = None
@@ -486,7 +498,7 @@ def main():
                 d["x_moe"][0].copy_(hi["x_moe"], non_blocking=True)
                 wl.op_in(B)
                 wl.op_o(B)
-                wl.op_front(B)
+                wl.op_front(B, prefetch=wl.prefetch)
                 wl.op_experts(B)
                 ho["y_in"].copy_(d["y_in"], non_blocking=True)
                 ho["y_o"].copy_(d["y_o"], non_blocking=True)
@@ -540,6 +552,7 @@ def main():
                            "l2": "cold: every weight tensor is re-read only after >3x L2 of "
                                  "other weight traffic (step), rotating copies >=3x L2 (sweep)",
                            "timing": "CUDA graph replay, CUDA events on the replay stream",
+                           "l2_prefetch": wl.prefetch,
                            "parallelism": f"replicas x{world}"},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": per_step_launches * args.steps, "clocks": clocks,

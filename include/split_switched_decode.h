@@ -205,7 +205,8 @@ DEC_API size_t moe_route_map_ints(int B, int E, int topk);
  * X [B,K]; latent [B,L] (NULL allowed when L == 0); topk_idx int32 [B,topk];
  * topk_w fp32 [B,topk]; probs_opt fp32 [B,E] or NULL; route_map_opt int32
  * [moe_route_map_ints(B,E,topk)] or NULL. E in 1..512, topk in 1..min(E,16), L >= 0.
- * One launch: the last CTA to finish the product does the routing.
+ * Two launches on `s`: the product, then a routing kernel (one warp per token) that
+ * starts as the product's CTAs retire (programmatic dependent launch).
  */
 DEC_API size_t moe_front_workspace_bytes(int B, int E, int L, int K);
 DEC_API dec_status moe_front(const dec_bf16 *X, const dec_bf16 *Wcat, int B, int K, int E, int L,

@@ -237,8 +237,20 @@ struct FrontPlan {
   size_t done_off, logits_off, total;
 };
 
-bool plan_front(int B, int E, int L, int K, int num_sms, FrontPlan *fp) {
-  if (!plan_splitk(B, E + L, K, 0, num_sms, &fp->sk)) return false;
+// k-splits per front tile (0 = one worker per SM). Fewer splits mean fewer partial
+// tiles for each tile's last worker to add, which dominates at large B.
+int front_splits(int B, int E, int L, int num_sms) {
+  int s = 0;
+  if (const char *e = std::getenv("DEC_FRONT_SPLIT")) s = std::atoi(e);
+  (void)B;
+  if (s <= 0) return 0;
+  const int T = ceil_div(E + L, TILE_N);
+  if (s * T > num_sms) s = num_sms / T;
+  return s < 1 ? 1 : s;
+}
+
+bool plan_front(int B, int E, int L, int K, int num_sms, FrontPlan *fp, int splits = 0) {
+  if (!plan_splitk(B, E + L, K, splits, num_sms, &fp->sk)) return false;
   fp->done_off = fp->sk.total;
   fp->logits_off = fp->done_off + kAlign;
   fp->total = fp->logits_off + align_up(static_cast<size_t>(B) * E * sizeof(float));
@@ -458,7 +470,9 @@ dec_status moe_front(const dec_bf16 *X, const dec_bf16 *Wcat, int B, int K, int 
   DeviceInfo *d = device_info(&ce);
   if (!d) return DEC_ERR_CUDA;
   FrontPlan fp;
-  if (!plan_front(B, E, L, K, d->num_sms, &fp)) return DEC_ERR_UNSUPPORTED_SHAPE;
+  int splits = front_splits(B, E, L, d->num_sms);
+  if (splits > ceil_div(K, TILE_K)) splits = ceil_div(K, TILE_K);
+  if (!plan_front(B, E, L, K, d->num_sms, &fp, splits)) return DEC_ERR_UNSUPPORTED_SHAPE;
   if (ws_bytes < fp.total) return DEC_ERR_WORKSPACE_TOO_SMALL;
   CUtensorMap wmap, xmap;
   if (!make_map(&wmap, Wcat, K, E + L, WBOX_ROWS) || !make_map(&xmap, X, K, B, XBOX_ROWS))
@@ -482,6 +496,9 @@ dec_status moe_front(const dec_bf16 *X, const dec_bf16 *Wcat, int B, int K, int 
   ce = tc ? launch_engine_tc(fp.sk.maxc, wmap, xmap, p, reinterpret_cast<cudaStream_t>(s))
           : launch_engine_cc(fp.sk.maxc, wmap, xmap, p, reinterpret_cast<cudaStream_t>(s));
   if (ce == cudaErrorNotSupported) return DEC_ERR_UNSUPPORTED_SHAPE;
+  if (ce != cudaSuccess) return DEC_ERR_CUDA;
+  ce = launch_route(p.logits, B, E, topk, topk_idx, topk_w, probs_opt, route_map_opt,
+                    p.done_counter, reinterpret_cast<cudaStream_t>(s));
   if (ce != cudaSuccess) return DEC_ERR_CUDA;
   t_last_variant = tc ? DEC_VARIANT_SPLITK_TC : DEC_VARIANT_SPLITK;
   return DEC_OK;

@@ -20,6 +20,8 @@ constexpr int XBOX_ROWS = 16;   // activation rows per TMA box (MMA N granularit
 constexpr int MAX_B = 64;
 constexpr int MAX_E = 512;
 constexpr int MAX_TOPK = 16;
+// shared memory of the routing tail: ids [B*topk], token masks [E], offsets [E]
+constexpr int ROUTE_SCRATCH_BYTES = 4 * MAX_B * MAX_TOPK + 8 * MAX_E + 4 * MAX_E;
 
 // Device status bits (dec_sync_status maps them to dec_status).
 constexpr unsigned ST_TIMEOUT = 1u;
@@ -28,7 +30,7 @@ constexpr unsigned ST_BAD_ROUTING = 2u;  // an expert index out of range or repe
 // Mode of the split-K engine's epilogue.
 enum EngineMode : int {
   MODE_LINEAR = 0,   // Y = bf16(acc (+R))
-  MODE_FRONT = 1,    // router logits (fp32) + latent (bf16), then routing
+  MODE_FRONT = 1,    // router logits (fp32) + latent (bf16); routing is a dependent kernel
   MODE_GATEUP = 2,   // A = bf16(silu(gate) * up)
   MODE_DOWN = 3      // Yp = acc (fp32)
 };
@@ -149,6 +151,18 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void *addr, uint32_t byte
                    reinterpret_cast<uint64_t>(addr)),
                "r"(bytes)
                : "memory");
+}
+
+// ---------------------------------------------------------------- atomics ----
+// GPU-scope acquire-release add. Issued by one thread after a CTA barrier, it publishes
+// every write the CTA made before the barrier (release is cumulative) and, for the
+// thread that sees the final count, makes every other CTA's published writes visible
+// (acquire); a following CTA barrier extends that to the whole CTA.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int *p, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
 }
 
 // ------------------------------------------------ programmatic dependent launch ----

@@ -142,6 +142,9 @@ __device__ __forceinline__ void engine_produce(const EngineParams &p, const CUte
     }
     it += s.kb1 - s.kb0;
   }
+  // every weight and activation load of this CTA is issued: the next kernel of the
+  // stream may be scheduled onto SMs as they free up
+  griddep_launch_dependents();
   if (flags[0]) {
     // after a time-out: let this CTA's copies still in flight land before it exits
     const uint32_t q0 = q > STAGES ? q - STAGES : 0u;
@@ -165,17 +168,15 @@ __device__ __forceinline__ bool reduce_tile(const EngineParams &p, const SegInfo
 #pragma unroll
   for (int j = 0; j < MAXC; ++j)
     if (j < s.ncols) slot[j * 128 + r] = v[j];
-  __threadfence();
   named_bar_sync(bar_id, 128);
   const int first = sk_worker_of(total, p.G, tb);
   const int last = sk_worker_of(total, p.G, tb + p.KB - 1);
   if (r == 0) {
-    const int old = atomicAdd(&p.counters[s.gt], 1);
+    const int old = atom_add_acq_rel_gpu(&p.counters[s.gt], 1);
     flags[1] = (old == last - first) ? 1 : 0;
   }
   named_bar_sync(bar_id, 128);
   if (!flags[1]) return false;
-  __threadfence();
   // Add the contributors' partials in worker order. Only the first contributor can
   // have started before this tile (its slot 1); every later one began inside it (slot
   // 0). Loads of RD contributors are issued before their adds so they overlap.
@@ -239,12 +240,6 @@ __device__ __forceinline__ void epilogue_rows(const EngineParams &p, const SegIn
           p.latent[static_cast<size_t>(j) * p.L + (n - p.E)] = f32_to_bf16_rn(v[j]);
       }
     }
-    __threadfence();
-    named_bar_sync(bar_id, 128);
-    if (r == 0) {
-      const int old = atomicAdd(p.done_counter, 1);
-      if (old == p.T - 1) flags[2] = 1;  // this CTA finished the last tile: it routes
-    }
   } else if (p.mode == MODE_GATEUP) {
     named_bar_sync(bar_id, 128);
     if (r >= 64) {
@@ -273,25 +268,6 @@ __device__ __forceinline__ void epilogue_rows(const EngineParams &p, const SegIn
         if (j < s.ncols) p.Yp[static_cast<size_t>(s.xrow0 + j) * p.N + n] = v[j];
     }
   }
-}
-
-// Routing tail of MODE_FRONT, run by `nwarps` warps (wid = 0..nwarps-1, named barrier
-// bar_id over nwarps*32 threads) of the CTA that finished the last tile. `work` is free
-// shared memory of >= 10 KB. `leader` marks the one thread that resets the counter.
-__device__ __forceinline__ void front_route_tail(const EngineParams &p, uint8_t *work, int wid,
-                                                 int nwarps, int bar_id, bool leader) {
-  __threadfence();
-  int32_t *sidx = reinterpret_cast<int32_t *>(work);
-  unsigned long long *smask = reinterpret_cast<unsigned long long *>(work + 4 * MAX_B * MAX_TOPK);
-  int *soff = reinterpret_cast<int *>(work + 4 * MAX_B * MAX_TOPK + 8 * MAX_E);
-  route_tokens_warp(p.logits, p.B, p.E, p.topk, p.topk_idx, p.topk_w, p.probs, sidx, wid,
-                    nwarps);
-  if (p.route_map_out != nullptr) {
-    named_bar_sync(bar_id, nwarps * 32);
-    build_route_map(sidx, p.B, p.topk, p.E, p.route_map_out, smask, soff, nwarps * 32, bar_id,
-                    wid * 32 + (threadIdx.x & 31));
-  }
-  if (leader) *p.done_counter = 0;
 }
 
 }  // namespace ssd

@@ -29,7 +29,6 @@ struct CCConfig {
   static constexpr int STAGES = FIT > 8 ? 8 : FIT;
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + SCRATCH_BYTES + 256;
   static_assert(STAGES >= 4, "pipeline too shallow");
-  static_assert(STAGES * STAGE_BYTES >= 4 * MAX_B * MAX_TOPK + 12 * MAX_E, "routing space");
 };
 
 template <int MAXC>
@@ -108,8 +107,6 @@ __global__ void __launch_bounds__(CC_THREADS, 1)
   }
   __syncthreads();
 
-  griddep_launch_dependents();
-
   if (warp == 8) {
     // ---------------------------------------------------------------- producer
     if (lane == 0)
@@ -155,8 +152,6 @@ __global__ void __launch_bounds__(CC_THREADS, 1)
     }
   }
   __syncthreads();
-  if (p.mode == MODE_FRONT && flags[2] && !flags[0])  // every warp of the CTA routes
-    front_route_tail(p, stage_mem, warp, CC_THREADS / 32, 1, tid == 0);
 }
 
 // The shared-memory opt-in is a per-device function attribute: set it on the first

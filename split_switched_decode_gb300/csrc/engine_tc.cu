@@ -40,7 +40,6 @@ struct TCConfig {
   static constexpr int STAGES = FIT > 8 ? 8 : FIT;
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + SCRATCH_BYTES + TAIL;
   static_assert(STAGES >= 4, "pipeline too shallow");
-  static_assert(STAGES * STAGE_BYTES >= 4 * MAX_B * MAX_TOPK + 12 * MAX_E, "routing space");
 };
 
 // ------------------------------------------------------------ tcgen05 PTX ----
@@ -169,8 +168,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  griddep_launch_dependents();
-
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
     if (lane == 0)
@@ -255,8 +252,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (p.mode == MODE_FRONT && flags[2] && !flags[0])  // every warp of the CTA routes
-    front_route_tail(p, stage_mem, warp, TC_THREADS / 32, 3, tid == 0);
   if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
 }
 

@@ -70,7 +70,6 @@ __global__ void __launch_bounds__(TINY_THREADS, 2)
   const uint8_t *Wb = reinterpret_cast<const uint8_t *>(W);
   const uint8_t *Xb = reinterpret_cast<const uint8_t *>(X);
   const size_t row_bytes = static_cast<size_t>(K) * 2;
-  griddep_launch_dependents();
   bool waited = false;  // the first weight loads go out before the dependency wait
 
   for (int rl = slot; rl < nrows; rl += S * TINY_RG) {
@@ -125,7 +124,8 @@ __global__ void __launch_bounds__(TINY_THREADS, 2)
       }
     }
   }
-  griddep_wait();  // before the residual read and the output write
+  griddep_launch_dependents();  // all weight loads of this CTA are done
+  griddep_wait();               // before the residual read and the output write
   __syncthreads();
   for (int i = threadIdx.x; i < nrows * NB; i += TINY_THREADS) {
     const int row = i / NB, b = i - row * NB;

@@ -90,6 +90,9 @@ cudaError_t launch_gemv_tiny(const uint16_t *X, const uint16_t *W, const uint16_
 // --------------------------------------------------------------- moe_aux.cu --
 cudaError_t launch_route_map_rebuild(const int32_t *topk_idx, int B, int topk, int E,
                                      int32_t *route_map, unsigned *status, cudaStream_t s);
+cudaError_t launch_route(const float *logits, int B, int E, int topk, int32_t *topk_idx,
+                         float *topk_w, float *probs, int32_t *route_map, int *done_counter,
+                         cudaStream_t s);
 cudaError_t launch_gather_rows(const uint16_t *X, const int32_t *route_map, int B, int topk,
                                int E, int K, uint16_t *Xg, cudaStream_t s);
 cudaError_t launch_combine(const float *topk_w, const int32_t *route_map, const float *Yp,

@@ -41,6 +41,35 @@ __global__ void __launch_bounds__(256) route_map_kernel(const int32_t *topk_idx,
   build_route_map(sidx, B, topk, E, rm, smask, soff, 256, 1, threadIdx.x);
 }
 
+// Routing of a decode batch from the front end's fp32 logits: one warp per token over
+// ceil(B/4) CTAs, so B tokens are routed on many SMs at once; the CTA that finishes
+// last (acquire-release counter, reset after use) builds the route map. Launched as a
+// programmatic dependent of the router + latent product, it is scheduled as that
+// kernel's CTAs retire and waits for its logits with griddepcontrol.wait.
+__global__ void __launch_bounds__(128) route_kernel(const float *logits, int B, int E, int topk,
+                                                    int32_t *topk_idx, float *topk_w,
+                                                    float *probs, int32_t *rm,
+                                                    int *done_counter) {
+  __shared__ int32_t sidx[MAX_B * MAX_TOPK];
+  __shared__ unsigned long long smask[MAX_E];
+  __shared__ int soff[MAX_E];
+  __shared__ int last;
+  griddep_wait();
+  griddep_launch_dependents();
+  const int warp = threadIdx.x >> 5;
+  route_tokens_warp(logits, B, E, topk, topk_idx, topk_w, probs, nullptr,
+                    blockIdx.x * 4 + warp, gridDim.x * 4);
+  if (rm == nullptr) return;
+  __syncthreads();
+  if (threadIdx.x == 0) last = (atom_add_acq_rel_gpu(done_counter, 1) == gridDim.x - 1);
+  __syncthreads();
+  if (!last) return;
+  for (int q = threadIdx.x; q < B * topk; q += 128) sidx[q] = __ldcg(topk_idx + q);
+  __syncthreads();
+  build_route_map(sidx, B, topk, E, rm, smask, soff, 128, 1, threadIdx.x);
+  if (threadIdx.x == 0) *done_counter = 0;
+}
+
 // Xg[q, :] = X[pairs[q] / topk, :] -- the activation rows of every (token, slot) entry
 // in expert order, so each expert's rows are contiguous for the TMA tile loads.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t *X, const int32_t *rm,
@@ -133,6 +162,13 @@ cudaError_t launch_route_map_rebuild(const int32_t *topk_idx, int B, int topk, i
                                      int32_t *route_map, unsigned *status, cudaStream_t s) {
   return launch_pdl(route_map_kernel, dim3(1), dim3(256), 0, s, topk_idx, B, topk, E, route_map,
                     status);
+}
+
+cudaError_t launch_route(const float *logits, int B, int E, int topk, int32_t *topk_idx,
+                         float *topk_w, float *probs, int32_t *route_map, int *done_counter,
+                         cudaStream_t s) {
+  return launch_pdl(route_kernel, dim3((B + 3) / 4), dim3(128), 0, s, logits, B, E, topk,
+                    topk_idx, topk_w, probs, route_map, done_counter);
 }
 
 cudaError_t launch_gather_rows(const uint16_t *X, const int32_t *route_map, int B, int topk,

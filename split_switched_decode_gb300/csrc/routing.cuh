@@ -16,22 +16,26 @@ __device__ __forceinline__ float order_key_to_f32(uint32_t k) {
   return (k & 0x80000000u) ? __uint_as_float(k & 0x7FFFFFFFu) : __uint_as_float(~k);
 }
 
-// One warp routes token rows b = warp_id, warp_id + nwarps, ... of logits [B,E].
-// Writes topk_idx/topk_w (global) and, when given, probs (global) and sidx (shared
-// copy of topk_idx for the route map).
-__device__ __noinline__ static void route_tokens_warp(const float *logits, int B, int E, int topk,
-                                  int32_t *topk_idx, float *topk_w, float *probs,
-                                  int32_t *sidx, int warp_id, int nwarps) {
+// One warp routes token rows b = warp_id, warp_id + nwarps, ... of logits [B,E] (shared
+// or global memory). Writes topk_idx/topk_w (global) and, when given, probs (global)
+// and sidx (shared copy of topk_idx for the route map). Register-only: every array
+// index below is a compile-time constant after unrolling.
+__device__ __forceinline__ void route_tokens_warp(const float *logits, int B, int E, int topk,
+                                                  int32_t *topk_idx, float *topk_w,
+                                                  float *probs, int32_t *sidx, int warp_id,
+                                                  int nwarps) {
   constexpr int VPL = MAX_E / 32;  // logits per lane
   const int lane = threadIdx.x & 31;
   const unsigned FULL = 0xFFFFFFFFu;
   for (int b = warp_id; b < B; b += nwarps) {
     const float *l = logits + static_cast<size_t>(b) * E;
     float v[VPL];
+    uint32_t key[VPL];
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
       const int e = lane + 32 * i;
-      v[i] = (e < E) ? __ldcg(l + e) : -INFINITY;
+      v[i] = (e < E) ? l[e] : -INFINITY;
+      key[i] = (e < E) ? f32_order_key(v[i]) : 0u;  // 0: below every real key
     }
     float m = -INFINITY;
 #pragma unroll
@@ -53,38 +57,36 @@ __device__ __noinline__ static void route_tokens_warp(const float *logits, int B
       }
     }
 
-    // top-k: k rounds of a warp-wide arg-max on (logit desc, index asc). Each lane
-    // caches the best of its own remaining logits; only the lane that wins a round
-    // rescans.
-    uint32_t key[VPL];
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) key[i] = f32_order_key(v[i]);
-    uint32_t taken = 0;
-    int bi = -1;
+    // top-k: k rounds of a warp-wide arg-max on (logit desc, index asc). A lane keeps
+    // the best of its remaining logits (bk, bi); a taken logit's key is zeroed and only
+    // the lane that won the round rescans.
     uint32_t bk = 0;
-    auto rescan = [&]() {
-      bi = -1;
-      bk = 0;
+    int bi = 0;
 #pragma unroll
-      for (int i = 0; i < VPL; ++i) {
-        const bool ok = (lane + 32 * i < E) && !((taken >> i) & 1u);
-        if (ok && (bi < 0 || key[i] > bk)) {  // strict: lower index (smaller i) wins ties
-          bi = i;
-          bk = key[i];
-        }
+    for (int i = 0; i < VPL; ++i)
+      if (key[i] > bk) {  // strict: the lower index (smaller i) wins ties
+        bk = key[i];
+        bi = i;
       }
-    };
-    rescan();
     int my_e = 0;
     float my_v = 0.f;
     for (int j = 0; j < topk; ++j) {
-      const uint32_t kmax = __reduce_max_sync(FULL, bi >= 0 ? bk : 0u);
-      const uint32_t cand =
-          (bi >= 0 && bk == kmax) ? static_cast<uint32_t>(lane + 32 * bi) : 0xFFFFFFFFu;
+      const uint32_t kmax = __reduce_max_sync(FULL, bk);
+      const uint32_t cand = (bk == kmax && bk != 0u) ? static_cast<uint32_t>(lane + 32 * bi)
+                                                     : 0xFFFFFFFFu;
       const uint32_t win = __reduce_min_sync(FULL, cand);
       if (lane == static_cast<int>(win & 31u)) {
-        taken |= 1u << (win >> 5);
-        rescan();
+        const int wi = static_cast<int>(win >> 5);
+        bk = 0;
+        bi = 0;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+          if (i == wi) key[i] = 0u;
+          if (key[i] > bk) {
+            bk = key[i];
+            bi = i;
+          }
+        }
       }
       if (lane == j) {
         my_e = static_cast<int>(win);
