@@ -234,7 +234,7 @@ int tc_min_batch() {
 
 struct FrontPlan {
   SplitPlan sk;
-  size_t done_off, logits_off, total;
+  size_t done_off, logits_off, total;  // done_off: tok_done[MAX_B] then all_done
 };
 
 // k-splits per front tile (0 = one worker per SM). Fewer splits mean fewer partial
@@ -252,7 +252,7 @@ int front_splits(int B, int E, int L, int num_sms) {
 bool plan_front(int B, int E, int L, int K, int num_sms, FrontPlan *fp, int splits = 0) {
   if (!plan_splitk(B, E + L, K, splits, num_sms, &fp->sk)) return false;
   fp->done_off = fp->sk.total;
-  fp->logits_off = fp->done_off + kAlign;
+  fp->logits_off = fp->done_off + align_up((MAX_B + 1) * sizeof(int));
   fp->total = fp->logits_off + align_up(static_cast<size_t>(B) * E * sizeof(float));
   return true;
 }
@@ -479,17 +479,9 @@ dec_status moe_front(const dec_bf16 *X, const dec_bf16 *Wcat, int B, int K, int 
     return DEC_ERR_CUDA;
   EngineParams p;
   fill_engine_common(p, fp.sk, MODE_FRONT, E + L, K, B, ws, d);
+  if (fp.sk.G < fp.sk.T) return DEC_ERR_UNSUPPORTED_SHAPE;  // a worker may span 2 tiles at most
+  p.defer = 1;  // partial tiles only; front_finish adds them
   char *wsb = static_cast<char *>(ws);
-  p.done_counter = reinterpret_cast<int *>(wsb + fp.done_off);
-  p.logits = reinterpret_cast<float *>(wsb + fp.logits_off);
-  p.E = E;
-  p.L = L;
-  p.topk = topk;
-  p.latent = latent;
-  p.topk_idx = topk_idx;
-  p.topk_w = topk_w;
-  p.probs = probs_opt;
-  p.route_map_out = route_map_opt;
   if (consume_fault()) return DEC_ERR_CUDA;
   int v = force_variant();
   const bool tc = (v == DEC_VARIANT_SPLITK_TC) || (v == DEC_VARIANT_NONE && B >= tc_min_batch());
@@ -497,8 +489,26 @@ dec_status moe_front(const dec_bf16 *X, const dec_bf16 *Wcat, int B, int K, int 
           : launch_engine_cc(fp.sk.maxc, wmap, xmap, p, reinterpret_cast<cudaStream_t>(s));
   if (ce == cudaErrorNotSupported) return DEC_ERR_UNSUPPORTED_SHAPE;
   if (ce != cudaSuccess) return DEC_ERR_CUDA;
-  ce = launch_route(p.logits, B, E, topk, topk_idx, topk_w, probs_opt, route_map_opt,
-                    p.done_counter, reinterpret_cast<cudaStream_t>(s));
+  FrontFinishParams f;
+  f.partials = p.partials;
+  f.slot_cols = p.slot_cols;
+  f.G = p.G;
+  f.T = p.T;
+  f.KB = p.KB;
+  f.total = static_cast<long long>(p.T) * p.KB;
+  f.B = B;
+  f.E = E;
+  f.L = L;
+  f.topk = topk;
+  f.logits = reinterpret_cast<float *>(wsb + fp.logits_off);
+  f.latent = latent;
+  f.topk_idx = topk_idx;
+  f.topk_w = topk_w;
+  f.probs = probs_opt;
+  f.route_map = route_map_opt;
+  f.tok_done = reinterpret_cast<int *>(wsb + fp.done_off);
+  f.all_done = f.tok_done + MAX_B;
+  ce = launch_front_finish(f, reinterpret_cast<cudaStream_t>(s));
   if (ce != cudaSuccess) return DEC_ERR_CUDA;
   t_last_variant = tc ? DEC_VARIANT_SPLITK_TC : DEC_VARIANT_SPLITK;
   return DEC_OK;

@@ -30,7 +30,7 @@ constexpr unsigned ST_BAD_ROUTING = 2u;  // an expert index out of range or repe
 // Mode of the split-K engine's epilogue.
 enum EngineMode : int {
   MODE_LINEAR = 0,   // Y = bf16(acc (+R))
-  MODE_FRONT = 1,    // router logits (fp32) + latent (bf16); routing is a dependent kernel
+  MODE_FRONT = 1,    // router + latent product: partial tiles only, added by a dependent kernel
   MODE_GATEUP = 2,   // A = bf16(silu(gate) * up)
   MODE_DOWN = 3      // Yp = acc (fp32)
 };

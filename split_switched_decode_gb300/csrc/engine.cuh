@@ -160,7 +160,7 @@ template <int MAXC>
 __device__ __forceinline__ bool reduce_tile(const EngineParams &p, const SegInfo &s, int64_t total, int w,
                             int64_t begin, int r, float (&v)[MAXC], int bar_id,
                             volatile int *flags) {
-  if (s.full) return true;
+  if (s.full && !p.defer) return true;
   const int64_t tb = static_cast<int64_t>(s.gt) * p.KB;
   const int which_me = (begin >= tb) ? 0 : 1;
   const size_t slot_floats = static_cast<size_t>(128) * p.slot_cols;
@@ -168,6 +168,7 @@ __device__ __forceinline__ bool reduce_tile(const EngineParams &p, const SegInfo
 #pragma unroll
   for (int j = 0; j < MAXC; ++j)
     if (j < s.ncols) slot[j * 128 + r] = v[j];
+  if (p.defer) return false;  // a dependent kernel adds the partials (front end)
   named_bar_sync(bar_id, 128);
   const int first = sk_worker_of(total, p.G, tb);
   const int last = sk_worker_of(total, p.G, tb + p.KB - 1);
@@ -227,17 +228,6 @@ __device__ __forceinline__ void epilogue_rows(const EngineParams &p, const SegIn
           if (p.R != nullptr) y += bf16_to_f32(p.R[static_cast<size_t>(j) * p.N + n]);
           p.Y[static_cast<size_t>(j) * p.N + n] = f32_to_bf16_rn(y);
         }
-      }
-    }
-  } else if (p.mode == MODE_FRONT) {
-    const int n = s.t * 128 + r;
-#pragma unroll
-    for (int j = 0; j < MAXC; ++j) {
-      if (j < s.ncols) {
-        if (n < p.E)
-          p.logits[static_cast<size_t>(j) * p.E + n] = v[j];
-        else if (n < p.E + p.L)
-          p.latent[static_cast<size_t>(j) * p.L + (n - p.E)] = f32_to_bf16_rn(v[j]);
       }
     }
   } else if (p.mode == MODE_GATEUP) {

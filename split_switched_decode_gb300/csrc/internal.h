@@ -21,22 +21,13 @@ struct EngineParams {
   int w_group_rows;  // W rows per group in the weight bank (grouped)
   int up_row_off;    // GATEUP: row offset of the up half inside a group (= I)
   int slot_cols;     // columns per partial slot (slot = 128 * slot_cols floats)
+  int defer;         // 1: store every segment's partial tile and stop (MODE_FRONT)
   int E;             // experts (grouped route map, FRONT router rows)
   int P;             // B * topk (grouped route map)
   const int32_t *route_map;  // grouped: counts | offsets | pairs | pos | num_used | used
   // MODE_LINEAR
   uint16_t *Y;
   const uint16_t *R;
-  // MODE_FRONT
-  float *logits;     // [B,E] fp32
-  uint16_t *latent;  // [B,L] bf16
-  int L;
-  int topk;
-  int32_t *topk_idx;
-  float *topk_w;
-  float *probs;
-  int32_t *route_map_out;
-  int *done_counter;
   // MODE_GATEUP / MODE_DOWN: output row = group's first activation row + column
   uint16_t *A;  // [rows, N] bf16
   float *Yp;    // [rows, N] fp32
@@ -90,9 +81,23 @@ cudaError_t launch_gemv_tiny(const uint16_t *X, const uint16_t *W, const uint16_
 // --------------------------------------------------------------- moe_aux.cu --
 cudaError_t launch_route_map_rebuild(const int32_t *topk_idx, int B, int topk, int E,
                                      int32_t *route_map, unsigned *status, cudaStream_t s);
-cudaError_t launch_route(const float *logits, int B, int E, int topk, int32_t *topk_idx,
-                         float *topk_w, float *probs, int32_t *route_map, int *done_counter,
-                         cudaStream_t s);
+// Second half of the front end: adds the product's partial tiles in worker order,
+// writes logits and latent, routes each token and builds the route map.
+struct FrontFinishParams {
+  const float *partials;
+  int slot_cols, G, T, KB;
+  long long total;
+  int B, E, L, topk;
+  float *logits;
+  uint16_t *latent;
+  int32_t *topk_idx;
+  float *topk_w;
+  float *probs;
+  int32_t *route_map;
+  int *tok_done;  // [B], zero between launches
+  int *all_done;  // [1], zero between launches
+};
+cudaError_t launch_front_finish(const FrontFinishParams &f, cudaStream_t s);
 cudaError_t launch_gather_rows(const uint16_t *X, const int32_t *route_map, int B, int topk,
                                int E, int K, uint16_t *Xg, cudaStream_t s);
 cudaError_t launch_combine(const float *topk_w, const int32_t *route_map, const float *Yp,

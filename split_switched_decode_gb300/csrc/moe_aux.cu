@@ -41,33 +41,71 @@ __global__ void __launch_bounds__(256) route_map_kernel(const int32_t *topk_idx,
   build_route_map(sidx, B, topk, E, rm, smask, soff, 256, 1, threadIdx.x);
 }
 
-// Routing of a decode batch from the front end's fp32 logits: one warp per token over
-// ceil(B/4) CTAs, so B tokens are routed on many SMs at once; the CTA that finishes
-// last (acquire-release counter, reset after use) builds the route map. Launched as a
-// programmatic dependent of the router + latent product, it is scheduled as that
-// kernel's CTAs retire and waits for its logits with griddepcontrol.wait.
-__global__ void __launch_bounds__(128) route_kernel(const float *logits, int B, int E, int topk,
-                                                    int32_t *topk_idx, float *topk_w,
-                                                    float *probs, int32_t *rm,
-                                                    int *done_counter) {
+// Second half of the MoE front end, launched programmatically after the router +
+// latent product (which only stored its partial tiles). CTA (t, b) owns rows
+// t*128 .. t*128+127 of token b: thread r adds row r's partials of every worker that
+// contributed to tile t, in worker order (the split of the product kernel, recomputed
+// here), with all loads issued together. Router rows go to the fp32 logits, latent
+// rows to bf16. The CTA that completes a token's last router tile (acquire-release
+// counter per token) routes that token with one warp; the CTA that routes the last
+// token builds the route map. Spread over T*B CTAs, the reduction and the routing take
+// one memory round trip each instead of one CTA per tile adding tens of partial tiles.
+__global__ void __launch_bounds__(128) front_finish_kernel(const FrontFinishParams f) {
   __shared__ int32_t sidx[MAX_B * MAX_TOPK];
   __shared__ unsigned long long smask[MAX_E];
   __shared__ int soff[MAX_E];
-  __shared__ int last;
+  __shared__ int flag;
   griddep_wait();
   griddep_launch_dependents();
-  const int warp = threadIdx.x >> 5;
-  route_tokens_warp(logits, B, E, topk, topk_idx, topk_w, probs, nullptr,
-                    blockIdx.x * 4 + warp, gridDim.x * 4);
-  if (rm == nullptr) return;
+  const int t = blockIdx.x, b = blockIdx.y, r = threadIdx.x;
+  const int n = t * 128 + r;
+  const int64_t tb = static_cast<int64_t>(t) * f.KB;
+  const int first = static_cast<int>(((tb + 1) * f.G - 1) / f.total);
+  const int last = static_cast<int>(((tb + f.KB) * f.G - 1) / f.total);
+  const int which_first = (static_cast<int64_t>(first) * f.total / f.G >= tb) ? 0 : 1;
+  const size_t slot_floats = static_cast<size_t>(128) * f.slot_cols;
+  const float *base = f.partials + static_cast<size_t>(b) * 128 + r;
+  float z = 0.f;
+  constexpr int D = 8;
+  for (int wk0 = first; wk0 <= last; wk0 += D) {
+    float part[D];
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+      const int wk = wk0 + d;
+      const int which = (wk == first) ? which_first : 0;
+      part[d] = (wk <= last) ? __ldcg(base + static_cast<size_t>(wk * 2 + which) * slot_floats)
+                             : 0.f;
+    }
+#pragma unroll
+    for (int d = 0; d < D; ++d)
+      if (wk0 + d <= last) z += part[d];
+  }
+  if (n < f.E)
+    f.logits[static_cast<size_t>(b) * f.E + n] = z;
+  else if (n < f.E + f.L)
+    f.latent[static_cast<size_t>(b) * f.L + (n - f.E)] = f32_to_bf16_rn(z);
+  const int t_router = (f.E + 127) / 128;
+  if (t >= t_router) return;  // latent tile: done (uniform per CTA)
   __syncthreads();
-  if (threadIdx.x == 0) last = (atom_add_acq_rel_gpu(done_counter, 1) == gridDim.x - 1);
+  if (r == 0) flag = (atom_add_acq_rel_gpu(&f.tok_done[b], 1) == t_router - 1);
   __syncthreads();
-  if (!last) return;
-  for (int q = threadIdx.x; q < B * topk; q += 128) sidx[q] = __ldcg(topk_idx + q);
+  if (!flag) return;
+  if (r < 32) {
+    route_tokens_warp(f.logits + static_cast<size_t>(b) * f.E, 1, f.E, f.topk,
+                      f.topk_idx + static_cast<size_t>(b) * f.topk,
+                      f.topk_w + static_cast<size_t>(b) * f.topk,
+                      f.probs ? f.probs + static_cast<size_t>(b) * f.E : nullptr, nullptr, 0, 1);
+  }
+  if (r == 0) f.tok_done[b] = 0;
+  if (f.route_map == nullptr) return;
   __syncthreads();
-  build_route_map(sidx, B, topk, E, rm, smask, soff, 128, 1, threadIdx.x);
-  if (threadIdx.x == 0) *done_counter = 0;
+  if (r == 0) flag = (atom_add_acq_rel_gpu(f.all_done, 1) == f.B - 1);
+  __syncthreads();
+  if (!flag) return;
+  for (int q = r; q < f.B * f.topk; q += 128) sidx[q] = __ldcg(f.topk_idx + q);
+  __syncthreads();
+  build_route_map(sidx, f.B, f.topk, f.E, f.route_map, smask, soff, 128, 1, r);
+  if (r == 0) *f.all_done = 0;
 }
 
 // Xg[q, :] = X[pairs[q] / topk, :] -- the activation rows of every (token, slot) entry
@@ -164,11 +202,8 @@ cudaError_t launch_route_map_rebuild(const int32_t *topk_idx, int B, int topk, i
                     status);
 }
 
-cudaError_t launch_route(const float *logits, int B, int E, int topk, int32_t *topk_idx,
-                         float *topk_w, float *probs, int32_t *route_map, int *done_counter,
-                         cudaStream_t s) {
-  return launch_pdl(route_kernel, dim3((B + 3) / 4), dim3(128), 0, s, logits, B, E, topk,
-                    topk_idx, topk_w, probs, route_map, done_counter);
+cudaError_t launch_front_finish(const FrontFinishParams &f, cudaStream_t s) {
+  return launch_pdl(front_finish_kernel, dim3(f.T, f.B), dim3(128), 0, s, f);
 }
 
 cudaError_t launch_gather_rows(const uint16_t *X, const int32_t *route_map, int B, int topk,
