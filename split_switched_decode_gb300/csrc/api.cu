@@ -165,6 +165,17 @@ bool plan_splitk(int B, int N, int K, int split_k, int num_sms, SplitPlan *pl) {
   return true;
 }
 
+// k-blocks of weights each worker prefetches to L2 before its dependency wait
+// (DEC_L2PF_KB overrides; 0 turns it off).
+int l2_prefetch_kblocks() {
+  if (const char *s = std::getenv("DEC_L2PF_KB")) return std::atoi(s) < 0 ? 0 : std::atoi(s);
+  return 0;  // measured: the projections slow down (prefetch traffic competes); off
+}
+
+// Activation box height for a launch whose groups have at most maxc columns: one box
+// covers them all (fewer TMA instructions per stage).
+int xbox_rows_for(int maxc) { return 16 * ((maxc + 15) / 16); }
+
 void fill_engine_common(EngineParams &p, const SplitPlan &pl, int mode, int N, int K, int B,
                         void *ws, const DeviceInfo *d) {
   std::memset(&p, 0, sizeof p);
@@ -176,6 +187,9 @@ void fill_engine_common(EngineParams &p, const SplitPlan &pl, int mode, int N, i
   p.G = pl.G;
   p.B = B;
   p.slot_cols = pl.maxc;
+  p.wbox_rows = 128;
+  p.xbox_rows = xbox_rows_for(pl.maxc);
+  p.l2pf_kb = l2_prefetch_kblocks();
   p.partials = static_cast<float *>(ws);
   p.counters = reinterpret_cast<int *>(static_cast<char *>(ws) + pl.partial_bytes);
   p.status = d->status;
@@ -193,31 +207,16 @@ dec_status check_linear_args(const dec_bf16 *X, const dec_bf16 *W, dec_bf16 *Y, 
   return DEC_OK;
 }
 
-dec_status run_splitk(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 *R, dec_bf16 *Y,
-                      int B, int N, int K, int split_k, int use_tc, void *ws, size_t ws_bytes,
-                      cudaStream_t s) {
-  cudaError_t ce;
-  DeviceInfo *d = device_info(&ce);
-  if (!d) return DEC_ERR_CUDA;
-  SplitPlan pl;
-  if (!plan_splitk(B, N, K, split_k, d->num_sms, &pl)) return DEC_ERR_UNSUPPORTED_SHAPE;
-  if (!ws) return DEC_ERR_INVALID_ARG;
-  if (!aligned16(ws)) return DEC_ERR_MISALIGNED;
-  if (ws_bytes < pl.total) return DEC_ERR_WORKSPACE_TOO_SMALL;
-  CUtensorMap wmap, xmap;
-  if (!make_map(&wmap, W, K, N, WBOX_ROWS) || !make_map(&xmap, X, K, B, XBOX_ROWS))
-    return DEC_ERR_CUDA;
-  EngineParams p;
-  fill_engine_common(p, pl, MODE_LINEAR, N, K, B, ws, d);
-  p.Y = Y;
-  p.R = R;
-  if (consume_fault()) return DEC_ERR_CUDA;
-  ce = use_tc ? launch_engine_tc(pl.maxc, wmap, xmap, p, s)
-              : launch_engine_cc(pl.maxc, wmap, xmap, p, s);
-  if (ce == cudaErrorNotSupported) return DEC_ERR_UNSUPPORTED_SHAPE;
-  if (ce != cudaSuccess) return DEC_ERR_CUDA;
-  t_last_variant = use_tc ? DEC_VARIANT_SPLITK_TC : DEC_VARIANT_SPLITK;
-  return DEC_OK;
+// Batch at and above which split-K projections with K >= 12288 defer their reduction
+// to a finishing kernel (DEC_DEFER_MIN_B overrides the batch; the K condition stays).
+// With long K each tile's workers hold long ranges and the last worker's 32..64-column
+// reduction is a visible tail; with short K the extra launch costs more than it saves.
+int defer_min_batch() {
+  if (const char *s = std::getenv("DEC_DEFER_MIN_B")) {
+    int v = std::atoi(s);
+    if (v >= 1) return v;
+  }
+  return 32;  // measured on the K = 16384 output projection: B = 32 and 64 gain 2-8 us
 }
 
 // The batch-size switch: the B at and above which tensor-core tiles are used
@@ -230,11 +229,59 @@ int tc_min_batch() {
   return 3;  // measured: tensor-core tiles win from B = 3 (CUDA cores are ALU-bound)
 }
 
+dec_status run_splitk(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 *R, dec_bf16 *Y,
+                      int B, int N, int K, int split_k, int use_tc, void *ws, size_t ws_bytes,
+                      cudaStream_t s) {
+  cudaError_t ce;
+  DeviceInfo *d = device_info(&ce);
+  if (!d) return DEC_ERR_CUDA;
+  SplitPlan pl;
+  if (!plan_splitk(B, N, K, split_k, d->num_sms, &pl)) return DEC_ERR_UNSUPPORTED_SHAPE;
+  if (!ws) return DEC_ERR_INVALID_ARG;
+  if (!aligned16(ws)) return DEC_ERR_MISALIGNED;
+  if (ws_bytes < pl.total) return DEC_ERR_WORKSPACE_TOO_SMALL;
+  CUtensorMap wmap, xmap;
+  if (!make_map(&wmap, W, K, N, 128) || !make_map(&xmap, X, K, B, xbox_rows_for(pl.maxc)))
+    return DEC_ERR_CUDA;
+  EngineParams p;
+  fill_engine_common(p, pl, MODE_LINEAR, N, K, B, ws, d);
+  p.Y = Y;
+  p.R = R;
+  p.w_base = reinterpret_cast<const uint8_t *>(W);
+  p.w_rows = N;
+  // Large batches: the product kernel only stores partial tiles and a finishing kernel
+  // over (tile, 16 columns) adds them, instead of each tile's last worker adding 64-wide
+  // partials at the end of the product (the product's tail). Needs workers that span
+  // at most two tiles.
+  p.defer = (B >= defer_min_batch() && K >= 12288 && pl.G >= pl.T) ? 1 : 0;
+  if (consume_fault()) return DEC_ERR_CUDA;
+  ce = use_tc ? launch_engine_tc(pl.maxc, wmap, xmap, p, s)
+              : launch_engine_cc(pl.maxc, wmap, xmap, p, s);
+  if (ce == cudaErrorNotSupported) return DEC_ERR_UNSUPPORTED_SHAPE;
+  if (ce != cudaSuccess) return DEC_ERR_CUDA;
+  if (p.defer) {
+    LinearFinishParams f;
+    f.partials = p.partials;
+    f.slot_cols = p.slot_cols;
+    f.G = p.G;
+    f.T = p.T;
+    f.KB = p.KB;
+    f.total = static_cast<long long>(p.T) * p.KB;
+    f.B = B;
+    f.N = N;
+    f.R = R;
+    f.Y = Y;
+    if (launch_linear_finish(f, s) != cudaSuccess) return DEC_ERR_CUDA;
+  }
+  t_last_variant = use_tc ? DEC_VARIANT_SPLITK_TC : DEC_VARIANT_SPLITK;
+  return DEC_OK;
+}
+
 // ------------------------------------------------------------- MoE planning --
 
 struct FrontPlan {
   SplitPlan sk;
-  size_t done_off, logits_off, total;  // done_off: tok_done[MAX_B] then all_done
+  size_t done_off, logits_off, total;  // done_off: the route-map counter
 };
 
 // k-splits per front tile (0 = one worker per SM). Fewer splits mean fewer partial
@@ -252,7 +299,7 @@ int front_splits(int B, int E, int L, int num_sms) {
 bool plan_front(int B, int E, int L, int K, int num_sms, FrontPlan *fp, int splits = 0) {
   if (!plan_splitk(B, E + L, K, splits, num_sms, &fp->sk)) return false;
   fp->done_off = fp->sk.total;
-  fp->logits_off = fp->done_off + align_up((MAX_B + 1) * sizeof(int));
+  fp->logits_off = fp->done_off + kAlign;
   fp->total = fp->logits_off + align_up(static_cast<size_t>(B) * E * sizeof(float));
   return true;
 }
@@ -475,11 +522,14 @@ dec_status moe_front(const dec_bf16 *X, const dec_bf16 *Wcat, int B, int K, int 
   if (!plan_front(B, E, L, K, d->num_sms, &fp, splits)) return DEC_ERR_UNSUPPORTED_SHAPE;
   if (ws_bytes < fp.total) return DEC_ERR_WORKSPACE_TOO_SMALL;
   CUtensorMap wmap, xmap;
-  if (!make_map(&wmap, Wcat, K, E + L, WBOX_ROWS) || !make_map(&xmap, X, K, B, XBOX_ROWS))
+  if (!make_map(&wmap, Wcat, K, E + L, 128) ||
+      !make_map(&xmap, X, K, B, xbox_rows_for(fp.sk.maxc)))
     return DEC_ERR_CUDA;
   EngineParams p;
   fill_engine_common(p, fp.sk, MODE_FRONT, E + L, K, B, ws, d);
   if (fp.sk.G < fp.sk.T) return DEC_ERR_UNSUPPORTED_SHAPE;  // a worker may span 2 tiles at most
+  p.w_base = reinterpret_cast<const uint8_t *>(Wcat);
+  p.w_rows = E + L;
   p.defer = 1;  // partial tiles only; front_finish adds them
   char *wsb = static_cast<char *>(ws);
   if (consume_fault()) return DEC_ERR_CUDA;
@@ -506,8 +556,7 @@ dec_status moe_front(const dec_bf16 *X, const dec_bf16 *Wcat, int B, int K, int 
   f.topk_w = topk_w;
   f.probs = probs_opt;
   f.route_map = route_map_opt;
-  f.tok_done = reinterpret_cast<int *>(wsb + fp.done_off);
-  f.all_done = f.tok_done + MAX_B;
+  f.all_done = reinterpret_cast<int *>(wsb + fp.done_off);
   ce = launch_front_finish(f, reinterpret_cast<cudaStream_t>(s));
   if (ce != cudaSuccess) return DEC_ERR_CUDA;
   t_last_variant = tc ? DEC_VARIANT_SPLITK_TC : DEC_VARIANT_SPLITK;
@@ -584,14 +633,16 @@ dec_status moe_experts(const dec_bf16 *X, const int32_t *topk_idx, const float *
   const int g_main = d->num_sms - g_side;
 
   CUtensorMap m_wgu, m_wd, m_xg, m_a;
-  if (!make_map(&m_wgu, Wgu, H, static_cast<uint64_t>(E) * 2 * I, WBOX_ROWS) ||
-      !make_map(&m_wd, Wd, I, static_cast<uint64_t>(E) * H, WBOX_ROWS) ||
+  // grouped launches keep 16-row activation boxes: most experts have few tokens
+  if (!make_map(&m_wgu, Wgu, H, static_cast<uint64_t>(E) * 2 * I, 64) ||
+      !make_map(&m_wd, Wd, I, static_cast<uint64_t>(E) * H, 128) ||
       !make_map(&m_xg, Xg, H, P, XBOX_ROWS) || !make_map(&m_a, A, I, P, XBOX_ROWS))
     return DEC_ERR_CUDA;
   CUtensorMap m_wgus, m_wds, m_x, m_as;
-  if (shared && (!make_map(&m_wgus, Wgu_shared, H, 2 * I, WBOX_ROWS) ||
-                 !make_map(&m_wds, Wd_shared, I, H, WBOX_ROWS) ||
-                 !make_map(&m_x, X, H, B, XBOX_ROWS) || !make_map(&m_as, As, I, B, XBOX_ROWS)))
+  const int xb_shared = xbox_rows_for(ep.maxc);
+  if (shared && (!make_map(&m_wgus, Wgu_shared, H, 2 * I, 64) ||
+                 !make_map(&m_wds, Wd_shared, I, H, 128) ||
+                 !make_map(&m_x, X, H, B, xb_shared) || !make_map(&m_as, As, I, B, xb_shared)))
     return DEC_ERR_CUDA;
 
   if (consume_fault()) return DEC_ERR_CUDA;
@@ -616,6 +667,8 @@ dec_status moe_experts(const dec_bf16 *X, const int32_t *topk_idx, const float *
     p.grouped = grouped;
     p.B = B;
     p.slot_cols = ep.maxc;
+    p.wbox_rows = (mode == MODE_GATEUP) ? 64 : 128;
+    p.xbox_rows = grouped ? XBOX_ROWS : xb_shared;
     p.E = E;
     p.P = P;
     p.route_map = rm;
@@ -639,11 +692,17 @@ dec_status moe_experts(const dec_bf16 *X, const int32_t *topk_idx, const float *
     p.w_group_rows = 2 * I;
     p.up_row_off = I;
     p.A = As;
+    p.w_base = reinterpret_cast<const uint8_t *>(Wgu_shared);
+    p.w_rows = 2LL * I;
+    p.l2pf_kb = l2_prefetch_kblocks();
     if ((ce = engine(m_wgus, m_x, p, sst)) != cudaSuccess) return DEC_ERR_CUDA;
     base(p, MODE_DOWN, H, I, ep.Td, ep.KBd, gs < ep.Td * ep.KBd ? gs : ep.Td * ep.KBd, 0,
          overlap ? ep.side_part_off : ep.main_part_off, overlap ? ep.side_cnt_off : ep.main_cnt_off);
     p.w_group_rows = H;
     p.Yp = S;
+    p.w_base = reinterpret_cast<const uint8_t *>(Wd_shared);
+    p.w_rows = H;
+    p.l2pf_kb = l2_prefetch_kblocks();
     if ((ce = engine(m_wds, m_as, p, sst)) != cudaSuccess) return DEC_ERR_CUDA;
     if (overlap && (ce = cudaEventRecord(ev->join, ss)) != cudaSuccess) return DEC_ERR_CUDA;
   }
@@ -736,7 +795,7 @@ extern "C" dec_status dec_splitk_gemm_noalloc(const dec_bf16 *X, const dec_bf16 
   if (!plan_splitk(B, N, K, 0, d->num_sms, &pl)) return DEC_ERR_UNSUPPORTED_SHAPE;
   if (pl.total > kNoAllocScratchBytes) return DEC_ERR_WORKSPACE_TOO_SMALL;
   CUtensorMap wmap, xmap;
-  if (!make_map(&wmap, W, K, N, WBOX_ROWS) || !make_map(&xmap, X, K, B, XBOX_ROWS))
+  if (!make_map(&wmap, W, K, N, 128) || !make_map(&xmap, X, K, B, xbox_rows_for(pl.maxc)))
     return DEC_ERR_CUDA;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
   // The array keeps whatever the previous call left; the arrival counters must start

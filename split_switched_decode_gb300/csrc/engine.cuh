@@ -88,6 +88,52 @@ __device__ __forceinline__ int seg_xboxes(const SegInfo &s) {
   return s.ncols > 16 ? (s.ncols + 15) >> 4 : 1;
 }
 
+// Bytes one stage receives: the 128-row weight tile plus the activation boxes.
+__device__ __forceinline__ uint32_t stage_tx_bytes(const EngineParams &p, const SegInfo &s) {
+  const int nxb = (16 * seg_xboxes(s) + p.xbox_rows - 1) / p.xbox_rows;
+  return 16384u + static_cast<uint32_t>(nxb * p.xbox_rows) * 128u;
+}
+
+// Weight boxes of one k-block: one 128-row box, or the 64 gate rows and the 64 matching
+// up rows (two boxes) in gate/up mode.
+__device__ __forceinline__ void load_weights(const EngineParams &p, const SegInfo &s,
+                                             const CUtensorMap *wmap, uint8_t *dst,
+                                             uint64_t *bar, int kb, uint64_t pol) {
+  tma_load_2d_evict_first(dst, wmap, bar, kb * TILE_K, s.wrow0, pol);
+  if (p.wbox_rows == 64)
+    tma_load_2d_evict_first(dst + 8192, wmap, bar, kb * TILE_K, s.wrow1, pol);
+}
+
+// Before the dependency wait, while the previous kernel of the stream is still
+// finishing and HBM is underused, the producer warp asks L2 for the next l2pf_kb
+// k-blocks of this CTA's weights beyond the ones already requested into shared memory
+// (one bulk prefetch per weight row and segment; weights only, so this may precede the
+// wait). The later TMA loads of those blocks then hit L2.
+__device__ __forceinline__ void prefetch_weights_l2(const EngineParams &p, int64_t begin,
+                                                    int64_t end, uint32_t skip, int lane) {
+  if (p.l2pf_kb <= 0 || p.w_base == nullptr) return;
+  const long long row_bytes = static_cast<long long>(p.K) * 2;
+  int64_t it = begin + skip;
+  int64_t stop = it + p.l2pf_kb;
+  if (stop > end) stop = end;
+  while (it < stop) {
+    SegInfo s;
+    seg_info(p, it, stop, s);
+    const long long k0 = static_cast<long long>(s.kb0) * TILE_K * 2;
+    long long k1 = static_cast<long long>(s.kb1) * TILE_K * 2;
+    if (k1 > row_bytes) k1 = row_bytes;
+    if (k1 > k0) {
+      for (int r = lane; r < TILE_N; r += 32) {
+        const long long row = (r < 64) ? s.wrow0 + r
+                                        : (p.wbox_rows == 64 ? s.wrow1 + (r - 64) : s.wrow0 + r);
+        if (row < p.w_rows)
+          prefetch_l2_bulk(p.w_base + row * row_bytes + k0, static_cast<uint32_t>(k1 - k0));
+      }
+    }
+    it += s.kb1 - s.kb0;
+  }
+}
+
 // TMA producer of both engines, run by one thread. The weight boxes of the first
 // STAGES k-blocks do not depend on the previous kernel of the stream, so for a
 // projection they are issued before griddep_wait (programmatic dependent launch); the
@@ -106,12 +152,11 @@ __device__ __forceinline__ void engine_produce(const EngineParams &p, const CUte
     for (int64_t it = begin; it < end && pre < STAGES;) {
       SegInfo s;
       seg_info(p, it, end, s);
-      const uint32_t bytes = 16384u + static_cast<uint32_t>(seg_xboxes(s)) * 2048u;
+      const uint32_t bytes = stage_tx_bytes(p, s);
       for (int kb = s.kb0; kb < s.kb1 && pre < STAGES; ++kb, ++pre) {
         uint8_t *dst = stage_mem + pre * STAGE_BYTES;
         mbar_arrive_expect_tx(&full[pre], bytes);  // first use of the stage: it is empty
-        tma_load_2d_evict_first(dst, wmap, &full[pre], kb * TILE_K, s.wrow0, pol);
-        tma_load_2d_evict_first(dst + 8192, wmap, &full[pre], kb * TILE_K, s.wrow1, pol);
+        load_weights(p, s, wmap, dst, &full[pre], kb, pol);
       }
       it += s.kb1 - s.kb0;
     }
@@ -122,8 +167,8 @@ __device__ __forceinline__ void engine_produce(const EngineParams &p, const CUte
   for (int64_t it = begin; it < end && ok;) {
     SegInfo s;
     seg_info(p, it, end, s);
-    const int nxb = seg_xboxes(s);
-    const uint32_t bytes = 16384u + static_cast<uint32_t>(nxb) * 2048u;
+    const int nxb = (16 * seg_xboxes(s) + p.xbox_rows - 1) / p.xbox_rows;
+    const uint32_t bytes = stage_tx_bytes(p, s);
     for (int kb = s.kb0; kb < s.kb1; ++kb, ++q) {
       const int st = static_cast<int>(q % STAGES);
       uint8_t *dst = stage_mem + st * STAGE_BYTES;
@@ -134,11 +179,11 @@ __device__ __forceinline__ void engine_produce(const EngineParams &p, const CUte
           break;
         }
         mbar_arrive_expect_tx(&full[st], bytes);
-        tma_load_2d_evict_first(dst, wmap, &full[st], kb * TILE_K, s.wrow0, pol);
-        tma_load_2d_evict_first(dst + 8192, wmap, &full[st], kb * TILE_K, s.wrow1, pol);
+        load_weights(p, s, wmap, dst, &full[st], kb, pol);
       }
       for (int i = 0; i < nxb; ++i)
-        tma_load_2d(dst + 16384 + i * 2048, xmap, &full[st], kb * TILE_K, s.xrow0 + XBOX_ROWS * i);
+        tma_load_2d(dst + 16384 + i * p.xbox_rows * 128, xmap, &full[st], kb * TILE_K,
+                    s.xrow0 + p.xbox_rows * i);
     }
     it += s.kb1 - s.kb0;
   }

@@ -109,6 +109,7 @@ __global__ void __launch_bounds__(CC_THREADS, 1)
 
   if (warp == 8) {
     // ---------------------------------------------------------------- producer
+    if (!p.grouped) prefetch_weights_l2(p, begin, end, C::STAGES, lane);
     if (lane == 0)
       engine_produce<C::STAGES, C::STAGE_BYTES>(p, &wmap, &xmap, stage_mem, full, empty, flags,
                                                 begin, end);

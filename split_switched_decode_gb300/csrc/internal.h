@@ -22,6 +22,11 @@ struct EngineParams {
   int up_row_off;    // GATEUP: row offset of the up half inside a group (= I)
   int slot_cols;     // columns per partial slot (slot = 128 * slot_cols floats)
   int defer;         // 1: store every segment's partial tile and stop (MODE_FRONT)
+  int wbox_rows;     // rows per weight TMA box: 128 (one box per tile) or 64 (gate/up)
+  const uint8_t *w_base;  // weight matrix (raw pointer, for L2 prefetch)
+  long long w_rows;       // rows of the weight matrix (all groups)
+  int l2pf_kb;            // k-blocks beyond the smem ring prefetched to L2 before the wait
+  int xbox_rows;     // rows per activation TMA box: 16, or 16 x boxes of the widest group
   int E;             // experts (grouped route map, FRONT router rows)
   int P;             // B * topk (grouped route map)
   const int32_t *route_map;  // grouped: counts | offsets | pairs | pos | num_used | used
@@ -94,10 +99,21 @@ struct FrontFinishParams {
   float *topk_w;
   float *probs;
   int32_t *route_map;
-  int *tok_done;  // [B], zero between launches
   int *all_done;  // [1], zero between launches
 };
 cudaError_t launch_front_finish(const FrontFinishParams &f, cudaStream_t s);
+
+// Second half of a deferred split-K projection: adds the partial tiles of every worker
+// in worker order, adds R and rounds to bf16.
+struct LinearFinishParams {
+  const float *partials;
+  int slot_cols, G, T, KB;
+  long long total;
+  int B, N;
+  const uint16_t *R;
+  uint16_t *Y;
+};
+cudaError_t launch_linear_finish(const LinearFinishParams &f, cudaStream_t s);
 cudaError_t launch_gather_rows(const uint16_t *X, const int32_t *route_map, int B, int topk,
                                int E, int K, uint16_t *Xg, cudaStream_t s);
 cudaError_t launch_combine(const float *topk_w, const int32_t *route_map, const float *Yp,

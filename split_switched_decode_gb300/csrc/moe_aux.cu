@@ -41,71 +41,123 @@ __global__ void __launch_bounds__(256) route_map_kernel(const int32_t *topk_idx,
   build_route_map(sidx, B, topk, E, rm, smask, soff, 256, 1, threadIdx.x);
 }
 
+// Contributors of tile t of a split of `total` iterations (KB per tile) over G workers
+// (each worker spans at most two tiles): workers first..last, and the slot that holds
+// the first worker's part (0 when its range starts inside the tile, else 1; the later
+// workers all start inside it).
+struct TileContrib {
+  int first, last, which_first;
+};
+__device__ __forceinline__ TileContrib tile_contrib(int t, int KB, int G, long long total) {
+  const long long tb = static_cast<long long>(t) * KB;
+  TileContrib c;
+  c.first = static_cast<int>(((tb + 1) * G - 1) / total);
+  c.last = static_cast<int>(((tb + KB) * G - 1) / total);
+  c.which_first = (static_cast<long long>(c.first) * total / G >= tb) ? 0 : 1;
+  return c;
+}
+
+// Sum in worker order of element `off` (column * 128 + row) of tile t's partial slots.
+__device__ __forceinline__ float sum_partials(const float *partials, size_t slot_floats,
+                                              const TileContrib &c, size_t off) {
+  constexpr int D = 8;
+  float z = 0.f;
+  for (int wk0 = c.first; wk0 <= c.last; wk0 += D) {
+    float part[D];
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+      const int wk = wk0 + d;
+      const int which = (wk == c.first) ? c.which_first : 0;
+      part[d] = (wk <= c.last)
+                    ? __ldcg(partials + static_cast<size_t>(wk * 2 + which) * slot_floats + off)
+                    : 0.f;
+    }
+#pragma unroll
+    for (int d = 0; d < D; ++d)
+      if (wk0 + d <= c.last) z += part[d];
+  }
+  return z;
+}
+
 // Second half of the MoE front end, launched programmatically after the router +
-// latent product (which only stored its partial tiles). CTA (t, b) owns rows
-// t*128 .. t*128+127 of token b: thread r adds row r's partials of every worker that
-// contributed to tile t, in worker order (the split of the product kernel, recomputed
-// here), with all loads issued together. Router rows go to the fp32 logits, latent
-// rows to bf16. The CTA that completes a token's last router tile (acquire-release
-// counter per token) routes that token with one warp; the CTA that routes the last
-// token builds the route map. Spread over T*B CTAs, the reduction and the routing take
-// one memory round trip each instead of one CTA per tile adding tens of partial tiles.
-__global__ void __launch_bounds__(128) front_finish_kernel(const FrontFinishParams f) {
+// latent product (which only stored its partial tiles). CTA (c, b) owns rows
+// 512c .. 512c+511 of token b; thread i adds row 512c+i's partials of every worker of
+// its tile in worker order (the product kernel's split, recomputed here) with all
+// loads in flight. Latent rows go out as bf16. CTA (0, b) holds all E <= 512 router
+// logits of token b in shared memory and routes the token with one warp; the CTA that
+// routes the last token (acquire-release counter) builds the route map. Spread over
+// B * ceil((E+L)/512) CTAs, the reduction costs one memory round trip.
+__global__ void __launch_bounds__(512) front_finish_kernel(const FrontFinishParams f) {
+  __shared__ float slog[MAX_E];
   __shared__ int32_t sidx[MAX_B * MAX_TOPK];
   __shared__ unsigned long long smask[MAX_E];
   __shared__ int soff[MAX_E];
   __shared__ int flag;
   griddep_wait();
   griddep_launch_dependents();
-  const int t = blockIdx.x, b = blockIdx.y, r = threadIdx.x;
-  const int n = t * 128 + r;
-  const int64_t tb = static_cast<int64_t>(t) * f.KB;
-  const int first = static_cast<int>(((tb + 1) * f.G - 1) / f.total);
-  const int last = static_cast<int>(((tb + f.KB) * f.G - 1) / f.total);
-  const int which_first = (static_cast<int64_t>(first) * f.total / f.G >= tb) ? 0 : 1;
+  const int c = blockIdx.x, b = blockIdx.y, i = threadIdx.x;
+  const int n = c * 512 + i;
   const size_t slot_floats = static_cast<size_t>(128) * f.slot_cols;
-  const float *base = f.partials + static_cast<size_t>(b) * 128 + r;
-  float z = 0.f;
-  constexpr int D = 8;
-  for (int wk0 = first; wk0 <= last; wk0 += D) {
-    float part[D];
-#pragma unroll
-    for (int d = 0; d < D; ++d) {
-      const int wk = wk0 + d;
-      const int which = (wk == first) ? which_first : 0;
-      part[d] = (wk <= last) ? __ldcg(base + static_cast<size_t>(wk * 2 + which) * slot_floats)
-                             : 0.f;
+  if (n < f.E + f.L) {
+    const TileContrib tc = tile_contrib(n >> 7, f.KB, f.G, f.total);
+    const float z =
+        sum_partials(f.partials, slot_floats, tc, static_cast<size_t>(b) * 128 + (n & 127));
+    if (n < f.E) {
+      slog[n] = z;
+      f.logits[static_cast<size_t>(b) * f.E + n] = z;
+    } else {
+      f.latent[static_cast<size_t>(b) * f.L + (n - f.E)] = f32_to_bf16_rn(z);
     }
-#pragma unroll
-    for (int d = 0; d < D; ++d)
-      if (wk0 + d <= last) z += part[d];
   }
-  if (n < f.E)
-    f.logits[static_cast<size_t>(b) * f.E + n] = z;
-  else if (n < f.E + f.L)
-    f.latent[static_cast<size_t>(b) * f.L + (n - f.E)] = f32_to_bf16_rn(z);
-  const int t_router = (f.E + 127) / 128;
-  if (t >= t_router) return;  // latent tile: done (uniform per CTA)
+  if (c != 0) return;  // only the chunk holding the router rows routes (uniform per CTA)
   __syncthreads();
-  if (r == 0) flag = (atom_add_acq_rel_gpu(&f.tok_done[b], 1) == t_router - 1);
-  __syncthreads();
-  if (!flag) return;
-  if (r < 32) {
-    route_tokens_warp(f.logits + static_cast<size_t>(b) * f.E, 1, f.E, f.topk,
-                      f.topk_idx + static_cast<size_t>(b) * f.topk,
+  if (i < 32)
+    route_tokens_warp(slog, 1, f.E, f.topk, f.topk_idx + static_cast<size_t>(b) * f.topk,
                       f.topk_w + static_cast<size_t>(b) * f.topk,
                       f.probs ? f.probs + static_cast<size_t>(b) * f.E : nullptr, nullptr, 0, 1);
-  }
-  if (r == 0) f.tok_done[b] = 0;
   if (f.route_map == nullptr) return;
   __syncthreads();
-  if (r == 0) flag = (atom_add_acq_rel_gpu(f.all_done, 1) == f.B - 1);
+  if (i == 0) flag = (atom_add_acq_rel_gpu(f.all_done, 1) == f.B - 1);
   __syncthreads();
   if (!flag) return;
-  for (int q = r; q < f.B * f.topk; q += 128) sidx[q] = __ldcg(f.topk_idx + q);
+  for (int q = i; q < f.B * f.topk; q += 512) sidx[q] = __ldcg(f.topk_idx + q);
   __syncthreads();
-  build_route_map(sidx, f.B, f.topk, f.E, f.route_map, smask, soff, 128, 1, r);
-  if (r == 0) *f.all_done = 0;
+  build_route_map(sidx, f.B, f.topk, f.E, f.route_map, smask, soff, 512, 1, i);
+  if (i == 0) *f.all_done = 0;
+}
+
+// Second half of a deferred split-K projection (launched programmatically): CTA
+// (t, cb) owns rows t*128 .. t*128+127 and batch columns 16cb .. 16cb+15; thread r adds
+// row r's partials in worker order, adds the residual and rounds once to bf16.
+__global__ void __launch_bounds__(128) linear_finish_kernel(const LinearFinishParams f) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int t = blockIdx.x, j0 = blockIdx.y * 16, r = threadIdx.x;
+  const int n = t * 128 + r;
+  const TileContrib tc = tile_contrib(t, f.KB, f.G, f.total);
+  const size_t slot_floats = static_cast<size_t>(128) * f.slot_cols;
+  float z[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) z[j] = 0.f;
+  for (int wk = tc.first; wk <= tc.last; ++wk) {
+    const int which = (wk == tc.first) ? tc.which_first : 0;
+    const float *sl = f.partials + static_cast<size_t>(wk * 2 + which) * slot_floats + r;
+    float part[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      part[j] = (j0 + j < f.B) ? __ldcg(sl + static_cast<size_t>(j0 + j) * 128) : 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) z[j] += part[j];
+  }
+  if (n >= f.N) return;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    if (j0 + j < f.B) {
+      float y = z[j];
+      if (f.R != nullptr) y += bf16_to_f32(f.R[static_cast<size_t>(j0 + j) * f.N + n]);
+      f.Y[static_cast<size_t>(j0 + j) * f.N + n] = f32_to_bf16_rn(y);
+    }
+  }
 }
 
 // Xg[q, :] = X[pairs[q] / topk, :] -- the activation rows of every (token, slot) entry
@@ -203,7 +255,11 @@ cudaError_t launch_route_map_rebuild(const int32_t *topk_idx, int B, int topk, i
 }
 
 cudaError_t launch_front_finish(const FrontFinishParams &f, cudaStream_t s) {
-  return launch_pdl(front_finish_kernel, dim3(f.T, f.B), dim3(128), 0, s, f);
+  return launch_pdl(front_finish_kernel, dim3((f.E + f.L + 511) / 512, f.B), dim3(512), 0, s, f);
+}
+
+cudaError_t launch_linear_finish(const LinearFinishParams &f, cudaStream_t s) {
+  return launch_pdl(linear_finish_kernel, dim3(f.T, (f.B + 15) / 16), dim3(128), 0, s, f);
 }
 
 cudaError_t launch_gather_rows(const uint16_t *X, const int32_t *route_map, int B, int topk,

@@ -240,3 +240,25 @@ def test_bounded_wait_reports_timeout_and_context_survives(env):
     ssd.dec_splitk_gemm(X, W, R, Y, ws)
     torch.cuda.synchronize()
     assert_close(to_f64(oracle, Y), _oracle_rows(env, X, W, R), "after time-out")
+
+
+@pytest.mark.parametrize("B,N,K,residual", [(32, 8192, 12288, False), (64, 7168, 16384, True),
+                                            (17, 300, 12288, True), (64, 130, 16384, False)])
+@pytest.mark.parametrize("tc", [0, 1])
+def test_deferred_reduction_matches_oracle(env, monkeypatch, B, N, K, residual, tc):
+    """Split-K with the reduction deferred to the finishing kernel (the large-batch path),
+    forced on at every batch; bit-identical on repeat."""
+    torch, ssd, oracle, dev = env
+    monkeypatch.setenv("DEC_DEFER_MIN_B", "1")
+    X, W, R, Y = _case(env, B, N, K, 14, residual=residual)
+    ws = ssd.workspace(ssd.dec_splitk_workspace_bytes(B, N, K, 0), dev)
+    ssd.dec_splitk_gemm(X, W, R, Y, ws, use_tc=tc)
+    torch.cuda.synchronize()
+    Y1 = Y.clone()
+    ssd.dec_splitk_gemm(X, W, R, Y, ws, use_tc=tc)
+    torch.cuda.synchronize()
+    assert torch.equal(Y, Y1)
+    rng = np.random.default_rng(B + N)
+    rows = np.unique(np.concatenate([rng.choice(N, min(N, 256), replace=False), [0, N - 1]]))
+    y_ref = _oracle_rows(env, X, W, R, rows)
+    assert_close(to_f64(oracle, Y)[:, rows], y_ref, f"deferred B={B} N={N} K={K} tc={tc}")
