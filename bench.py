@@ -347,6 +347,19 @@ def max_over_ranks(torch, world, x, dev):
     return float(t.item())
 
 
+def aggregate_replicas(torch, world, ms_local, bytes_local, dev):
+    """Whole-job figures of N independent replicas: the step time is the slowest rank's,
+    the bytes are every rank's. Returns (ms_max, total_bytes, GB/s)."""
+    ms = max_over_ranks(torch, world, ms_local, dev)
+    total = bytes_local
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([float(bytes_local)], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.SUM)
+        total = float(t.item())
+    return ms, total, total / (ms * 1e-3) / 1e9
+
+
 def barrier(torch, world):
     if world > 1:
         import torch.distributed as dist
@@ -467,8 +480,7 @@ def main():
     barrier(torch, world)
     clocks = clk.stop()
     ms = a.elapsed_time(b) / args.steps
-    ms = max_over_ranks(torch, world, ms, dev)
-    value = step_bytes * world / (ms * 1e-3) / 1e9
+    ms, _, value = aggregate_replicas(torch, world, ms, step_bytes, dev)
     assert ssd.dec_sync_status() == ssd.DEC_OK
     if args.step_only:
         if rank == 0:
@@ -513,8 +525,9 @@ def main():
             e2e_step()
         eb.record(st)
         torch.cuda.synchronize()
-        ems = max_over_ranks(torch, world, ea.elapsed_time(eb) / args.steps, dev)
-        e2e = {"value": step_bytes * world / (ems * 1e-3) / 1e9, "unit": "GB/s",
+        ems, _, evalue = aggregate_replicas(torch, world, ea.elapsed_time(eb) / args.steps,
+                                            step_bytes, dev)
+        e2e = {"value": evalue, "unit": "GB/s",
                "ms_per_step": ems, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "path": "eager public-API calls, pinned host inputs/outputs copied every step"}
 
