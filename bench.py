@@ -199,7 +199,8 @@ class Workload:
         self.ssd.dec_linear(d["x_o"], self.W_o[rot % len(self.W_o)], d["r_o"], d["y_o"], d["ws_o"])
         self.launches += 1
 
-    def op_front(self, B, rot=0, v=0, prefetch=True):
+    def op_front(self, B, rot=0, v=0, prefetch=True, with_map=False):
+        """moe_front; the route map is left to moe_experts' gather launch unless with_map."""
         torch, ssd, d = self.torch, self.ssd, self.t[B]
         if prefetch:
             main = torch.cuda.current_stream()
@@ -208,12 +209,14 @@ class Workload:
             ssd.l2_prefetch(self.Wgs, nbytes=PREFETCH_BYTES, max_ctas=8, stream=self.side)
             self.launches += 1
         ssd.moe_front(d["x_moe"][v], self.W_cat[rot % len(self.W_cat)], self.E, L, TOPK, d["lat"][v],
-                      d["idx"][v], d["w"][v], d["ws_f"], route_map=d["rm"][v])
+                      d["idx"][v], d["w"][v], d["ws_f"],
+                      route_map=d["rm"][v] if with_map else None)
         self.launches += 1
 
     def op_experts(self, B, v=0):
         d = self.t[B]
-        self.ssd.moe_experts(d["x_moe"][v], d["idx"][v], d["w"][v], d["rm"][v], self.Wgu, self.Wd,
+        # no route map: the gather launch validates topk_idx and builds it
+        self.ssd.moe_experts(d["x_moe"][v], d["idx"][v], d["w"][v], None, self.Wgu, self.Wd,
                              self.Wgs, self.Wds, d["y_moe"], d["ws_e"], side_stream=self.side)
         self.launches += 6  # gather, shared gate/up + down, routed gate/up + down, combine
 
@@ -418,7 +421,7 @@ def main():
     # routing of every X set (fixed inputs -> fixed routing -> fixed bytes)
     for B in batches:
         for v in range(3):
-            wl.op_front(B, v=v, prefetch=False)
+            wl.op_front(B, v=v, prefetch=False, with_map=True)
     torch.cuda.synchronize()
 
     # ---- per-operation sweep: graphs of R calls over rotating weight copies

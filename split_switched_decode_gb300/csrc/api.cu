@@ -708,11 +708,11 @@ dec_status moe_experts(const dec_bf16 *X, const int32_t *topk_idx, const float *
   }
 
   // ---- routed experts, main stream
-  if (!route_map) {
-    if ((ce = launch_route_map_rebuild(topk_idx, B, topk, E, rm, d->status, ms)) != cudaSuccess)
-      return DEC_ERR_CUDA;
-  }
-  if ((ce = launch_gather_rows(X, rm, B, topk, E, H, Xg, ms)) != cudaSuccess) return DEC_ERR_CUDA;
+  // without a caller route map the gather launch validates topk_idx and builds it
+  ce = route_map ? launch_gather_rows(X, rm, B, topk, E, H, Xg, ms)
+                 : launch_gather_map(X, topk_idx, B, topk, E, H, Xg, rm, d->status,
+                                     2 * d->num_sms, ms);
+  if (ce != cudaSuccess) return DEC_ERR_CUDA;
   {
     EngineParams p;
     // G <= T*KB keeps every worker range non-empty even with a single used expert

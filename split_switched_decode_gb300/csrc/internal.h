@@ -84,8 +84,6 @@ cudaError_t launch_gemv_tiny(const uint16_t *X, const uint16_t *W, const uint16_
                              uint16_t *Y, int B, int N, int K, int num_sms, cudaStream_t s);
 
 // --------------------------------------------------------------- moe_aux.cu --
-cudaError_t launch_route_map_rebuild(const int32_t *topk_idx, int B, int topk, int E,
-                                     int32_t *route_map, unsigned *status, cudaStream_t s);
 // Second half of the front end: adds the product's partial tiles in worker order,
 // writes logits and latent, routes each token and builds the route map.
 struct FrontFinishParams {
@@ -114,6 +112,11 @@ struct LinearFinishParams {
   uint16_t *Y;
 };
 cudaError_t launch_linear_finish(const LinearFinishParams &f, cudaStream_t s);
+// Validates topk_idx, builds the route map (written to route_map) and gathers in one
+// launch of at most max_ctas CTAs.
+cudaError_t launch_gather_map(const uint16_t *X, const int32_t *topk_idx, int B, int topk, int E,
+                              int K, uint16_t *Xg, int32_t *route_map, unsigned *status,
+                              int max_ctas, cudaStream_t s);
 cudaError_t launch_gather_rows(const uint16_t *X, const int32_t *route_map, int B, int topk,
                                int E, int K, uint16_t *Xg, cudaStream_t s);
 cudaError_t launch_combine(const float *topk_w, const int32_t *route_map, const float *Yp,

@@ -8,37 +8,88 @@ namespace ssd {
 
 namespace {
 
-// Rebuild the route map from topk_idx when the caller did not keep moe_front's.
-// Caller indices are validated first (0 <= e < E, distinct within a token); any
-// violation yields an empty map (no used expert, zeros elsewhere) and ST_BAD_ROUTING.
-__global__ void __launch_bounds__(256) route_map_kernel(const int32_t *topk_idx, int B, int topk,
-                                                        int E, int32_t *rm, unsigned *status) {
-  griddep_wait();
-  griddep_launch_dependents();
-  __shared__ int32_t sidx[MAX_B * MAX_TOPK];
-  __shared__ unsigned long long smask[MAX_E];
-  __shared__ int soff[MAX_E];
-  __shared__ int bad;
-  if (threadIdx.x == 0) bad = 0;
+// Copy the caller's topk_idx [B*topk] into shared `sidx` and check it (0 <= e < E,
+// distinct within a token). Run by all 256 threads of the CTA; `bad` is a shared flag.
+// Returns the same verdict in every thread.
+__device__ __forceinline__ bool load_routing(const int32_t *topk_idx, int B, int topk, int E,
+                                             int32_t *sidx, volatile int *bad) {
+  if (threadIdx.x == 0) *bad = 0;
   __syncthreads();
   for (int q = threadIdx.x; q < B * topk; q += 256) {
     const int e = topk_idx[q];
     sidx[q] = e;
-    if (e < 0 || e >= E) bad = 1;
+    if (e < 0 || e >= E) *bad = 1;
   }
   __syncthreads();
   for (int b = threadIdx.x; b < B; b += 256)
     for (int i = 0; i < topk; ++i)
       for (int j = i + 1; j < topk; ++j)
-        if (sidx[b * topk + i] == sidx[b * topk + j]) bad = 1;
+        if (sidx[b * topk + i] == sidx[b * topk + j]) *bad = 1;
   __syncthreads();
-  if (bad) {
-    const int n = 3 * E + 2 + 2 * B * topk;
-    for (int i = threadIdx.x; i < n; i += 256) rm[i] = 0;
-    if (threadIdx.x == 0) atomicOr(status, ST_BAD_ROUTING);
+  return *bad == 0;
+}
+
+// An invalid routing yields an empty map (no used expert, zeros elsewhere) and
+// ST_BAD_ROUTING, so no later launch reads a weight or row out of range.
+__device__ __forceinline__ void empty_route_map(int B, int topk, int E, int32_t *rm,
+                                                unsigned *status) {
+  const int n = 3 * E + 2 + 2 * B * topk;
+  for (int i = threadIdx.x; i < n; i += 256) rm[i] = 0;
+  if (threadIdx.x == 0) atomicOr(status, ST_BAD_ROUTING);
+}
+
+// Routed-expert gather for a caller without a route map, in one launch: every CTA
+// validates topk_idx and builds the whole route map in shared memory (a few KB, cheaper
+// than a second launch and its memory round trip), CTA 0 publishes it to rm for the
+// grouped launches and the combine, and every CTA copies its share of the rows
+// Xg[q, :] = X[pairs[q] / topk, :] with UNR independent 16-byte loads in flight per thread.
+__global__ void __launch_bounds__(256) gather_map_kernel(const uint16_t *X,
+                                                         const int32_t *topk_idx, int B,
+                                                         int topk, int E, int K, uint16_t *Xg,
+                                                         int32_t *rm, unsigned *status) {
+  griddep_wait();
+  griddep_launch_dependents();
+  __shared__ int32_t sidx[MAX_B * MAX_TOPK];
+  __shared__ unsigned long long smask[MAX_E];
+  __shared__ int soff[MAX_E];
+  __shared__ int32_t smap[3 * MAX_E + 2 + 2 * MAX_B * MAX_TOPK];
+  __shared__ int bad;
+  if (!load_routing(topk_idx, B, topk, E, sidx, &bad)) {
+    if (blockIdx.x == 0) empty_route_map(B, topk, E, rm, status);
     return;
   }
-  build_route_map(sidx, B, topk, E, rm, smask, soff, 256, 1, threadIdx.x);
+  build_route_map(sidx, B, topk, E, smap, smask, soff, 256, 1, threadIdx.x);
+  __syncthreads();
+  const int P = B * topk;
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < 3 * E + 2 + 2 * P; i += 256) rm[i] = smap[i];
+  const int32_t *pairs = smap + 2 * E + 1;
+  const int chunks = K / 8;  // 16-byte chunks per row
+  const int64_t n = static_cast<int64_t>(P) * chunks;
+  constexpr int UNR = 4;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * 256;
+  for (int64_t i0 = blockIdx.x * 256ll + threadIdx.x; i0 < n; i0 += stride * UNR) {
+    uint4 v[UNR];
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const int64_t i = i0 + u * stride;
+      if (i < n) {
+        const int q = static_cast<int>(i / chunks);
+        const int c = static_cast<int>(i - static_cast<int64_t>(q) * chunks);
+        const int b = pairs[q] / topk;  // a valid map: 0 <= b < B
+        v[u] = reinterpret_cast<const uint4 *>(X + static_cast<size_t>(b) * K)[c];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const int64_t i = i0 + u * stride;
+      if (i < n) {
+        const int q = static_cast<int>(i / chunks);
+        const int c = static_cast<int>(i - static_cast<int64_t>(q) * chunks);
+        reinterpret_cast<uint4 *>(Xg + static_cast<size_t>(q) * K)[c] = v[u];
+      }
+    }
+  }
 }
 
 // Contributors of tile t of a split of `total` iterations (KB per tile) over G workers
@@ -60,7 +111,7 @@ __device__ __forceinline__ TileContrib tile_contrib(int t, int KB, int G, long l
 // Sum in worker order of element `off` (column * 128 + row) of tile t's partial slots.
 __device__ __forceinline__ float sum_partials(const float *partials, size_t slot_floats,
                                               const TileContrib &c, size_t off) {
-  constexpr int D = 8;
+  constexpr int D = 32;  // a front tile has ~G*KB/total + 1 contributors: all in flight
   float z = 0.f;
   for (int wk0 = c.first; wk0 <= c.last; wk0 += D) {
     float part[D];
@@ -248,18 +299,23 @@ __global__ void wait_selftest_kernel(unsigned *status, uint64_t limit_ns) {
 
 }  // namespace
 
-cudaError_t launch_route_map_rebuild(const int32_t *topk_idx, int B, int topk, int E,
-                                     int32_t *route_map, unsigned *status, cudaStream_t s) {
-  return launch_pdl(route_map_kernel, dim3(1), dim3(256), 0, s, topk_idx, B, topk, E, route_map,
-                    status);
-}
-
 cudaError_t launch_front_finish(const FrontFinishParams &f, cudaStream_t s) {
   return launch_pdl(front_finish_kernel, dim3((f.E + f.L + 511) / 512, f.B), dim3(512), 0, s, f);
 }
 
 cudaError_t launch_linear_finish(const LinearFinishParams &f, cudaStream_t s) {
   return launch_pdl(linear_finish_kernel, dim3(f.T, (f.B + 15) / 16), dim3(128), 0, s, f);
+}
+
+cudaError_t launch_gather_map(const uint16_t *X, const int32_t *topk_idx, int B, int topk, int E,
+                              int K, uint16_t *Xg, int32_t *route_map, unsigned *status,
+                              int max_ctas, cudaStream_t s) {
+  const int64_t n = static_cast<int64_t>(B) * topk * (K / 8);
+  int64_t need = (n + 1023) / 1024;  // 256 threads x 4 chunks per CTA and sweep
+  int grid = static_cast<int>(need < max_ctas ? need : max_ctas);
+  if (grid < 1) grid = 1;
+  return launch_pdl(gather_map_kernel, dim3(grid), dim3(256), 0, s, X, topk_idx, B, topk, E, K,
+                    Xg, route_map, status);
 }
 
 cudaError_t launch_gather_rows(const uint16_t *X, const int32_t *route_map, int B, int topk,
