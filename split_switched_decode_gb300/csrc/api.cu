@@ -247,6 +247,7 @@ dec_status run_splitk(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 *R, d
   fill_engine_common(p, pl, MODE_LINEAR, N, K, B, ws, d);
   p.Y = Y;
   p.R = R;
+  p.vec_y = (N % 8 == 0 && aligned16(Y) && (R == nullptr || aligned16(R))) ? 1 : 0;
   p.w_base = reinterpret_cast<const uint8_t *>(W);
   p.w_rows = N;
   // Large batches: the product kernel only stores partial tiles and a finishing kernel
@@ -807,6 +808,7 @@ extern "C" dec_status dec_splitk_gemm_noalloc(const dec_bf16 *X, const dec_bf16 
   fill_engine_common(p, pl, MODE_LINEAR, N, K, B, nd.scratch, d);
   p.Y = Y;
   p.R = R;
+  p.vec_y = (N % 8 == 0 && aligned16(Y) && (R == nullptr || aligned16(R))) ? 1 : 0;
   if (consume_fault()) return DEC_ERR_CUDA;
   ce = use_tc ? launch_engine_tc(pl.maxc, wmap, xmap, p, cs)
               : launch_engine_cc(pl.maxc, wmap, xmap, p, cs);

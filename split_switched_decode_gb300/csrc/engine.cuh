@@ -198,6 +198,40 @@ __device__ __forceinline__ void engine_produce(const EngineParams &p, const CUte
   }
 }
 
+// Y rows n0 .. n0+7 of batch column j: y (+ R) rounded once to bf16, one 16-byte store
+// (or element by element for a ragged tail). Requires N % 8 == 0 and 16-byte aligned Y
+// and R (p.vec_y).
+__device__ __forceinline__ void store_y8(const EngineParams &p, int j, int n0, const float4 &a,
+                                         const float4 &b) {
+  float y[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  const size_t off = static_cast<size_t>(j) * p.N + n0;
+  if (n0 + 8 <= p.N) {
+    if (p.R != nullptr) {
+      const uint4 rr = *reinterpret_cast<const uint4 *>(p.R + off);
+      y[0] += bf16lo(rr.x);
+      y[1] += bf16hi(rr.x);
+      y[2] += bf16lo(rr.y);
+      y[3] += bf16hi(rr.y);
+      y[4] += bf16lo(rr.z);
+      y[5] += bf16hi(rr.z);
+      y[6] += bf16lo(rr.w);
+      y[7] += bf16hi(rr.w);
+    }
+    uint4 o;
+    o.x = f32_to_bf16_rn(y[0]) | (static_cast<uint32_t>(f32_to_bf16_rn(y[1])) << 16);
+    o.y = f32_to_bf16_rn(y[2]) | (static_cast<uint32_t>(f32_to_bf16_rn(y[3])) << 16);
+    o.z = f32_to_bf16_rn(y[4]) | (static_cast<uint32_t>(f32_to_bf16_rn(y[5])) << 16);
+    o.w = f32_to_bf16_rn(y[6]) | (static_cast<uint32_t>(f32_to_bf16_rn(y[7])) << 16);
+    *reinterpret_cast<uint4 *>(p.Y + off) = o;
+  } else {
+    for (int e = 0; e < 8 && n0 + e < p.N; ++e) {
+      float ye = y[e];
+      if (p.R != nullptr) ye += bf16_to_f32(p.R[off + e]);
+      p.Y[off + e] = f32_to_bf16_rn(ye);
+    }
+  }
+}
+
 // Split-K reduction of one tile, run by the 128 threads that hold the segment's values
 // (thread r holds row r, columns 0..ncols-1 in v). Returns true when v holds the final
 // tile values on return (whole-tile segment, or this worker arrived last).
@@ -263,7 +297,29 @@ __device__ __forceinline__ bool reduce_tile(const EngineParams &p, const SegInfo
 template <int MAXC>
 __device__ __forceinline__ void epilogue_rows(const EngineParams &p, const SegInfo &s, int r, float (&v)[MAXC],
                               float *scratch, int bar_id, volatile int *flags) {
-  if (p.mode == MODE_LINEAR) {
+  if (p.mode == MODE_LINEAR && p.vec_y) {
+    // Through shared memory, half the columns at a time (scratch holds 128 x MAXC/2
+    // fp32): thread r parks row r, then each thread adds R to and stores runs of 8 rows
+    // of one column with 16-byte accesses. Per-lane 2-byte stores of 64 columns were
+    // the slow part of a wide tile's epilogue.
+    constexpr int CW = MAXC >= 2 ? MAXC / 2 : 1;
+#pragma unroll
+    for (int h = 0; h < MAXC / CW; ++h) {
+      named_bar_sync(bar_id, 128);
+#pragma unroll
+      for (int jj = 0; jj < CW; ++jj)
+        if (h * CW + jj < s.ncols) scratch[jj * 128 + r] = v[h * CW + jj];
+      named_bar_sync(bar_id, 128);
+      for (int c = r; c < CW * 16; c += 128) {
+        const int jj = c >> 4, j = h * CW + jj;
+        const int row8 = (c & 15) * 8, n0 = s.t * 128 + row8;
+        if (j >= s.ncols || n0 >= p.N) continue;
+        const float4 a = *reinterpret_cast<const float4 *>(scratch + jj * 128 + row8);
+        const float4 b = *reinterpret_cast<const float4 *>(scratch + jj * 128 + row8 + 4);
+        store_y8(p, j, n0, a, b);
+      }
+    }
+  } else if (p.mode == MODE_LINEAR) {
     const int n = s.t * 128 + r;
     if (n < p.N) {
 #pragma unroll

@@ -262,3 +262,24 @@ def test_deferred_reduction_matches_oracle(env, monkeypatch, B, N, K, residual, 
     rows = np.unique(np.concatenate([rng.choice(N, min(N, 256), replace=False), [0, N - 1]]))
     y_ref = _oracle_rows(env, X, W, R, rows)
     assert_close(to_f64(oracle, Y)[:, rows], y_ref, f"deferred B={B} N={N} K={K} tc={tc}")
+
+
+@pytest.mark.parametrize("B,N,K", [(16, 1024, 512), (64, 2048, 1024), (5, 1000, 256)])
+@pytest.mark.parametrize("shift_y,shift_r", [(0, 0), (1, 0), (0, 1)])
+def test_output_alignment_paths(env, B, N, K, shift_y, shift_r):
+    """Y and R one element off a 16-byte boundary take the per-element epilogue; aligned
+    ones the 16-byte one. Both match the oracle and each other bit for bit."""
+    torch, ssd, oracle, dev = env
+    X, W, R, _ = _case(env, B, N, K, 17)
+    Rb = torch.empty(B * N + 8, dtype=torch.bfloat16, device=dev)
+    Rv = Rb[shift_r:shift_r + B * N].view(B, N)
+    Rv.copy_(R)
+    Yb = torch.empty(B * N + 8, dtype=torch.bfloat16, device=dev)
+    Yv = Yb[shift_y:shift_y + B * N].view(B, N)
+    ws = ssd.workspace(ssd.dec_linear_workspace_bytes(B, N, K), dev)
+    ssd.dec_linear(X, W, Rv, Yv, ws)
+    Y0 = torch.empty(B, N, dtype=torch.bfloat16, device=dev)
+    ssd.dec_linear(X, W, R, Y0, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(Yv, Y0)
+    assert_close(to_f64(oracle, Y0), _oracle_rows(env, X, W, R), f"aligned B={B} N={N}")

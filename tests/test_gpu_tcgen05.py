@@ -168,3 +168,22 @@ def test_tensor_core_experts(env, force_tc, B, k):
                                   inputs.bits(Wgu), inputs.bits(Wd), inputs.bits(Wgs),
                                   inputs.bits(Wds))
     assert_close(to_f64(oracle, Y), y_ref, f"tc experts B={B} k={k}")
+
+
+@pytest.mark.parametrize("B,N,K,split_k", [(64, 512, 1024, 7), (64, 384, 1024, 16),
+                                           (33, 300, 2048, 11), (40, 256, 1024, 16),
+                                           (8, 200, 1024, 16), (3, 130, 4096, 64)])
+def test_many_contributor_tiles(env, B, N, K, split_k):
+    """Tiles with many split-K contributors (up to 64), added by the last arriver in
+    worker order; bit-identical on repeat."""
+    torch, ssd, oracle, dev = env
+    X, W, R, Y = _case(env, B, N, K, 16, residual=True)
+    ws = ssd.workspace(ssd.dec_splitk_workspace_bytes(B, N, K, split_k), dev)
+    ssd.dec_splitk_gemm(X, W, R, Y, ws, split_k=split_k, use_tc=1)
+    torch.cuda.synchronize()
+    Y1 = Y.clone()
+    ssd.dec_splitk_gemm(X, W, R, Y, ws, split_k=split_k, use_tc=1)
+    torch.cuda.synchronize()
+    assert ssd.dec_sync_status() == ssd.DEC_OK
+    assert torch.equal(Y, Y1)
+    assert_close(to_f64(oracle, Y), _ref(X, W, R), f"tc B={B} N={N} K={K} S={split_k}")
