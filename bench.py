@@ -63,7 +63,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--ops", default="in,o,front,experts",
-                    help="operations of the sweep (profiling subsets: in,o,front,experts)")
+                    help="operations of the sweep (profiling subsets: in,o,front,experts; "
+                         "pfscen = output projection behind a simulated communication phase)")
     ap.add_argument("--sweep-only", action="store_true",
                     help="only the per-operation sweep (for profiler captures)")
     ap.add_argument("--num-experts", type=int, default=E,
@@ -182,6 +183,7 @@ class Workload:
         self.Wgs, self.Wds = inputs.shared_expert(H, I, dev, seed, "bank_shared")
         self.side = torch.cuda.Stream(device=dev)
         self.fork = torch.cuda.Event()
+        self.join = torch.cuda.Event()
         self.t = {}
         for B in batches:
             d = {}
@@ -283,6 +285,56 @@ def time_graph(torch, g, reps):
         b.synchronize()
         ts.append(a.elapsed_time(b) * 1e3)  # us
     return ts
+
+
+# ------------------------------------------------------- prefetch scenario ----
+
+PF_WAIT_US = 20.0
+
+
+def prefetch_scenario(torch, ssd, wl, batches, reps):
+    """The output projection behind a communication phase, without and with a side-stream
+    L2 prefetch of its weights during that phase ("Part 1 / 4. Prefetching upcoming
+    weights into cache"). The phase is dec_sim_comm_wait (the stream busy, HBM idle);
+    the prefetch pulls the last `prefetch_bytes` of the weight copy read next. Each mode
+    is a graph of R (phase, projection) pairs over the rotating weight copies; the
+    projection's time is the pair's minus the phase's."""
+    ns = int(PF_WAIT_US * 1000)
+    pf_bytes = min(int(PF_WAIT_US * 1e-6 * 5.0e12), int(0.6 * wl.l2)) // 16 * 16
+    R = 12
+    out = {"wait_us": PF_WAIT_US, "prefetch_bytes": pf_bytes, "prefetch_ctas": 64,
+           "weights_bytes": wl.W_o[0].numel() * 2, "per_batch": {}}
+
+    def seq(B, mode):
+        d = wl.t[B]
+        main = torch.cuda.current_stream()
+        for r in range(R):
+            W = wl.W_o[r % len(wl.W_o)]
+            if mode == "prefetch":
+                wl.fork.record(main)
+                wl.side.wait_event(wl.fork)
+                flat = W.view(-1)
+                ssd.l2_prefetch(flat[flat.numel() - pf_bytes // 2:], max_ctas=64, stream=wl.side)
+                wl.join.record(wl.side)
+            ssd.dec_sim_comm_wait(ns)
+            if mode == "prefetch":
+                main.wait_event(wl.join)
+            if mode != "wait":
+                ssd.dec_linear(d["x_o"], W, d["r_o"], d["y_o"], d["ws_o"])
+
+    for B in batches:
+        t = {}
+        for mode in ("wait", "none", "prefetch"):
+            g = capture(torch, lambda: seq(B, mode))
+            t[mode] = statistics.median(time_graph(torch, g, reps)) / R
+            del g
+        nb = bytes_linear(B, H, K_O, True)
+        o_none, o_pf = t["none"] - t["wait"], t["prefetch"] - t["wait"]
+        out["per_batch"][str(B)] = {
+            "phase_us": t["wait"], "o_proj_us_after_phase": o_none,
+            "o_proj_us_with_prefetch": o_pf, "GBps_after_phase": nb / o_none / 1e3,
+            "GBps_with_prefetch": nb / o_pf / 1e3, "speedup": o_none / o_pf}
+    return out
 
 
 # -------------------------------------------------------------- CPU baseline ----
@@ -431,7 +483,7 @@ def main():
     batches = [int(b) for b in args.batches.split(",")]
     ops = set(args.ops.split(","))
     if not args.sweep_only:
-        ops = {"in", "o", "front", "experts"}
+        ops = {"in", "o", "front", "experts", "pfscen"}
     wl = Workload(torch, ssd, inputs, dev, batches, num_experts=args.num_experts,
                   experts="experts" in ops)
     wl.prefetch = not args.no_prefetch
@@ -473,10 +525,15 @@ def main():
             del g
         sweep[str(B)] = row
     torch.cuda.synchronize()
+    pfscen = None
+    if "pfscen" in ops and not args.step_only:
+        pfscen = prefetch_scenario(torch, ssd, wl, [b for b in (1, 64) if b in batches],
+                                   max(3, args.reps))
     if args.sweep_only:
         if rank == 0:
             print(json.dumps({"sweep_only": True, "batches": batches, "ops": sorted(ops),
-                              "num_experts": wl.E, "sweep": sweep}), flush=True)
+                              "num_experts": wl.E, "sweep": sweep,
+                              "prefetch_scenario": pfscen}), flush=True)
         return 0
 
     # ---- the step as one CUDA graph
@@ -590,7 +647,7 @@ def main():
                            "parallelism": f"replicas x{world}"},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": per_step_launches * args.steps, "clocks": clocks,
-                "sweep": sweep}
+                "sweep": sweep, "prefetch_scenario": pfscen}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

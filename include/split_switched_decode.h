@@ -258,6 +258,16 @@ DEC_API dec_status moe_experts(const dec_bf16 *X, const int32_t *topk_idx, const
  */
 DEC_API dec_status l2_prefetch(const void *p, size_t bytes, int max_ctas, dec_stream_t s);
 
+/*
+ * Stand-in for a communication phase, for measuring the prefetch of "Part 1 / 4.
+ * Prefetching upcoming weights into cache" on one GPU (the all-reduce that precedes
+ * the output projection in "Part 1 / 2. Overlap computation and communication" is
+ * multi-GPU): one CTA on `s` that keeps the stream busy for `ns` nanoseconds
+ * (1e3 .. 1e9, else DEC_ERR_INVALID_ARG, nothing launched) by the GPU's global timer
+ * and touches no memory, so HBM is idle meanwhile. It always ends on time.
+ */
+DEC_API dec_status dec_sim_comm_wait(uint64_t ns, dec_stream_t s);
+
 #ifdef __cplusplus
 }
 #endif

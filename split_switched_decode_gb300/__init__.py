@@ -36,7 +36,7 @@ EXPORTS = [
     "dec_sync_status", "dec_debug_wait_timeout", "dec_gemv", "dec_splitk_workspace_bytes",
     "dec_splitk_gemm", "dec_linear_workspace_bytes", "dec_linear", "moe_route_map_ints",
     "moe_front_workspace_bytes", "moe_front", "moe_experts_workspace_bytes", "moe_experts",
-    "l2_prefetch", "dec_splitk_gemm_noalloc",
+    "l2_prefetch", "dec_sim_comm_wait", "dec_splitk_gemm_noalloc",
 ]
 
 _lib = None
@@ -86,6 +86,7 @@ def _load():
         "moe_experts_workspace_bytes": (S, [I, I, I, I, I]),
         "moe_experts": (I, [P, P, P, P, P, P, I, P, P, I, I, I, I, P, P, S, P, P, I]),
         "l2_prefetch": (I, [P, S, I, P]),
+        "dec_sim_comm_wait": (I, [U64, P]),
         "dec_splitk_gemm_noalloc": (I, [P, P, P, P, I, I, I, I, P]),
     }
     for name, (res, args) in sig.items():
@@ -259,3 +260,10 @@ def moe_experts(X, topk_idx, topk_w, route_map, Wgu, Wd, Wgu_shared, Wd_shared, 
 def l2_prefetch(t, nbytes=None, max_ctas=0, stream=None):
     n = t.numel() * t.element_size() if nbytes is None else int(nbytes)
     _check(_load().l2_prefetch(_ptr(t), n, max_ctas, _stream(stream)), "l2_prefetch")
+
+
+def dec_sim_comm_wait(ns: int, stream=None):
+    """Keep `stream` busy for ns nanoseconds without memory traffic (a stand-in for a
+    communication phase)."""
+    _check(_load().dec_sim_comm_wait(int(ns), _stream(stream)), "dec_sim_comm_wait")
+

@@ -748,6 +748,12 @@ dec_status l2_prefetch(const void *p, size_t bytes, int max_ctas, dec_stream_t s
   return cuda_status(launch_l2_prefetch(p, bytes, ctas, reinterpret_cast<cudaStream_t>(s)));
 }
 
+dec_status dec_sim_comm_wait(uint64_t ns, dec_stream_t s) {
+  if (ns < 1000ull || ns > 1000000000ull) return DEC_ERR_INVALID_ARG;
+  if (consume_fault()) return DEC_ERR_CUDA;
+  return cuda_status(launch_comm_wait(ns, reinterpret_cast<cudaStream_t>(s)));
+}
+
 }  // extern "C"
 
 // ======================================================= no-allocation variant ====

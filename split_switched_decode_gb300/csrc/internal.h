@@ -118,6 +118,7 @@ cudaError_t launch_linear_finish(const LinearFinishParams &f, cudaStream_t s);
 cudaError_t launch_gather_map(const uint16_t *X, const int32_t *topk_idx, int B, int topk, int E,
                               int K, uint16_t *Xg, int32_t *route_map, unsigned *status,
                               int max_ctas, cudaStream_t s);
+cudaError_t launch_comm_wait(uint64_t ns, cudaStream_t s);
 cudaError_t launch_gather_rows(const uint16_t *X, const int32_t *route_map, int B, int topk,
                                int E, int K, uint16_t *Xg, cudaStream_t s);
 cudaError_t launch_combine(const float *topk_w, const int32_t *route_map, const float *Yp,

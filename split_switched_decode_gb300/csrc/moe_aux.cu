@@ -1,5 +1,5 @@
-// moe_aux.cu -- small kernels around the grouped expert GEMV, the L2 prefetch kernel
-// and the bounded-wait self-test.
+// moe_aux.cu -- small kernels around the grouped expert GEMV, the L2 prefetch kernel,
+// the simulated communication phase and the bounded-wait self-test.
 #include "common.cuh"
 #include "internal.h"
 #include "routing.cuh"
@@ -297,7 +297,19 @@ __global__ void wait_selftest_kernel(unsigned *status, uint64_t limit_ns) {
   (void)mbar_wait_bounded(&bar, 0u, status, &abort_flag, limit_ns);
 }
 
+// Occupies its stream for ns nanoseconds (globaltimer) while touching no memory: a
+// stand-in for a communication phase that leaves HBM idle.
+__global__ void comm_wait_kernel(uint64_t ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 < ns) __nanosleep(256);
+}
+
 }  // namespace
+
+cudaError_t launch_comm_wait(uint64_t ns, cudaStream_t s) {
+  comm_wait_kernel<<<1, 32, 0, s>>>(ns);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_front_finish(const FrontFinishParams &f, cudaStream_t s) {
   return launch_pdl(front_finish_kernel, dim3((f.E + f.L + 511) / 512, f.B), dim3(512), 0, s, f);

@@ -90,4 +90,6 @@ def test_host_argument_checks_need_no_device(ssd):
     assert lib.dec_set_force_variant(7) == ssd.DEC_ERR_INVALID_ARG
     assert lib.dec_set_wait_limit_ns(10) == ssd.DEC_ERR_INVALID_ARG
     assert lib.dec_debug_wait_timeout(10, s) == ssd.DEC_ERR_INVALID_ARG
+    assert lib.dec_sim_comm_wait(999, s) == ssd.DEC_ERR_INVALID_ARG
+    assert lib.dec_sim_comm_wait(1000000001, s) == ssd.DEC_ERR_INVALID_ARG
     assert lib.dec_set_fault_inject(-1) == ssd.DEC_ERR_INVALID_ARG

@@ -236,9 +236,12 @@ def big_layer(env):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("B", [1, 64])
-def test_moe_layer_full_size(env, big_layer, B):
-    """Front end -> routed experts + shared expert (side stream) on the full-size layer;
+@pytest.mark.parametrize("B,with_map", [(1, True), (1, False), (2, False), (4, False),
+                                        (8, False), (16, False), (32, False), (64, True),
+                                        (64, False)])
+def test_moe_layer_full_size(env, big_layer, B, with_map):
+    """Front end -> routed experts + shared expert (side stream) on the full-size layer,
+    with the route map from the front end or built by the experts' gather launch;
     sampled tokens checked against the oracle with their experts copied to the host."""
     torch, ssd, oracle, dev = env
     from split_switched_decode_gb300 import inputs
@@ -246,12 +249,13 @@ def test_moe_layer_full_size(env, big_layer, B):
     E, H, I, L, k = g["E"], g["H"], g["I"], g["L"], 8
     X = inputs.activations(B, H, dev, 0, "layer_x")
     _, idx, w, _, rm = _run_front(env, X, g["Wc"], E, L, k)
-    Y = _run_experts(env, X, idx, w, g["Wgu"], g["Wd"], g["Wgs"], g["Wds"], rm=rm, side=True)
+    Y = _run_experts(env, X, idx, w, g["Wgu"], g["Wd"], g["Wgs"], g["Wds"],
+                     rm=rm if with_map else None, side=True)
     idx_np, w_np = idx.cpu().numpy(), w.cpu().numpy().astype(np.float64)
     Yf = to_f64(oracle, Y)
     xb = inputs.bits(X)
     gs, ds = inputs.bits(g["Wgs"]), inputs.bits(g["Wds"])
-    tokens = [0] if B == 1 else [0, 37, B - 1]
+    tokens = sorted({0, (37 * B) // 64, B - 1})
     y_ref = np.empty((len(tokens), H))
     for t, b in enumerate(tokens):
         yp = np.empty((1, k, H))
@@ -282,6 +286,42 @@ def test_l2_prefetch_does_not_change_results(env):
     ssd.dec_linear(X, W, None, Y2, ws)
     torch.cuda.synchronize()
     assert torch.equal(Y1, Y2)
+
+
+@pytest.mark.parametrize("B", [1, 16, 64])
+def test_prefetch_during_communication_phase_keeps_results(env, B):
+    """The output projection behind a simulated communication phase, with the second
+    half of its weights prefetched into L2 on a side stream meanwhile: bit-identical
+    output, and the phase ends on time."""
+    torch, ssd, oracle, dev = env
+    from split_switched_decode_gb300 import inputs
+    N, K = 7168, 4096
+    X = inputs.activations(B, K, dev, 10)
+    W = inputs.weight(N, K, dev, 10)
+    R = inputs.residual(B, N, dev, 10)
+    Y1 = torch.empty(B, N, dtype=torch.bfloat16, device=dev)
+    Y2 = torch.empty_like(Y1)
+    ws = ssd.workspace(ssd.dec_linear_workspace_bytes(B, N, K), dev)
+    ssd.dec_sim_comm_wait(20_000)
+    ssd.dec_linear(X, W, R, Y1, ws)
+    side = torch.cuda.Stream(device=dev)
+    main = torch.cuda.current_stream()
+    fork, join = torch.cuda.Event(), torch.cuda.Event()
+    fork.record(main)
+    side.wait_event(fork)
+    flat = W.view(-1)
+    ssd.l2_prefetch(flat[flat.numel() // 2:], max_ctas=64, stream=side)
+    join.record(side)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(main)
+    ssd.dec_sim_comm_wait(2_000_000)
+    b.record(main)
+    main.wait_event(join)
+    ssd.dec_linear(X, W, R, Y2, ws)
+    torch.cuda.synchronize()
+    assert ssd.dec_sync_status() == ssd.DEC_OK
+    assert torch.equal(Y1, Y2)
+    assert 1.9 <= a.elapsed_time(b) <= 50.0  # ms: the 2 ms phase ends on time
 
 
 def test_invalid_routing_is_reported_not_faulted(env):
