@@ -31,7 +31,11 @@
  *    DEC_ERR_CUDA. Every wait inside a kernel is bounded in time; a wait that runs out
  *    makes the kernel stop early and sets a device status word that dec_sync_status()
  *    reports (DEC_ERR_TIMEOUT). No kernel traps.
- *  - Batch. Decode batch B is 1..64.
+ *  - Batch. Decode batch B is 1..64. The tensor-core projections (dec_splitk_gemm with
+ *    use_tc = 1, dec_linear) also take B = 65..256 rows: speculative-decoding
+ *    verification scores B sequences x (draft length + 1) tokens in one projection
+ *    ("Part 3: Performance Deep Dive", decode with DSpark, seven draft tokens: 8 rows
+ *    per sequence, so up to 32 sequences).
  */
 #ifndef SPLIT_SWITCHED_DECODE_H
 #define SPLIT_SWITCHED_DECODE_H
@@ -136,14 +140,19 @@ DEC_API dec_status dec_gemv(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16
  *
  * W is cut into 128-row tiles and 64-wide k-blocks. The (tile, k-block) sequence is
  * divided into contiguous ranges, one per CTA ("worker"); partial sums of a tile
- * produced by several workers go to the workspace and the last worker to finish the
- * tile adds them in worker order (fixed order: bit-identical results for a fixed
- * split), adds R and rounds once.
+ * produced by several workers go to the workspace and are added in worker order
+ * (fixed order: bit-identical results for a fixed split), R is added and the sum is
+ * rounded once. The adding is done by the last worker to finish the tile or, for
+ * B >= 32 with K >= 12288 (DEC_DEFER_MIN_B sets the batch), by a second kernel
+ * launched behind the first on the same stream.
  *
  *   split_k == 0 : one worker per SM, ranges of equal length (stream-K style).
  *   split_k == S : every tile split into S equal k-ranges (S <= k-blocks per tile).
- * use_tc: 0 = CUDA-core tiles, 1 = tcgen05 tensor-core tiles (W rows are the MMA M
- * dimension, the batch is the MMA N dimension, accumulator in tensor memory).
+ * use_tc: 0 = CUDA-core tiles (B <= 64), 1 = tcgen05 tensor-core tiles (W rows are
+ * the MMA M dimension, the batch is the MMA N dimension, accumulator in tensor
+ * memory). With use_tc = 1, B may be 65..256 (speculative verification rows): groups
+ * of 64 batch columns share every weight tile, each group reduced separately;
+ * use_tc = 0 then returns DEC_ERR_UNSUPPORTED_SHAPE.
  */
 DEC_API size_t dec_splitk_workspace_bytes(int B, int N, int K, int split_k);
 DEC_API dec_status dec_splitk_gemm(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 *R,
@@ -170,7 +179,8 @@ DEC_API dec_status dec_splitk_gemm_noalloc(const dec_bf16 *X, const dec_bf16 *W,
 
 /*
  * The batch-size switch: picks dec_gemv for B <= 2, the split-K tiles on CUDA cores
- * for small B and on tensor cores from a threshold batch upward, then runs it.
+ * for small B and on tensor cores from a threshold batch upward (always for
+ * B = 65..256), then runs it.
  * dec_linear_workspace_bytes() covers whichever variant the switch can pick.
  */
 DEC_API size_t dec_linear_workspace_bytes(int B, int N, int K);

@@ -140,7 +140,7 @@ dec_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DEC_OK : DEC_E
 // ------------------------------------------------------------ split-K planning --
 
 struct SplitPlan {
-  int T, KB, G, maxc;
+  int T, KB, G, maxc, ngrp;  // ngrp: groups of 64 batch columns (B > 64: tensor cores only)
   size_t partial_bytes, counter_bytes, total;
 };
 
@@ -158,9 +158,11 @@ bool plan_splitk(int B, int N, int K, int split_k, int num_sms, SplitPlan *pl) {
     pl->G = static_cast<int>(g);
   }
   if (pl->G < 1) return false;
-  pl->maxc = engine_maxc_for(B);
-  pl->partial_bytes = align_up(static_cast<size_t>(2) * pl->G * 128 * pl->maxc * sizeof(float));
-  pl->counter_bytes = align_up(static_cast<size_t>(pl->T) * sizeof(int));
+  pl->ngrp = B > MAX_B ? (B <= 2 * MAX_B ? 2 : 4) : 1;
+  pl->maxc = engine_maxc_for(B > MAX_B ? MAX_B : B);
+  pl->partial_bytes = align_up(static_cast<size_t>(2) * pl->G * pl->ngrp * 128 * pl->maxc *
+                               sizeof(float));
+  pl->counter_bytes = align_up(static_cast<size_t>(pl->T) * pl->ngrp * sizeof(int));
   pl->total = pl->partial_bytes + pl->counter_bytes;
   return true;
 }
@@ -173,8 +175,12 @@ int l2_prefetch_kblocks() {
 }
 
 // Activation box height for a launch whose groups have at most maxc columns: one box
-// covers them all (fewer TMA instructions per stage).
+// covers them all (fewer TMA instructions per stage). A wide projection's box holds
+// every batch row (B <= 256 rows).
 int xbox_rows_for(int maxc) { return 16 * ((maxc + 15) / 16); }
+int xbox_rows_for(const SplitPlan &pl, int B) {
+  return pl.ngrp > 1 ? 16 * ((B + 15) / 16) : xbox_rows_for(pl.maxc);
+}
 
 void fill_engine_common(EngineParams &p, const SplitPlan &pl, int mode, int N, int K, int B,
                         void *ws, const DeviceInfo *d) {
@@ -187,8 +193,9 @@ void fill_engine_common(EngineParams &p, const SplitPlan &pl, int mode, int N, i
   p.G = pl.G;
   p.B = B;
   p.slot_cols = pl.maxc;
+  p.ngrp = pl.ngrp;
   p.wbox_rows = 128;
-  p.xbox_rows = xbox_rows_for(pl.maxc);
+  p.xbox_rows = xbox_rows_for(pl, B);
   p.l2pf_kb = l2_prefetch_kblocks();
   p.partials = static_cast<float *>(ws);
   p.counters = reinterpret_cast<int *>(static_cast<char *>(ws) + pl.partial_bytes);
@@ -200,7 +207,7 @@ dec_status check_linear_args(const dec_bf16 *X, const dec_bf16 *W, dec_bf16 *Y, 
                              int K) {
   if (!X || !W || !Y) return DEC_ERR_INVALID_ARG;
   if (B < 1 || N < 1 || K < 1) return DEC_ERR_INVALID_ARG;
-  if (B > MAX_B) return DEC_ERR_UNSUPPORTED_SHAPE;
+  if (B > MAX_B_WIDE) return DEC_ERR_UNSUPPORTED_SHAPE;
   if (K % 8 != 0) return DEC_ERR_MISALIGNED;
   if (!aligned16(X) || !aligned16(W)) return DEC_ERR_MISALIGNED;
   if (static_cast<int64_t>(N) * K > (int64_t(1) << 40)) return DEC_ERR_UNSUPPORTED_SHAPE;
@@ -235,13 +242,14 @@ dec_status run_splitk(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 *R, d
   cudaError_t ce;
   DeviceInfo *d = device_info(&ce);
   if (!d) return DEC_ERR_CUDA;
+  if (B > MAX_B && !use_tc) return DEC_ERR_UNSUPPORTED_SHAPE;  // wide: tensor cores only
   SplitPlan pl;
   if (!plan_splitk(B, N, K, split_k, d->num_sms, &pl)) return DEC_ERR_UNSUPPORTED_SHAPE;
   if (!ws) return DEC_ERR_INVALID_ARG;
   if (!aligned16(ws)) return DEC_ERR_MISALIGNED;
   if (ws_bytes < pl.total) return DEC_ERR_WORKSPACE_TOO_SMALL;
   CUtensorMap wmap, xmap;
-  if (!make_map(&wmap, W, K, N, 128) || !make_map(&xmap, X, K, B, xbox_rows_for(pl.maxc)))
+  if (!make_map(&wmap, W, K, N, 128) || !make_map(&xmap, X, K, B, xbox_rows_for(pl, B)))
     return DEC_ERR_CUDA;
   EngineParams p;
   fill_engine_common(p, pl, MODE_LINEAR, N, K, B, ws, d);
@@ -254,7 +262,7 @@ dec_status run_splitk(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 *R, d
   // over (tile, 16 columns) adds them, instead of each tile's last worker adding 64-wide
   // partials at the end of the product (the product's tail). Needs workers that span
   // at most two tiles.
-  p.defer = (B >= defer_min_batch() && K >= 12288 && pl.G >= pl.T) ? 1 : 0;
+  p.defer = (pl.ngrp == 1 && B >= defer_min_batch() && K >= 12288 && pl.G >= pl.T) ? 1 : 0;
   if (consume_fault()) return DEC_ERR_CUDA;
   ce = use_tc ? launch_engine_tc(pl.maxc, wmap, xmap, p, s)
               : launch_engine_cc(pl.maxc, wmap, xmap, p, s);
@@ -456,7 +464,7 @@ dec_status dec_gemv(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 *R, dec
 }
 
 size_t dec_splitk_workspace_bytes(int B, int N, int K, int split_k) {
-  if (B < 1 || B > MAX_B || N < 1 || K < 1 || split_k < 0) return 0;
+  if (B < 1 || B > MAX_B_WIDE || N < 1 || K < 1 || split_k < 0) return 0;
   SplitPlan pl;
   const int sms = current_num_sms();
   if (sms <= 0 || !plan_splitk(B, N, K, split_k, sms, &pl)) return 0;
@@ -484,7 +492,7 @@ dec_status dec_linear(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 *R, d
   int v = force_variant();
   if (v == DEC_VARIANT_NONE)
     v = (B <= 2) ? DEC_VARIANT_TINY
-                 : (B >= tc_min_batch() ? DEC_VARIANT_SPLITK_TC : DEC_VARIANT_SPLITK);
+                 : (B >= tc_min_batch() || B > MAX_B ? DEC_VARIANT_SPLITK_TC : DEC_VARIANT_SPLITK);
   if (v == DEC_VARIANT_TINY) return dec_gemv(X, W, R, Y, B, N, K, s);
   return run_splitk(X, W, R, Y, B, N, K, 0, v == DEC_VARIANT_SPLITK_TC ? 1 : 0, ws, ws_bytes,
                     reinterpret_cast<cudaStream_t>(s));
@@ -668,6 +676,7 @@ dec_status moe_experts(const dec_bf16 *X, const int32_t *topk_idx, const float *
     p.grouped = grouped;
     p.B = B;
     p.slot_cols = ep.maxc;
+    p.ngrp = 1;
     p.wbox_rows = (mode == MODE_GATEUP) ? 64 : 128;
     p.xbox_rows = grouped ? XBOX_ROWS : xb_shared;
     p.E = E;
@@ -786,6 +795,7 @@ extern "C" dec_status dec_splitk_gemm_noalloc(const dec_bf16 *X, const dec_bf16 
   dec_status st = check_linear_args(X, W, Y, B, N, K);
   if (st != DEC_OK) return st;
   if (use_tc != 0 && use_tc != 1) return DEC_ERR_INVALID_ARG;
+  if (B > MAX_B && !use_tc) return DEC_ERR_UNSUPPORTED_SHAPE;  // wide: tensor cores only
   cudaError_t ce;
   DeviceInfo *d = device_info(&ce);
   if (!d) return DEC_ERR_CUDA;
@@ -802,7 +812,7 @@ extern "C" dec_status dec_splitk_gemm_noalloc(const dec_bf16 *X, const dec_bf16 
   if (!plan_splitk(B, N, K, 0, d->num_sms, &pl)) return DEC_ERR_UNSUPPORTED_SHAPE;
   if (pl.total > kNoAllocScratchBytes) return DEC_ERR_WORKSPACE_TOO_SMALL;
   CUtensorMap wmap, xmap;
-  if (!make_map(&wmap, W, K, N, 128) || !make_map(&xmap, X, K, B, xbox_rows_for(pl.maxc)))
+  if (!make_map(&wmap, W, K, N, 128) || !make_map(&xmap, X, K, B, xbox_rows_for(pl, B)))
     return DEC_ERR_CUDA;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
   // The array keeps whatever the previous call left; the arrival counters must start

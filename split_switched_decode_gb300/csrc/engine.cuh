@@ -44,7 +44,8 @@ struct SegInfo {
   int kb0;     // first k-block of the segment
   int kb1;     // one past the last k-block
   int ncols;   // activation rows (batch columns) of the group
-  int xrow0;   // first activation row of the group
+  int xrow0;   // first activation row of the group (of the column group: wide projections)
+  int cgrp;    // column group of 64 batch columns (wide projections; else 0)
   int wrow0;   // W row of tile rows 0..63
   int wrow1;   // W row of tile rows 64..127
   bool full;   // the segment covers the whole tile
@@ -69,7 +70,7 @@ __device__ __forceinline__ void seg_info(const EngineParams &p, int64_t it, int6
     s.ncols = min(max(rm[e], 0), min(p.slot_cols, p.P - s.xrow0));
     wbase = e * p.w_group_rows;
   } else {
-    s.ncols = p.B;
+    s.ncols = p.B;  // every batch column; wide projections split it into column groups
     s.xrow0 = 0;
     wbase = 0;
   }
@@ -81,6 +82,7 @@ __device__ __forceinline__ void seg_info(const EngineParams &p, int64_t it, int6
     s.wrow1 = s.wrow0 + 64;
   }
   s.full = (s.kb0 == 0 && s.kb1 == p.KB);
+  s.cgrp = 0;
 }
 
 // Activation boxes (16 rows each) a segment needs: at least one.
@@ -243,7 +245,9 @@ __device__ __forceinline__ bool reduce_tile(const EngineParams &p, const SegInfo
   const int64_t tb = static_cast<int64_t>(s.gt) * p.KB;
   const int which_me = (begin >= tb) ? 0 : 1;
   const size_t slot_floats = static_cast<size_t>(128) * p.slot_cols;
-  float *slot = p.partials + static_cast<size_t>(w * 2 + which_me) * slot_floats;
+  // slot of (worker, which, column group); column groups only exist when p.ngrp > 1
+  float *slot =
+      p.partials + (static_cast<size_t>(w * 2 + which_me) * p.ngrp + s.cgrp) * slot_floats;
 #pragma unroll
   for (int j = 0; j < MAXC; ++j)
     if (j < s.ncols) slot[j * 128 + r] = v[j];
@@ -252,7 +256,7 @@ __device__ __forceinline__ bool reduce_tile(const EngineParams &p, const SegInfo
   const int first = sk_worker_of(total, p.G, tb);
   const int last = sk_worker_of(total, p.G, tb + p.KB - 1);
   if (r == 0) {
-    const int old = atom_add_acq_rel_gpu(&p.counters[s.gt], 1);
+    const int old = atom_add_acq_rel_gpu(&p.counters[s.gt * p.ngrp + s.cgrp], 1);
     flags[1] = (old == last - first) ? 1 : 0;
   }
   named_bar_sync(bar_id, 128);
@@ -271,7 +275,8 @@ __device__ __forceinline__ bool reduce_tile(const EngineParams &p, const SegInfo
     for (int d = 0; d < RD; ++d) {
       const int wk = wk0 + d;
       const int which = (wk == first) ? which_first : 0;
-      const float *sl = p.partials + static_cast<size_t>(wk * 2 + which) * slot_floats;
+      const float *sl =
+          p.partials + (static_cast<size_t>(wk * 2 + which) * p.ngrp + s.cgrp) * slot_floats;
       const bool other = (wk <= last) && (wk != w);
 #pragma unroll
       for (int j = 0; j < MAXC; ++j)
@@ -288,7 +293,7 @@ __device__ __forceinline__ bool reduce_tile(const EngineParams &p, const SegInfo
   }
 #pragma unroll
   for (int j = 0; j < MAXC; ++j) v[j] = t[j];
-  if (r == 0) p.counters[s.gt] = 0;
+  if (r == 0) p.counters[s.gt * p.ngrp + s.cgrp] = 0;
   return true;
 }
 
@@ -316,7 +321,7 @@ __device__ __forceinline__ void epilogue_rows(const EngineParams &p, const SegIn
         if (j >= s.ncols || n0 >= p.N) continue;
         const float4 a = *reinterpret_cast<const float4 *>(scratch + jj * 128 + row8);
         const float4 b = *reinterpret_cast<const float4 *>(scratch + jj * 128 + row8 + 4);
-        store_y8(p, j, n0, a, b);
+        store_y8(p, s.xrow0 + j, n0, a, b);
       }
     }
   } else if (p.mode == MODE_LINEAR) {
@@ -326,8 +331,9 @@ __device__ __forceinline__ void epilogue_rows(const EngineParams &p, const SegIn
       for (int j = 0; j < MAXC; ++j) {
         if (j < s.ncols) {
           float y = v[j];
-          if (p.R != nullptr) y += bf16_to_f32(p.R[static_cast<size_t>(j) * p.N + n]);
-          p.Y[static_cast<size_t>(j) * p.N + n] = f32_to_bf16_rn(y);
+          const size_t off = static_cast<size_t>(s.xrow0 + j) * p.N + n;
+          if (p.R != nullptr) y += bf16_to_f32(p.R[off]);
+          p.Y[off] = f32_to_bf16_rn(y);
         }
       }
     }

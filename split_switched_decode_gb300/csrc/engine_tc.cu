@@ -16,6 +16,12 @@
 // The accumulator is double-buffered (2 x 64 columns) so the epilogue of one segment
 // overlaps the MMAs of the next. The tensor cores keep the multiply off the CUDA
 // cores, which would bound the CUDA-core tiles from about 8 batch columns upward.
+//
+// Wide projections (speculative-decode verification: B x (draft length + 1) rows, up
+// to 256): NG groups of 64 batch columns share every weight tile -- one MMA with
+// N = 16 x boxes <= 256 per K step into 2 x 64*NG accumulator columns (all 512 at
+// NG = 4) -- and the epilogue reduces and stores the column groups one after another,
+// each with its own partial slots and arrival counter.
 #include <atomic>
 
 #include "engine.cuh"
@@ -26,12 +32,11 @@ namespace {
 
 constexpr int TC_THREADS = 192;  // 6 warps
 constexpr int TC_SMEM_LIMIT = 232448;
-constexpr uint32_t TMEM_COLS = 128;  // two accumulators of up to 64 fp32 columns
-
-template <int MAXC>
+template <int MAXC, int NG>
 struct TCConfig {
+  static constexpr uint32_t TMEM_COLS = 128u * NG;  // two accumulators of 64*NG columns
   static constexpr int NC = MAXC < 16 ? 16 : MAXC;  // accumulator columns read back
-  static constexpr int NXB = NC / 16;
+  static constexpr int NXB = NC / 16 * NG;          // 16-row activation boxes per stage
   static constexpr int STAGE_BYTES = 16384 + NXB * 2048;
   static constexpr int SCRATCH_BYTES = 64 * MAXC * 4;  // gate/up pairing
   static constexpr int TAIL = 256;
@@ -117,11 +122,11 @@ __device__ __forceinline__ uint32_t idesc_bf16(int n) {
          (static_cast<uint32_t>(128 >> 4) << 24);
 }
 
-template <int MAXC>
+template <int MAXC, int NG>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     engine_tc_kernel(const __grid_constant__ CUtensorMap wmap,
                      const __grid_constant__ CUtensorMap xmap, const EngineParams p) {
-  using C = TCConfig<MAXC>;
+  using C = TCConfig<MAXC, NG>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -160,7 +165,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -193,7 +198,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + buf * 64u;
+        const uint32_t d_tmem = tmem_base + buf * 64u * NG;
         for (int kb = s.kb0; kb < s.kb1; ++kb, ++q) {
           const int st = static_cast<int>(q % C::STAGES);
           if (!mbar_wait_bounded(&full[st], (q / C::STAGES) & 1u, p.status, flags,
@@ -233,62 +238,80 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       named_bar_sync(2, 128);
       if (flags[0]) break;  // uniform across the 128 epilogue threads after the barrier
       tc_fence_after();
-      float v[C::NC];
-      const uint32_t taddr =
-          tmem_base + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + buf * 64u;
+      const int ng = NG == 1 ? 1 : (s.ncols + 63) >> 6;  // column groups of this segment
+#pragma unroll 1
+      for (int g = 0; g < ng; ++g) {
+        float v[C::NC];
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * (warp & 3)) << 16) +
+                               buf * 64u * NG + 64u * g;
 #pragma unroll
-      for (int c = 0; c < C::NC / 16; ++c) tmem_ld16(taddr + 16u * c, v + 16 * c);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[buf]);
-      float acc[MAXC];
+        for (int c = 0; c < C::NC / 16; ++c) tmem_ld16(taddr + 16u * c, v + 16 * c);
+        tmem_wait_ld();
+        if (g == ng - 1) {  // every column group read: the buffer is free for the MMAs
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        }
+        float acc[MAXC];
 #pragma unroll
-      for (int j = 0; j < MAXC; ++j) acc[j] = v[j];
-      if (reduce_tile<MAXC>(p, s, total, w, begin, r, acc, 2, flags))
-        epilogue_rows<MAXC>(p, s, r, acc, scratch, 2, flags);
+        for (int j = 0; j < MAXC; ++j) acc[j] = v[j];
+        SegInfo sg = s;
+        if (NG > 1) {
+          sg.cgrp = g;
+          sg.xrow0 = 64 * g;
+          sg.ncols = min(64, s.ncols - 64 * g);
+        }
+        if (reduce_tile<MAXC>(p, sg, total, w, begin, r, acc, 2, flags))
+          epilogue_rows<MAXC>(p, sg, r, acc, scratch, 2, flags);
+      }
       it += s.kb1 - s.kb0;
     }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+  if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
 }
 
-template <int MAXC>
+template <int MAXC, int NG = 1>
 cudaError_t launch_t(const CUtensorMap &wmap, const CUtensorMap &xmap, const EngineParams &p,
                      cudaStream_t s) {
-  using C = TCConfig<MAXC>;
+  using C = TCConfig<MAXC, NG>;
   static std::atomic<uint64_t> attr_set{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
   if (!(attr_set.load() & bit)) {
-    e = cudaFuncSetAttribute(engine_tc_kernel<MAXC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM);
+    e = cudaFuncSetAttribute(engine_tc_kernel<MAXC, NG>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr_set.fetch_or(bit);
   }
-  return launch_pdl(engine_tc_kernel<MAXC>, dim3(p.G), dim3(TC_THREADS), C::SMEM, s, wmap, xmap, p);
+  return launch_pdl(engine_tc_kernel<MAXC, NG>, dim3(p.G), dim3(TC_THREADS), C::SMEM, s, wmap,
+                    xmap, p);
 }
 
 }  // namespace
 
 size_t engine_tc_smem_bytes(int maxc) {
   switch (maxc) {
-    case 2: return TCConfig<2>::SMEM;
-    case 4: return TCConfig<4>::SMEM;
-    case 8: return TCConfig<8>::SMEM;
-    case 16: return TCConfig<16>::SMEM;
-    case 32: return TCConfig<32>::SMEM;
-    default: return TCConfig<64>::SMEM;
+    case 2: return TCConfig<2, 1>::SMEM;
+    case 4: return TCConfig<4, 1>::SMEM;
+    case 8: return TCConfig<8, 1>::SMEM;
+    case 16: return TCConfig<16, 1>::SMEM;
+    case 32: return TCConfig<32, 1>::SMEM;
+    default: return TCConfig<64, 1>::SMEM;
   }
 }
 
 cudaError_t launch_engine_tc(int maxc, const CUtensorMap &wmap, const CUtensorMap &xmap,
                              const EngineParams &p, cudaStream_t s) {
+  if (p.ngrp > 1) {  // wide projection: 64-column groups, 2 or up to 4 of them
+    if (maxc != 64 || p.ngrp > 4 || p.mode != MODE_LINEAR || p.grouped || p.defer)
+      return cudaErrorInvalidValue;
+    return p.ngrp == 2 ? launch_t<64, 2>(wmap, xmap, p, s) : launch_t<64, 4>(wmap, xmap, p, s);
+  }
   switch (maxc) {
     case 2: return launch_t<2>(wmap, xmap, p, s);
     case 4: return launch_t<4>(wmap, xmap, p, s);

@@ -23,6 +23,8 @@ struct EngineParams {
   int slot_cols;     // columns per partial slot (slot = 128 * slot_cols floats)
   int defer;         // 1: store every segment's partial tile and stop (MODE_FRONT)
   int vec_y;         // LINEAR: N % 8 == 0 and Y (and R) 16-byte aligned: 16-byte stores
+  int ngrp;          // LINEAR, tensor cores: groups of 64 batch columns sharing each weight
+                     // tile (B > 64: up to 4); 1 everywhere else
   int wbox_rows;     // rows per weight TMA box: 128 (one box per tile) or 64 (gate/up)
   const uint8_t *w_base;  // weight matrix (raw pointer, for L2 prefetch)
   long long w_rows;       // rows of the weight matrix (all groups)
