@@ -64,7 +64,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--ops", default="in,o,front,experts",
                     help="operations of the sweep (profiling subsets: in,o,front,experts; "
-                         "pfscen = output projection behind a simulated communication phase)")
+                         "pfscen = output projection behind a simulated communication phase; "
+                         "spec = projections at speculative verification row counts)")
     ap.add_argument("--sweep-only", action="store_true",
                     help="only the per-operation sweep (for profiler captures)")
     ap.add_argument("--num-experts", type=int, default=E,
@@ -337,6 +338,38 @@ def prefetch_scenario(torch, ssd, wl, batches, reps):
     return out
 
 
+# ------------------------------------------- speculative verification rows ----
+
+SPEC_ROWS = (64, 128, 256)
+
+
+def spec_sweep(torch, ssd, inputs, wl, dev, reps):
+    """The decode projections at speculative-decoding verification row counts
+    (sequences x (draft length + 1) tokens, up to 256 rows per call; "Part 3: Performance
+    Deep Dive", decode with DSpark): wide tensor-core tiles, CUDA graph of R calls over
+    the rotating weight copies. Reports HBM GB/s and tensor TFLOP/s (2*M*N*K)."""
+    R = 12
+    out = {}
+    for M in SPEC_ROWS:
+        row = {}
+        for name, N, K, pool, res in (("input_projection", N_IN, H, wl.W_in, False),
+                                      ("output_projection", H, K_O, wl.W_o, True)):
+            X = inputs.activations(M, K, dev, 0, "spec_x")
+            Rr = inputs.residual(M, N, dev, 0, "spec_r") if res else None
+            Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+            ws = ssd.workspace(ssd.dec_linear_workspace_bytes(M, N, K), dev)
+            g = capture(torch, lambda: [ssd.dec_linear(X, pool[r % len(pool)], Rr, Y, ws)
+                                        for r in range(R)])
+            us = statistics.median(time_graph(torch, g, reps)) / R
+            del g
+            nb = bytes_linear(M, N, K, res)
+            row[name] = {"us_per_call": us, "GBps": nb / us / 1e3,
+                         "TFLOPs": 2.0 * M * N * K / us / 1e6,
+                         "variant": ssd.dec_variant_name(ssd.dec_last_variant())}
+        out[str(M)] = row
+    return out
+
+
 # -------------------------------------------------------------- CPU baseline ----
 
 def cpu_sample_fn(batches, seed=0):
@@ -483,7 +516,7 @@ def main():
     batches = [int(b) for b in args.batches.split(",")]
     ops = set(args.ops.split(","))
     if not args.sweep_only:
-        ops = {"in", "o", "front", "experts", "pfscen"}
+        ops = {"in", "o", "front", "experts", "pfscen", "spec"}
     wl = Workload(torch, ssd, inputs, dev, batches, num_experts=args.num_experts,
                   experts="experts" in ops)
     wl.prefetch = not args.no_prefetch
@@ -525,6 +558,9 @@ def main():
             del g
         sweep[str(B)] = row
     torch.cuda.synchronize()
+    spec = None
+    if "spec" in ops and not args.step_only:
+        spec = spec_sweep(torch, ssd, inputs, wl, dev, args.reps)
     pfscen = None
     if "pfscen" in ops and not args.step_only:
         pfscen = prefetch_scenario(torch, ssd, wl, [b for b in (1, 64) if b in batches],
@@ -533,7 +569,7 @@ def main():
         if rank == 0:
             print(json.dumps({"sweep_only": True, "batches": batches, "ops": sorted(ops),
                               "num_experts": wl.E, "sweep": sweep,
-                              "prefetch_scenario": pfscen}), flush=True)
+                              "prefetch_scenario": pfscen, "spec_rows": spec}), flush=True)
         return 0
 
     # ---- the step as one CUDA graph
@@ -627,6 +663,11 @@ def main():
     for Bk, row in sweep.items():
         for op in row.values():
             op["frac"] = op["GBps"] / peak
+    tc_peak = peaks.get("bf16_tflops") or 1900.0
+    for Mk, row in (spec or {}).items():
+        for op in row.values():
+            op["frac_hbm"] = op["GBps"] / peak
+            op["frac_tensor"] = op["TFLOPs"] / tc_peak
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -647,7 +688,7 @@ def main():
                            "parallelism": f"replicas x{world}"},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": per_step_launches * args.steps, "clocks": clocks,
-                "sweep": sweep, "prefetch_scenario": pfscen}
+                "sweep": sweep, "prefetch_scenario": pfscen, "spec_rows": spec}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

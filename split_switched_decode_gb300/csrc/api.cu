@@ -226,6 +226,13 @@ int defer_min_batch() {
   return 32;  // measured on the K = 16384 output projection: B = 32 and 64 gain 2-8 us
 }
 
+// Wide projections (B > 64) defer their reduction to the finishing kernel unless
+// DEC_WIDE_DEFER=0.
+bool wide_defer() {
+  if (const char *s = std::getenv("DEC_WIDE_DEFER")) return std::atoi(s) != 0;
+  return true;
+}
+
 // The batch-size switch: the B at and above which tensor-core tiles are used
 // (B <= 2 always takes the tiny kernel in dec_linear).
 int tc_min_batch() {
@@ -262,7 +269,10 @@ dec_status run_splitk(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 *R, d
   // over (tile, 16 columns) adds them, instead of each tile's last worker adding 64-wide
   // partials at the end of the product (the product's tail). Needs workers that span
   // at most two tiles.
-  p.defer = (pl.ngrp == 1 && B >= defer_min_batch() && K >= 12288 && pl.G >= pl.T) ? 1 : 0;
+  if (pl.ngrp > 1)  // wide: four 64-column reductions per tile are too long a tail
+    p.defer = (pl.G >= pl.T && wide_defer()) ? 1 : 0;
+  else
+    p.defer = (B >= defer_min_batch() && K >= 12288 && pl.G >= pl.T) ? 1 : 0;
   if (consume_fault()) return DEC_ERR_CUDA;
   ce = use_tc ? launch_engine_tc(pl.maxc, wmap, xmap, p, s)
               : launch_engine_cc(pl.maxc, wmap, xmap, p, s);
@@ -275,6 +285,7 @@ dec_status run_splitk(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 *R, d
     f.G = p.G;
     f.T = p.T;
     f.KB = p.KB;
+    f.ngrp = p.ngrp;
     f.total = static_cast<long long>(p.T) * p.KB;
     f.B = B;
     f.N = N;

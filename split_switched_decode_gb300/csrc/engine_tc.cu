@@ -308,7 +308,7 @@ size_t engine_tc_smem_bytes(int maxc) {
 cudaError_t launch_engine_tc(int maxc, const CUtensorMap &wmap, const CUtensorMap &xmap,
                              const EngineParams &p, cudaStream_t s) {
   if (p.ngrp > 1) {  // wide projection: 64-column groups, 2 or up to 4 of them
-    if (maxc != 64 || p.ngrp > 4 || p.mode != MODE_LINEAR || p.grouped || p.defer)
+    if (maxc != 64 || p.ngrp > 4 || p.mode != MODE_LINEAR || p.grouped)
       return cudaErrorInvalidValue;
     return p.ngrp == 2 ? launch_t<64, 2>(wmap, xmap, p, s) : launch_t<64, 4>(wmap, xmap, p, s);
   }

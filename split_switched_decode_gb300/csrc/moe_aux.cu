@@ -187,16 +187,19 @@ __global__ void __launch_bounds__(128) linear_finish_kernel(const LinearFinishPa
   const int n = t * 128 + r;
   const TileContrib tc = tile_contrib(t, f.KB, f.G, f.total);
   const size_t slot_floats = static_cast<size_t>(128) * f.slot_cols;
+  // columns j0..j0+15 lie in one group of 64 (wide projections keep a slot per group)
+  const int g = j0 >> 6, jj0 = j0 & 63;
   float z[16];
 #pragma unroll
   for (int j = 0; j < 16; ++j) z[j] = 0.f;
   for (int wk = tc.first; wk <= tc.last; ++wk) {
     const int which = (wk == tc.first) ? tc.which_first : 0;
-    const float *sl = f.partials + static_cast<size_t>(wk * 2 + which) * slot_floats + r;
+    const float *sl =
+        f.partials + (static_cast<size_t>(wk * 2 + which) * f.ngrp + g) * slot_floats + r;
     float part[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j)
-      part[j] = (j0 + j < f.B) ? __ldcg(sl + static_cast<size_t>(j0 + j) * 128) : 0.f;
+      part[j] = (j0 + j < f.B) ? __ldcg(sl + static_cast<size_t>(jj0 + j) * 128) : 0.f;
 #pragma unroll
     for (int j = 0; j < 16; ++j) z[j] += part[j];
   }
