@@ -226,6 +226,15 @@ int defer_min_batch() {
   return 32;  // measured on the K = 16384 output projection: B = 32 and 64 gain 2-8 us
 }
 
+// Reduction depth (K) from which wide-batch projections defer (DEC_DEFER_MIN_K).
+int defer_min_k() {
+  if (const char *s = std::getenv("DEC_DEFER_MIN_K")) {
+    int v = std::atoi(s);
+    if (v >= 0) return v;
+  }
+  return 12288;
+}
+
 // Wide projections (B > 64) defer their reduction to the finishing kernel unless
 // DEC_WIDE_DEFER=0.
 bool wide_defer() {
@@ -272,7 +281,7 @@ dec_status run_splitk(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 *R, d
   if (pl.ngrp > 1)  // wide: four 64-column reductions per tile are too long a tail
     p.defer = (pl.G >= pl.T && wide_defer()) ? 1 : 0;
   else
-    p.defer = (B >= defer_min_batch() && K >= 12288 && pl.G >= pl.T) ? 1 : 0;
+    p.defer = (B >= defer_min_batch() && K >= defer_min_k() && pl.G >= pl.T) ? 1 : 0;
   if (consume_fault()) return DEC_ERR_CUDA;
   ce = use_tc ? launch_engine_tc(pl.maxc, wmap, xmap, p, s)
               : launch_engine_cc(pl.maxc, wmap, xmap, p, s);
@@ -286,6 +295,7 @@ dec_status run_splitk(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 *R, d
     f.T = p.T;
     f.KB = p.KB;
     f.ngrp = p.ngrp;
+    f.vec_y = p.vec_y;
     f.total = static_cast<long long>(p.T) * p.KB;
     f.B = B;
     f.N = N;

@@ -108,7 +108,7 @@ cudaError_t launch_front_finish(const FrontFinishParams &f, cudaStream_t s);
 // in worker order, adds R and rounds to bf16.
 struct LinearFinishParams {
   const float *partials;
-  int slot_cols, G, T, KB, ngrp;
+  int slot_cols, G, T, KB, ngrp, vec_y;
   long long total;
   int B, N;
   const uint16_t *R;

@@ -203,6 +203,42 @@ __global__ void __launch_bounds__(128) linear_finish_kernel(const LinearFinishPa
 #pragma unroll
     for (int j = 0; j < 16; ++j) z[j] += part[j];
   }
+  if (f.vec_y) {
+    // transpose through shared memory: each thread then finishes 8 consecutive rows of
+    // one column with 16-byte R loads and Y stores
+    __shared__ __align__(16) float sz[16][128];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) sz[j][r] = z[j];
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int c = r + 128 * q;  // 16 columns x 16 runs of 8 rows
+      const int j = c >> 4, row8 = (c & 15) * 8, n0 = t * 128 + row8;
+      if (j0 + j >= f.B || n0 >= f.N) continue;
+      float y[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) y[e] = sz[j][row8 + e];
+      const size_t off = static_cast<size_t>(j0 + j) * f.N + n0;  // N % 8 == 0: whole run
+      if (f.R != nullptr) {
+        const uint4 rr = *reinterpret_cast<const uint4 *>(f.R + off);
+        y[0] += bf16lo(rr.x);
+        y[1] += bf16hi(rr.x);
+        y[2] += bf16lo(rr.y);
+        y[3] += bf16hi(rr.y);
+        y[4] += bf16lo(rr.z);
+        y[5] += bf16hi(rr.z);
+        y[6] += bf16lo(rr.w);
+        y[7] += bf16hi(rr.w);
+      }
+      uint4 o;
+      o.x = f32_to_bf16_rn(y[0]) | (static_cast<uint32_t>(f32_to_bf16_rn(y[1])) << 16);
+      o.y = f32_to_bf16_rn(y[2]) | (static_cast<uint32_t>(f32_to_bf16_rn(y[3])) << 16);
+      o.z = f32_to_bf16_rn(y[4]) | (static_cast<uint32_t>(f32_to_bf16_rn(y[5])) << 16);
+      o.w = f32_to_bf16_rn(y[6]) | (static_cast<uint32_t>(f32_to_bf16_rn(y[7])) << 16);
+      *reinterpret_cast<uint4 *>(f.Y + off) = o;
+    }
+    return;
+  }
   if (n >= f.N) return;
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
