@@ -220,8 +220,9 @@ class Workload:
         self.ssd.dec_linear(d["x_o"], self.W_o[rot % len(self.W_o)], d["r_o"], d["y_o"], d["ws_o"])
         self.launches += 1
 
-    def op_front(self, B, rot=0, v=0, prefetch=True, with_map=False):
-        """moe_front; the route map is left to moe_experts' gather launch unless with_map."""
+    def op_front(self, B, rot=0, v=0, prefetch=True, with_map=True):
+        """moe_front, building the route map the experts' launches read (measured: the
+        whole layer is 1-11 us faster than leaving the map to moe_experts' gather)."""
         torch, ssd, d = self.torch, self.ssd, self.t[B]
         if prefetch:
             main = torch.cuda.current_stream()
@@ -236,8 +237,7 @@ class Workload:
 
     def op_experts(self, B, v=0):
         d = self.t[B]
-        # no route map: the gather launch validates topk_idx and builds it
-        self.ssd.moe_experts(d["x_moe"][v], d["idx"][v], d["w"][v], None, self.Wgu, self.Wd,
+        self.ssd.moe_experts(d["x_moe"][v], d["idx"][v], d["w"][v], d["rm"][v], self.Wgu, self.Wd,
                              self.Wgs, self.Wds, d["y_moe"], d["ws_e"], side_stream=self.side)
         self.launches += 6  # gather, shared gate/up + down, routed gate/up + down, combine
 
@@ -291,6 +291,7 @@ def time_graph(torch, g, reps):
 # ------------------------------------------------------- prefetch scenario ----
 
 PF_WAIT_US = 20.0
+EXPERTS_TRAFFIC_RATIO = 1.0125
 
 
 def prefetch_scenario(torch, ssd, wl, batches, reps):
@@ -657,9 +658,13 @@ def main():
     peak = peak or 6800.0
     Bmax = str(max(batches))
     dom = sweep[Bmax]["moe_experts"]
+    # DRAM bytes per call / algorithmic bytes, from one ncu capture of the same kernels
+    # on a 32-expert bank (profiles/moe_experts_traffic_B64_E32.md), scaled to the call
+    nb_dom = statistics.mean(bytes_experts(int(Bmax), u) for u in dom["distinct_experts"])
     roofline = {"bound": "hbm", "kernel": f"moe_experts grouped expert GEMV, B={Bmax}",
                 "achieved": dom["GBps"], "peak": peak, "peak_source": peak_src, "unit": "GB/s",
-                "frac": dom["GBps"] / peak, "traffic": None}
+                "frac": dom["GBps"] / peak, "traffic": EXPERTS_TRAFFIC_RATIO * nb_dom,
+                "traffic_unit": "bytes per call"}
     for Bk, row in sweep.items():
         for op in row.values():
             op["frac"] = op["GBps"] / peak
