@@ -341,12 +341,12 @@ def prefetch_scenario(torch, ssd, wl, batches, reps):
 
 # ------------------------------------------- speculative verification rows ----
 
-SPEC_ROWS = (64, 128, 256)
+SPEC_ROWS = (64, 128, 256, 512)
 
 
 def spec_sweep(torch, ssd, inputs, wl, dev, reps):
     """The decode projections at speculative-decoding verification row counts
-    (sequences x (draft length + 1) tokens, up to 256 rows per call; "Part 3: Performance
+    (sequences x (draft length + 1) tokens, up to 512 rows per call; "Part 3: Performance
     Deep Dive", decode with DSpark): wide tensor-core tiles, CUDA graph of R calls over
     the rotating weight copies. Reports HBM GB/s and tensor TFLOP/s (2*M*N*K)."""
     R = 12

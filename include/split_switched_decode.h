@@ -32,10 +32,11 @@
  *    makes the kernel stop early and sets a device status word that dec_sync_status()
  *    reports (DEC_ERR_TIMEOUT). No kernel traps.
  *  - Batch. Decode batch B is 1..64. The tensor-core projections (dec_splitk_gemm with
- *    use_tc = 1, dec_linear) also take B = 65..256 rows: speculative-decoding
+ *    use_tc = 1, dec_linear) also take B = 65..512 rows: speculative-decoding
  *    verification scores B sequences x (draft length + 1) tokens in one projection
  *    ("Part 3: Performance Deep Dive", decode with DSpark, seven draft tokens: 8 rows
- *    per sequence, so up to 32 sequences).
+ *    per sequence, so up to 64 sequences). Up to 256 rows run as one launch; more run
+ *    as consecutive launches over row blocks of at most 256, each reading W again.
  */
 #ifndef SPLIT_SWITCHED_DECODE_H
 #define SPLIT_SWITCHED_DECODE_H
@@ -150,9 +151,10 @@ DEC_API dec_status dec_gemv(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16
  *   split_k == S : every tile split into S equal k-ranges (S <= k-blocks per tile).
  * use_tc: 0 = CUDA-core tiles (B <= 64), 1 = tcgen05 tensor-core tiles (W rows are
  * the MMA M dimension, the batch is the MMA N dimension, accumulator in tensor
- * memory). With use_tc = 1, B may be 65..256 (speculative verification rows): groups
- * of 64 batch columns share every weight tile, each group reduced separately;
- * use_tc = 0 then returns DEC_ERR_UNSUPPORTED_SHAPE.
+ * memory). With use_tc = 1, B may be 65..512 (speculative verification rows): groups
+ * of 64 batch columns share every weight tile, each group reduced separately, at most
+ * 256 rows per launch; use_tc = 0 then returns DEC_ERR_UNSUPPORTED_SHAPE.
+ * dec_splitk_workspace_bytes() covers every launch of the call (they reuse it in turn).
  */
 DEC_API size_t dec_splitk_workspace_bytes(int B, int N, int K, int split_k);
 DEC_API dec_status dec_splitk_gemm(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 *R,
@@ -166,7 +168,8 @@ DEC_API dec_status dec_splitk_gemm(const dec_bf16 *X, const dec_bf16 *W, const d
  * it is an addition of this library. Same result and arguments as dec_splitk_gemm with
  * split_k = 0; the scratch lives in a fixed 16 MiB device array inside the library
  * (held on every GPU that loads it until the process exits), so a shape whose split-K
- * scratch would exceed 16 MiB is rejected with DEC_ERR_WORKSPACE_TOO_SMALL. The first
+ * scratch would exceed 16 MiB is rejected with DEC_ERR_WORKSPACE_TOO_SMALL, and more than
+ * 256 rows with DEC_ERR_UNSUPPORTED_SHAPE. The first
  * call on a device looks up the array's address: make it before any stream capture.
  * Every call on a device shares the one array (its counters are cleared at the start
  * of each call): two calls that can overlap on that GPU race, so issue them on one
@@ -180,7 +183,7 @@ DEC_API dec_status dec_splitk_gemm_noalloc(const dec_bf16 *X, const dec_bf16 *W,
 /*
  * The batch-size switch: picks dec_gemv for B <= 2, the split-K tiles on CUDA cores
  * for small B and on tensor cores from a threshold batch upward (always for
- * B = 65..256), then runs it.
+ * B = 65..512), then runs it.
  * dec_linear_workspace_bytes() covers whichever variant the switch can pick.
  */
 DEC_API size_t dec_linear_workspace_bytes(int B, int N, int K);

@@ -207,7 +207,7 @@ dec_status check_linear_args(const dec_bf16 *X, const dec_bf16 *W, dec_bf16 *Y, 
                              int K) {
   if (!X || !W || !Y) return DEC_ERR_INVALID_ARG;
   if (B < 1 || N < 1 || K < 1) return DEC_ERR_INVALID_ARG;
-  if (B > MAX_B_WIDE) return DEC_ERR_UNSUPPORTED_SHAPE;
+  if (B > MAX_ROWS) return DEC_ERR_UNSUPPORTED_SHAPE;
   if (K % 8 != 0) return DEC_ERR_MISALIGNED;
   if (!aligned16(X) || !aligned16(W)) return DEC_ERR_MISALIGNED;
   if (static_cast<int64_t>(N) * K > (int64_t(1) << 40)) return DEC_ERR_UNSUPPORTED_SHAPE;
@@ -252,9 +252,41 @@ int tc_min_batch() {
   return 3;  // measured: tensor-core tiles win from B = 3 (CUDA cores are ALU-bound)
 }
 
+// Rows of each launch of a projection call with B rows: B itself up to 256, else the
+// call is cut into equal launches of at most 256 rows.
+int rows_per_launch(int B) {
+  const int n = (B + MAX_B_WIDE - 1) / MAX_B_WIDE;
+  return (B + n - 1) / n;
+}
+
+dec_status run_splitk_rows(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 *R, dec_bf16 *Y,
+                           int B, int N, int K, int split_k, int use_tc, void *ws,
+                           size_t ws_bytes, cudaStream_t s);
+
+// A projection of more than 256 rows (speculative verification of up to 64 sequences x
+// 8 tokens) runs as consecutive launches over row blocks, each reading W again; on one
+// stream, each launch's workspace use begins after the previous launch has finished
+// with it (the stream order, or the dependency wait of a programmatic launch).
 dec_status run_splitk(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 *R, dec_bf16 *Y,
                       int B, int N, int K, int split_k, int use_tc, void *ws, size_t ws_bytes,
                       cudaStream_t s) {
+  if (B <= MAX_B_WIDE)
+    return run_splitk_rows(X, W, R, Y, B, N, K, split_k, use_tc, ws, ws_bytes, s);
+  if (!use_tc) return DEC_ERR_UNSUPPORTED_SHAPE;
+  const int rows = rows_per_launch(B);
+  for (int r0 = 0; r0 < B; r0 += rows) {
+    const int rb = B - r0 < rows ? B - r0 : rows;
+    const size_t xo = static_cast<size_t>(r0) * K, yo = static_cast<size_t>(r0) * N;
+    const dec_status st = run_splitk_rows(X + xo, W, R ? R + yo : nullptr, Y + yo, rb, N, K,
+                                          split_k, use_tc, ws, ws_bytes, s);
+    if (st != DEC_OK) return st;
+  }
+  return DEC_OK;
+}
+
+dec_status run_splitk_rows(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 *R, dec_bf16 *Y,
+                           int B, int N, int K, int split_k, int use_tc, void *ws,
+                           size_t ws_bytes, cudaStream_t s) {
   cudaError_t ce;
   DeviceInfo *d = device_info(&ce);
   if (!d) return DEC_ERR_CUDA;
@@ -485,7 +517,8 @@ dec_status dec_gemv(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 *R, dec
 }
 
 size_t dec_splitk_workspace_bytes(int B, int N, int K, int split_k) {
-  if (B < 1 || B > MAX_B_WIDE || N < 1 || K < 1 || split_k < 0) return 0;
+  if (B < 1 || B > MAX_ROWS || N < 1 || K < 1 || split_k < 0) return 0;
+  B = rows_per_launch(B);  // every launch of the call reuses the workspace
   SplitPlan pl;
   const int sms = current_num_sms();
   if (sms <= 0 || !plan_splitk(B, N, K, split_k, sms, &pl)) return 0;
@@ -817,6 +850,7 @@ extern "C" dec_status dec_splitk_gemm_noalloc(const dec_bf16 *X, const dec_bf16 
   if (st != DEC_OK) return st;
   if (use_tc != 0 && use_tc != 1) return DEC_ERR_INVALID_ARG;
   if (B > MAX_B && !use_tc) return DEC_ERR_UNSUPPORTED_SHAPE;  // wide: tensor cores only
+  if (B > MAX_B_WIDE) return DEC_ERR_UNSUPPORTED_SHAPE;          // one launch only
   cudaError_t ce;
   DeviceInfo *d = device_info(&ce);
   if (!d) return DEC_ERR_CUDA;

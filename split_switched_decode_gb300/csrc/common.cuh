@@ -18,7 +18,8 @@ constexpr int TILE_K = 64;      // k per block: one 128-byte swizzle row of bf16
 constexpr int WBOX_ROWS = 64;   // rows per W TMA box (two boxes per tile)
 constexpr int XBOX_ROWS = 16;   // activation rows per TMA box (MMA N granularity)
 constexpr int MAX_B = 64;        // decode batch of every operation
-constexpr int MAX_B_WIDE = 256;  // rows of a tensor-core projection (speculative verification)
+constexpr int MAX_B_WIDE = 256;  // rows of one tensor-core projection launch
+constexpr int MAX_ROWS = 512;    // rows of a projection call (launches of <= 256 rows each)
 constexpr int MAX_E = 512;
 constexpr int MAX_TOPK = 16;
 // shared memory of the routing tail: ids [B*topk], token masks [E], offsets [E]

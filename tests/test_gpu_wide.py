@@ -1,7 +1,8 @@
-"""GPU parity of the wide tensor-core projection: 65..256 rows per call, the shape of
+"""GPU parity of the wide tensor-core projection: 65..512 rows per call, the shape of
 speculative-decoding verification (B sequences x (draft length + 1) tokens; "Hyper
 Optimizing Kimi K3 in vLLM", Part 3: Performance Deep Dive, decode with DSpark), where
-groups of 64 batch columns share each weight tile and are reduced separately."""
+groups of 64 batch columns share each weight tile and are reduced separately (launches
+of at most 256 rows)."""
 import numpy as np
 import pytest
 
@@ -48,7 +49,8 @@ def _ref(X, W, R, rows=None):
 
 @pytest.mark.parametrize("B,N,K", [(65, 256, 512), (72, 300, 456), (128, 1000, 1000),
                                    (129, 130, 136), (200, 640, 2048), (256, 512, 1024),
-                                   (256, 77, 64), (96, 1, 64)])
+                                   (256, 77, 64), (96, 1, 64), (257, 256, 512),
+                                   (300, 300, 456), (512, 512, 1024)])
 @pytest.mark.parametrize("split_k", [0, 3])
 def test_wide_projection_matches_oracle(env, B, N, K, split_k):
     torch, ssd, oracle, dev = env
@@ -67,7 +69,7 @@ def test_wide_projection_matches_oracle(env, B, N, K, split_k):
     assert_close(to_f64(oracle, Y), _ref(X, W, R), f"wide B={B} N={N} K={K} S={split_k}")
 
 
-@pytest.mark.parametrize("B", [72, 128, 256])
+@pytest.mark.parametrize("B", [72, 128, 256, 512])
 @pytest.mark.parametrize("which", ["input", "output"])
 def test_wide_full_size_projections(env, B, which):
     """The decode input projection (7168 -> 8192) and the output projection
@@ -110,7 +112,25 @@ def test_wide_needs_tensor_cores(env):
     ws = ssd.workspace(ssd.dec_splitk_workspace_bytes(B, N, K, 0), dev)
     with pytest.raises(ssd.DecError):
         ssd.dec_splitk_gemm(X, W, R, Y, ws, use_tc=0)
-    Xb = torch.zeros(257, K, dtype=torch.bfloat16, device=dev)
-    Yb = torch.empty(257, N, dtype=torch.bfloat16, device=dev)
+    Xb = torch.zeros(513, K, dtype=torch.bfloat16, device=dev)
+    Yb = torch.empty(513, N, dtype=torch.bfloat16, device=dev)
     with pytest.raises(ssd.DecError):
         ssd.dec_linear(Xb, W, None, Yb, ws)
+
+
+@pytest.mark.parametrize("B,N,K", [(72, 300, 456), (256, 512, 1024), (160, 1000, 2048)])
+def test_wide_last_arriver_reduction(env, monkeypatch, B, N, K):
+    """Wide projections with the reduction in each tile's last arriver (DEC_WIDE_DEFER=0)
+    instead of the finishing kernel: same results within tolerance, deterministic."""
+    torch, ssd, oracle, dev = env
+    monkeypatch.setenv("DEC_WIDE_DEFER", "0")
+    X, W, R, Y = _case(env, B, N, K, 24)
+    ws = ssd.workspace(ssd.dec_splitk_workspace_bytes(B, N, K, 0), dev)
+    ssd.dec_splitk_gemm(X, W, R, Y, ws, use_tc=1)
+    torch.cuda.synchronize()
+    Y1 = Y.clone()
+    ssd.dec_splitk_gemm(X, W, R, Y, ws, use_tc=1)
+    torch.cuda.synchronize()
+    assert ssd.dec_sync_status() == ssd.DEC_OK
+    assert torch.equal(Y, Y1)
+    assert_close(to_f64(oracle, Y), _ref(X, W, R), f"wide last-arriver B={B} N={N} K={K}")
