@@ -144,6 +144,16 @@ struct SplitPlan {
   size_t partial_bytes, counter_bytes, total;
 };
 
+// Batch from which a projection with 2 * tiles >= 80 % of the SMs splits every tile into
+// two halves instead of one equal range per SM (DEC_PAIR_SPLIT_MIN_B; 0 = never).
+int pair_split_min_batch() {
+  if (const char *s = std::getenv("DEC_PAIR_SPLIT_MIN_B")) {
+    int v = std::atoi(s);
+    return v >= 1 ? v : 1 << 30;
+  }
+  return 32;
+}
+
 // Workers: split_k == 0 -> one per SM (at most T*KB); S > 0 -> T*S (classic split-K).
 bool plan_splitk(int B, int N, int K, int split_k, int num_sms, SplitPlan *pl) {
   pl->T = ceil_div(N, TILE_N);
@@ -151,6 +161,12 @@ bool plan_splitk(int B, int N, int K, int split_k, int num_sms, SplitPlan *pl) {
   const int64_t iters = static_cast<int64_t>(pl->T) * pl->KB;
   if (split_k == 0) {
     pl->G = static_cast<int>(iters < num_sms ? iters : num_sms);
+    // Wide batches, where each tile's reduction is a visible tail: when two workers per
+    // tile still cover at least 80 % of the SMs, give every tile exactly two halves
+    // (one partial to add instead of two or three).
+    if (B >= pair_split_min_batch() && B <= MAX_B && 2 * pl->T <= num_sms &&
+        10 * pl->T >= 4 * num_sms && pl->KB >= 2)
+      pl->G = 2 * pl->T;
   } else {
     if (split_k > pl->KB) return false;
     const int64_t g = static_cast<int64_t>(pl->T) * split_k;
