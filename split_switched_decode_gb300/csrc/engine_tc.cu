@@ -103,6 +103,28 @@ __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// ---------------------------------------------------- 2-CTA cluster helpers ----
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_map(const void *p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+// Every thread of both CTAs arrives (release) and waits (acquire): the partner's
+// distributed-shared-memory stores made before it are visible after it.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Shared-memory matrix descriptor of a K-major operand stored with the 128-byte
 // swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart (stride byte offset),
 // leading byte offset unused for this layout, descriptor version 1, layout 2 (128B).
@@ -143,6 +165,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int w = blockIdx.x;
+  // pair mode: this CTA's own half of the columns of its (single) segment
+  constexpr int PH = MAXC >= 2 ? MAXC / 2 : 1;
+  float keep[PH];
+  int pair_t = 0, pair_ncols = 0;
   if (p.grouped) griddep_wait();  // the route map comes from the previous kernel
   const int ngroups = p.grouped ? rm_num_used(p) : 1;
   const int64_t total = static_cast<int64_t>(ngroups) * p.T * p.KB;
@@ -255,6 +281,28 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         float acc[MAXC];
 #pragma unroll
         for (int j = 0; j < MAXC; ++j) acc[j] = v[j];
+        if (NG == 1 && p.pair) {
+          // the two k-halves of the tile are this CTA and its cluster partner: send the
+          // partner the columns it finishes, keep the ones this CTA finishes
+          const uint32_t me = cluster_ctarank();
+          const uint32_t dst = cluster_map(scratch, me ^ 1u) + 4u * r;
+          if (me == 0) {  // keeps columns 0..PH-1, sends PH..2PH-1 (indices fixed per branch)
+#pragma unroll
+            for (int jj = 0; jj < PH; ++jj) {
+              if (PH + jj < s.ncols) st_cluster_f32(dst + 512u * jj, acc[PH + jj]);
+              keep[jj] = acc[jj];
+            }
+          } else {        // keeps PH..2PH-1, sends 0..PH-1
+#pragma unroll
+            for (int jj = 0; jj < PH; ++jj) {
+              if (jj < s.ncols) st_cluster_f32(dst + 512u * jj, acc[jj]);
+              keep[jj] = acc[PH + jj];
+            }
+          }
+          pair_t = s.t;
+          pair_ncols = s.ncols;
+          continue;
+        }
         SegInfo sg = s;
         if (NG > 1) {
           sg.cgrp = g;
@@ -271,6 +319,42 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+  if (NG == 1 && p.pair) {
+    // Both CTAs of the pair reach this point on every path (also after a time-out), so
+    // the cluster barrier always completes. Then each adds its half of the columns in
+    // worker order (first k-half + second k-half), adds R, rounds once and stores.
+    cluster_sync_all();
+    if (warp >= 2) {
+      const int r = 32 * (warp & 3) + lane;
+      const int me = static_cast<int>(cluster_ctarank());
+#pragma unroll
+      for (int jj = 0; jj < PH; ++jj) {
+        const float o = scratch[jj * 128 + r];
+        scratch[jj * 128 + r] = me == 0 ? keep[jj] + o : o + keep[jj];
+      }
+      named_bar_sync(2, 128);
+      if (p.vec_y) {
+        for (int c = r; c < PH * 16; c += 128) {
+          const int jj = c >> 4, row8 = (c & 15) * 8;
+          const int j = me * PH + jj, n0 = pair_t * 128 + row8;
+          if (j >= pair_ncols || n0 >= p.N) continue;
+          const float4 a = *reinterpret_cast<const float4 *>(scratch + jj * 128 + row8);
+          const float4 b = *reinterpret_cast<const float4 *>(scratch + jj * 128 + row8 + 4);
+          store_y8(p, j, n0, a, b);
+        }
+      } else {
+        const int n = pair_t * 128 + r;
+        for (int jj = 0; jj < PH; ++jj) {
+          const int j = me * PH + jj;
+          if (j >= pair_ncols || n >= p.N) continue;
+          float y = scratch[jj * 128 + r];
+          const size_t off = static_cast<size_t>(j) * p.N + n;
+          if (p.R != nullptr) y += bf16_to_f32(p.R[off]);
+          p.Y[off] = f32_to_bf16_rn(y);
+        }
+      }
+    }
+  }
 }
 
 template <int MAXC, int NG = 1>
@@ -288,6 +372,9 @@ cudaError_t launch_t(const CUtensorMap &wmap, const CUtensorMap &xmap, const Eng
     if (e != cudaSuccess) return e;
     attr_set.fetch_or(bit);
   }
+  if (p.pair)
+    return launch_pdl_cluster(engine_tc_kernel<MAXC, NG>, dim3(p.G), dim3(TC_THREADS), C::SMEM,
+                              s, 2, wmap, xmap, p);
   return launch_pdl(engine_tc_kernel<MAXC, NG>, dim3(p.G), dim3(TC_THREADS), C::SMEM, s, wmap,
                     xmap, p);
 }
@@ -307,6 +394,9 @@ size_t engine_tc_smem_bytes(int maxc) {
 
 cudaError_t launch_engine_tc(int maxc, const CUtensorMap &wmap, const CUtensorMap &xmap,
                              const EngineParams &p, cudaStream_t s) {
+  if (p.pair && (p.ngrp != 1 || p.grouped || p.defer || p.mode != MODE_LINEAR || p.G != 2 * p.T ||
+                 p.KB % 2 != 0))
+    return cudaErrorInvalidValue;
   if (p.ngrp > 1) {  // wide projection: 64-column groups, 2 or up to 4 of them
     if (maxc != 64 || p.ngrp > 4 || p.mode != MODE_LINEAR || p.grouped)
       return cudaErrorInvalidValue;

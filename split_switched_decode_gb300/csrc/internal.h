@@ -23,6 +23,8 @@ struct EngineParams {
   int slot_cols;     // columns per partial slot (slot = 128 * slot_cols floats)
   int defer;         // 1: store every segment's partial tile and stop (MODE_FRONT)
   int vec_y;         // LINEAR: N % 8 == 0 and Y (and R) 16-byte aligned: 16-byte stores
+  int pair;          // LINEAR, tensor cores: 2-CTA clusters, CTA pair (2t, 2t+1) holds the two
+                     // k-halves of tile t and adds them through distributed shared memory
   int ngrp;          // LINEAR, tensor cores: groups of 64 batch columns sharing each weight
                      // tile (B > 64: up to 4); 1 everywhere else
   int wbox_rows;     // rows per weight TMA box: 128 (one box per tile) or 64 (gate/up)
@@ -66,6 +68,29 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// The same with thread-block clusters of `cluster_x` CTAs along x (co-scheduled; their
+// shared memory is mutually addressable).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                               cudaStream_t s, int cluster_x, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 2 : 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -187,3 +187,26 @@ def test_many_contributor_tiles(env, B, N, K, split_k):
     assert ssd.dec_sync_status() == ssd.DEC_OK
     assert torch.equal(Y, Y1)
     assert_close(to_f64(oracle, Y), _ref(X, W, R), f"tc B={B} N={N} K={K} S={split_k}")
+
+
+@pytest.mark.parametrize("B,N,K", [(3, 300, 512), (16, 1000, 1024), (40, 130, 2048),
+                                   (64, 8192, 7168), (64, 256, 128)])
+def test_cluster_pair_reduction_matches_global_one(env, monkeypatch, B, N, K):
+    """Tiles split into two k-halves (split_k = 2, even k-block count): the two halves
+    added through distributed shared memory inside a 2-CTA cluster give the same bits as
+    the last-arriver reduction through global memory (same order: first half + second),
+    and match the oracle."""
+    torch, ssd, oracle, dev = env
+    monkeypatch.setenv("DEC_PAIR_DSMEM_COLS", "64")
+    X, W, R, Y = _case(env, B, N, K, 25, residual=True)
+    ws = ssd.workspace(ssd.dec_splitk_workspace_bytes(B, N, K, 2), dev)
+    ssd.dec_splitk_gemm(X, W, R, Y, ws, split_k=2, use_tc=1)
+    torch.cuda.synchronize()
+    assert ssd.dec_sync_status() == ssd.DEC_OK
+    monkeypatch.setenv("DEC_PAIR_DSMEM_COLS", "0")
+    Y0 = torch.empty_like(Y)
+    ssd.dec_splitk_gemm(X, W, R, Y0, ws, split_k=2, use_tc=1)
+    torch.cuda.synchronize()
+    assert torch.equal(Y, Y0)
+    rows = np.unique(np.concatenate([np.linspace(0, N - 1, min(N, 200)).astype(int), [N - 1]]))
+    assert_close(to_f64(oracle, Y)[:, rows], _ref(X, W, R, rows), f"pair B={B} N={N} K={K}")
