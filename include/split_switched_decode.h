@@ -181,7 +181,9 @@ DEC_API dec_status dec_splitk_gemm_noalloc(const dec_bf16 *X, const dec_bf16 *W,
                                            int use_tc, dec_stream_t s);
 
 /*
- * The batch-size switch: picks dec_gemv for B <= 2, the split-K tiles on CUDA cores
+ * The batch-size switch: picks dec_gemv for B <= 2 (B = 1 only for shapes whose tiles,
+ * split into two k-halves, still occupy >= 80 % of the SMs: there the tensor-core
+ * two-halves schedule is measured faster from B = 2), the split-K tiles on CUDA cores
  * for small B and on tensor cores from a threshold batch upward (always for
  * B = 65..512), then runs it.
  * dec_linear_workspace_bytes() covers whichever variant the switch can pick.

@@ -152,7 +152,7 @@ int pair_split_min_batch() {
     int v = std::atoi(s);
     return v >= 1 ? v : 1 << 30;
   }
-  return 3;  // measured on the input projection: 0.8-3.4 us faster at B = 3..64
+  return 2;  // measured on the input projection: 0.8-3.4 us faster at B = 2..64
 }
 
 // Widest tile (batch columns, a power of two) whose two k-halves are added inside a
@@ -169,6 +169,23 @@ int pair_dsmem_max_cols() {
 int pair_split_min_sm_pct() {
   if (const char *s = std::getenv("DEC_PAIR_SPLIT_MIN_SM_PCT")) return std::atoi(s);
   return 80;
+}
+
+// Whether a projection of this shape splits its tiles into two k-halves that run as
+// 2-CTA clusters (the "pair" schedule; batch threshold aside).
+bool pair_shape(int N, int K, int num_sms) {
+  const int T = ceil_div(N, TILE_N), KB = ceil_div(K, TILE_K);
+  return 2 * T <= num_sms && 200 * T >= pair_split_min_sm_pct() * num_sms && KB >= 2 &&
+         KB % 2 == 0 && pair_dsmem_max_cols() >= 2;
+}
+
+// The batch-size switch's tiny-kernel range: B <= 2, except that a shape on the pair
+// schedule takes tensor cores from B = 2 (measured on the input projection: 21.7
+// instead of 22.6 us at B = 2; at B = 1 the tiny kernel stays ahead, 20.5 vs 21.8 us).
+// DEC_TINY_MAX_B overrides.
+int tiny_max_batch(int N, int K, int num_sms) {
+  if (const char *s = std::getenv("DEC_TINY_MAX_B")) return std::atoi(s);
+  return pair_shape(N, K, num_sms) && pair_split_min_batch() <= 2 ? 1 : 2;
 }
 
 // Workers: split_k == 0 -> one per SM (at most T*KB); S > 0 -> T*S (classic split-K).
@@ -584,9 +601,17 @@ dec_status dec_linear(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 *R, d
   dec_status st = check_linear_args(X, W, Y, B, N, K);
   if (st != DEC_OK) return st;
   int v = force_variant();
-  if (v == DEC_VARIANT_NONE)
-    v = (B <= 2) ? DEC_VARIANT_TINY
-                 : (B >= tc_min_batch() || B > MAX_B ? DEC_VARIANT_SPLITK_TC : DEC_VARIANT_SPLITK);
+  if (v == DEC_VARIANT_NONE) {
+    cudaError_t ce;
+    const DeviceInfo *d = device_info(&ce);
+    if (!d) return DEC_ERR_CUDA;
+    if (B <= tiny_max_batch(N, K, d->num_sms))
+      v = DEC_VARIANT_TINY;
+    else if (B <= 2 || B >= tc_min_batch() || B > MAX_B)  // B <= 2 here: a pair shape
+      v = DEC_VARIANT_SPLITK_TC;
+    else
+      v = DEC_VARIANT_SPLITK;
+  }
   if (v == DEC_VARIANT_TINY) return dec_gemv(X, W, R, Y, B, N, K, s);
   return run_splitk(X, W, R, Y, B, N, K, 0, v == DEC_VARIANT_SPLITK_TC ? 1 : 0, ws, ws_bytes,
                     reinterpret_cast<cudaStream_t>(s));

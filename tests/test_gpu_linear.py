@@ -92,8 +92,10 @@ def test_decode_input_projection_full_size(env, B):
     ws = ssd.workspace(ssd.dec_linear_workspace_bytes(B, N, K), dev)
     ssd.dec_linear(X, W, None, Y, ws)
     torch.cuda.synchronize()
-    if B <= 2:
+    if B == 1:
         assert ssd.dec_last_variant() == ssd.VARIANT_TINY
+    elif B == 2:  # tiny, or tensor cores where the shape is on the two-halves schedule
+        assert ssd.dec_last_variant() in (ssd.VARIANT_TINY, ssd.VARIANT_SPLITK_TC)
     else:
         assert ssd.dec_last_variant() in (ssd.VARIANT_SPLITK, ssd.VARIANT_SPLITK_TC)
     rng = np.random.default_rng(B)

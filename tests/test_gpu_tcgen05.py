@@ -189,8 +189,9 @@ def test_many_contributor_tiles(env, B, N, K, split_k):
     assert_close(to_f64(oracle, Y), _ref(X, W, R), f"tc B={B} N={N} K={K} S={split_k}")
 
 
-@pytest.mark.parametrize("B,N,K", [(3, 300, 512), (16, 1000, 1024), (40, 130, 2048),
-                                   (64, 8192, 7168), (64, 256, 128)])
+@pytest.mark.parametrize("B,N,K", [(1, 200, 256), (2, 8192, 7168), (3, 300, 512),
+                                   (16, 1000, 1024), (40, 130, 2048), (64, 8192, 7168),
+                                   (64, 256, 128)])
 def test_cluster_pair_reduction_matches_global_one(env, monkeypatch, B, N, K):
     """Tiles split into two k-halves (split_k = 2, even k-block count): the two halves
     added through distributed shared memory inside a 2-CTA cluster give the same bits as
