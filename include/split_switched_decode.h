@@ -145,7 +145,11 @@ DEC_API dec_status dec_gemv(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16
  * (fixed order: bit-identical results for a fixed split), R is added and the sum is
  * rounded once. The adding is done by the last worker to finish the tile or, for
  * B >= 32 with K >= 12288 (DEC_DEFER_MIN_B sets the batch), by a second kernel
- * launched behind the first on the same stream.
+ * launched behind the first on the same stream. When twice the tile count still
+ * occupies at least 80 % of the SMs (and B >= 2, B <= 64), every tile is split into
+ * exactly two k-halves instead; with use_tc = 1 and an even k-block count the two
+ * halves run as a 2-CTA thread-block cluster and are added on chip through
+ * distributed shared memory (same order, same bits).
  *
  *   split_k == 0 : one worker per SM, ranges of equal length (stream-K style).
  *   split_k == S : every tile split into S equal k-ranges (S <= k-blocks per tile).
