@@ -292,14 +292,17 @@ bool wide_defer() {
   return true;
 }
 
-// The batch-size switch: the B at and above which tensor-core tiles are used
-// (B <= 2 always takes the tiny kernel in dec_linear).
+// The batch at and above which split-K work uses tensor-core tiles rather than CUDA-core
+// tiles (dec_linear sends the smallest batches to the tiny kernel first).
 int tc_min_batch() {
   if (const char *s = std::getenv("DEC_TC_MIN_B")) {
     int v = std::atoi(s);
     if (v >= 1) return v;
   }
-  return 3;  // measured: tensor-core tiles win from B = 3 (CUDA cores are ALU-bound)
+  // measured: tensor-core tiles win at every batch -- projections from B = 2 (CUDA
+  // cores are ALU-bound from B ~ 4), the front end at B = 1-2 (13.1 vs 13.8 us) and the
+  // expert layer at B = 2 (232 vs 238 us)
+  return 1;
 }
 
 // Rows of each launch of a projection call with B rows: B itself up to 256, else the
