@@ -285,6 +285,13 @@ int defer_min_k() {
   return 12288;
 }
 
+// Whether grouped launches whose route map is already complete read it, and issue their
+// first weight loads, before the dependency wait (DEC_EARLY_ROUTE_MAP=0 turns it off).
+bool early_route_map() {
+  if (const char *s = std::getenv("DEC_EARLY_ROUTE_MAP")) return std::atoi(s) != 0;
+  return true;
+}
+
 // Wide projections (B > 64) defer their reduction to the finishing kernel unless
 // DEC_WIDE_DEFER=0.
 bool wide_defer() {
@@ -850,14 +857,20 @@ dec_status moe_experts(const dec_bf16 *X, const int32_t *topk_idx, const float *
     // G <= T*KB keeps every worker range non-empty even with a single used expert
     const int gg = g_main < ep.Tg * ep.KBg ? g_main : ep.Tg * ep.KBg;
     const int gd = g_main < ep.Td * ep.KBd ? g_main : ep.Td * ep.KBd;
+    // The gather launch waits for whatever wrote the route map and only then lets the
+    // gate/up launch start; so when the map is not the gather's own output, it is
+    // complete before gate/up starts, and likewise before down starts: both may then
+    // read it, and issue their first weight loads, before their dependency wait.
     base(p, MODE_GATEUP, I, H, ep.Tg, ep.KBg, gg, 1, ep.main_part_off, ep.main_cnt_off);
     p.w_group_rows = 2 * I;
     p.up_row_off = I;
     p.A = A;
+    p.rm_ready = (route_map != nullptr && early_route_map()) ? 1 : 0;
     if ((ce = engine(m_wgu, m_xg, p, ms)) != cudaSuccess) return DEC_ERR_CUDA;
     base(p, MODE_DOWN, H, I, ep.Td, ep.KBd, gd, 1, ep.main_part_off, ep.main_cnt_off);
     p.w_group_rows = H;
     p.Yp = Yp;
+    p.rm_ready = early_route_map() ? 1 : 0;
     if ((ce = engine(m_wd, m_a, p, ms)) != cudaSuccess) return DEC_ERR_CUDA;
   }
   if (overlap && (ce = cudaStreamWaitEvent(ms, ev->join, 0)) != cudaSuccess) return DEC_ERR_CUDA;

@@ -137,10 +137,10 @@ __device__ __forceinline__ void prefetch_weights_l2(const EngineParams &p, int64
 }
 
 // TMA producer of both engines, run by one thread. The weight boxes of the first
-// STAGES k-blocks do not depend on the previous kernel of the stream, so for a
-// projection they are issued before griddep_wait (programmatic dependent launch); the
-// activation boxes, and everything of a grouped launch (which reads the route map),
-// only after it.
+// STAGES k-blocks do not depend on the previous kernel of the stream, so they are
+// issued before griddep_wait (programmatic dependent launch) -- for a grouped launch
+// only when its route map was complete before the previous kernel started (rm_ready),
+// since the map picks the weights; the activation boxes only after it.
 template <int STAGES, int STAGE_BYTES>
 __device__ __forceinline__ void engine_produce(const EngineParams &p, const CUtensorMap *wmap,
                                                const CUtensorMap *xmap, uint8_t *stage_mem,
@@ -150,7 +150,7 @@ __device__ __forceinline__ void engine_produce(const EngineParams &p, const CUte
   prefetch_tensormap(xmap);
   const uint64_t pol = policy_evict_first();
   uint32_t pre = 0;
-  if (!p.grouped) {
+  if (!p.grouped || p.rm_ready) {
     for (int64_t it = begin; it < end && pre < STAGES;) {
       SegInfo s;
       seg_info(p, it, end, s);

@@ -89,7 +89,9 @@ __global__ void __launch_bounds__(CC_THREADS, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int w = blockIdx.x;
-  if (p.grouped) griddep_wait();  // the route map comes from the previous kernel
+  // a grouped launch reads the route map right away: wait for the previous kernel
+  // unless the map was complete before that kernel started (rm_ready)
+  if (p.grouped && !p.rm_ready) griddep_wait();
   const int ngroups = p.grouped ? rm_num_used(p) : 1;
   const int64_t total = static_cast<int64_t>(ngroups) * p.T * p.KB;
   const int64_t begin = sk_start(total, p.G, w);

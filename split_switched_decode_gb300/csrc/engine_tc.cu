@@ -169,7 +169,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   constexpr int PH = MAXC >= 2 ? MAXC / 2 : 1;
   float keep[PH];
   int pair_t = 0, pair_ncols = 0;
-  if (p.grouped) griddep_wait();  // the route map comes from the previous kernel
+  // a grouped launch reads the route map right away: wait for the previous kernel
+  // unless the map was complete before that kernel started (rm_ready)
+  if (p.grouped && !p.rm_ready) griddep_wait();
   const int ngroups = p.grouped ? rm_num_used(p) : 1;
   const int64_t total = static_cast<int64_t>(ngroups) * p.T * p.KB;
   const int64_t begin = sk_start(total, p.G, w);

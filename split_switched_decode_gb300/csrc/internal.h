@@ -17,6 +17,8 @@ struct EngineParams {
   int KB;            // 64-wide k-blocks per tile
   int G;             // workers (== gridDim.x), G <= T*KB
   int grouped;       // 0: one group of B columns; 1: groups = used experts of a route map
+  int rm_ready;      // grouped: the route map was complete before the previous kernel of
+                     // the stream started, so it may be read before the dependency wait
   int B;             // columns of the single group
   int w_group_rows;  // W rows per group in the weight bank (grouped)
   int up_row_off;    // GATEUP: row offset of the up half inside a group (= I)
