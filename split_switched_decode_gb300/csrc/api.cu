@@ -198,7 +198,7 @@ bool plan_splitk(int B, int N, int K, int split_k, int num_sms, SplitPlan *pl) {
     // When two workers per tile still cover at least 80 % of the SMs, give every tile
     // exactly two k-halves: one partial to add instead of two or three, and on tensor
     // cores the two halves run as a 2-CTA cluster that adds them on chip.
-    if (B >= pair_split_min_batch() && B <= MAX_B && 2 * pl->T <= num_sms &&
+    if (B >= pair_split_min_batch() && 2 * pl->T <= num_sms &&
         200 * pl->T >= pair_split_min_sm_pct() * num_sms && pl->KB >= 2)
       pl->G = 2 * pl->T;
   } else {
@@ -366,21 +366,23 @@ dec_status run_splitk_rows(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 
   p.vec_y = (N % 8 == 0 && aligned16(Y) && (R == nullptr || aligned16(R))) ? 1 : 0;
   p.w_base = reinterpret_cast<const uint8_t *>(W);
   p.w_rows = N;
-  // Large batches: the product kernel only stores partial tiles and a finishing kernel
-  // over (tile, 16 columns) adds them, instead of each tile's last worker adding 64-wide
-  // partials at the end of the product (the product's tail). Needs workers that span
-  // at most two tiles.
-  if (pl.ngrp > 1)  // wide: four 64-column reductions per tile are too long a tail
-    p.defer = (pl.G >= pl.T && wide_defer()) ? 1 : 0;
-  else
-    p.defer = (B >= defer_min_batch() && K >= defer_min_k() && pl.G >= pl.T) ? 1 : 0;
   // Every tile split into exactly two k-halves (G = 2 T, KB even): on tensor cores the
   // two workers of a tile run as a 2-CTA cluster and add their halves through
   // distributed shared memory, with no partial tiles in global memory and no counter.
-  p.pair = (use_tc && pl.ngrp == 1 && pl.maxc <= pair_dsmem_max_cols() && !p.defer &&
-            pl.G == 2 * pl.T && pl.KB % 2 == 0)
-               ? 1
-               : 0;
+  const bool pair_ok = use_tc && pl.G == 2 * pl.T && pl.KB % 2 == 0 &&
+                       (pl.ngrp > 1 ? pair_dsmem_max_cols() >= MAX_B
+                                    : pl.maxc <= pair_dsmem_max_cols());
+  // Otherwise, for large batches, the product kernel only stores partial tiles and a
+  // finishing kernel over (tile, 16 columns) adds them, instead of each tile's last
+  // worker adding 64-wide partials at the end of the product (the product's tail).
+  // Needs workers that span at most two tiles.
+  if (pair_ok)
+    p.defer = 0;
+  else if (pl.ngrp > 1)  // wide: four 64-column reductions per tile are too long a tail
+    p.defer = (pl.G >= pl.T && wide_defer()) ? 1 : 0;
+  else
+    p.defer = (B >= defer_min_batch() && K >= defer_min_k() && pl.G >= pl.T) ? 1 : 0;
+  p.pair = pair_ok ? 1 : 0;
   if (consume_fault()) return DEC_ERR_CUDA;
   ce = use_tc ? launch_engine_tc(pl.maxc, wmap, xmap, p, s)
               : launch_engine_cc(pl.maxc, wmap, xmap, p, s);

@@ -266,6 +266,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       named_bar_sync(2, 128);
       if (flags[0]) break;  // uniform across the 128 epilogue threads after the barrier
       tc_fence_after();
+      if (NG > 1 && p.pair) {  // the accumulator stays in tensor memory for the pair tail
+        pair_t = s.t;
+        pair_ncols = s.ncols;
+        it += s.kb1 - s.kb0;
+        continue;
+      }
       const int ng = NG == 1 ? 1 : (s.ncols + 63) >> 6;  // column groups of this segment
 #pragma unroll 1
       for (int g = 0; g < ng; ++g) {
@@ -320,6 +326,75 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (NG > 1 && p.pair) {
+    // Wide pair tail. Column group g is finished by the CTA of rank g % 2 (rank 0: groups
+    // 0 and 2, rank 1: groups 1 and 3). Once both CTAs are past their MMAs (barrier 1:
+    // every stage buffer on both sides is idle), each reads its accumulator from tensor
+    // memory group by group and puts it in its own stage memory (its groups) or in the
+    // partner's (the partner's groups); after barrier 2 each adds first k-half + second
+    // k-half for its groups, adds R, rounds once and stores.
+    float *own = reinterpret_cast<float *>(stage_mem);           // [2][64][128]
+    float *recv = reinterpret_cast<float *>(stage_mem + 65536);  // [2][64][128]
+    const uint32_t me = cluster_ctarank();
+    const int ng = (pair_ncols + 63) >> 6;
+    cluster_sync_all();
+    if (warp >= 2) {
+      const int r = 32 * (warp & 3) + lane;
+      const uint32_t recv_remote = cluster_map(recv, me ^ 1u) + 4u * r;
+      for (int g = 0; g < ng; ++g) {
+        float v[64];
+        const uint32_t taddr =
+            tmem_base + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + 64u * g;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld16(taddr + 16u * c, v + 16 * c);
+        tmem_wait_ld();
+        const int gi = g >> 1;  // index among the owner's groups
+        if ((g & 1) == static_cast<int>(me)) {
+#pragma unroll
+          for (int j = 0; j < 64; ++j) own[(gi * 64 + j) * 128 + r] = v[j];
+        } else {
+#pragma unroll
+          for (int j = 0; j < 64; ++j)
+            st_cluster_f32(recv_remote + 512u * static_cast<uint32_t>(gi * 64 + j), v[j]);
+        }
+      }
+    }
+    tc_fence_before();
+    cluster_sync_all();
+    tc_fence_after();
+    if (warp >= 2) {
+      const int r = 32 * (warp & 3) + lane;
+      for (int g = static_cast<int>(me); g < ng; g += 2) {
+        const int gi = g >> 1;
+#pragma unroll 8
+        for (int j = 0; j < 64; ++j) {
+          const int at = (gi * 64 + j) * 128 + r;
+          own[at] = me == 0 ? own[at] + recv[at] : recv[at] + own[at];
+        }
+      }
+      named_bar_sync(2, 128);
+      for (int g = static_cast<int>(me); g < ng; g += 2) {
+        const int gi = g >> 1;
+        for (int c = r; c < 64 * 16; c += 128) {
+          const int j = c >> 4, row8 = (c & 15) * 8;
+          const int col = 64 * g + j, n0 = pair_t * 128 + row8;
+          if (col >= pair_ncols || n0 >= p.N) continue;
+          const float *src = own + (gi * 64 + j) * 128 + row8;
+          if (p.vec_y) {
+            store_y8(p, col, n0, *reinterpret_cast<const float4 *>(src),
+                     *reinterpret_cast<const float4 *>(src + 4));
+          } else {
+            for (int e = 0; e < 8 && n0 + e < p.N; ++e) {
+              float y = src[e];
+              const size_t off = static_cast<size_t>(col) * p.N + n0 + e;
+              if (p.R != nullptr) y += bf16_to_f32(p.R[off]);
+              p.Y[off] = f32_to_bf16_rn(y);
+            }
+          }
+        }
+      }
+    }
+  }
   if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
   if (NG == 1 && p.pair) {
     // Both CTAs of the pair reach this point on every path (also after a time-out), so
@@ -396,8 +471,8 @@ size_t engine_tc_smem_bytes(int maxc) {
 
 cudaError_t launch_engine_tc(int maxc, const CUtensorMap &wmap, const CUtensorMap &xmap,
                              const EngineParams &p, cudaStream_t s) {
-  if (p.pair && (p.ngrp != 1 || p.grouped || p.defer || p.mode != MODE_LINEAR || p.G != 2 * p.T ||
-                 p.KB % 2 != 0))
+  if (p.pair && ((p.ngrp > 1 && maxc != 64) || p.grouped || p.defer || p.mode != MODE_LINEAR ||
+                 p.G != 2 * p.T || p.KB % 2 != 0))
     return cudaErrorInvalidValue;
   if (p.ngrp > 1) {  // wide projection: 64-column groups, 2 or up to 4 of them
     if (maxc != 64 || p.ngrp > 4 || p.mode != MODE_LINEAR || p.grouped)

@@ -134,3 +134,25 @@ def test_wide_last_arriver_reduction(env, monkeypatch, B, N, K):
     assert ssd.dec_sync_status() == ssd.DEC_OK
     assert torch.equal(Y, Y1)
     assert_close(to_f64(oracle, Y), _ref(X, W, R), f"wide last-arriver B={B} N={N} K={K}")
+
+
+@pytest.mark.parametrize("B", [72, 128, 129, 200, 256, 300])
+def test_wide_cluster_pair_matches_finishing_kernel(env, monkeypatch, B):
+    """A wide projection whose tiles split into two k-halves (64 tiles: the two-halves
+    schedule): the halves added inside 2-CTA clusters through distributed shared memory,
+    column group by column group, give the same bits as the finishing kernel adding the
+    same two partial tiles, and match the oracle."""
+    torch, ssd, oracle, dev = env
+    N, K = 8192, 1024
+    X, W, R, Y = _case(env, B, N, K, 26)
+    ws = ssd.workspace(ssd.dec_linear_workspace_bytes(B, N, K), dev)
+    ssd.dec_linear(X, W, R, Y, ws)
+    torch.cuda.synchronize()
+    assert ssd.dec_sync_status() == ssd.DEC_OK
+    monkeypatch.setenv("DEC_PAIR_DSMEM_COLS", "0")
+    Y0 = torch.empty_like(Y)
+    ssd.dec_linear(X, W, R, Y0, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(Y, Y0)
+    rows = np.unique(np.concatenate([np.linspace(0, N - 1, 160).astype(int), [127, 128]]))
+    assert_close(to_f64(oracle, Y)[:, rows], _ref(X, W, R, rows), f"wide pair B={B}")
