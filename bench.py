@@ -47,8 +47,8 @@ PREFETCH_BYTES = 24 << 20
 WORKLOAD = ("Kimi-K3-shaped decode layer hot path, B in {1,2,4,8,16,32,64}: input projection "
             "7168->8192 (batch-size kernel switch), output projection 16384->7168 + residual, "
             "MoE front end 7168->384 router + 512 latent with softmax/top-8, 384 routed experts "
-            "(gate/up 2x2048x7168, down 7168x2048) + shared expert on a side stream, "
-            "L2 prefetch of the shared expert's weights")
+            "(gate/up 2x2048x7168, down 7168x2048) + shared expert on a side stream "
+            "overlapping the routed experts")
 
 
 def parse_args():
@@ -73,8 +73,11 @@ def parse_args():
     ap.add_argument("--reps", type=int, default=7, help="graph replays per sweep entry")
     ap.add_argument("--step-only", action="store_true",
                     help="only the step graph (no sweep, e2e or CPU baseline), for profiler captures")
-    ap.add_argument("--no-prefetch", action="store_true",
-                    help="leave out the L2 prefetch of the shared expert's weights")
+    ap.add_argument("--layer", action="store_true",
+                    help="step: moe_layer (shared expert overlapping the front end) instead of "
+                         "moe_front + moe_experts")
+    ap.add_argument("--prefetch", action="store_true",
+                    help="step: L2 prefetch of the shared expert's weights during the front end")
     return ap.parse_args()
 
 
@@ -204,9 +207,13 @@ class Workload:
             d["ws_o"] = ssd.workspace(ssd.dec_linear_workspace_bytes(B, H, K_O), dev)
             d["ws_f"] = ssd.workspace(ssd.moe_front_workspace_bytes(B, self.E, L, H), dev)
             d["ws_e"] = ssd.workspace(ssd.moe_experts_workspace_bytes(B, self.E, TOPK, H, I), dev)
+            if experts:
+                d["ws_l"] = ssd.workspace(ssd.moe_layer_workspace_bytes(B, self.E, L, H, I, TOPK),
+                                          dev)
             self.t[B] = d
         self.launches = 0
-        self.prefetch = True
+        self.prefetch = False
+        self.layer = False
         torch.cuda.synchronize()
 
     # -- operations (each adds the kernels it launches to self.launches) --
@@ -241,12 +248,28 @@ class Workload:
                              self.Wgs, self.Wds, d["y_moe"], d["ws_e"], side_stream=self.side)
         self.launches += 6  # gather, shared gate/up + down, routed gate/up + down, combine
 
+    def op_layer(self, B, v=0):
+        """moe_layer: the front end runs while the shared expert streams its weights on the
+        side stream, then the routed experts (no separate L2 prefetch: the shared expert's
+        own reads fill the front end's idle HBM time)."""
+        d = self.t[B]
+        self.ssd.moe_layer(d["x_moe"][v], self.W_cat[0], self.E, L, TOPK, self.Wgu, self.Wd,
+                           self.Wgs, self.Wds, d["lat"][v], d["idx"][v], d["w"][v], d["y_moe"],
+                           d["ws_l"], route_map=d["rm"][v], side_stream=self.side)
+        self.launches += 8  # front product + finish, gather, 4 expert GEMVs, combine
+
+    def op_moe(self, B):
+        if self.layer:
+            self.op_layer(B)
+        else:
+            self.op_front(B, prefetch=self.prefetch)
+            self.op_experts(B)
+
     def step(self):
         for B in self.batches:
             self.op_in(B)
             self.op_o(B)
-            self.op_front(B, prefetch=self.prefetch)
-            self.op_experts(B)
+            self.op_moe(B)
 
     def used_experts(self, B, v=0):
         rm = self.t[B]["rm"][v]
@@ -520,7 +543,14 @@ def main():
         ops = {"in", "o", "front", "experts", "pfscen", "spec"}
     wl = Workload(torch, ssd, inputs, dev, batches, num_experts=args.num_experts,
                   experts="experts" in ops)
-    wl.prefetch = not args.no_prefetch
+    # Measured (graphs of 3 layers, B = 1/4/16/64): front end + experts as separate calls
+    # 147.0 / 441.3 / 1437.7 / 3615.5 us; with the L2 prefetch of the shared expert's
+    # weights during the front end 152.1 / 443.1 / 1440.6 / 3623.9; as moe_layer 149.2 /
+    # 443.3 / 1441.8 / 3621.9. The front end is latency-bound and on the critical path:
+    # any traffic next to it slows it more than it saves later. The prefetch is measured
+    # where it pays, behind a communication phase (prefetch_scenario).
+    wl.prefetch = args.prefetch
+    wl.layer = args.layer
 
     # routing of every X set (fixed inputs -> fixed routing -> fixed bytes)
     for B in batches:
@@ -601,7 +631,8 @@ def main():
         if rank == 0:
             print(json.dumps({"step_only": True, "value": value, "unit": "GB/s", "ms_per_step": ms,
                               "batches": batches, "num_experts": wl.E,
-                              "l2_prefetch": wl.prefetch}), flush=True)
+                              "moe_call": "moe_layer" if wl.layer else "moe_front + moe_experts",
+                              "l2_prefetch": wl.prefetch and not wl.layer}), flush=True)
         return 0
 
     # ---- end to end through the public API with host buffers
@@ -625,8 +656,7 @@ def main():
                 d["x_moe"][0].copy_(hi["x_moe"], non_blocking=True)
                 wl.op_in(B)
                 wl.op_o(B)
-                wl.op_front(B, prefetch=wl.prefetch)
-                wl.op_experts(B)
+                wl.op_moe(B)
                 ho["y_in"].copy_(d["y_in"], non_blocking=True)
                 ho["y_o"].copy_(d["y_o"], non_blocking=True)
                 ho["y_moe"].copy_(d["y_moe"], non_blocking=True)
@@ -689,7 +719,9 @@ def main():
                            "l2": "cold: every weight tensor is re-read only after >3x L2 of "
                                  "other weight traffic (step), rotating copies >=3x L2 (sweep)",
                            "timing": "CUDA graph replay, CUDA events on the replay stream",
-                           "l2_prefetch": wl.prefetch,
+                           "moe_call": "moe_layer (shared expert overlapping the front end)"
+                                       if wl.layer else "moe_front + l2_prefetch + moe_experts",
+                           "l2_prefetch_in_step": wl.prefetch and not wl.layer,
                            "parallelism": f"replicas x{world}"},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": per_step_launches * args.steps, "clocks": clocks,

@@ -265,6 +265,26 @@ DEC_API dec_status moe_experts(const dec_bf16 *X, const int32_t *topk_idx, const
                        int H, int I, int topk, dec_bf16 *Y, void *ws, size_t ws_bytes,
                        dec_stream_t main_stream, dec_stream_t side_stream, int side_max_ctas);
 
+/*
+ * The MoE layer in one call: moe_front followed by moe_experts, with the shared expert
+ * overlapping the routing ("Part 1 / 3. Improve MoE scheduling and overlap": the shared
+ * expert runs on a separate stream overlapping routing or routed-expert work). The
+ * shared expert's launches go on `side_stream` first; the front end then runs on
+ * `main_stream` on the remaining SMs while the shared expert streams its weights, and
+ * the routed experts and the combine follow on `main_stream`, which waits for
+ * `side_stream` before the combine. Outputs: latent [B,L] (when L > 0), topk_idx and
+ * topk_w [B,topk], route_map_opt (optional, as moe_front), Y [B,H] as moe_experts.
+ * Same shapes, alignment and errors as moe_front (K = H) and moe_experts;
+ * ws = moe_layer_workspace_bytes(B, E, L, H, I, topk) bytes.
+ */
+DEC_API size_t moe_layer_workspace_bytes(int B, int E, int L, int H, int I, int topk);
+DEC_API dec_status moe_layer(const dec_bf16 *X, const dec_bf16 *Wcat, int E, int L, int topk,
+                             const dec_bf16 *Wgu, const dec_bf16 *Wd, const dec_bf16 *Wgu_shared,
+                             const dec_bf16 *Wd_shared, int B, int H, int I, dec_bf16 *latent,
+                             int32_t *topk_idx, float *topk_w, int32_t *route_map_opt,
+                             dec_bf16 *Y, void *ws, size_t ws_bytes, dec_stream_t main_stream,
+                             dec_stream_t side_stream, int side_max_ctas);
+
 /* ------------------------------------------------------------ L2 prefetch ----- */
 
 /*

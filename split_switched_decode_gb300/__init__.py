@@ -36,6 +36,7 @@ EXPORTS = [
     "dec_sync_status", "dec_debug_wait_timeout", "dec_gemv", "dec_splitk_workspace_bytes",
     "dec_splitk_gemm", "dec_linear_workspace_bytes", "dec_linear", "moe_route_map_ints",
     "moe_front_workspace_bytes", "moe_front", "moe_experts_workspace_bytes", "moe_experts",
+    "moe_layer_workspace_bytes", "moe_layer",
     "l2_prefetch", "dec_sim_comm_wait", "dec_splitk_gemm_noalloc",
 ]
 
@@ -85,6 +86,8 @@ def _load():
         "moe_front": (I, [P, P, I, I, I, I, I, P, P, P, P, P, P, S, P]),
         "moe_experts_workspace_bytes": (S, [I, I, I, I, I]),
         "moe_experts": (I, [P, P, P, P, P, P, I, P, P, I, I, I, I, P, P, S, P, P, I]),
+        "moe_layer_workspace_bytes": (S, [I, I, I, I, I, I]),
+        "moe_layer": (I, [P, P, I, I, I, P, P, P, P, I, I, I, P, P, P, P, P, P, S, P, P, I]),
         "l2_prefetch": (I, [P, S, I, P]),
         "dec_sim_comm_wait": (I, [U64, P]),
         "dec_splitk_gemm_noalloc": (I, [P, P, P, P, I, I, I, I, P]),
@@ -267,3 +270,24 @@ def dec_sim_comm_wait(ns: int, stream=None):
     communication phase)."""
     _check(_load().dec_sim_comm_wait(int(ns), _stream(stream)), "dec_sim_comm_wait")
 
+
+
+def moe_layer_workspace_bytes(B, E, L, H, I, topk) -> int:
+    return int(_load().moe_layer_workspace_bytes(B, E, L, H, I, topk))
+
+
+def moe_layer(X, Wcat, E, L, topk, Wgu, Wd, Wgu_shared, Wd_shared, latent, topk_idx, topk_w,
+              Y, ws, route_map=None, stream=None, side_stream=None, side_max_ctas=0):
+    """moe_front + moe_experts with the shared expert overlapping the routing."""
+    for t, n in ((X, "X"), (Wcat, "Wcat"), (Wgu, "Wgu"), (Wd, "Wd"), (Wgu_shared, "Wgu_shared"),
+                 (Wd_shared, "Wd_shared"), (latent, "latent"), (Y, "Y")):
+        _bf16(t, n)
+    B, H = X.shape
+    I = Wgu.shape[1] // 2
+    main = _stream(stream)
+    side = _stream(side_stream) if side_stream is not None else main
+    _check(_load().moe_layer(_ptr(X), _ptr(Wcat), E, L, topk, _ptr(Wgu), _ptr(Wd),
+                             _ptr(Wgu_shared), _ptr(Wd_shared), B, H, I, _ptr(latent),
+                             _ptr(topk_idx), _ptr(topk_w), _ptr(route_map), _ptr(Y), _ptr(ws),
+                             ws.numel() * ws.element_size(), main, side, side_max_ctas),
+           "moe_layer")

@@ -495,6 +495,11 @@ dec_status get_events(StreamEvents **out) {
   return DEC_OK;
 }
 
+dec_status run_front(const dec_bf16 *X, const dec_bf16 *Wcat, int B, int K, int E, int L,
+                     int topk, dec_bf16 *latent, int32_t *topk_idx, float *topk_w,
+                     float *probs_opt, int32_t *route_map_opt, void *ws, size_t ws_bytes,
+                     int sms, cudaStream_t s);
+
 }  // namespace
 
 // =================================================================== C ABI ====
@@ -656,10 +661,27 @@ dec_status moe_front(const dec_bf16 *X, const dec_bf16 *Wcat, int B, int K, int 
   cudaError_t ce;
   DeviceInfo *d = device_info(&ce);
   if (!d) return DEC_ERR_CUDA;
+  return run_front(X, Wcat, B, K, E, L, topk, latent, topk_idx, topk_w, probs_opt, route_map_opt,
+                   ws, ws_bytes, d->num_sms, reinterpret_cast<cudaStream_t>(s));
+}
+
+}  // extern "C"
+
+namespace {
+
+// The front end (product + finishing kernel) on at most `sms` workers, arguments
+// already checked.
+dec_status run_front(const dec_bf16 *X, const dec_bf16 *Wcat, int B, int K, int E, int L,
+                     int topk, dec_bf16 *latent, int32_t *topk_idx, float *topk_w,
+                     float *probs_opt, int32_t *route_map_opt, void *ws, size_t ws_bytes,
+                     int sms, cudaStream_t s) {
+  cudaError_t ce;
+  DeviceInfo *d = device_info(&ce);
+  if (!d) return DEC_ERR_CUDA;
   FrontPlan fp;
-  int splits = front_splits(B, E, L, d->num_sms);
+  int splits = front_splits(B, E, L, sms);
   if (splits > ceil_div(K, TILE_K)) splits = ceil_div(K, TILE_K);
-  if (!plan_front(B, E, L, K, d->num_sms, &fp, splits)) return DEC_ERR_UNSUPPORTED_SHAPE;
+  if (!plan_front(B, E, L, K, sms, &fp, splits)) return DEC_ERR_UNSUPPORTED_SHAPE;
   if (ws_bytes < fp.total) return DEC_ERR_WORKSPACE_TOO_SMALL;
   CUtensorMap wmap, xmap;
   if (!make_map(&wmap, Wcat, K, E + L, 128) ||
@@ -675,8 +697,8 @@ dec_status moe_front(const dec_bf16 *X, const dec_bf16 *Wcat, int B, int K, int 
   if (consume_fault()) return DEC_ERR_CUDA;
   int v = force_variant();
   const bool tc = (v == DEC_VARIANT_SPLITK_TC) || (v == DEC_VARIANT_NONE && B >= tc_min_batch());
-  ce = tc ? launch_engine_tc(fp.sk.maxc, wmap, xmap, p, reinterpret_cast<cudaStream_t>(s))
-          : launch_engine_cc(fp.sk.maxc, wmap, xmap, p, reinterpret_cast<cudaStream_t>(s));
+  ce = tc ? launch_engine_tc(fp.sk.maxc, wmap, xmap, p, s)
+          : launch_engine_cc(fp.sk.maxc, wmap, xmap, p, s);
   if (ce == cudaErrorNotSupported) return DEC_ERR_UNSUPPORTED_SHAPE;
   if (ce != cudaSuccess) return DEC_ERR_CUDA;
   FrontFinishParams f;
@@ -697,11 +719,32 @@ dec_status moe_front(const dec_bf16 *X, const dec_bf16 *Wcat, int B, int K, int 
   f.probs = probs_opt;
   f.route_map = route_map_opt;
   f.all_done = reinterpret_cast<int *>(wsb + fp.done_off);
-  ce = launch_front_finish(f, reinterpret_cast<cudaStream_t>(s));
+  ce = launch_front_finish(f, s);
   if (ce != cudaSuccess) return DEC_ERR_CUDA;
   t_last_variant = tc ? DEC_VARIANT_SPLITK_TC : DEC_VARIANT_SPLITK;
   return DEC_OK;
 }
+
+// A front end launched by moe_layer between the shared expert's and the routed
+// experts' launches.
+struct FrontCall {
+  const dec_bf16 *Wcat;
+  int L;
+  dec_bf16 *latent;
+  void *ws;
+  size_t ws_bytes;
+};
+
+dec_status moe_experts_impl(const dec_bf16 *X, const int32_t *topk_idx, const float *topk_w,
+                            const int32_t *route_map, const dec_bf16 *Wgu, const dec_bf16 *Wd,
+                            int E, const dec_bf16 *Wgu_shared, const dec_bf16 *Wd_shared, int B,
+                            int H, int I, int topk, dec_bf16 *Y, void *ws, size_t ws_bytes,
+                            dec_stream_t main_stream, dec_stream_t side_stream,
+                            int side_max_ctas, const FrontCall *fc);
+
+}  // namespace
+
+extern "C" {
 
 size_t moe_experts_workspace_bytes(int B, int E, int topk, int H, int I) {
   if (B < 1 || B > MAX_B || E < 1 || E > MAX_E || topk < 1 || topk > MAX_TOPK || H < 1 || I < 1)
@@ -717,6 +760,55 @@ dec_status moe_experts(const dec_bf16 *X, const int32_t *topk_idx, const float *
                        const dec_bf16 *Wgu_shared, const dec_bf16 *Wd_shared, int B, int H,
                        int I, int topk, dec_bf16 *Y, void *ws, size_t ws_bytes,
                        dec_stream_t main_stream, dec_stream_t side_stream, int side_max_ctas) {
+  return moe_experts_impl(X, topk_idx, topk_w, route_map, Wgu, Wd, E, Wgu_shared, Wd_shared, B,
+                          H, I, topk, Y, ws, ws_bytes, main_stream, side_stream, side_max_ctas,
+                          nullptr);
+}
+
+size_t moe_layer_workspace_bytes(int B, int E, int L, int H, int I, int topk) {
+  const size_t e = moe_experts_workspace_bytes(B, E, topk, H, I);
+  const size_t f = moe_front_workspace_bytes(B, E, L, H);
+  return (e == 0 || f == 0) ? 0 : align_up(e) + f;
+}
+
+dec_status moe_layer(const dec_bf16 *X, const dec_bf16 *Wcat, int E, int L, int topk,
+                     const dec_bf16 *Wgu, const dec_bf16 *Wd, const dec_bf16 *Wgu_shared,
+                     const dec_bf16 *Wd_shared, int B, int H, int I, dec_bf16 *latent,
+                     int32_t *topk_idx, float *topk_w, int32_t *route_map_opt, dec_bf16 *Y,
+                     void *ws, size_t ws_bytes, dec_stream_t main_stream,
+                     dec_stream_t side_stream, int side_max_ctas) {
+  if (!X || !Wcat || !ws) return DEC_ERR_INVALID_ARG;
+  if (L < 0 || (L > 0 && !latent)) return DEC_ERR_INVALID_ARG;
+  if (!aligned16(Wcat)) return DEC_ERR_MISALIGNED;
+  const size_t e = moe_experts_workspace_bytes(B, E, topk, H, I);
+  const size_t f = moe_front_workspace_bytes(B, E, L, H);
+  if (e == 0 || f == 0) {
+    if (B < 1 || E < 1 || topk < 1 || H < 1 || I < 1) return DEC_ERR_INVALID_ARG;
+    return DEC_ERR_UNSUPPORTED_SHAPE;
+  }
+  if (ws_bytes < align_up(e) + f) return DEC_ERR_WORKSPACE_TOO_SMALL;
+  if (H % 8 != 0) return DEC_ERR_MISALIGNED;
+  FrontCall fc;
+  fc.Wcat = Wcat;
+  fc.L = L;
+  fc.latent = latent;
+  fc.ws = static_cast<char *>(ws) + align_up(e);
+  fc.ws_bytes = f;
+  return moe_experts_impl(X, topk_idx, topk_w, route_map_opt, Wgu, Wd, E, Wgu_shared, Wd_shared,
+                          B, H, I, topk, Y, ws, align_up(e), main_stream, side_stream,
+                          side_max_ctas, &fc);
+}
+
+}  // extern "C"
+
+namespace {
+
+dec_status moe_experts_impl(const dec_bf16 *X, const int32_t *topk_idx, const float *topk_w,
+                            const int32_t *route_map, const dec_bf16 *Wgu, const dec_bf16 *Wd,
+                            int E, const dec_bf16 *Wgu_shared, const dec_bf16 *Wd_shared, int B,
+                            int H, int I, int topk, dec_bf16 *Y, void *ws, size_t ws_bytes,
+                            dec_stream_t main_stream, dec_stream_t side_stream,
+                            int side_max_ctas, const FrontCall *fc) {
   if (!X || !topk_idx || !topk_w || !Wgu || !Wd || !Y || !ws) return DEC_ERR_INVALID_ARG;
   if ((Wgu_shared == nullptr) != (Wd_shared == nullptr)) return DEC_ERR_INVALID_ARG;
   if (B < 1 || E < 1 || H < 1 || I < 1 || topk < 1 || side_max_ctas < 0)
@@ -848,11 +940,21 @@ dec_status moe_experts(const dec_bf16 *X, const int32_t *topk_idx, const float *
     if (overlap && (ce = cudaEventRecord(ev->join, ss)) != cudaSuccess) return DEC_ERR_CUDA;
   }
 
+  // ---- moe_layer: the front end runs now, while the shared expert streams its
+  // weights on the side stream, on the SMs the routed experts will use; it writes the
+  // routing and the route map the routed launches read
+  if (fc != nullptr) {
+    st = run_front(X, fc->Wcat, B, H, E, fc->L, topk, fc->latent, const_cast<int32_t *>(topk_idx),
+                   const_cast<float *>(topk_w), nullptr, rm, fc->ws, fc->ws_bytes, g_main, ms);
+    if (st != DEC_OK) return st;
+  }
+  const bool have_map = route_map != nullptr || fc != nullptr;
+
   // ---- routed experts, main stream
-  // without a caller route map the gather launch validates topk_idx and builds it
-  ce = route_map ? launch_gather_rows(X, rm, B, topk, E, H, Xg, ms)
-                 : launch_gather_map(X, topk_idx, B, topk, E, H, Xg, rm, d->status,
-                                     2 * d->num_sms, ms);
+  // without a route map the gather launch validates topk_idx and builds it
+  ce = have_map ? launch_gather_rows(X, rm, B, topk, E, H, Xg, ms)
+                : launch_gather_map(X, topk_idx, B, topk, E, H, Xg, rm, d->status,
+                                    2 * d->num_sms, ms);
   if (ce != cudaSuccess) return DEC_ERR_CUDA;
   {
     EngineParams p;
@@ -867,7 +969,7 @@ dec_status moe_experts(const dec_bf16 *X, const int32_t *topk_idx, const float *
     p.w_group_rows = 2 * I;
     p.up_row_off = I;
     p.A = A;
-    p.rm_ready = (route_map != nullptr && early_route_map()) ? 1 : 0;
+    p.rm_ready = (have_map && early_route_map()) ? 1 : 0;
     if ((ce = engine(m_wgu, m_xg, p, ms)) != cudaSuccess) return DEC_ERR_CUDA;
     base(p, MODE_DOWN, H, I, ep.Td, ep.KBd, gd, 1, ep.main_part_off, ep.main_cnt_off);
     p.w_group_rows = H;
@@ -881,6 +983,10 @@ dec_status moe_experts(const dec_bf16 *X, const int32_t *topk_idx, const float *
     return DEC_ERR_CUDA;
   return DEC_OK;
 }
+
+}  // namespace
+
+extern "C" {
 
 // ------------------------------------------------------------- L2 prefetch ----
 

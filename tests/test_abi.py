@@ -91,5 +91,10 @@ def test_host_argument_checks_need_no_device(ssd):
     assert lib.dec_set_wait_limit_ns(10) == ssd.DEC_ERR_INVALID_ARG
     assert lib.dec_debug_wait_timeout(10, s) == ssd.DEC_ERR_INVALID_ARG
     assert lib.dec_sim_comm_wait(999, s) == ssd.DEC_ERR_INVALID_ARG
+    l_args = [N0, A, 384, 512, 8, A, A, A, A, 4, 7168, 2048, A, A, A, N0, A, A, 1 << 30, s, s, 0]
+    assert lib.moe_layer(*l_args) == ssd.DEC_ERR_INVALID_ARG  # X missing
+    bad = list(l_args)
+    bad[0], bad[12] = A, N0  # latent missing with L > 0
+    assert lib.moe_layer(*bad) == ssd.DEC_ERR_INVALID_ARG
     assert lib.dec_sim_comm_wait(1000000001, s) == ssd.DEC_ERR_INVALID_ARG
     assert lib.dec_set_fault_inject(-1) == ssd.DEC_ERR_INVALID_ARG

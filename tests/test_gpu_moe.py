@@ -345,3 +345,43 @@ def test_invalid_routing_is_reported_not_faulted(env):
     y_ref, _ = oracle.moe_experts(inputs.bits(X), idx.cpu().numpy(), w.cpu().numpy().astype(np.float64),
                                   inputs.bits(Wgu), inputs.bits(Wd))
     assert_close(to_f64(oracle, Y), y_ref, "valid routing after invalid ones")
+
+
+@pytest.mark.parametrize("B,k", [(1, 4), (5, 2), (17, 4), (64, 8)])
+@pytest.mark.parametrize("side", [True, False])
+def test_moe_layer_matches_oracle(env, B, k, side):
+    """moe_layer (front end while the shared expert streams on the side stream, then
+    the routed experts): routing bit-exact against the oracle, latent, weights and Y
+    within tolerance, route map equal to the rebuilt one."""
+    torch, ssd, oracle, dev = env
+    from split_switched_decode_gb300 import inputs
+    E, L, H, I = 40, 24, 256, 128
+    X = inputs.activations(B, H, dev, 11, "layer")
+    Wc = inputs.weight(E + L, H, dev, 11, "layer_wc")
+    Wgu, Wd = inputs.expert_bank(E, H, I, dev, 11, "layer_bank")
+    Wgs, Wds = inputs.shared_expert(H, I, dev, 11, "layer_shared")
+    lat = torch.empty(B, L, dtype=torch.bfloat16, device=dev)
+    idx = torch.full((B, k), -1, dtype=torch.int32, device=dev)
+    w = torch.empty(B, k, dtype=torch.float32, device=dev)
+    rm = torch.full((ssd.moe_route_map_ints(B, E, k),), -7, dtype=torch.int32, device=dev)
+    Y = torch.empty(B, H, dtype=torch.bfloat16, device=dev)
+    ws = ssd.workspace(ssd.moe_layer_workspace_bytes(B, E, L, H, I, k), dev)
+    ss = torch.cuda.Stream(device=dev) if side else None
+    ssd.moe_layer(X, Wc, E, L, k, Wgu, Wd, Wgs, Wds, lat, idx, w, Y, ws, route_map=rm,
+                  side_stream=ss)
+    torch.cuda.synchronize()
+    assert ssd.dec_sync_status() == ssd.DEC_OK
+    ref = oracle.moe_front(inputs.bits(X), inputs.bits(Wc), E, L, k)
+    assert np.array_equal(idx.cpu().numpy(), ref["idx"]), "top-k differs from the oracle"
+    assert_close(w.cpu().numpy().astype(np.float64), ref["w"], "routing weights")
+    assert_close(to_f64(oracle, lat), oracle.bf16_to_f64(ref["latent"]), "latent")
+    m = oracle.route_map(ref["idx"], E)
+    r, P = rm.cpu().numpy(), B * k
+    assert np.array_equal(r[:E], m["counts"])
+    assert np.array_equal(r[E:2 * E + 1], m["offsets"])
+    assert np.array_equal(r[2 * E + 1:2 * E + 1 + P], m["pairs"])
+    assert np.array_equal(r[2 * E + 1 + P:2 * E + 1 + 2 * P], m["pos"])
+    assert r[2 * E + 1 + 2 * P] == m["num_used"]
+    y_ref, _ = oracle.moe_experts(inputs.bits(X), ref["idx"], ref["w"], inputs.bits(Wgu),
+                                  inputs.bits(Wd), inputs.bits(Wgs), inputs.bits(Wds))
+    assert_close(to_f64(oracle, Y), y_ref, f"moe_layer B={B}")
