@@ -719,8 +719,10 @@ def main():
                            "l2": "cold: every weight tensor is re-read only after >3x L2 of "
                                  "other weight traffic (step), rotating copies >=3x L2 (sweep)",
                            "timing": "CUDA graph replay, CUDA events on the replay stream",
-                           "moe_call": "moe_layer (shared expert overlapping the front end)"
-                                       if wl.layer else "moe_front + l2_prefetch + moe_experts",
+                           "moe_call": ("moe_layer (shared expert overlapping the front end)"
+                                        if wl.layer else
+                                        "moe_front + l2_prefetch + moe_experts" if wl.prefetch
+                                        else "moe_front + moe_experts"),
                            "l2_prefetch_in_step": wl.prefetch and not wl.layer,
                            "parallelism": f"replicas x{world}"},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
