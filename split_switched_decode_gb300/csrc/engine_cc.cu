@@ -185,17 +185,6 @@ int engine_maxc_for(int ncols) {
   return m;
 }
 
-size_t engine_cc_smem_bytes(int maxc) {
-  switch (maxc) {
-    case 2: return CCConfig<2>::SMEM;
-    case 4: return CCConfig<4>::SMEM;
-    case 8: return CCConfig<8>::SMEM;
-    case 16: return CCConfig<16>::SMEM;
-    case 32: return CCConfig<32>::SMEM;
-    default: return CCConfig<64>::SMEM;
-  }
-}
-
 cudaError_t launch_engine_cc(int maxc, const CUtensorMap &wmap, const CUtensorMap &xmap,
                              const EngineParams &p, cudaStream_t s) {
   if (p.ngrp != 1) return cudaErrorInvalidValue;  // wide projections: tensor cores only

@@ -458,17 +458,6 @@ cudaError_t launch_t(const CUtensorMap &wmap, const CUtensorMap &xmap, const Eng
 
 }  // namespace
 
-size_t engine_tc_smem_bytes(int maxc) {
-  switch (maxc) {
-    case 2: return TCConfig<2, 1>::SMEM;
-    case 4: return TCConfig<4, 1>::SMEM;
-    case 8: return TCConfig<8, 1>::SMEM;
-    case 16: return TCConfig<16, 1>::SMEM;
-    case 32: return TCConfig<32, 1>::SMEM;
-    default: return TCConfig<64, 1>::SMEM;
-  }
-}
-
 cudaError_t launch_engine_tc(int maxc, const CUtensorMap &wmap, const CUtensorMap &xmap,
                              const EngineParams &p, cudaStream_t s) {
   if (p.pair && ((p.ngrp > 1 && maxc != 64) || p.grouped || p.defer || p.mode != MODE_LINEAR ||

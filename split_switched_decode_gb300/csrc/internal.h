@@ -99,12 +99,10 @@ cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, 
 
 // ------------------------------------------------------------- engine_cc.cu --
 int engine_maxc_for(int ncols);                 // 2, 4, 8, 16, 32 or 64
-size_t engine_cc_smem_bytes(int maxc);
 cudaError_t launch_engine_cc(int maxc, const CUtensorMap &wmap, const CUtensorMap &xmap,
                              const EngineParams &p, cudaStream_t s);
 
 // ------------------------------------------------------------- engine_tc.cu --
-size_t engine_tc_smem_bytes(int maxc);
 cudaError_t launch_engine_tc(int maxc, const CUtensorMap &wmap, const CUtensorMap &xmap,
                              const EngineParams &p, cudaStream_t s);
 
