@@ -104,7 +104,7 @@ def test_decode_input_projection_full_size(env, B):
     assert_close(to_f64(oracle, Y)[:, rows], y_ref, f"input projection B={B}")
 
 
-@pytest.mark.parametrize("B", [1, 3, 16, 64])
+@pytest.mark.parametrize("B", [1, 2, 3, 4, 8, 16, 32, 64])
 def test_output_projection_with_residual_full_size(env, B):
     """K=16384, N=7168 with the fused residual; sampled rows against the oracle."""
     torch, ssd, oracle, dev = env
