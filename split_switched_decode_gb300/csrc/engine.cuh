@@ -16,7 +16,10 @@
 // workspace slot and bumps the tile's arrival counter, and the worker that arrives
 // last adds the partials of all contributors in worker order (fixed order, so the
 // result is bit-identical run to run for a fixed G), runs the epilogue and resets the
-// counter to zero for the next launch. Nobody waits on another CTA.
+// counter to zero for the next launch; no CTA waits on another. The one exception is
+// the tensor-core "pair" schedule (engine_tc.cu): when every tile is split into two
+// k-halves, the two workers of a tile are launched as a 2-CTA cluster, which the
+// hardware co-schedules, and add their halves on chip after a cluster barrier.
 #pragma once
 
 #include "common.cuh"

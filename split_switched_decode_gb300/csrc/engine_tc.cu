@@ -22,6 +22,14 @@
 // N = 16 x boxes <= 256 per K step into 2 x 64*NG accumulator columns (all 512 at
 // NG = 4) -- and the epilogue reduces and stores the column groups one after another,
 // each with its own partial slots and arrival counter.
+//
+// Pair schedule (p.pair): every tile is split into exactly two k-halves and the two
+// workers of a tile run as a 2-CTA cluster. Instead of partial tiles in global memory
+// and an arrival counter, each CTA hands the partner the accumulator columns the
+// partner finishes through distributed shared memory (the epilogue scratch, or for
+// wide tiles the idle stage buffers once both CTAs are past their MMAs) and, after a
+// cluster barrier, adds first half + second half for its own columns -- the same order
+// as the global reduction -- and stores Y.
 #include <atomic>
 
 #include "engine.cuh"
