@@ -292,6 +292,14 @@ bool early_route_map() {
   return true;
 }
 
+// Whether the front end's finishing kernel builds the route map inside one thread-block
+// cluster over the tokens (B <= 8) instead of in the CTA that routes the last token
+// (DEC_FRONT_CLUSTER=0 turns it off).
+bool front_cluster() {
+  if (const char *s = std::getenv("DEC_FRONT_CLUSTER")) return std::atoi(s) != 0;
+  return true;
+}
+
 // Wide projections (B > 64) defer their reduction to the finishing kernel unless
 // DEC_WIDE_DEFER=0.
 bool wide_defer() {
@@ -719,6 +727,7 @@ dec_status run_front(const dec_bf16 *X, const dec_bf16 *Wcat, int B, int K, int 
   f.probs = probs_opt;
   f.route_map = route_map_opt;
   f.all_done = reinterpret_cast<int *>(wsb + fp.done_off);
+  f.cluster = (route_map_opt != nullptr && B <= 8 && front_cluster()) ? 1 : 0;
   ce = launch_front_finish(f, s);
   if (ce != cudaSuccess) return DEC_ERR_CUDA;
   t_last_variant = tc ? DEC_VARIANT_SPLITK_TC : DEC_VARIANT_SPLITK;

@@ -111,28 +111,6 @@ __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// ---------------------------------------------------- 2-CTA cluster helpers ----
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// Address of the same shared-memory location in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t cluster_map(const void *p, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-// Every thread of both CTAs arrives (release) and waits (acquire): the partner's
-// distributed-shared-memory stores made before it are visible after it.
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 // Shared-memory matrix descriptor of a K-major operand stored with the 128-byte
 // swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart (stride byte offset),
 // leading byte offset unused for this layout, descriptor version 1, layout 2 (128B).
@@ -208,6 +186,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // pair mode: every thread arrives here and waits before this CTA's first store into
+  // the partner's shared memory (epilogue warps: before their loop; producer and MMA
+  // warps: after theirs), so no store reaches a CTA that has not started
+  if (p.pair) cluster_arrive_relaxed();
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
@@ -264,6 +246,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   } else {
     // --------------------------------------------------------------- epilogue
     griddep_wait();
+    if (p.pair) cluster_wait();
     const int r = 32 * (warp & 3) + lane;  // tile row == tensor-memory lane
     uint32_t seg = 0;
     for (int64_t it = begin; it < end; ++seg) {
@@ -331,6 +314,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       it += s.kb1 - s.kb0;
     }
   }
+  if (p.pair && warp < 2) cluster_wait();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

@@ -126,6 +126,7 @@ struct FrontFinishParams {
   float *probs;
   int32_t *route_map;
   int *all_done;  // [1], zero between launches
+  int cluster;    // 1: chunk 0's B <= 8 CTAs form a cluster that builds the route map
 };
 cudaError_t launch_front_finish(const FrontFinishParams &f, cudaStream_t s);
 

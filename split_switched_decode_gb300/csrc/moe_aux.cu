@@ -131,22 +131,29 @@ __device__ __forceinline__ float sum_partials(const float *partials, size_t slot
 }
 
 // Second half of the MoE front end, launched programmatically after the router +
-// latent product (which only stored its partial tiles). CTA (c, b) owns rows
+// latent product (which only stored its partial tiles). CTA (b, c) owns rows
 // 512c .. 512c+511 of token b; thread i adds row 512c+i's partials of every worker of
 // its tile in worker order (the product kernel's split, recomputed here) with all
-// loads in flight. Latent rows go out as bf16. CTA (0, b) holds all E <= 512 router
-// logits of token b in shared memory and routes the token with one warp; the CTA that
-// routes the last token (acquire-release counter) builds the route map. Spread over
+// loads in flight. Latent rows go out as bf16. CTA (b, 0) holds all E <= 512 router
+// logits of token b in shared memory and routes the token with one warp. Spread over
 // B * ceil((E+L)/512) CTAs, the reduction costs one memory round trip.
+// The route map needs every token's routing. With f.cluster (B <= 8), the B CTAs of
+// chunk 0 form one thread-block cluster: each puts its token's expert ids into CTA 0's
+// shared memory and CTA 0 builds the map after a cluster barrier -- no global round
+// trip. Otherwise the CTA that routes the last token (acquire-release counter) reads
+// every token's ids back and builds it.
 __global__ void __launch_bounds__(512) front_finish_kernel(const FrontFinishParams f) {
   __shared__ float slog[MAX_E];
   __shared__ int32_t sidx[MAX_B * MAX_TOPK];
   __shared__ unsigned long long smask[MAX_E];
   __shared__ int soff[MAX_E];
   __shared__ int flag;
+  const int b = blockIdx.x, c = blockIdx.y, i = threadIdx.x;
+  // c is uniform over a cluster (clusters span tokens only)
+  const bool clustered = f.cluster && c == 0;
+  if (clustered) cluster_arrive_relaxed();
   griddep_wait();
   griddep_launch_dependents();
-  const int c = blockIdx.x, b = blockIdx.y, i = threadIdx.x;
   const int n = c * 512 + i;
   const size_t slot_floats = static_cast<size_t>(128) * f.slot_cols;
   if (n < f.E + f.L) {
@@ -165,7 +172,19 @@ __global__ void __launch_bounds__(512) front_finish_kernel(const FrontFinishPara
   if (i < 32)
     route_tokens_warp(slog, 1, f.E, f.topk, f.topk_idx + static_cast<size_t>(b) * f.topk,
                       f.topk_w + static_cast<size_t>(b) * f.topk,
-                      f.probs ? f.probs + static_cast<size_t>(b) * f.E : nullptr, nullptr, 0, 1);
+                      f.probs ? f.probs + static_cast<size_t>(b) * f.E : nullptr,
+                      clustered ? sidx : nullptr, 0, 1);
+  if (clustered) {
+    // rank b == token b: its ids go to sidx[b*topk ..] of rank 0 (rank 0 writes its own
+    // ids onto themselves); every CTA of the cluster has started once the wait returns
+    cluster_wait();
+    if (i < f.topk)  // lane i wrote sidx[i] itself
+      st_cluster_u32(cluster_map(sidx + b * f.topk + i, 0u), static_cast<uint32_t>(sidx[i]));
+    cluster_sync_all();
+    if (b != 0) return;
+    build_route_map(sidx, f.B, f.topk, f.E, f.route_map, smask, soff, 512, 1, i);
+    return;
+  }
   if (f.route_map == nullptr) return;
   __syncthreads();
   if (i == 0) flag = (atom_add_acq_rel_gpu(f.all_done, 1) == f.B - 1);
@@ -351,7 +370,9 @@ cudaError_t launch_comm_wait(uint64_t ns, cudaStream_t s) {
 }
 
 cudaError_t launch_front_finish(const FrontFinishParams &f, cudaStream_t s) {
-  return launch_pdl(front_finish_kernel, dim3((f.E + f.L + 511) / 512, f.B), dim3(512), 0, s, f);
+  const dim3 grid(f.B, (f.E + f.L + 511) / 512);
+  if (f.cluster) return launch_pdl_cluster(front_finish_kernel, grid, dim3(512), 0, s, f.B, f);
+  return launch_pdl(front_finish_kernel, grid, dim3(512), 0, s, f);
 }
 
 cudaError_t launch_linear_finish(const LinearFinishParams &f, cudaStream_t s) {

@@ -88,6 +88,28 @@ def test_moe_front_ragged_shapes(env, B, E, L, K, k):
     _check_front(env, X, Wc, E, L, k, f"front B={B} E={E} L={L} K={K} k={k}")
 
 
+@pytest.mark.parametrize("B", [1, 2, 3, 7, 8, 9])
+def test_moe_front_cluster_route_map_equals_counter_path(env, monkeypatch, B):
+    """Up to 8 tokens, the finishing kernel's router CTAs form one thread-block cluster
+    and CTA 0 builds the route map from the ids the others put in its shared memory;
+    DEC_FRONT_CLUSTER=0 builds it in the CTA that routes the last token instead. Every
+    output is bit-identical, and both match the oracle (B = 9 takes the counter path
+    either way)."""
+    torch, ssd, oracle, dev = env
+    from split_switched_decode_gb300 import inputs
+    E, L, K, k = 384, 512, 7168, 8
+    X = inputs.activations(B, K, dev, 8, "cfx")
+    Wc = inputs.weight(E + L, K, dev, 8, "cfw")
+    ref = _check_front(env, X, Wc, E, L, k, f"front cluster B={B}")
+    a = _run_front(env, X, Wc, E, L, k)
+    monkeypatch.setenv("DEC_FRONT_CLUSTER", "0")
+    c = _run_front(env, X, Wc, E, L, k)
+    for x, y, name in zip(a, c, ["latent", "idx", "w", "probs", "route map"]):
+        assert torch.equal(x, y), name
+    assert ssd.dec_sync_status() == ssd.DEC_OK
+    assert np.array_equal(c[1].cpu().numpy(), ref["idx"])
+
+
 def test_moe_front_ties_go_to_lower_index(env):
     """Duplicate router rows in one tile give bit-identical fp32 logits: lower index first.
     All-zero router rows give equal logits: experts 0..k-1, weights 1/k, probs 1/E."""
