@@ -168,8 +168,8 @@ DEC_API dec_status dec_splitk_gemm(const dec_bf16 *X, const dec_bf16 *W, const d
 /*
  * dec_splitk_gemm without a workspace, for callers that cannot allocate device memory
  * (for example a plugin running inside another runtime that owns the GPU memory pool,
- * or a serving loop whose memory is frozen after warm-up). The paper has no counterpart:
- * it is an addition of this library. Same result and arguments as dec_splitk_gemm with
+ * or a serving loop whose memory is frozen after warm-up). The blog post has no
+ * counterpart: it is an addition of this library. Same result and arguments as dec_splitk_gemm with
  * split_k = 0; the scratch lives in a fixed 16 MiB device array inside the library
  * (held on every GPU that loads it until the process exits), so a shape whose split-K
  * scratch would exceed 16 MiB is rejected with DEC_ERR_WORKSPACE_TOO_SMALL, and more than
@@ -224,8 +224,11 @@ DEC_API size_t moe_route_map_ints(int B, int E, int topk);
  * X [B,K]; latent [B,L] (NULL allowed when L == 0); topk_idx int32 [B,topk];
  * topk_w fp32 [B,topk]; probs_opt fp32 [B,E] or NULL; route_map_opt int32
  * [moe_route_map_ints(B,E,topk)] or NULL. E in 1..512, topk in 1..min(E,16), L >= 0.
- * Two launches on `s`: the product, then a routing kernel (one warp per token) that
- * starts as the product's CTAs retire (programmatic dependent launch).
+ * Two launches on `s`: the product, then a finishing kernel that starts as the
+ * product's CTAs retire (programmatic dependent launch): it adds the partial tiles,
+ * routes each token with one warp and builds the route map -- for B <= 8 inside one
+ * thread-block cluster of the routing CTAs, otherwise in the CTA that routes the last
+ * token. Both ways give the same bits.
  */
 DEC_API size_t moe_front_workspace_bytes(int B, int E, int L, int K);
 DEC_API dec_status moe_front(const dec_bf16 *X, const dec_bf16 *Wcat, int B, int K, int E, int L,
