@@ -1,6 +1,7 @@
 // api.cu -- host side of the C ABI declared in include/split_switched_decode.h:
 // argument checks, the batch-size kernel switch, workspace planning, TMA descriptor
 // encoding, side-stream scheduling of the shared expert, and error reporting.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdlib>
@@ -182,9 +183,11 @@ bool pair_shape(int N, int K, int num_sms) {
 // The batch-size switch's tiny-kernel range: B <= 2, except that a shape on the pair
 // schedule takes tensor cores from B = 2 (measured on the input projection: 21.7
 // instead of 22.6 us at B = 2; at B = 1 the tiny kernel stays ahead, 20.5 vs 21.8 us).
-// DEC_TINY_MAX_B overrides.
+// The kernel takes up to 4 rows, but from 3 rows it is issue-bound (output projection
+// 40.7 / 47.7 us at B = 3 / 4 against 41.2 / 41.1 us on tensor cores). DEC_TINY_MAX_B
+// overrides (at most 4).
 int tiny_max_batch(int N, int K, int num_sms) {
-  if (const char *s = std::getenv("DEC_TINY_MAX_B")) return std::atoi(s);
+  if (const char *s = std::getenv("DEC_TINY_MAX_B")) return std::min(std::atoi(s), TINY_MAX_NB);
   return pair_shape(N, K, num_sms) && pair_split_min_batch() <= 2 ? 1 : 2;
 }
 
@@ -587,7 +590,7 @@ dec_status dec_gemv(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 *R, dec
                     int N, int K, dec_stream_t s) {
   dec_status st = check_linear_args(X, W, Y, B, N, K);
   if (st != DEC_OK) return st;
-  if (B > 2) return DEC_ERR_UNSUPPORTED_SHAPE;
+  if (B > TINY_MAX_NB) return DEC_ERR_UNSUPPORTED_SHAPE;
   cudaError_t ce;
   DeviceInfo *d = device_info(&ce);
   if (!d) return DEC_ERR_CUDA;

@@ -1,12 +1,13 @@
-// gemv_tiny.cu -- tiny-matrix projection for decode batches of 1 and 2.
+// gemv_tiny.cu -- tiny-matrix projection for decode batches of 1 to 4.
 //
 // "Hyper Optimizing Kimi K3 in vLLM", Part 1 / 1 "Tune shapes for the workload": at
 // batch sizes 1-2 the projections use a dedicated small-matrix kernel.
 //
-//     Y[b,n] = bf16( sum_k X[b,k] W[n,k] (+ R[b,n]) ),  b < NB in {1,2}
+//     Y[b,n] = bf16( sum_k X[b,k] W[n,k] (+ R[b,n]) ),  b < NB in 1..4
 //
 // Design (GB300): the op moves N*K*2 bytes of weights and does 2*NB flops per weight,
-// so it is bound by HBM bandwidth. Each CTA owns a contiguous block of rows; its 8
+// so at NB = 1-2 it is bound by HBM bandwidth (from NB = 3 on, by instruction issue:
+// bf16 unpacking plus NB fp32 FMAs per weight). Each CTA owns a contiguous block of rows; its 8
 // warps split every row into P k-pieces and cover the rows in R row-slots
 // (8 = P * R). A lane streams 16-byte weight chunks with the non-coherent,
 // no-L1-allocate load (16 loads in flight per lane: 4 rows x 4 chunks), multiplies
@@ -160,11 +161,22 @@ cudaError_t launch_gemv_tiny(const uint16_t *X, const uint16_t *W, const uint16_
   const int P = tiny_pieces(K);
   const int rows = (N + G - 1) / G;
   const size_t smem = static_cast<size_t>(rows) * P * B * sizeof(float);
-  if (B == 1)
-    return launch_pdl(gemv_tiny_kernel<1>, dim3(G), dim3(TINY_THREADS), smem, s, X, W, R, Y, N, K,
-                      P);
-  return launch_pdl(gemv_tiny_kernel<2>, dim3(G), dim3(TINY_THREADS), smem, s, X, W, R, Y, N, K,
-                    P);
+  switch (B) {
+    case 1:
+      return launch_pdl(gemv_tiny_kernel<1>, dim3(G), dim3(TINY_THREADS), smem, s, X, W, R, Y, N,
+                        K, P);
+    case 2:
+      return launch_pdl(gemv_tiny_kernel<2>, dim3(G), dim3(TINY_THREADS), smem, s, X, W, R, Y, N,
+                        K, P);
+    case 3:
+      return launch_pdl(gemv_tiny_kernel<3>, dim3(G), dim3(TINY_THREADS), smem, s, X, W, R, Y, N,
+                        K, P);
+    case 4:
+      return launch_pdl(gemv_tiny_kernel<4>, dim3(G), dim3(TINY_THREADS), smem, s, X, W, R, Y, N,
+                        K, P);
+    default:
+      return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace ssd

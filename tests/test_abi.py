@@ -64,7 +64,7 @@ def test_host_argument_checks_need_no_device(ssd):
     assert lib.dec_gemv(A, A, N0, A, 65, 8, 8, s) == ssd.DEC_ERR_UNSUPPORTED_SHAPE
     assert lib.dec_gemv(A, A, N0, A, 1, 8, 12, s) == ssd.DEC_ERR_MISALIGNED
     assert lib.dec_gemv(U, A, N0, A, 1, 8, 8, s) == ssd.DEC_ERR_MISALIGNED
-    assert lib.dec_gemv(A, A, N0, A, 3, 8, 8, s) == ssd.DEC_ERR_UNSUPPORTED_SHAPE
+    assert lib.dec_gemv(A, A, N0, A, 5, 8, 8, s) == ssd.DEC_ERR_UNSUPPORTED_SHAPE
     assert lib.dec_splitk_gemm(A, A, N0, A, 4, 8, 8, -1, 0, A, 0, s) == ssd.DEC_ERR_INVALID_ARG
     assert lib.dec_splitk_gemm(A, A, N0, A, 4, 8, 8, 0, 2, A, 0, s) == ssd.DEC_ERR_INVALID_ARG
     assert lib.dec_linear(A, N0, N0, A, 4, 8, 8, A, 0, s) == ssd.DEC_ERR_INVALID_ARG

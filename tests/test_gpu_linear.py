@@ -54,7 +54,9 @@ def _oracle_rows(env, X, W, R, rows=None):
 
 @pytest.mark.parametrize("B,N,K", [(1, 2048, 1024), (2, 2048, 1024), (1, 1000, 328),
                                    (2, 77, 8), (1, 8192, 7168), (2, 8192, 7168),
-                                   (1, 3, 16392)])
+                                   (1, 3, 16392), (3, 2048, 1024), (4, 2048, 1024),
+                                   (3, 77, 8), (4, 1000, 328), (3, 3, 16392),
+                                   (4, 7168, 16384)])
 @pytest.mark.parametrize("residual", [False, True])
 def test_tiny_kernel_matches_oracle(env, B, N, K, residual):
     torch, ssd, oracle, dev = env
@@ -149,8 +151,8 @@ def test_workspace_reusable_across_calls(env):
     assert int(ws[-counter_bytes:].view(torch.int32).abs().sum()) == 0
 
 
-@pytest.mark.parametrize("variant,B", [("tiny", 1), ("tiny", 2), ("splitk", 1), ("splitk", 2),
-                                       ("splitk", 7)])
+@pytest.mark.parametrize("variant,B", [("tiny", 1), ("tiny", 2), ("tiny", 3), ("tiny", 4),
+                                       ("splitk", 1), ("splitk", 2), ("splitk", 7)])
 def test_exact_pins_on_gpu(env, variant, B):
     """One-hot rows give weight columns exactly; W=0 gives R exactly; small integers sum
     exactly in fp32 (|partial sums| < 2^24)."""
@@ -161,7 +163,7 @@ def test_exact_pins_on_gpu(env, variant, B):
         N, K = 260, 520
         W = inputs.weight(N, K, dev, 5)
         X = torch.zeros(B, K, dtype=torch.bfloat16, device=dev)
-        ks = [3, K - 1][:B]
+        ks = [3, K - 1, 100, 257, 8, 9, 10][:B]
         for b, k in enumerate(ks):
             X[b, k] = 1.0
         Y = torch.empty(B, N, dtype=torch.bfloat16, device=dev)
