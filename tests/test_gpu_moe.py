@@ -79,7 +79,8 @@ def test_moe_front_full_size(env, B):
 
 @pytest.mark.parametrize("B,E,L,K,k", [(1, 40, 24, 200, 3), (5, 130, 0, 456, 16),
                                        (33, 512, 8, 64, 1), (64, 16, 100, 1032, 16),
-                                       (2, 1, 0, 8, 1)])
+                                       (2, 1, 0, 8, 1), (64, 512, 0, 128, 16),
+                                       (8, 512, 512, 136, 16)])
 def test_moe_front_ragged_shapes(env, B, E, L, K, k):
     torch, ssd, oracle, dev = env
     from split_switched_decode_gb300 import inputs
@@ -195,6 +196,27 @@ def test_moe_experts_small_bank(env, B, k, shared, side):
                                   None if Wgs is None else inputs.bits(Wgs),
                                   None if Wds is None else inputs.bits(Wds))
     assert_close(to_f64(oracle, Y), y_ref, f"experts B={B} k={k} shared={shared} side={side}")
+
+
+@pytest.mark.parametrize("B,E,k", [(64, 512, 16), (3, 1, 1), (64, 2, 2)])
+def test_moe_experts_routing_extremes(env, B, E, k):
+    """The largest routing the library takes (64 tokens x 16 slots over 512 experts:
+    1024 (token, slot) entries, most experts with one or two tokens), a single expert
+    with one slot, and two experts that every token uses."""
+    torch, ssd, oracle, dev = env
+    from split_switched_decode_gb300 import inputs
+    H, I = 128, 64
+    Wgu, Wd = inputs.expert_bank(E, H, I, dev, 9, "extreme_bank")
+    Wgs, Wds = inputs.shared_expert(H, I, dev, 9, "extreme_shared")
+    X = inputs.activations(B, H, dev, 9, "extreme_x")
+    idx_np, w_np = _routing(B, E, k, 90 + B + E)
+    idx = torch.from_numpy(idx_np).to(dev)
+    w = torch.from_numpy(w_np).to(dev)
+    Y = _run_experts(env, X, idx, w, Wgu, Wd, Wgs, Wds, side=True)
+    y_ref, _ = oracle.moe_experts(inputs.bits(X), idx_np, w_np.astype(np.float64),
+                                  inputs.bits(Wgu), inputs.bits(Wd), inputs.bits(Wgs),
+                                  inputs.bits(Wds))
+    assert_close(to_f64(oracle, Y), y_ref, f"experts extremes B={B} E={E} k={k}")
 
 
 def test_moe_experts_every_token_on_one_expert(env):
