@@ -18,8 +18,9 @@
  *    allocates or frees memory. Where a call needs scratch memory it takes a caller
  *    workspace whose size comes from the matching *_workspace_bytes() query; the
  *    workspace must be zero-filled once before its first use (cudaMemset), every
- *    completed call leaves it ready for the next, and one workspace must not be used
- *    by two calls that can run at the same time.
+ *    completed call leaves it ready for the next (a call whose kernels timed out, see
+ *    Errors, does not: zero-fill it again), and one workspace must not be used by two
+ *    calls that can run at the same time.
  *  - Alignment. X, W, Wcat, Wgu, Wd and every workspace must be 16-byte aligned; K and
  *    every other reduction length must be a multiple of 8 (rows are then 16-byte
  *    multiples). Other pointers need their natural alignment.
@@ -262,6 +263,9 @@ DEC_API dec_status moe_front(const dec_bf16 *X, const dec_bf16 *Wcat, int B, int
  * the expected weight bytes); the routed experts use the remaining SMs on `main`.
  * `side` may equal `main` (then no overlap). The call records events so that `main`
  * waits for `side` before the combine; on return all work is ordered after `main`.
+ * The combine is its own launch; with a route map and the environment switch
+ * DEC_FUSED_COMBINE=1 it runs instead inside the down launches (the tile that completes
+ * a token's 128-row block adds it up, in the same order: the same bits).
  * H % 128 == 0, I % 64 == 0, topk <= 16, E <= 512.
  */
 DEC_API size_t moe_experts_workspace_bytes(int B, int E, int topk, int H, int I);

@@ -303,6 +303,14 @@ bool front_cluster() {
   return true;
 }
 
+// Whether moe_experts, given a route map, adds the routed and shared outputs into Y
+// inside the down launches' epilogues (the tile that completes a (token, block) does
+// it) instead of in a separate combine launch (DEC_FUSED_COMBINE=0/1 overrides).
+bool fused_combine() {
+  if (const char *s = std::getenv("DEC_FUSED_COMBINE")) return std::atoi(s) != 0;
+  return false;
+}
+
 // Wide projections (B > 64) defer their reduction to the finishing kernel unless
 // DEC_WIDE_DEFER=0.
 bool wide_defer() {
@@ -449,7 +457,7 @@ bool plan_front(int B, int E, int L, int K, int num_sms, FrontPlan *fp, int spli
 struct ExpertsPlan {
   int maxc, Tg, Td, KBg, KBd;
   size_t rm_off, xg_off, a_off, yp_off, as_off, s_off;
-  size_t main_part_off, main_cnt_off, side_part_off, side_cnt_off, total;
+  size_t main_part_off, main_cnt_off, side_part_off, side_cnt_off, cmb_off, total;
 };
 
 bool plan_experts(int B, int E, int topk, int H, int I, int num_sms, ExpertsPlan *ep) {
@@ -482,6 +490,8 @@ bool plan_experts(int B, int E, int topk, int H, int I, int num_sms, ExpertsPlan
   o += part;
   ep->side_cnt_off = o;
   o += align_up(static_cast<size_t>(tmax) * sizeof(int));
+  ep->cmb_off = o;  // fused combine: one arrival counter per (token, 128-row block of H)
+  o += align_up(static_cast<size_t>(B) * ep->Td * sizeof(int));
   ep->total = o;
   return true;
 }
@@ -844,6 +854,9 @@ dec_status moe_experts_impl(const dec_bf16 *X, const int32_t *topk_idx, const fl
   cudaStream_t ms = reinterpret_cast<cudaStream_t>(main_stream);
   cudaStream_t ss = reinterpret_cast<cudaStream_t>(side_stream);
   const bool shared = (Wgu_shared != nullptr);
+  // The fused combine counts every (token, block)'s contributions, so it needs a routing
+  // that is valid by construction: a route map from the caller (moe_front) or moe_layer.
+  const bool fused = (route_map != nullptr || fc != nullptr) && fused_combine();
   const bool overlap = shared && (ss != ms);
   const int P = B * topk;
   char *wsb = static_cast<char *>(ws);
@@ -923,6 +936,16 @@ dec_status moe_experts_impl(const dec_bf16 *X, const int32_t *topk_idx, const fl
     p.wait_limit_ns = g_wait_limit_ns.load();
   };
 
+  auto set_combine = [&](EngineParams &p) {
+    p.cmb_cnt = reinterpret_cast<int *>(wsb + ep.cmb_off);
+    p.cmb_need = topk + (shared ? 1 : 0);
+    p.topk = topk;
+    p.topk_w = topk_w;
+    p.cmb_yp = Yp;
+    p.cmb_s = shared ? S : nullptr;
+    p.cmb_y = reinterpret_cast<uint16_t *>(Y);
+  };
+
   // ---- shared expert, side stream (or main when no second stream was given)
   if (shared) {
     cudaStream_t sst = overlap ? ss : ms;
@@ -945,6 +968,7 @@ dec_status moe_experts_impl(const dec_bf16 *X, const int32_t *topk_idx, const fl
          overlap ? ep.side_part_off : ep.main_part_off, overlap ? ep.side_cnt_off : ep.main_cnt_off);
     p.w_group_rows = H;
     p.Yp = S;
+    if (fused) set_combine(p);
     p.w_base = reinterpret_cast<const uint8_t *>(Wd_shared);
     p.w_rows = H;
     p.l2pf_kb = l2_prefetch_kblocks();
@@ -986,12 +1010,15 @@ dec_status moe_experts_impl(const dec_bf16 *X, const int32_t *topk_idx, const fl
     base(p, MODE_DOWN, H, I, ep.Td, ep.KBd, gd, 1, ep.main_part_off, ep.main_cnt_off);
     p.w_group_rows = H;
     p.Yp = Yp;
+    if (fused) set_combine(p);
     p.rm_ready = early_route_map() ? 1 : 0;
     if ((ce = engine(m_wd, m_a, p, ms)) != cudaSuccess) return DEC_ERR_CUDA;
   }
+  // Y is complete once both streams are done: the main stream waits for the side one
   if (overlap && (ce = cudaStreamWaitEvent(ms, ev->join, 0)) != cudaSuccess) return DEC_ERR_CUDA;
-  if ((ce = launch_combine(topk_w, rm, Yp, shared ? S : nullptr, B, topk, E, H, Y, ms)) !=
-      cudaSuccess)
+  if (!fused &&
+      (ce = launch_combine(topk_w, rm, Yp, shared ? S : nullptr, B, topk, E, H, Y, ms)) !=
+          cudaSuccess)
     return DEC_ERR_CUDA;
   return DEC_OK;
 }

@@ -300,6 +300,55 @@ __device__ __forceinline__ bool reduce_tile(const EngineParams &p, const SegInfo
   return true;
 }
 
+// Fused combine, after a down tile's rows are stored (128 threads, thread r = row r):
+// every column's token counts one more contribution to its (token, block t) counter;
+// the arrival that completes it (acquire-release, after a barrier over the 128 writers)
+// computes Y[b, block] = bf16( sum_{j ascending} w[b,j] * Yp[pos[b,j]] (+ S[b]) ) in the
+// same order and precision as the separate combine kernel, so the bits do not depend on
+// which tile finishes a block, and resets the counter for the next call.
+template <int MAXC>
+__device__ __forceinline__ void combine_tail(const EngineParams &p, const SegInfo &s, int r,
+                                             float *scratch, int bar_id) {
+  int *last = reinterpret_cast<int *>(scratch);  // [MAXC]: token this tile finishes, or -1
+  named_bar_sync(bar_id, 128);  // every row of this tile is stored
+  if (r < s.ncols) {
+    int b;
+    if (p.grouped) {
+      const int q = p.route_map[2 * p.E + 1 + min(max(s.xrow0 + r, 0), p.P - 1)];  // pairs
+      b = q / p.topk;
+    } else {
+      b = s.xrow0 + r;
+    }
+    b = min(max(b, 0), p.B - 1);
+    int *cnt = p.cmb_cnt + static_cast<size_t>(b) * p.T + s.t;
+    const bool done = atom_add_acq_rel_gpu(cnt, 1) == p.cmb_need - 1;
+    if (done) *cnt = 0;  // every contribution is in: nothing else touches it this call
+    last[r] = done ? b : -1;
+  }
+  named_bar_sync(bar_id, 128);
+  const int n = s.t * 128 + r;
+  const int32_t *pos = p.route_map + 2 * p.E + 1 + p.P;
+  for (int j = 0; j < s.ncols; ++j) {
+    const int b = last[j];
+    if (b < 0 || n >= p.N) continue;
+    float y[MAX_TOPK];
+#pragma unroll
+    for (int k = 0; k < MAX_TOPK; ++k) {
+      y[k] = 0.f;
+      if (k < p.topk) {
+        const int at = min(max(pos[b * p.topk + k], 0), p.P - 1);
+        y[k] = __ldcg(p.cmb_yp + static_cast<size_t>(at) * p.N + n);
+      }
+    }
+    float acc = 0.f;
+#pragma unroll
+    for (int k = 0; k < MAX_TOPK; ++k)
+      if (k < p.topk) acc = fmaf(p.topk_w[b * p.topk + k], y[k], acc);
+    if (p.cmb_s != nullptr) acc += __ldcg(p.cmb_s + static_cast<size_t>(b) * p.N + n);
+    p.cmb_y[static_cast<size_t>(b) * p.N + n] = f32_to_bf16_rn(acc);
+  }
+}
+
 // Epilogue of one finished tile, run by the same 128 threads. `scratch` holds at least
 // 64 * MAXC floats and is free on entry.
 template <int MAXC>
@@ -367,6 +416,7 @@ __device__ __forceinline__ void epilogue_rows(const EngineParams &p, const SegIn
       for (int j = 0; j < MAXC; ++j)
         if (j < s.ncols) p.Yp[static_cast<size_t>(s.xrow0 + j) * p.N + n] = v[j];
     }
+    if (p.cmb_cnt != nullptr) combine_tail<MAXC>(p, s, r, scratch, bar_id);
   }
 }
 

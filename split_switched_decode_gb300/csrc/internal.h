@@ -43,6 +43,16 @@ struct EngineParams {
   // MODE_GATEUP / MODE_DOWN: output row = group's first activation row + column
   uint16_t *A;  // [rows, N] bf16
   float *Yp;    // [rows, N] fp32
+  // MODE_DOWN inside moe_experts with the combine fused in: the tile that completes the
+  // last of a (token, 128-row block)'s contributions (its routed experts' down tiles and
+  // the shared expert's) writes that block of Y. nullptr: no fused combine.
+  int *cmb_cnt;          // [B][T] arrivals, zero between calls
+  int cmb_need;          // contributions per (token, block): topk (+1 with a shared expert)
+  int topk;
+  const float *topk_w;   // [B, topk]
+  const float *cmb_yp;   // routed down outputs [P, N] fp32, rows in route-map order
+  const float *cmb_s;    // shared expert output [B, N] fp32, or nullptr
+  uint16_t *cmb_y;       // Y [B, N] bf16
   // split-K reduction
   float *partials;  // [2*G][128*slot_cols]
   int *counters;    // one per (group, tile), zero between launches

@@ -164,13 +164,14 @@ def _routing(B, E, k, seed):
     return idx, w.astype(np.float32)
 
 
-def _run_experts(env, X, idx, w, Wgu, Wd, Wgs, Wds, rm=None, side=True, side_ctas=0):
+def _run_experts(env, X, idx, w, Wgu, Wd, Wgs, Wds, rm=None, side=True, side_ctas=0, ws=None):
     torch, ssd, oracle, dev = env
     B, H = X.shape
     E, twoI, _ = Wgu.shape
     k = idx.shape[1]
     Y = torch.empty(B, H, dtype=torch.bfloat16, device=dev)
-    ws = ssd.workspace(ssd.moe_experts_workspace_bytes(B, E, k, H, twoI // 2), dev)
+    if ws is None:
+        ws = ssd.workspace(ssd.moe_experts_workspace_bytes(B, E, k, H, twoI // 2), dev)
     ss = torch.cuda.Stream(device=dev) if side else None
     ssd.moe_experts(X, idx, w, rm, Wgu, Wd, Wgs, Wds, Y, ws, side_stream=ss, side_max_ctas=side_ctas)
     torch.cuda.synchronize()
@@ -217,6 +218,50 @@ def test_moe_experts_routing_extremes(env, B, E, k):
                                   inputs.bits(Wgu), inputs.bits(Wd), inputs.bits(Wgs),
                                   inputs.bits(Wds))
     assert_close(to_f64(oracle, Y), y_ref, f"experts extremes B={B} E={E} k={k}")
+
+
+def _host_route_map(oracle, idx_np, E, dev):
+    """The route-map layout of the header, assembled from the oracle's counting sort."""
+    import torch
+    m = oracle.route_map(idx_np, E)
+    B, k = idx_np.shape
+    used = np.zeros(E, dtype=np.int32)
+    used[:m["num_used"]] = m["used"]
+    rm = np.concatenate([m["counts"], m["offsets"], m["pairs"], m["pos"],
+                         np.array([m["num_used"]], dtype=np.int32), used]).astype(np.int32)
+    return torch.from_numpy(rm).to(dev)
+
+
+@pytest.mark.parametrize("B,k", [(1, 8), (5, 3), (17, 8), (64, 8), (64, 16)])
+@pytest.mark.parametrize("shared,side", [(True, True), (True, False), (False, False)])
+def test_fused_combine_equals_combine_launch(env, monkeypatch, B, k, shared, side):
+    """With a route map, the combine can run inside the down launches' epilogues (the
+    tile that completes a (token, 128-row block) adds it up, DEC_FUSED_COMBINE=1) or as
+    its own launch: the same bits either way, both within tolerance of the oracle, and a
+    second call on the same workspace (counters back at zero) gives the same bits."""
+    torch, ssd, oracle, dev = env
+    from split_switched_decode_gb300 import inputs
+    E, H, I = 24, 384, 128
+    Wgu, Wd = inputs.expert_bank(E, H, I, dev, 12, "fc_bank")
+    Wgs, Wds = inputs.shared_expert(H, I, dev, 12, "fc_shared") if shared else (None, None)
+    X = inputs.activations(B, H, dev, 12, "fc_x")
+    idx_np, w_np = _routing(B, E, k, 120 + B)
+    idx = torch.from_numpy(idx_np).to(dev)
+    w = torch.from_numpy(w_np).to(dev)
+    rm = _host_route_map(oracle, idx_np, E, dev)
+    ws = ssd.workspace(ssd.moe_experts_workspace_bytes(B, E, k, H, I), dev)
+    monkeypatch.setenv("DEC_FUSED_COMBINE", "1")
+    Y1 = _run_experts(env, X, idx, w, Wgu, Wd, Wgs, Wds, rm=rm, side=side, ws=ws)
+    Y1b = _run_experts(env, X, idx, w, Wgu, Wd, Wgs, Wds, rm=rm, side=side, ws=ws)
+    monkeypatch.setenv("DEC_FUSED_COMBINE", "0")
+    Y0 = _run_experts(env, X, idx, w, Wgu, Wd, Wgs, Wds, rm=rm, side=side)
+    assert torch.equal(Y1, Y0)
+    assert torch.equal(Y1, Y1b)
+    y_ref, _ = oracle.moe_experts(inputs.bits(X), idx_np, w_np.astype(np.float64),
+                                  inputs.bits(Wgu), inputs.bits(Wd),
+                                  None if Wgs is None else inputs.bits(Wgs),
+                                  None if Wds is None else inputs.bits(Wds))
+    assert_close(to_f64(oracle, Y1), y_ref, f"fused combine B={B} k={k} shared={shared}")
 
 
 def test_moe_experts_every_token_on_one_expert(env):
