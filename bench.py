@@ -43,6 +43,7 @@ if ROOT not in sys.path:
 METRIC = "achieved HBM GB/s (fraction of GB300 roofline) and µs/call per decode batch 1–64"
 BATCHES = [1, 2, 4, 8, 16, 32, 64]
 H, N_IN, K_O, E, L, I, TOPK = 7168, 8192, 16384, 384, 512, 2048, 8
+N_SK, K_SK = 2048, 1024  # the single skinny GEMM (B = 1), timed in the sweep
 PREFETCH_BYTES = 24 << 20
 WORKLOAD = ("Kimi-K3-shaped decode layer hot path, B in {1,2,4,8,16,32,64}: input projection "
             "7168->8192 (batch-size kernel switch), output projection 16384->7168 + residual, "
@@ -65,7 +66,8 @@ def parse_args():
     ap.add_argument("--ops", default="in,o,front,experts",
                     help="operations of the sweep (profiling subsets: in,o,front,experts; "
                          "pfscen = output projection behind a simulated communication phase; "
-                         "spec = projections at speculative verification row counts)")
+                         "spec = projections at speculative verification row counts; "
+                         "skinny = the single B=1 1024->2048 GEMM)")
     ap.add_argument("--sweep-only", action="store_true",
                     help="only the per-operation sweep (for profiler captures)")
     ap.add_argument("--num-experts", type=int, default=E,
@@ -110,13 +112,13 @@ class ClockSampler:
         self.proc = None
 
     def start(self):
-        """Start sampling every 100 ms and return once the first sample has arrived (or
+        """Start sampling every 20 ms and return once the first sample has arrived (or
         after 5 s), so the timed region that follows is covered from its start."""
         self.lines = []
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -388,9 +390,54 @@ def spec_sweep(torch, ssd, inputs, wl, dev, reps):
             del g
             nb = bytes_linear(M, N, K, res)
             row[name] = {"us_per_call": us, "GBps": nb / us / 1e3,
-                         "TFLOPs": 2.0 * M * N * K / us / 1e6,
+                         "TFLOPs": 2.0 * M * N * K / us / 1e6, "tok_per_s": M * 1e6 / us,
                          "variant": ssd.dec_variant_name(ssd.dec_last_variant())}
         out[str(M)] = row
+    return out
+
+
+# --------------------------------------------------------- single skinny GEMM ----
+
+def skinny_sweep(torch, ssd, inputs, dev, l2, reps):
+    """The single skinny GEMM Y = X . W^T at B = 1, K = 1024, N = 2048 through the batch
+    switch (the tiny-matrix kernel: "Part 1 / 1. Tune shapes for the workload", small
+    matrices at batch 1-2). Its 4.2 MB of weights fit in L2, so the graph makes one call
+    per copy of a pool >= 3x L2: every copy is read again only after the whole pool."""
+    B = 1
+    W0 = inputs.weight(N_SK, K_SK, dev, 0, "w_skinny")
+    n = max(2, math.ceil(3 * l2 / (W0.numel() * 2)))
+    pool = [W0] + [W0.clone() for _ in range(n - 1)]
+    X = inputs.activations(B, K_SK, dev, 0, "x_skinny")
+    Y = torch.empty(B, N_SK, dtype=torch.bfloat16, device=dev)
+    ws = ssd.workspace(ssd.dec_linear_workspace_bytes(B, N_SK, K_SK), dev)
+    g = capture(torch, lambda: [ssd.dec_linear(X, w, None, Y, ws) for w in pool])
+    us = statistics.median(time_graph(torch, g, reps)) / len(pool)
+    del g
+    nb = bytes_linear(B, N_SK, K_SK, False)
+    return {"B": B, "K": K_SK, "N": N_SK, "us_per_call": us, "GBps": nb / us / 1e3,
+            "tok_per_s": B * 1e6 / us, "calls_per_graph": len(pool),
+            "variant": ssd.dec_variant_name(ssd.dec_last_variant())}
+
+
+def compact_table(sweep, skinny, batches):
+    """Per-(operation, B) figures as flat strings (one value per batch, in the order of
+    `batches`), so that a consumer keeping only scalar fields still has them."""
+    out = {}
+    names = (("input_projection", "in"), ("output_projection", "o"), ("moe_front", "front"),
+             ("moe_experts", "experts"))
+    for name, short in names:
+        rows = [sweep.get(str(B), {}).get(name) for B in batches]
+        if not any(rows):
+            continue
+        fmt = lambda key, f: "/".join("-" if r is None else f(r[key]) for r in rows)
+        out[f"{short}_us"] = fmt("us_per_call", lambda v: f"{v:.2f}")
+        out[f"{short}_frac"] = fmt("frac", lambda v: f"{v:.3f}")
+        out[f"{short}_tok_s"] = fmt("tok_per_s", lambda v: f"{v:.0f}")
+    if skinny:
+        out["skinny_B1_K1024_N2048"] = (f"us {skinny['us_per_call']:.2f} GBps "
+                                        f"{skinny['GBps']:.0f} frac {skinny['frac']:.3f} "
+                                        f"tok_s {skinny['tok_per_s']:.0f}")
+    out["table_batches"] = "/".join(map(str, batches))
     return out
 
 
@@ -540,7 +587,7 @@ def main():
     batches = [int(b) for b in args.batches.split(",")]
     ops = set(args.ops.split(","))
     if not args.sweep_only:
-        ops = {"in", "o", "front", "experts", "pfscen", "spec"}
+        ops = {"in", "o", "front", "experts", "pfscen", "spec", "skinny"}
     wl = Workload(torch, ssd, inputs, dev, batches, num_experts=args.num_experts,
                   experts="experts" in ops)
     # Measured (graphs of 3 layers, B = 1/4/16/64): front end + experts as separate calls
@@ -576,7 +623,7 @@ def main():
             g = capture(torch, fn)
             ts = time_graph(torch, g, args.reps)
             us = statistics.median(ts) / R_SMALL
-            row[name] = {"us_per_call": us, "GBps": nb / us / 1e3,
+            row[name] = {"us_per_call": us, "GBps": nb / us / 1e3, "tok_per_s": B * 1e6 / us,
                          "variant": ssd.dec_variant_name(ssd.dec_last_variant())}
             del g
         if "experts" in ops:
@@ -585,10 +632,14 @@ def main():
             nb_e = sum(bytes_experts(B, wl.used_experts(B, v)) for v in range(3)) / 3
             us = statistics.median(ts) / 3
             row["moe_experts"] = {"us_per_call": us, "GBps": nb_e / us / 1e3,
+                                  "tok_per_s": B * 1e6 / us,
                                   "distinct_experts": [wl.used_experts(B, v) for v in range(3)]}
             del g
         sweep[str(B)] = row
     torch.cuda.synchronize()
+    skinny = None
+    if "skinny" in ops and not args.step_only:
+        skinny = skinny_sweep(torch, ssd, inputs, dev, wl.l2, args.reps)
     spec = None
     if "spec" in ops and not args.step_only:
         spec = spec_sweep(torch, ssd, inputs, wl, dev, args.reps)
@@ -599,7 +650,7 @@ def main():
     if args.sweep_only:
         if rank == 0:
             print(json.dumps({"sweep_only": True, "batches": batches, "ops": sorted(ops),
-                              "num_experts": wl.E, "sweep": sweep,
+                              "num_experts": wl.E, "sweep": sweep, "skinny_gemm": skinny,
                               "prefetch_scenario": pfscen, "spec_rows": spec}), flush=True)
         return 0
 
@@ -698,6 +749,8 @@ def main():
     for Bk, row in sweep.items():
         for op in row.values():
             op["frac"] = op["GBps"] / peak
+    if skinny:
+        skinny["frac"] = skinny["GBps"] / peak
     tc_peak = peaks.get("bf16_tflops") or 1900.0
     for Mk, row in (spec or {}).items():
         for op in row.values():
@@ -724,10 +777,12 @@ def main():
                                         "moe_front + l2_prefetch + moe_experts" if wl.prefetch
                                         else "moe_front + moe_experts"),
                            "l2_prefetch_in_step": wl.prefetch and not wl.layer,
-                           "parallelism": f"replicas x{world}"},
+                           "parallelism": f"replicas x{world}",
+                           **compact_table(sweep, skinny, batches)},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": per_step_launches * args.steps, "clocks": clocks,
-                "sweep": sweep, "prefetch_scenario": pfscen, "spec_rows": spec}
+                "sweep": sweep, "skinny_gemm": skinny, "prefetch_scenario": pfscen,
+                "spec_rows": spec}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
