@@ -173,16 +173,18 @@ DEC_API dec_status dec_splitk_gemm(const dec_bf16 *X, const dec_bf16 *W, const d
  * dec_splitk_gemm without a workspace, for callers that cannot allocate device memory
  * (for example a plugin running inside another runtime that owns the GPU memory pool,
  * or a serving loop whose memory is frozen after warm-up). The blog post has no
- * counterpart: it is an addition of this library. Same result and arguments as dec_splitk_gemm with
- * split_k = 0; the scratch lives in a fixed 16 MiB device array inside the library
- * (held on every GPU that loads it until the process exits), so a shape whose split-K
- * scratch would exceed 16 MiB is rejected with DEC_ERR_WORKSPACE_TOO_SMALL, and more than
- * 256 rows with DEC_ERR_UNSUPPORTED_SHAPE. The first
- * call on a device looks up the array's address: make it before any stream capture.
- * Every call on a device shares the one array (its counters are cleared at the start
- * of each call): two calls that can overlap on that GPU race, so issue them on one
- * stream or otherwise serialise them. No cudaMalloc, cudaFree or allocating library
- * routine is called.
+ * counterpart: it is an addition of this library. Same arguments as dec_splitk_gemm
+ * with split_k = 0, and the same kernels, schedule and bits; the scratch lives in a
+ * fixed 16 MiB device array inside the library (held on every GPU that loads it until
+ * the process exits), so a shape whose split-K scratch would exceed 16 MiB is rejected
+ * with DEC_ERR_WORKSPACE_TOO_SMALL, more than 256 rows (or more than 64 with use_tc = 0)
+ * with DEC_ERR_UNSUPPORTED_SHAPE. The first call on a device looks up the array's
+ * address (a failed lookup is retried on the next call): make it before any stream
+ * capture. Every call on a device shares the one array, and each call first clears its
+ * arrival counters with an asynchronous memset on s (so a call after one that gave up
+ * on a bounded wait still starts from zero): two calls that can overlap on that GPU
+ * race, so issue them on one stream or otherwise serialise them. No cudaMalloc,
+ * cudaFree or allocating library routine is called.
  */
 DEC_API dec_status dec_splitk_gemm_noalloc(const dec_bf16 *X, const dec_bf16 *W,
                                            const dec_bf16 *R, dec_bf16 *Y, int B, int N, int K,

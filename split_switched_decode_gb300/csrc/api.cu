@@ -431,7 +431,9 @@ dec_status run_splitk_rows(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 
 
 struct FrontPlan {
   SplitPlan sk;
-  size_t done_off, logits_off, total;  // done_off: the route-map counter
+  size_t done_off, logits_off;  // done_off: the route-map counter of the two-launch path
+  size_t cand_off, fcnt_off;    // one-launch path: per-tile top-k candidates, arrivals
+  size_t total;
 };
 
 // k-splits per front tile (0 = one worker per SM). Fewer splits mean fewer partial
@@ -450,8 +452,88 @@ bool plan_front(int B, int E, int L, int K, int num_sms, FrontPlan *fp, int spli
   if (!plan_splitk(B, E + L, K, splits, num_sms, &fp->sk)) return false;
   fp->done_off = fp->sk.total;
   fp->logits_off = fp->done_off + kAlign;
-  fp->total = fp->logits_off + align_up(static_cast<size_t>(B) * E * sizeof(float));
+  fp->cand_off = fp->logits_off + align_up(static_cast<size_t>(B) * E * sizeof(float));
+  const size_t router_tiles = static_cast<size_t>(ceil_div(E, TILE_N));
+  fp->fcnt_off = fp->cand_off + align_up(static_cast<size_t>(B) * router_tiles * MAX_TOPK * 8);
+  fp->total = fp->fcnt_off + kAlign;
   return true;
+}
+
+// Whether moe_front with B tokens runs as one launch (front_fused.cu) where the device
+// can schedule it: up to DEC_FRONT_FUSED_MAX_B tokens (default 8: measured faster than
+// the product kernel + finishing kernel up to 8 tokens, slower from 16);
+// DEC_FRONT_FUSED=0/1 turns it off / on at every batch.
+bool front_fused_enabled(int B) {
+  if (const char *s = std::getenv("DEC_FRONT_FUSED")) return std::atoi(s) != 0;
+  int max_b = 8;
+  if (const char *s = std::getenv("DEC_FRONT_FUSED_MAX_B")) max_b = std::atoi(s);
+  return B <= max_b;
+}
+
+// Stage-ring depth of the one-launch front end (DEC_FRONT_STAGES; default 4). Even,
+// because the two MMA-issuing warps each own every other stage. A ring at least as
+// deep as a CTA's k-range loads all its weights before the dependency wait.
+int front_stages_override() {
+  if (const char *s = std::getenv("DEC_FRONT_STAGES")) {
+    const int v = std::atoi(s) & ~1;
+    return v >= 2 && v <= 12 ? v : 0;
+  }
+  return 0;
+}
+
+struct FusedFrontPlan {
+  int S, log2S, nxb, nst, nsl;
+  size_t smem;
+};
+
+// Clusters of S CTAs of the one-launch front end the device holds at once, per device,
+// activation-box count and cluster size, queried once with the largest shared-memory
+// footprint of that configuration (B = 64).
+std::atomic<int> g_ff_clusters[kMaxDevices][3][5];
+std::once_flag g_ff_init_once;
+
+int fused_front_clusters(int S, int nxb, int nst) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  std::call_once(g_ff_init_once, []() {
+    for (auto &d : g_ff_clusters)
+      for (auto &a : d)
+        for (auto &v : a) v.store(-1);
+  });
+  const int xi = nxb == 1 ? 0 : (nxb == 2 ? 1 : 2);
+  int si = 0;
+  while ((1 << si) < S) ++si;
+  std::atomic<int> &slot = g_ff_clusters[dev][xi][si];
+  int n = slot.load();
+  if (n < 0) {
+    const int nsl_max = (MAX_B + S - 1) / S;
+    n = front_fused_max_clusters(S, nxb, front_fused_smem(S, nxb, nst, nsl_max));
+    slot.store(n);
+  }
+  return n;
+}
+
+// Cluster size S: the largest power of two <= min(16, k-blocks) that the device can
+// schedule; every CTA of a cluster then owns KB/S (+-1) k-blocks of its tile. The stage
+// ring holds 4 k-blocks.
+bool plan_front_fused(int B, int K, FusedFrontPlan *f) {
+  const int KB = ceil_div(K, TILE_K);
+  f->nxb = B <= 16 ? 1 : (B <= 32 ? 2 : 4);
+  f->nst = 4;
+  int S = 16;
+  while (S > KB) S >>= 1;
+  for (; S >= 1; S >>= 1)
+    if (fused_front_clusters(S, f->nxb, f->nst) >= 1) break;
+  if (S < 1) return false;
+  f->S = S;
+  f->log2S = 0;
+  while ((1 << f->log2S) < S) ++f->log2S;
+  // 16-CTA clusters send every slot of a destination with one vector store
+  f->nsl = S == 16 ? f->nxb : (B + S - 1) / S;
+  const int ovr = front_stages_override();
+  if (ovr > 0) f->nst = ovr;
+  f->smem = front_fused_smem(S, f->nxb, f->nst, f->nsl);
+  return f->smem <= FRONT_FUSED_SMEM_MAX;
 }
 
 struct ExpertsPlan {
@@ -708,16 +790,49 @@ dec_status run_front(const dec_bf16 *X, const dec_bf16 *Wcat, int B, int K, int 
   if (!make_map(&wmap, Wcat, K, E + L, 128) ||
       !make_map(&xmap, X, K, B, xbox_rows_for(fp.sk.maxc)))
     return DEC_ERR_CUDA;
+  char *wsb = static_cast<char *>(ws);
+  const int fv = force_variant();
+  FusedFrontPlan ffp;
+  if (front_fused_enabled(B) && fv != DEC_VARIANT_SPLITK && plan_front_fused(B, K, &ffp)) {
+    CUtensorMap xmap1;
+    if (!make_map(&xmap1, X, K, B, 16 * ffp.nxb)) return DEC_ERR_CUDA;
+    FrontFusedParams f;
+    std::memset(&f, 0, sizeof f);
+    f.B = B;
+    f.E = E;
+    f.L = L;
+    f.KB = ceil_div(K, TILE_K);
+    f.T = ceil_div(E + L, TILE_N);
+    f.S = ffp.S;
+    f.log2S = ffp.log2S;
+    f.TR = ceil_div(E, TILE_N);
+    f.topk = topk;
+    f.nst = ffp.nst;
+    f.nsl = ffp.nsl;
+    f.latent = latent;
+    f.topk_idx = topk_idx;
+    f.topk_w = topk_w;
+    f.probs = probs_opt;
+    f.logits = reinterpret_cast<float *>(wsb + fp.logits_off);
+    f.cand = reinterpret_cast<uint32_t *>(wsb + fp.cand_off);
+    f.route_map = route_map_opt;
+    f.counter = reinterpret_cast<int *>(wsb + fp.fcnt_off);
+    f.status = d->status;
+    f.wait_limit_ns = g_wait_limit_ns.load();
+    if (consume_fault()) return DEC_ERR_CUDA;
+    ce = launch_front_fused(wmap, xmap1, f, ffp.nxb, ffp.smem, s);
+    if (ce != cudaSuccess) return DEC_ERR_CUDA;
+    t_last_variant = DEC_VARIANT_SPLITK_TC;
+    return DEC_OK;
+  }
   EngineParams p;
   fill_engine_common(p, fp.sk, MODE_FRONT, E + L, K, B, ws, d);
   if (fp.sk.G < fp.sk.T) return DEC_ERR_UNSUPPORTED_SHAPE;  // a worker may span 2 tiles at most
   p.w_base = reinterpret_cast<const uint8_t *>(Wcat);
   p.w_rows = E + L;
   p.defer = 1;  // partial tiles only; front_finish adds them
-  char *wsb = static_cast<char *>(ws);
   if (consume_fault()) return DEC_ERR_CUDA;
-  int v = force_variant();
-  const bool tc = (v == DEC_VARIANT_SPLITK_TC) || (v == DEC_VARIANT_NONE && B >= tc_min_batch());
+  const bool tc = (fv == DEC_VARIANT_SPLITK_TC) || (fv == DEC_VARIANT_NONE && B >= tc_min_batch());
   ce = tc ? launch_engine_tc(fp.sk.maxc, wmap, xmap, p, s)
           : launch_engine_cc(fp.sk.maxc, wmap, xmap, p, s);
   if (ce == cudaErrorNotSupported) return DEC_ERR_UNSUPPORTED_SHAPE;
@@ -1062,12 +1177,11 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB per device
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-struct NoAllocDevice {
-  std::once_flag once;
-  void *scratch = nullptr;  // device address of g_noalloc_scratch on this device
-  cudaError_t err = cudaSuccess;
-};
-NoAllocDevice g_noalloc_dev[kMaxDevices];
+// Device address of g_noalloc_scratch per device, looked up on the first call made with
+// that device current. A failed lookup is not cached, so a later call can succeed (for
+// example once a stream capture that made the first attempt fail has ended).
+std::mutex g_noalloc_mu;
+void *g_noalloc_addr[kMaxDevices] = {};
 
 }  // namespace
 
@@ -1084,35 +1198,31 @@ extern "C" dec_status dec_splitk_gemm_noalloc(const dec_bf16 *X, const dec_bf16 
   if (!d) return DEC_ERR_CUDA;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return DEC_ERR_CUDA;
-  // First call on this device (which is current here): look up the array's device
-  // address. The name g_noalloc_scratch is only a host-side stand-in.
-  NoAllocDevice &nd = g_noalloc_dev[dev];
-  std::call_once(nd.once, [&]() {
-    nd.err = cudaGetSymbolAddress(&nd.scratch, g_noalloc_scratch);
-  });
-  if (nd.err != cudaSuccess || nd.scratch == nullptr) return DEC_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return DEC_ERR_CUDA;
+  void *scratch = nullptr;
+  {
+    // The name g_noalloc_scratch is only a host-side stand-in: the array's device
+    // address on this device (current here) comes from the runtime.
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_addr[dev] == nullptr &&
+        cudaGetSymbolAddress(&g_noalloc_addr[dev], g_noalloc_scratch) != cudaSuccess) {
+      g_noalloc_addr[dev] = nullptr;
+      return DEC_ERR_CUDA;
+    }
+    scratch = g_noalloc_addr[dev];
+  }
   SplitPlan pl;
   if (!plan_splitk(B, N, K, 0, d->num_sms, &pl)) return DEC_ERR_UNSUPPORTED_SHAPE;
   if (pl.total > kNoAllocScratchBytes) return DEC_ERR_WORKSPACE_TOO_SMALL;
-  CUtensorMap wmap, xmap;
-  if (!make_map(&wmap, W, K, N, 128) || !make_map(&xmap, X, K, B, xbox_rows_for(pl, B)))
-    return DEC_ERR_CUDA;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
-  // The array keeps whatever the previous call left; the arrival counters must start
-  // at zero, so clear them (the partial tiles are always written before being read).
-  if (cudaMemsetAsync(static_cast<char *>(nd.scratch) + pl.partial_bytes, 0, pl.counter_bytes,
+  // The arrival counters must start at zero. Every call that completes leaves them at
+  // zero, and the array starts zeroed, but a call whose kernel gave up on a bounded
+  // wait can leave some set; clearing them here makes the next call correct anyway.
+  // The partial tiles are always written before they are read.
+  if (cudaMemsetAsync(static_cast<char *>(scratch) + pl.partial_bytes, 0, pl.counter_bytes,
                       cs) != cudaSuccess)
     return DEC_ERR_CUDA;
-  EngineParams p;
-  fill_engine_common(p, pl, MODE_LINEAR, N, K, B, nd.scratch, d);
-  p.Y = Y;
-  p.R = R;
-  p.vec_y = (N % 8 == 0 && aligned16(Y) && (R == nullptr || aligned16(R))) ? 1 : 0;
-  if (consume_fault()) return DEC_ERR_CUDA;
-  ce = use_tc ? launch_engine_tc(pl.maxc, wmap, xmap, p, cs)
-              : launch_engine_cc(pl.maxc, wmap, xmap, p, cs);
-  if (ce == cudaErrorNotSupported) return DEC_ERR_UNSUPPORTED_SHAPE;
-  if (ce != cudaSuccess) return DEC_ERR_CUDA;
-  t_last_variant = use_tc ? DEC_VARIANT_SPLITK_TC : DEC_VARIANT_SPLITK;
-  return DEC_OK;
+  // The same planning, schedule choice (two-halves clusters, deferred finish) and
+  // kernels as dec_splitk_gemm with split_k = 0, so the bits are the same too.
+  return run_splitk_rows(X, W, R, Y, B, N, K, 0, use_tc, scratch, kNoAllocScratchBytes, cs);
 }

@@ -141,6 +141,35 @@ struct FrontFinishParams {
 };
 cudaError_t launch_front_finish(const FrontFinishParams &f, cudaStream_t s);
 
+// The whole front end in one launch (front_fused.cu): T tiles of 128 W_cat rows, one
+// thread-block cluster of S CTAs per tile, CTA c of a cluster multiplying k-blocks
+// [c*KB/S, (c+1)*KB/S); the partials are added in the token-owning CTA (token b -> CTA
+// b % S) after bulk copies through distributed shared memory; router tiles publish
+// per-token top-k candidates, and the last router CTA (arrival counter) merges them,
+// renormalises and builds the route map.
+struct FrontFusedParams {
+  int B, E, L, KB, T, S, log2S, TR, topk;
+  int nst;  // stage-ring depth (weight + activation boxes of one k-block per stage)
+  int nsl;  // token slots per CTA: ceil(B / S)
+  uint16_t *latent;     // [B, L] bf16
+  int32_t *topk_idx;    // [B, topk]
+  float *topk_w;        // [B, topk]
+  float *probs;         // [B, E] or nullptr
+  float *logits;        // [B, E] workspace, written only with probs
+  uint32_t *cand;       // [B][TR][topk] x {order key, expert}: per-tile candidates
+  int32_t *route_map;   // or nullptr
+  int *counter;         // arrivals of the router CTAs; zero between calls
+  unsigned *status;
+  uint64_t wait_limit_ns;
+};
+constexpr size_t FRONT_FUSED_SMEM_MAX = 232448;  // the opt-in limit per CTA
+size_t front_fused_smem(int S, int nxb, int nst, int nsl);
+// Thread-block clusters of S CTAs with `smem` bytes each that the device can hold at once
+// (0: the configuration cannot be launched).
+int front_fused_max_clusters(int S, int nxb, size_t smem);
+cudaError_t launch_front_fused(const CUtensorMap &wmap, const CUtensorMap &xmap,
+                               const FrontFusedParams &p, int nxb, size_t smem, cudaStream_t s);
+
 // Second half of a deferred split-K projection: adds the partial tiles of every worker
 // in worker order, adds R and rounds to bf16.
 struct LinearFinishParams {

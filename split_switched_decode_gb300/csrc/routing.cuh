@@ -17,9 +17,11 @@ __device__ __forceinline__ float order_key_to_f32(uint32_t k) {
 }
 
 // One warp routes token rows b = warp_id, warp_id + nwarps, ... of logits [B,E] (shared
-// or global memory). Writes topk_idx/topk_w (global) and, when given, probs (global)
+// or global memory; L2_LOADS: global memory written by other CTAs of the same launch,
+// read at L2). Writes topk_idx/topk_w (global) and, when given, probs (global)
 // and sidx (shared copy of topk_idx for the route map). Register-only: every array
 // index below is a compile-time constant after unrolling.
+template <bool L2_LOADS = false>
 __device__ __forceinline__ void route_tokens_warp(const float *logits, int B, int E, int topk,
                                                   int32_t *topk_idx, float *topk_w,
                                                   float *probs, int32_t *sidx, int warp_id,
@@ -34,7 +36,7 @@ __device__ __forceinline__ void route_tokens_warp(const float *logits, int B, in
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
       const int e = lane + 32 * i;
-      v[i] = (e < E) ? l[e] : -INFINITY;
+      v[i] = (e < E) ? (L2_LOADS ? __ldcg(l + e) : l[e]) : -INFINITY;
       key[i] = (e < E) ? f32_order_key(v[i]) : 0u;  // 0: below every real key
     }
     float m = -INFINITY;
@@ -166,6 +168,68 @@ __device__ __noinline__ static void build_route_map(const int32_t *sidx, int B, 
     const int b = q / topk;
     const int rank = __popcll(smask[e] & ((1ull << b) - 1ull));
     const int at = soff[e] + rank;
+    pairs[at] = q;
+    pos[q] = at;
+  }
+}
+
+// The route map (layout of the public header) built by one warp without block
+// barriers: token masks per expert by shared atomics, one warp-wide scan of the
+// per-expert counts (each lane owns ceil(E/32) consecutive experts), then every
+// (token, slot) entry placed by the rank of its token among the expert's tokens.
+// sidx: shared [B*topk] expert ids (each in [0, E)); smask: shared uint64 [E]; soff:
+// shared int [E]. Requires B <= 64. Run by all 32 lanes of one warp.
+__device__ __noinline__ static void build_route_map_warp(const int32_t *sidx, int B, int topk,
+                                                         int E, int32_t *rm,
+                                                         unsigned long long *smask, int *soff) {
+  const int lane = threadIdx.x & 31;
+  const int P = B * topk;
+  int32_t *counts = rm;
+  int32_t *offsets = rm + E;
+  int32_t *pairs = rm + 2 * E + 1;
+  int32_t *pos = pairs + P;
+  int32_t *num_used = pos + P;
+  int32_t *used = num_used + 1;
+  for (int e = lane; e < E; e += 32) smask[e] = 0ull;
+  __syncwarp();
+  for (int q = lane; q < P; q += 32) atomicOr(&smask[sidx[q]], 1ull << (q / topk));
+  __syncwarp();
+  const int per = (E + 31) / 32;
+  const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+  int c = 0, u = 0;
+  for (int e = e0; e < e1; ++e) {
+    const int k = __popcll(smask[e]);
+    c += k;
+    u += (k > 0);
+  }
+  int ic = c, iu = u;  // inclusive scans across the lanes
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int a = __shfl_up_sync(0xFFFFFFFFu, ic, o);
+    const int b = __shfl_up_sync(0xFFFFFFFFu, iu, o);
+    if (lane >= o) {
+      ic += a;
+      iu += b;
+    }
+  }
+  int run = ic - c, runu = iu - u;
+  for (int e = e0; e < e1; ++e) {
+    const int k = __popcll(smask[e]);
+    counts[e] = k;
+    offsets[e] = run;
+    soff[e] = run;
+    if (k > 0) used[runu++] = e;
+    run += k;
+  }
+  if (lane == 31) {
+    offsets[E] = ic;
+    *num_used = iu;
+  }
+  __syncwarp();
+  for (int q = lane; q < P; q += 32) {
+    const int e = sidx[q];
+    const int b = q / topk;
+    const int at = soff[e] + __popcll(smask[e] & ((1ull << b) - 1ull));
     pairs[at] = q;
     pos[q] = at;
   }

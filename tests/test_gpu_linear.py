@@ -87,7 +87,7 @@ def test_splitk_cuda_core_matches_oracle(env, B, N, K, split_k):
 
 @pytest.mark.parametrize("B", [1, 2, 4, 8, 16, 32, 64])
 def test_decode_input_projection_full_size(env, B):
-    """K=7168, N=8192 through the batch-size switch; sampled rows against the oracle."""
+    """K=7168, N=8192 through the batch-size switch; every output row against the oracle."""
     torch, ssd, oracle, dev = env
     N, K = 8192, 7168
     X, W, _, Y = _case(env, B, N, K, 0, residual=False)
@@ -100,25 +100,19 @@ def test_decode_input_projection_full_size(env, B):
         assert ssd.dec_last_variant() in (ssd.VARIANT_TINY, ssd.VARIANT_SPLITK_TC)
     else:
         assert ssd.dec_last_variant() in (ssd.VARIANT_SPLITK, ssd.VARIANT_SPLITK_TC)
-    rng = np.random.default_rng(B)
-    rows = np.unique(np.concatenate([rng.choice(N, 384, replace=False), [0, 127, 128, N - 1]]))
-    y_ref = _oracle_rows(env, X, W, None, rows)
-    assert_close(to_f64(oracle, Y)[:, rows], y_ref, f"input projection B={B}")
+    assert_close(to_f64(oracle, Y), _oracle_rows(env, X, W, None), f"input projection B={B}")
 
 
 @pytest.mark.parametrize("B", [1, 2, 3, 4, 8, 16, 32, 64])
 def test_output_projection_with_residual_full_size(env, B):
-    """K=16384, N=7168 with the fused residual; sampled rows against the oracle."""
+    """K=16384, N=7168 with the fused residual; every output row against the oracle."""
     torch, ssd, oracle, dev = env
     N, K = 7168, 16384
     X, W, R, Y = _case(env, B, N, K, 4, residual=True)
     ws = ssd.workspace(ssd.dec_linear_workspace_bytes(B, N, K), dev)
     ssd.dec_linear(X, W, R, Y, ws)
     torch.cuda.synchronize()
-    rng = np.random.default_rng(100 + B)
-    rows = np.unique(np.concatenate([rng.choice(N, 256, replace=False), [0, N - 1]]))
-    y_ref = _oracle_rows(env, X, W, R, rows)
-    assert_close(to_f64(oracle, Y)[:, rows], y_ref, f"output projection B={B}")
+    assert_close(to_f64(oracle, Y), _oracle_rows(env, X, W, R), f"output projection B={B}")
 
 
 def test_splitk_is_deterministic_and_split_independent(env):

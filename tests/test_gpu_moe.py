@@ -91,13 +91,15 @@ def test_moe_front_ragged_shapes(env, B, E, L, K, k):
 
 @pytest.mark.parametrize("B", [1, 2, 3, 7, 8, 9])
 def test_moe_front_cluster_route_map_equals_counter_path(env, monkeypatch, B):
-    """Up to 8 tokens, the finishing kernel's router CTAs form one thread-block cluster
+    """The two-launch front end (DEC_FRONT_FUSED=0: product kernel + finishing kernel):
+    up to 8 tokens, the finishing kernel's router CTAs form one thread-block cluster
     and CTA 0 builds the route map from the ids the others put in its shared memory;
     DEC_FRONT_CLUSTER=0 builds it in the CTA that routes the last token instead. Every
     output is bit-identical, and both match the oracle (B = 9 takes the counter path
     either way)."""
     torch, ssd, oracle, dev = env
     from split_switched_decode_gb300 import inputs
+    monkeypatch.setenv("DEC_FRONT_FUSED", "0")
     E, L, K, k = 384, 512, 7168, 8
     X = inputs.activations(B, K, dev, 8, "cfx")
     Wc = inputs.weight(E + L, K, dev, 8, "cfw")
@@ -109,6 +111,68 @@ def test_moe_front_cluster_route_map_equals_counter_path(env, monkeypatch, B):
         assert torch.equal(x, y), name
     assert ssd.dec_sync_status() == ssd.DEC_OK
     assert np.array_equal(c[1].cpu().numpy(), ref["idx"])
+
+
+@pytest.mark.parametrize("B,E,L,K,k", [(1, 384, 512, 7168, 8), (8, 384, 512, 7168, 8),
+                                       (17, 384, 512, 7168, 8), (64, 384, 512, 7168, 8),
+                                       (5, 130, 0, 456, 16), (33, 512, 8, 64, 1),
+                                       (64, 16, 100, 1032, 16), (2, 1, 0, 8, 1)])
+def test_moe_front_one_launch_and_two_launch_paths(env, monkeypatch, B, E, L, K, k):
+    """The one-launch front end (clusters reduce the split-K partials on chip, per-tile
+    top-k candidates merged by the last router CTA) and the two-launch path both match
+    the oracle: the same top-k ids and route map bit for bit, latent and weights within
+    tolerance. The one-launch path repeated on the same workspace gives the same bits
+    (fixed reduction order; its arrival counter is back at zero after each call)."""
+    torch, ssd, oracle, dev = env
+    from split_switched_decode_gb300 import inputs
+    X = inputs.activations(B, K, dev, 13, "pfx")
+    Wc = inputs.randn_bf16((E + L, K), 0.02 if K > 1000 else 0.2, dev, 13, "pfw", E, L, K)
+    monkeypatch.setenv("DEC_FRONT_FUSED", "1")
+    _check_front(env, X, Wc, E, L, k, f"one-launch front B={B} E={E} L={L} K={K} k={k}")
+    a = _run_front(env, X, Wc, E, L, k)
+    b = _run_front(env, X, Wc, E, L, k)
+    for x, y, name in zip(a, b, ["latent", "idx", "w", "probs", "route map"]):
+        if x is not None:
+            assert torch.equal(x, y), f"one-launch {name} not repeatable"
+    monkeypatch.setenv("DEC_FRONT_FUSED", "0")
+    _check_front(env, X, Wc, E, L, k, f"two-launch front B={B} E={E} L={L} K={K} k={k}")
+    c = _run_front(env, X, Wc, E, L, k)
+    assert torch.equal(a[1], c[1]) and torch.equal(a[4], c[4]), "paths route differently"
+    assert ssd.dec_sync_status() == ssd.DEC_OK
+
+
+@pytest.mark.parametrize("B", [1, 9, 16, 17, 33, 64])
+@pytest.mark.parametrize("stages", ["4", "2", "8"])
+def test_moe_front_one_launch_chained_calls_are_deterministic(env, monkeypatch, B, stages):
+    """24 one-launch front ends queued back to back on one stream (each may start loading
+    weights while the previous one finishes) with several stage-ring depths: every call
+    gives bit-identical outputs to the first, and the first matches the oracle."""
+    torch, ssd, oracle, dev = env
+    from split_switched_decode_gb300 import inputs
+    monkeypatch.setenv("DEC_FRONT_FUSED", "1")
+    monkeypatch.setenv("DEC_FRONT_STAGES", stages)
+    E, L, K, k = 384, 512, 7168, 8
+    X = inputs.activations(B, K, dev, 14, "chx")
+    Wc = inputs.weight(E + L, K, dev, 14, "chw")
+    lat = torch.empty(B, L, dtype=torch.bfloat16, device=dev)
+    ws = ssd.workspace(ssd.moe_front_workspace_bytes(B, E, L, K), dev)
+    outs = []
+    for _ in range(24):
+        idx = torch.empty(B, k, dtype=torch.int32, device=dev)
+        w = torch.empty(B, k, dtype=torch.float32, device=dev)
+        # entries of used[] past num_used are left as they are: pre-fill them alike
+        rm = torch.full((ssd.moe_route_map_ints(B, E, k),), -7, dtype=torch.int32, device=dev)
+        lat_i = torch.empty_like(lat)
+        ssd.moe_front(X, Wc, E, L, k, lat_i, idx, w, ws, route_map=rm)
+        outs.append((lat_i, idx, w, rm))
+    torch.cuda.synchronize()
+    assert ssd.dec_sync_status() == ssd.DEC_OK
+    for i, o in enumerate(outs[1:]):
+        for x, y, name in zip(outs[0], o, ["latent", "idx", "w", "route map"]):
+            assert torch.equal(x, y), f"call {i + 1}: {name} differs from the first call"
+    ref = oracle.moe_front(inputs.bits(X), inputs.bits(Wc), E, L, k)
+    assert np.array_equal(outs[0][1].cpu().numpy(), ref["idx"])
+    assert_close(outs[0][2].cpu().numpy(), ref["w"], f"chained B={B} weights")
 
 
 def test_moe_front_ties_go_to_lower_index(env):
@@ -330,29 +394,42 @@ def big_layer(env):
                                         (64, False)])
 def test_moe_layer_full_size(env, big_layer, B, with_map):
     """Front end -> routed experts + shared expert (side stream) on the full-size layer,
-    with the route map from the front end or built by the experts' gather launch;
-    sampled tokens checked against the oracle with their experts copied to the host."""
+    with the route map from the front end or built by the experts' gather launch, end
+    to end against the oracle: the GPU's top-k ids must equal the oracle front end's on
+    the same X bit for bit, and the reference layer output uses the oracle's own fp64
+    routing weights. Up to 8 tokens (the first, the last and spread between) are checked
+    with their experts copied to the host."""
     torch, ssd, oracle, dev = env
     from split_switched_decode_gb300 import inputs
     g = big_layer
     E, H, I, L, k = g["E"], g["H"], g["I"], g["L"], 8
     X = inputs.activations(B, H, dev, 0, "layer_x")
-    _, idx, w, _, rm = _run_front(env, X, g["Wc"], E, L, k)
+    lat, idx, w, _, rm = _run_front(env, X, g["Wc"], E, L, k)
     Y = _run_experts(env, X, idx, w, g["Wgu"], g["Wd"], g["Wgs"], g["Wds"],
                      rm=rm if with_map else None, side=True)
-    idx_np, w_np = idx.cpu().numpy(), w.cpu().numpy().astype(np.float64)
-    Yf = to_f64(oracle, Y)
     xb = inputs.bits(X)
+    ref = oracle.moe_front(xb, inputs.bits(g["Wc"]), E, L, k)
+    gi = idx.cpu().numpy()
+    if not np.array_equal(gi, ref["idx"]):
+        bad = np.where((gi != ref["idx"]).any(1))[0]
+        gaps = [topk_gap(ref["logits"][b], k) for b in bad]
+        raise AssertionError(f"layer B={B}: top-k differs from the oracle for tokens "
+                             f"{bad.tolist()} (oracle near-tie gaps {gaps})")
+    assert_close(w.cpu().numpy(), ref["w"], f"layer B={B} routing weights")
+    assert_close(to_f64(oracle, lat), oracle.bf16_to_f64(ref["latent"]), f"layer B={B} latent")
+    Yf = to_f64(oracle, Y)
     gs, ds = inputs.bits(g["Wgs"]), inputs.bits(g["Wds"])
-    tokens = sorted({0, (37 * B) // 64, B - 1})
+    n_tok = min(B, 8)
+    tokens = sorted({0, B - 1} | {(t * (B - 1)) // max(n_tok - 1, 1) for t in range(n_tok)})
+    assert len(tokens) == n_tok
     y_ref = np.empty((len(tokens), H))
     for t, b in enumerate(tokens):
         yp = np.empty((1, k, H))
         for j in range(k):
-            e = int(idx_np[b, j])
+            e = int(ref["idx"][b, j])
             _, yp[0, j] = oracle.expert_mlp(xb[b], inputs.bits(g["Wgu"][e]), inputs.bits(g["Wd"][e]))
         _, s = oracle.expert_mlp(xb[b], gs, ds)
-        y_ref[t] = oracle.combine(w_np[b:b + 1], yp, s[None, :])[0][0]
+        y_ref[t] = oracle.combine(ref["w"][b:b + 1], yp, s[None, :])[0][0]
     assert_close(Yf[tokens], y_ref, f"MoE layer B={B}")
 
 
