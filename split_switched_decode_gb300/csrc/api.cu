@@ -460,19 +460,22 @@ bool plan_front(int B, int E, int L, int K, int num_sms, FrontPlan *fp, int spli
 }
 
 // Whether moe_front with B tokens runs as one launch (front_fused.cu) where the device
-// can schedule it: up to DEC_FRONT_FUSED_MAX_B tokens (default 8: measured faster than
-// the product kernel + finishing kernel up to 8 tokens, slower from 16);
-// DEC_FRONT_FUSED=0/1 turns it off / on at every batch.
+// can schedule it (measured at least as fast as the product kernel + finishing kernel
+// at every batch: 11.6 vs 12.8 us at B = 1, 16.4 vs 17.1 us at B = 64); up to
+// DEC_FRONT_FUSED_MAX_B tokens (default 64); DEC_FRONT_FUSED=0/1 turns it off / on at
+// every batch.
 bool front_fused_enabled(int B) {
   if (const char *s = std::getenv("DEC_FRONT_FUSED")) return std::atoi(s) != 0;
-  int max_b = 8;
+  int max_b = MAX_B;
   if (const char *s = std::getenv("DEC_FRONT_FUSED_MAX_B")) max_b = std::atoi(s);
   return B <= max_b;
 }
 
-// Stage-ring depth of the one-launch front end (DEC_FRONT_STAGES; default 4). Even,
-// because the two MMA-issuing warps each own every other stage. A ring at least as
-// deep as a CTA's k-range loads all its weights before the dependency wait.
+// Stage-ring depth of the one-launch front end (DEC_FRONT_STAGES; default 8, cut to what
+// fits in shared memory). Even, because the two MMA-issuing warps each own every other
+// stage. A ring at least as deep as a CTA's k-range (7 k-blocks at K = 7168) loads all
+// its weights before the dependency wait: measured 0.3-1.2 us faster per call than 4
+// stages, although the next call's CTAs can then no longer sit on the same SMs early.
 int front_stages_override() {
   if (const char *s = std::getenv("DEC_FRONT_STAGES")) {
     const int v = std::atoi(s) & ~1;
@@ -486,13 +489,20 @@ struct FusedFrontPlan {
   size_t smem;
 };
 
+// The deepest even ring, at most `want` stages, that fits in shared memory.
+int fit_stages(int S, int nxb, int nsl, int want) {
+  int nst = want;
+  while (nst > 2 && front_fused_smem(S, nxb, nst, nsl) > FRONT_FUSED_SMEM_MAX) nst -= 2;
+  return nst;
+}
+
 // Clusters of S CTAs of the one-launch front end the device holds at once, per device,
 // activation-box count and cluster size, queried once with the largest shared-memory
-// footprint of that configuration (B = 64).
+// footprint of that configuration (64 tokens, the ring cut to fit).
 std::atomic<int> g_ff_clusters[kMaxDevices][3][5];
 std::once_flag g_ff_init_once;
 
-int fused_front_clusters(int S, int nxb, int nst) {
+int fused_front_clusters(int S, int nxb, int want) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
   std::call_once(g_ff_init_once, []() {
@@ -507,6 +517,7 @@ int fused_front_clusters(int S, int nxb, int nst) {
   int n = slot.load();
   if (n < 0) {
     const int nsl_max = (MAX_B + S - 1) / S;
+    const int nst = fit_stages(S, nxb, nsl_max, want);
     n = front_fused_max_clusters(S, nxb, front_fused_smem(S, nxb, nst, nsl_max));
     slot.store(n);
   }
@@ -514,24 +525,23 @@ int fused_front_clusters(int S, int nxb, int nst) {
 }
 
 // Cluster size S: the largest power of two <= min(16, k-blocks) that the device can
-// schedule; every CTA of a cluster then owns KB/S (+-1) k-blocks of its tile. The stage
-// ring holds 4 k-blocks.
+// schedule; every CTA of a cluster then owns KB/S (+-1) k-blocks of its tile.
 bool plan_front_fused(int B, int K, FusedFrontPlan *f) {
   const int KB = ceil_div(K, TILE_K);
   f->nxb = B <= 16 ? 1 : (B <= 32 ? 2 : 4);
-  f->nst = 4;
+  const int ovr = front_stages_override();
+  const int want = ovr > 0 ? ovr : 8;
   int S = 16;
   while (S > KB) S >>= 1;
   for (; S >= 1; S >>= 1)
-    if (fused_front_clusters(S, f->nxb, f->nst) >= 1) break;
+    if (fused_front_clusters(S, f->nxb, want) >= 1) break;
   if (S < 1) return false;
   f->S = S;
   f->log2S = 0;
   while ((1 << f->log2S) < S) ++f->log2S;
   // 16-CTA clusters send every slot of a destination with one vector store
   f->nsl = S == 16 ? f->nxb : (B + S - 1) / S;
-  const int ovr = front_stages_override();
-  if (ovr > 0) f->nst = ovr;
+  f->nst = fit_stages(S, f->nxb, f->nsl, want);
   f->smem = front_fused_smem(S, f->nxb, f->nst, f->nsl);
   return f->smem <= FRONT_FUSED_SMEM_MAX;
 }
@@ -627,6 +637,7 @@ const char *dec_variant_name(int variant) {
     case DEC_VARIANT_TINY: return "tiny";
     case DEC_VARIANT_SPLITK: return "splitk";
     case DEC_VARIANT_SPLITK_TC: return "splitk_tc";
+    case DEC_VARIANT_FRONT_ONE_LAUNCH: return "front_one_launch";
     default: return "none";
   }
 }
@@ -822,7 +833,7 @@ dec_status run_front(const dec_bf16 *X, const dec_bf16 *Wcat, int B, int K, int 
     if (consume_fault()) return DEC_ERR_CUDA;
     ce = launch_front_fused(wmap, xmap1, f, ffp.nxb, ffp.smem, s);
     if (ce != cudaSuccess) return DEC_ERR_CUDA;
-    t_last_variant = DEC_VARIANT_SPLITK_TC;
+    t_last_variant = DEC_VARIANT_FRONT_ONE_LAUNCH;
     return DEC_OK;
   }
   EngineParams p;

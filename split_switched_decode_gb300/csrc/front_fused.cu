@@ -317,12 +317,12 @@ __global__ void __launch_bounds__(FF_THREADS, 2)
   }
   __syncthreads();
   // ------------------------------------------------- routing: last router CTA(s)
-  // Up to 16 tokens one arrival counter elects the last router CTA, which routes every
+  // Up to 8 tokens one arrival counter elects the last router CTA, which routes every
   // token (a warp per token) and builds the route map. Beyond, the three (TR) router
   // CTAs owning a token group (the same cluster rank) elect their last one, which
   // routes that group; a second counter over the groups elects the CTA that builds the
   // route map from the published top-k ids.
-  const bool single = p.B <= 16;
+  const bool single = p.B <= 8;
   int *cnt_all = p.counter;           // [0]: every router CTA (single) / every group
   int *cnt_grp = p.counter + 1 + c;   // [1 + c]: the TR router CTAs of group c
   if (router && nslc > 0 && tid == 0)
@@ -333,38 +333,44 @@ __global__ void __launch_bounds__(FF_THREADS, 2)
     if (tid == 0) (void)mbar_wait_bounded(sent_bar, 0u, p.status, flags, p.wait_limit_ns);
     return;
   }
-  int32_t *sidx = reinterpret_cast<int32_t *>(ring);                 // [B*topk]
+  // route-map scratch in the idle stage ring
+  int32_t *sidx = reinterpret_cast<int32_t *>(ring);                      // [B*topk]
   unsigned long long *smask =
-      reinterpret_cast<unsigned long long *>(sidx + MAX_B * MAX_TOPK);  // [E]
-  int *soff = reinterpret_cast<int *>(smask + MAX_E);                // [E]
+      reinterpret_cast<unsigned long long *>(sidx + MAX_B * MAX_TOPK);   // [E]
+  int *scnt = reinterpret_cast<int *>(smask + MAX_E);                     // [E]
+  int *soff = scnt + MAX_E;                                               // [E]
+  int *sused = soff + MAX_E;                                              // [E]
+  int *s_total = sused + MAX_E;                                           // [2]
   const int topk = p.topk;
   if (single) {
-    route_tokens_warp<true>(p.logits, p.B, p.E, topk, p.topk_idx, p.topk_w, p.probs, sidx, warp,
-                            FF_THREADS / 32);
+    for (int b = warp; b < p.B; b += FF_THREADS / 32)  // a warp per token
+      route_token_sorted(p.logits + static_cast<size_t>(b) * p.E, p.E, topk,
+                         p.topk_idx + b * topk, p.topk_w + b * topk,
+                         p.probs ? p.probs + static_cast<size_t>(b) * p.E : nullptr,
+                         sidx + b * topk);
     if (tid == 0) *cnt_all = 0;  // every arrival of this call is in: ready for the next
     __syncthreads();
-    if (warp == 0 && p.route_map != nullptr)
-      build_route_map_warp(sidx, p.B, topk, p.E, p.route_map, smask, soff);
+    if (p.route_map != nullptr)
+      build_route_map_cta(sidx, p.B, topk, p.E, p.route_map, smask, scnt, soff, sused, s_total);
   } else {
     // this group's tokens b = c + j*S, one warp each
     for (int j = warp; j < nslc; j += FF_THREADS / 32) {
       const int b = c + (j << p.log2S);
-      route_tokens_warp<true>(p.logits + static_cast<size_t>(b) * p.E, 1, p.E, topk,
-                              p.topk_idx + b * topk, p.topk_w + b * topk,
-                              p.probs ? p.probs + static_cast<size_t>(b) * p.E : nullptr,
-                              nullptr, 0, 1);
+      route_token_sorted(p.logits + static_cast<size_t>(b) * p.E, p.E, topk,
+                         p.topk_idx + b * topk, p.topk_w + b * topk,
+                         p.probs ? p.probs + static_cast<size_t>(b) * p.E : nullptr, nullptr);
     }
     if (tid == 0) *cnt_grp = 0;
     __syncthreads();
     if (tid == 0) flags[1] = (atom_add_acq_rel_gpu(cnt_all, 1) == ndst - 1);
     __syncthreads();
-    if (flags[1] && warp == 0) {
-      if (lane == 0) *cnt_all = 0;
+    if (flags[1]) {
+      if (tid == 0) *cnt_all = 0;
       const int P = p.B * topk;
-      for (int q = lane; q < P; q += 32) sidx[q] = __ldcg(p.topk_idx + q);
-      __syncwarp();
+      for (int q = tid; q < P; q += FF_THREADS) sidx[q] = __ldcg(p.topk_idx + q);
+      __syncthreads();
       if (p.route_map != nullptr)
-        build_route_map_warp(sidx, p.B, topk, p.E, p.route_map, smask, soff);
+        build_route_map_cta(sidx, p.B, topk, p.E, p.route_map, smask, scnt, soff, sused, s_total);
     }
   }
   // every receiver has taken this CTA's rows (and nothing else targets it) before exit

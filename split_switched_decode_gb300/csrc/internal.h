@@ -162,7 +162,9 @@ struct FrontFusedParams {
   unsigned *status;
   uint64_t wait_limit_ns;
 };
-constexpr size_t FRONT_FUSED_SMEM_MAX = 232448;  // the opt-in limit per CTA
+// dynamic shared memory the one-launch front end may request (below the 227 KB opt-in
+// limit per CTA, leaving room for the compiler's static shared memory)
+constexpr size_t FRONT_FUSED_SMEM_MAX = 220 * 1024;
 size_t front_fused_smem(int S, int nxb, int nst, int nsl);
 // Thread-block clusters of S CTAs with `smem` bytes each that the device can hold at once
 // (0: the configuration cannot be launched).

@@ -173,16 +173,113 @@ __device__ __noinline__ static void build_route_map(const int32_t *sidx, int B, 
   }
 }
 
-// The route map (layout of the public header) built by one warp without block
-// barriers: token masks per expert by shared atomics, one warp-wide scan of the
-// per-expert counts (each lane owns ceil(E/32) consecutive experts), then every
-// (token, slot) entry placed by the rank of its token among the expert's tokens.
-// sidx: shared [B*topk] expert ids (each in [0, E)); smask: shared uint64 [E]; soff:
-// shared int [E]. Requires B <= 64. Run by all 32 lanes of one warp.
-__device__ __noinline__ static void build_route_map_warp(const int32_t *sidx, int B, int topk,
-                                                         int E, int32_t *rm,
-                                                         unsigned long long *smask, int *soff) {
+// ------------------------------------------------------------ one-launch front end --
+
+// Composite routing key: the order key of the fp32 logit in the high word, the
+// inverted expert index in the low word. A larger key is a larger logit or, for equal
+// logits, a lower expert index; keys of distinct experts differ; 0 is below every real
+// candidate.
+__device__ __forceinline__ uint64_t route_key(float logit, uint32_t expert) {
+  return (static_cast<uint64_t>(f32_order_key(logit)) << 32) | (0xFFFFFFFFu - expert);
+}
+
+// Routes one token with one warp: softmax, the topk largest logits (ties to the lower
+// expert index, listed by descending logit), weights renormalised over the chosen k.
+// Lane l holds experts l, l+32, ... (16 per lane, E <= 512), read from global memory at
+// L2 (written by other CTAs of the launch). Each lane first sorts its 16 keys in
+// registers (bitonic network); each of the k rounds then takes a warp-wide max of the
+// lanes' heads and the lowest expert among equal heads, and the winning lane drops its
+// head -- two warp reductions per round and no rescan.
+// Outputs: idx/w [topk] (global), probs [E] (global, optional), sidx [topk] (shared,
+// optional).
+__device__ __forceinline__ void route_token_sorted(const float *logits, int E, int topk,
+                                                   int32_t *idx, float *w, float *probs,
+                                                   int32_t *sidx) {
+  constexpr int V = 16;
   const int lane = threadIdx.x & 31;
+  const unsigned FULL = 0xFFFFFFFFu;
+  float v[V];
+  uint64_t k[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = e < E ? __ldcg(logits + e) : -INFINITY;
+    k[i] = e < E ? route_key(v[i], static_cast<uint32_t>(e)) : 0ull;
+  }
+  if (probs != nullptr) {  // full softmax over the E logits
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < V; ++i) m = fmaxf(m, v[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, o));
+    float z = 0.f;
+#pragma unroll
+    for (int i = 0; i < V; ++i)
+      if (lane + 32 * i < E) z += expf(v[i] - m);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(FULL, z, o);
+#pragma unroll
+    for (int i = 0; i < V; ++i)
+      if (lane + 32 * i < E) probs[lane + 32 * i] = expf(v[i] - m) / z;
+  }
+#pragma unroll
+  for (int s = 2; s <= V; s <<= 1) {  // sort the lane's keys, descending
+#pragma unroll
+    for (int d = s >> 1; d > 0; d >>= 1) {
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        if ((i & d) == 0) {
+          const bool desc = (i & s) == 0;
+          const uint64_t a = k[i], b = k[i + d];
+          const uint64_t hi = a > b ? a : b, lo = a > b ? b : a;
+          k[i] = desc ? hi : lo;
+          k[i + d] = desc ? lo : hi;
+        }
+      }
+    }
+  }
+  uint32_t my_e = 0;
+  float my_v = 0.f;
+  for (int j = 0; j < topk; ++j) {
+    const uint32_t hk = static_cast<uint32_t>(k[0] >> 32);
+    const uint32_t kmax = __reduce_max_sync(FULL, hk);
+    const uint32_t cand = (hk == kmax && k[0] != 0ull) ? 0xFFFFFFFFu - static_cast<uint32_t>(k[0])
+                                                       : 0xFFFFFFFFu;
+    const uint32_t win = __reduce_min_sync(FULL, cand);  // lowest expert with the max logit
+    if (lane == static_cast<int>(win & 31u)) {           // expert win lives in lane win % 32
+#pragma unroll
+      for (int i = 0; i < V - 1; ++i) k[i] = k[i + 1];
+      k[V - 1] = 0ull;
+    }
+    if (lane == j) {
+      my_e = win;
+      my_v = order_key_to_f32(kmax);
+    }
+  }
+  const float m0 = __shfl_sync(FULL, my_v, 0);  // the largest logit
+  const float ex = lane < topk ? expf(my_v - m0) : 0.f;
+  float zs = ex;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) zs += __shfl_xor_sync(FULL, zs, o);
+  if (lane < topk) {
+    idx[lane] = static_cast<int32_t>(my_e);
+    w[lane] = ex / zs;
+    if (sidx != nullptr) sidx[lane] = static_cast<int32_t>(my_e);
+  }
+}
+
+// The route map (layout of the public header) built by every thread of the CTA:
+// per-expert token masks by shared atomics; counts per expert in shared memory; one
+// warp turns them into offsets and the used-expert list (each lane scans a contiguous
+// run of experts); then every thread writes counts / offsets / used with coalesced
+// stores and places each (token, slot) entry by the rank of its token among the
+// expert's tokens. sidx: shared [B*topk] expert ids in [0, E). Scratch in shared memory:
+// smask uint64 [E], scnt / soff / sused int [E], s_total int [2]. Requires B <= 64.
+__device__ __noinline__ static void build_route_map_cta(const int32_t *sidx, int B, int topk,
+                                                        int E, int32_t *rm,
+                                                        unsigned long long *smask, int *scnt,
+                                                        int *soff, int *sused, int *s_total) {
+  const int tid = threadIdx.x, nthr = blockDim.x;
   const int P = B * topk;
   int32_t *counts = rm;
   int32_t *offsets = rm + E;
@@ -190,43 +287,56 @@ __device__ __noinline__ static void build_route_map_warp(const int32_t *sidx, in
   int32_t *pos = pairs + P;
   int32_t *num_used = pos + P;
   int32_t *used = num_used + 1;
-  for (int e = lane; e < E; e += 32) smask[e] = 0ull;
-  __syncwarp();
-  for (int q = lane; q < P; q += 32) atomicOr(&smask[sidx[q]], 1ull << (q / topk));
-  __syncwarp();
-  const int per = (E + 31) / 32;
-  const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
-  int c = 0, u = 0;
-  for (int e = e0; e < e1; ++e) {
-    const int k = __popcll(smask[e]);
-    c += k;
-    u += (k > 0);
-  }
-  int ic = c, iu = u;  // inclusive scans across the lanes
+  for (int e = tid; e < E; e += nthr) smask[e] = 0ull;
+  __syncthreads();
+  for (int q = tid; q < P; q += nthr) atomicOr(&smask[sidx[q]], 1ull << (q / topk));
+  __syncthreads();
+  for (int e = tid; e < E; e += nthr) scnt[e] = __popcll(smask[e]);
+  __syncthreads();
+  if (tid < 32) {
+    const int lane = tid;
+    const int per = (E + 31) / 32;
+    const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+    int c = 0, u = 0;
+    for (int e = e0; e < e1; ++e) {
+      const int k = scnt[e];
+      c += k;
+      u += (k > 0);
+    }
+    int ic = c, iu = u;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int a = __shfl_up_sync(0xFFFFFFFFu, ic, o);
-    const int b = __shfl_up_sync(0xFFFFFFFFu, iu, o);
-    if (lane >= o) {
-      ic += a;
-      iu += b;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a = __shfl_up_sync(0xFFFFFFFFu, ic, o);
+      const int b = __shfl_up_sync(0xFFFFFFFFu, iu, o);
+      if (lane >= o) {
+        ic += a;
+        iu += b;
+      }
+    }
+    int run = ic - c, runu = iu - u;
+    for (int e = e0; e < e1; ++e) {
+      const int k = scnt[e];
+      soff[e] = run;
+      if (k > 0) sused[runu++] = e;
+      run += k;
+    }
+    if (lane == 31) {
+      s_total[0] = ic;
+      s_total[1] = iu;
     }
   }
-  int run = ic - c, runu = iu - u;
-  for (int e = e0; e < e1; ++e) {
-    const int k = __popcll(smask[e]);
-    counts[e] = k;
-    offsets[e] = run;
-    soff[e] = run;
-    if (k > 0) used[runu++] = e;
-    run += k;
+  __syncthreads();
+  const int nu = s_total[1];
+  for (int e = tid; e < E; e += nthr) {
+    counts[e] = scnt[e];
+    offsets[e] = soff[e];
   }
-  if (lane == 31) {
-    offsets[E] = ic;
-    *num_used = iu;
+  for (int u = tid; u < nu; u += nthr) used[u] = sused[u];
+  if (tid == 0) {
+    offsets[E] = s_total[0];
+    *num_used = nu;
   }
-  __syncwarp();
-  for (int q = lane; q < P; q += 32) {
+  for (int q = tid; q < P; q += nthr) {
     const int e = sidx[q];
     const int b = q / topk;
     const int at = soff[e] + __popcll(smask[e] & ((1ull << b) - 1ull));

@@ -129,6 +129,7 @@ def test_moe_front_one_launch_and_two_launch_paths(env, monkeypatch, B, E, L, K,
     Wc = inputs.randn_bf16((E + L, K), 0.02 if K > 1000 else 0.2, dev, 13, "pfw", E, L, K)
     monkeypatch.setenv("DEC_FRONT_FUSED", "1")
     _check_front(env, X, Wc, E, L, k, f"one-launch front B={B} E={E} L={L} K={K} k={k}")
+    assert ssd.dec_last_variant() == ssd.VARIANT_FRONT_ONE_LAUNCH  # no silent fallback
     a = _run_front(env, X, Wc, E, L, k)
     b = _run_front(env, X, Wc, E, L, k)
     for x, y, name in zip(a, b, ["latent", "idx", "w", "probs", "route map"]):
@@ -136,6 +137,7 @@ def test_moe_front_one_launch_and_two_launch_paths(env, monkeypatch, B, E, L, K,
             assert torch.equal(x, y), f"one-launch {name} not repeatable"
     monkeypatch.setenv("DEC_FRONT_FUSED", "0")
     _check_front(env, X, Wc, E, L, k, f"two-launch front B={B} E={E} L={L} K={K} k={k}")
+    assert ssd.dec_last_variant() == ssd.VARIANT_SPLITK_TC
     c = _run_front(env, X, Wc, E, L, k)
     assert torch.equal(a[1], c[1]) and torch.equal(a[4], c[4]), "paths route differently"
     assert ssd.dec_sync_status() == ssd.DEC_OK
@@ -164,6 +166,7 @@ def test_moe_front_one_launch_chained_calls_are_deterministic(env, monkeypatch, 
         rm = torch.full((ssd.moe_route_map_ints(B, E, k),), -7, dtype=torch.int32, device=dev)
         lat_i = torch.empty_like(lat)
         ssd.moe_front(X, Wc, E, L, k, lat_i, idx, w, ws, route_map=rm)
+        assert ssd.dec_last_variant() == ssd.VARIANT_FRONT_ONE_LAUNCH
         outs.append((lat_i, idx, w, rm))
     torch.cuda.synchronize()
     assert ssd.dec_sync_status() == ssd.DEC_OK
