@@ -599,10 +599,12 @@ def main():
     wl.prefetch = args.prefetch
     wl.layer = args.layer
 
-    # routing of every X set (fixed inputs -> fixed routing -> fixed bytes)
-    for B in batches:
-        for v in range(3):
-            wl.op_front(B, v=v, prefetch=False, with_map=True)
+    # routing of every X set (fixed inputs -> fixed routing -> fixed bytes); not needed
+    # when only projections are swept (profiler captures of those see only their kernels)
+    if ops & {"front", "experts"}:
+        for B in batches:
+            for v in range(3):
+                wl.op_front(B, v=v, prefetch=False, with_map=True)
     torch.cuda.synchronize()
 
     # ---- per-operation sweep: graphs of R calls over rotating weight copies
