@@ -56,7 +56,7 @@ __device__ __forceinline__ float dot8(const uint4 &w, const uint4 &x, float acc)
 template <int NB>
 __global__ void __launch_bounds__(TINY_THREADS, 2)
     gemv_tiny_kernel(const uint16_t *X, const uint16_t *__restrict__ W, const uint16_t *R,
-                     uint16_t *Y, int N, int K, int P) {
+                     uint16_t *Y, int N, int K, int P, int early_trigger) {
   extern __shared__ float red[];  // [rows of this CTA][P][NB]
   const int C = K >> 3;           // 16-byte chunks per row
   const int G = gridDim.x;
@@ -98,6 +98,9 @@ __global__ void __launch_bounds__(TINY_THREADS, 2)
       if (!waited) {  // activations are written by the previous kernel of the stream
         griddep_wait();
         waited = true;
+        // small matrices: every weight load of this CTA is out, let the next kernel of the
+        // stream start on the half of the SM this one leaves free (see gemv_tiny_grid)
+        if (early_trigger) griddep_launch_dependents();
       }
 #pragma unroll
       for (int u = 0; u < TINY_JU; ++u) {
@@ -145,10 +148,19 @@ int tiny_pieces(int K) {
   return P;
 }
 
+
+// Weight matrices up to this size get one CTA per SM instead of two: all of a CTA's
+// loads are in flight at once anyway, and the other half of each SM is left to the next
+// kernel of the stream, which then loads its own weights while this one finishes
+// (triggered right after the first weight loads).
+constexpr size_t TINY_SMALL_BYTES = size_t(16) << 20;
+
+bool tiny_small(int N, int K) { return static_cast<size_t>(N) * K * 2 <= TINY_SMALL_BYTES; }
+
 }  // namespace
 
-int gemv_tiny_grid(int N, int num_sms) {
-  int g = 2 * num_sms;
+int gemv_tiny_grid(int N, int K, int num_sms) {
+  int g = tiny_small(N, K) ? num_sms : 2 * num_sms;
   const int need = (N + TINY_MAX_ROWS_PER_CTA - 1) / TINY_MAX_ROWS_PER_CTA;
   if (g < need) g = need;
   if (g > N) g = N;
@@ -157,23 +169,24 @@ int gemv_tiny_grid(int N, int num_sms) {
 
 cudaError_t launch_gemv_tiny(const uint16_t *X, const uint16_t *W, const uint16_t *R,
                              uint16_t *Y, int B, int N, int K, int num_sms, cudaStream_t s) {
-  const int G = gemv_tiny_grid(N, num_sms);
+  const int G = gemv_tiny_grid(N, K, num_sms);
   const int P = tiny_pieces(K);
+  const int early = tiny_small(N, K) ? 1 : 0;
   const int rows = (N + G - 1) / G;
   const size_t smem = static_cast<size_t>(rows) * P * B * sizeof(float);
   switch (B) {
     case 1:
       return launch_pdl(gemv_tiny_kernel<1>, dim3(G), dim3(TINY_THREADS), smem, s, X, W, R, Y, N,
-                        K, P);
+                        K, P, early);
     case 2:
       return launch_pdl(gemv_tiny_kernel<2>, dim3(G), dim3(TINY_THREADS), smem, s, X, W, R, Y, N,
-                        K, P);
+                        K, P, early);
     case 3:
       return launch_pdl(gemv_tiny_kernel<3>, dim3(G), dim3(TINY_THREADS), smem, s, X, W, R, Y, N,
-                        K, P);
+                        K, P, early);
     case 4:
       return launch_pdl(gemv_tiny_kernel<4>, dim3(G), dim3(TINY_THREADS), smem, s, X, W, R, Y, N,
-                        K, P);
+                        K, P, early);
     default:
       return cudaErrorInvalidValue;
   }

@@ -118,7 +118,7 @@ cudaError_t launch_engine_tc(int maxc, const CUtensorMap &wmap, const CUtensorMa
 
 // ------------------------------------------------------------- gemv_tiny.cu --
 constexpr int TINY_MAX_NB = 4;  // batch rows of the tiny kernel (1..4)
-int gemv_tiny_grid(int N, int num_sms);
+int gemv_tiny_grid(int N, int K, int num_sms);
 cudaError_t launch_gemv_tiny(const uint16_t *X, const uint16_t *W, const uint16_t *R,
                              uint16_t *Y, int B, int N, int K, int num_sms, cudaStream_t s);
 
