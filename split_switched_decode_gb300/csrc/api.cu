@@ -343,7 +343,7 @@ dec_status run_splitk_rows(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 
                            size_t ws_bytes, cudaStream_t s);
 
 // A projection of more than 256 rows (speculative verification of up to 64 sequences x
-// 8 tokens) runs as consecutive launches over row blocks, each reading W again; on one
+// 8 tokens) runs as consecutive launches over row blocks, each reading W; on one
 // stream, each launch's workspace use begins after the previous launch has finished
 // with it (the stream order, or the dependency wait of a programmatic launch).
 dec_status run_splitk(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 *R, dec_bf16 *Y,

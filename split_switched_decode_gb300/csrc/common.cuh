@@ -161,8 +161,8 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
       : "memory");
 }
 
-// Same, with an L2 eviction-priority policy for data read exactly once (weights).
-__device__ __forceinline__ void tma_load_2d_evict_first(void *dst, const CUtensorMap *map,
+// Same, with an L2 cache policy from createpolicy (evict-first for weights read once).
+__device__ __forceinline__ void tma_load_2d_hint(void *dst, const CUtensorMap *map,
                                                         uint64_t *bar, int c0, int c1,
                                                         uint64_t policy) {
   asm volatile(

@@ -104,9 +104,9 @@ __device__ __forceinline__ uint32_t stage_tx_bytes(const EngineParams &p, const 
 __device__ __forceinline__ void load_weights(const EngineParams &p, const SegInfo &s,
                                              const CUtensorMap *wmap, uint8_t *dst,
                                              uint64_t *bar, int kb, uint64_t pol) {
-  tma_load_2d_evict_first(dst, wmap, bar, kb * TILE_K, s.wrow0, pol);
+  tma_load_2d_hint(dst, wmap, bar, kb * TILE_K, s.wrow0, pol);
   if (p.wbox_rows == 64)
-    tma_load_2d_evict_first(dst + 8192, wmap, bar, kb * TILE_K, s.wrow1, pol);
+    tma_load_2d_hint(dst + 8192, wmap, bar, kb * TILE_K, s.wrow1, pol);
 }
 
 // Before the dependency wait, while the previous kernel of the stream is still
@@ -151,7 +151,7 @@ __device__ __forceinline__ void engine_produce(const EngineParams &p, const CUte
                                                volatile int *flags, int64_t begin, int64_t end) {
   prefetch_tensormap(wmap);
   prefetch_tensormap(xmap);
-  const uint64_t pol = policy_evict_first();
+  const uint64_t pol = policy_evict_first();  // weights are read once per launch
   uint32_t pre = 0;
   if (!p.grouped || p.rm_ready) {
     for (int64_t it = begin; it < end && pre < STAGES;) {

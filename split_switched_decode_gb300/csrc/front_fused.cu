@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(FF_THREADS, 2)
       const int pre = nkb < nst ? nkb : nst;
       for (int q = 0; q < pre; ++q) {  // weights only: they do not depend on earlier kernels
         mbar_arrive_expect_tx(&full[q], STAGE);
-        tma_load_2d_evict_first(ring + q * STAGE, &wmap, &full[q], (kb0 + q) * TILE_K,
+        tma_load_2d_hint(ring + q * STAGE, &wmap, &full[q], (kb0 + q) * TILE_K,
                                 t * TILE_N, pol);
       }
       for (int kb = kb0 + pre; kb < kb1; ++kb) tma_prefetch_l2_2d(&wmap, kb * TILE_K, t * TILE_N);
@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(FF_THREADS, 2)
             break;
           }
           mbar_arrive_expect_tx(&full[st], STAGE);
-          tma_load_2d_evict_first(dst, &wmap, &full[st], (kb0 + q) * TILE_K, t * TILE_N, pol);
+          tma_load_2d_hint(dst, &wmap, &full[st], (kb0 + q) * TILE_K, t * TILE_N, pol);
         }
         tma_load_2d(dst + 16384, &xmap, &full[st], (kb0 + q) * TILE_K, 0);
       }
