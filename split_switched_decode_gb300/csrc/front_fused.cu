@@ -317,12 +317,12 @@ __global__ void __launch_bounds__(FF_THREADS, 2)
   }
   __syncthreads();
   // ------------------------------------------------- routing: last router CTA(s)
-  // Up to 8 tokens one arrival counter elects the last router CTA, which routes every
-  // token (a warp per token) and builds the route map. Beyond, the three (TR) router
+  // Up to 4 tokens one arrival counter elects the last router CTA, which routes every
+  // token (several warps per token) and builds the route map. Beyond, the three (TR) router
   // CTAs owning a token group (the same cluster rank) elect their last one, which
   // routes that group; a second counter over the groups elects the CTA that builds the
   // route map from the published top-k ids.
-  const bool single = p.B <= 8;
+  const bool single = p.B <= 4;
   int *cnt_all = p.counter;           // [0]: every router CTA (single) / every group
   int *cnt_grp = p.counter + 1 + c;   // [1 + c]: the TR router CTAs of group c
   if (router && nslc > 0 && tid == 0)
@@ -343,23 +343,62 @@ __global__ void __launch_bounds__(FF_THREADS, 2)
   int *s_total = sused + MAX_E;                                           // [2]
   const int topk = p.topk;
   if (single) {
-    for (int b = warp; b < p.B; b += FF_THREADS / 32)  // a warp per token
-      route_token_sorted(p.logits + static_cast<size_t>(b) * p.E, p.E, topk,
-                         p.topk_idx + b * topk, p.topk_w + b * topk,
-                         p.probs ? p.probs + static_cast<size_t>(b) * p.E : nullptr,
-                         sidx + b * topk);
+    // up to 4 tokens, several warps share a token (a slice of the experts each, then one
+    // merge); with the full softmax requested, or from 5 tokens, a warp per token
+    const int nw = p.probs != nullptr ? 1 : (p.B == 1 ? 8 : (p.B == 2 ? 4 : (p.B <= 4 ? 2 : 1)));
+    uint64_t *scand = reinterpret_cast<uint64_t *>(sused + MAX_E + 2);  // [8][MAX_TOPK]
+    const int b = warp / nw, wi = warp % nw;
+    if (nw > 1 && b < p.B) {
+      const float *lg = p.logits + static_cast<size_t>(b) * p.E;
+      uint64_t *sc = scand + b * nw * MAX_TOPK;
+      if (nw == 8)
+        route_token_split<8>(lg, p.E, topk, wi, sc, 3 + b, p.topk_idx + b * topk,
+                             p.topk_w + b * topk, sidx + b * topk);
+      else if (nw == 4)
+        route_token_split<4>(lg, p.E, topk, wi, sc, 3 + b, p.topk_idx + b * topk,
+                             p.topk_w + b * topk, sidx + b * topk);
+      else
+        route_token_split<2>(lg, p.E, topk, wi, sc, 3 + b, p.topk_idx + b * topk,
+                             p.topk_w + b * topk, sidx + b * topk);
+    }
+    if (nw == 1)
+      for (int bb = warp; bb < p.B; bb += FF_THREADS / 32)  // a warp per token
+        route_token_sorted(p.logits + static_cast<size_t>(bb) * p.E, p.E, topk,
+                           p.topk_idx + bb * topk, p.topk_w + bb * topk,
+                           p.probs ? p.probs + static_cast<size_t>(bb) * p.E : nullptr,
+                           sidx + bb * topk);
     if (tid == 0) *cnt_all = 0;  // every arrival of this call is in: ready for the next
     __syncthreads();
     if (p.route_map != nullptr)
       build_route_map_cta(sidx, p.B, topk, p.E, p.route_map, smask, scnt, soff, sused, s_total);
   } else {
-    // this group's tokens b = c + j*S, one warp each
-    for (int j = warp; j < nslc; j += FF_THREADS / 32) {
+    // this group's tokens b = c + j*S: 8, 4 or 2 warps each for up to 4 tokens (16-CTA
+    // clusters); one warp each for more (smaller clusters) or with the full softmax
+    const int nw = p.probs != nullptr ? 1 : (nslc == 1 ? 8 : (nslc == 2 ? 4 : (nslc <= 4 ? 2 : 1)));
+    uint64_t *scand = reinterpret_cast<uint64_t *>(sused + MAX_E + 2);  // [8][MAX_TOPK]
+    const int j = warp / nw, wi = warp % nw;
+    if (nw > 1 && j < nslc) {
       const int b = c + (j << p.log2S);
-      route_token_sorted(p.logits + static_cast<size_t>(b) * p.E, p.E, topk,
-                         p.topk_idx + b * topk, p.topk_w + b * topk,
-                         p.probs ? p.probs + static_cast<size_t>(b) * p.E : nullptr, nullptr);
+      const float *lg = p.logits + static_cast<size_t>(b) * p.E;
+      uint64_t *sc = scand + j * nw * MAX_TOPK;
+      if (nw == 8)
+        route_token_split<8>(lg, p.E, topk, wi, sc, 3 + j, p.topk_idx + b * topk,
+                             p.topk_w + b * topk, nullptr);
+      else if (nw == 4)
+        route_token_split<4>(lg, p.E, topk, wi, sc, 3 + j, p.topk_idx + b * topk,
+                             p.topk_w + b * topk, nullptr);
+      else
+        route_token_split<2>(lg, p.E, topk, wi, sc, 3 + j, p.topk_idx + b * topk,
+                             p.topk_w + b * topk, nullptr);
     }
+    if (nw == 1)
+      for (int jj = warp; jj < nslc; jj += FF_THREADS / 32) {
+        const int b = c + (jj << p.log2S);
+        route_token_sorted(p.logits + static_cast<size_t>(b) * p.E, p.E, topk,
+                           p.topk_idx + b * topk, p.topk_w + b * topk,
+                           p.probs ? p.probs + static_cast<size_t>(b) * p.E : nullptr,
+                           nullptr);
+      }
     if (tid == 0) *cnt_grp = 0;
     __syncthreads();
     if (tid == 0) flags[1] = (atom_add_acq_rel_gpu(cnt_all, 1) == ndst - 1);

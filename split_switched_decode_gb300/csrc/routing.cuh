@@ -268,6 +268,102 @@ __device__ __forceinline__ void route_token_sorted(const float *logits, int E, i
   }
 }
 
+// k rounds over the sorted per-lane lists k[0..V) of a warp: each round takes the
+// largest head logit and, among equal ones, the lowest expert; the winning lane drops
+// its head. Lane j < topk ends with the j-th choice (expert, logit); a lane with no
+// choice (fewer than topk real keys) keeps expert 0xFFFFFFFF.
+template <int V>
+__device__ __forceinline__ void warp_rounds(uint64_t (&k)[V], int topk, uint32_t &my_e,
+                                            float &my_v) {
+  const int lane = threadIdx.x & 31;
+  const unsigned FULL = 0xFFFFFFFFu;
+  my_e = 0xFFFFFFFFu;
+  my_v = 0.f;
+  for (int j = 0; j < topk; ++j) {
+    const uint32_t hk = static_cast<uint32_t>(k[0] >> 32);
+    const uint32_t kmax = __reduce_max_sync(FULL, hk);
+    const uint32_t cand = (hk == kmax && k[0] != 0ull) ? 0xFFFFFFFFu - static_cast<uint32_t>(k[0])
+                                                       : 0xFFFFFFFFu;
+    const uint32_t win = __reduce_min_sync(FULL, cand);
+    const uint32_t src = __ffs(__ballot_sync(FULL, cand == win && win != 0xFFFFFFFFu)) - 1;
+    if (win != 0xFFFFFFFFu && lane == static_cast<int>(src)) {
+#pragma unroll
+      for (int i = 0; i < V - 1; ++i) k[i] = k[i + 1];
+      k[V - 1] = 0ull;
+    }
+    if (lane == j) {
+      my_e = win;
+      my_v = order_key_to_f32(kmax);
+    }
+  }
+}
+
+template <int V>
+__device__ __forceinline__ void sort_desc_lane(uint64_t (&k)[V]) {
+#pragma unroll
+  for (int s = 2; s <= V; s <<= 1) {
+#pragma unroll
+    for (int d = s >> 1; d > 0; d >>= 1) {
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        if ((i & d) == 0) {
+          const bool desc = (i & s) == 0;
+          const uint64_t a = k[i], b = k[i + d];
+          const uint64_t hi = a > b ? a : b, lo = a > b ? b : a;
+          k[i] = desc ? hi : lo;
+          k[i + d] = desc ? lo : hi;
+        }
+      }
+    }
+  }
+}
+
+// Routes one token with NW warps of the CTA (warps wbase .. wbase+NW-1, named barrier
+// bar_id over their NW*32 threads; E <= 512, NW in 2, 4, 8). Warp wi takes the experts
+// [wi*32*V, (wi+1)*32*V) (V = 16/NW keys per lane, loads coalesced), sorts each lane's
+// keys and picks its slice's topk by k warp rounds; the first warp of the group then
+// picks the token's topk among the NW*topk candidates (<= 4 per lane) the same way and
+// renormalises. Same choices and weights formula as route_token_sorted.
+template <int NW>
+__device__ __forceinline__ void route_token_split(const float *logits, int E, int topk, int wi,
+                                                  uint64_t *scand, int bar_id, int32_t *idx,
+                                                  float *w, int32_t *sidx) {
+  constexpr int V = 16 / NW;
+  const int lane = threadIdx.x & 31;
+  const unsigned FULL = 0xFFFFFFFFu;
+  uint64_t k[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int e = (wi * V + i) * 32 + lane;
+    k[i] = e < E ? route_key(__ldcg(logits + e), static_cast<uint32_t>(e)) : 0ull;
+  }
+  sort_desc_lane<V>(k);
+  uint32_t my_e;
+  float my_v;
+  warp_rounds<V>(k, topk, my_e, my_v);
+  if (lane < MAX_TOPK)
+    scand[wi * MAX_TOPK + lane] =
+        (lane < topk && my_e != 0xFFFFFFFFu) ? route_key(my_v, my_e) : 0ull;
+  named_bar_sync(bar_id, NW * 32);
+  if (wi != 0) return;
+  constexpr int C = NW * MAX_TOPK / 32;  // candidates per lane: 1, 2 or 4
+  uint64_t c[C];
+#pragma unroll
+  for (int i = 0; i < C; ++i) c[i] = scand[lane * C + i];
+  sort_desc_lane<C>(c);
+  warp_rounds<C>(c, topk, my_e, my_v);
+  const float m0 = __shfl_sync(FULL, my_v, 0);  // the largest logit
+  const float ex = lane < topk ? expf(my_v - m0) : 0.f;
+  float zs = ex;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) zs += __shfl_xor_sync(FULL, zs, o);
+  if (lane < topk) {
+    idx[lane] = static_cast<int32_t>(my_e);
+    w[lane] = ex / zs;
+    if (sidx != nullptr) sidx[lane] = static_cast<int32_t>(my_e);
+  }
+}
+
 // The route map (layout of the public header) built by every thread of the CTA:
 // per-expert token masks by shared atomics; counts per expert in shared memory; one
 // warp turns them into offsets and the used-expert list (each lane scans a contiguous

@@ -113,10 +113,16 @@ def test_moe_front_cluster_route_map_equals_counter_path(env, monkeypatch, B):
     assert np.array_equal(c[1].cpu().numpy(), ref["idx"])
 
 
-@pytest.mark.parametrize("B,E,L,K,k", [(1, 384, 512, 7168, 8), (8, 384, 512, 7168, 8),
-                                       (17, 384, 512, 7168, 8), (64, 384, 512, 7168, 8),
+@pytest.mark.parametrize("B,E,L,K,k", [(1, 384, 512, 7168, 8), (2, 384, 512, 7168, 8),
+                                       (3, 384, 512, 7168, 8), (4, 384, 512, 7168, 8),
+                                       (5, 384, 512, 7168, 8), (8, 384, 512, 7168, 8),
+                                       (17, 384, 512, 7168, 8), (33, 384, 512, 7168, 8),
+                                       (64, 384, 512, 7168, 8), (64, 384, 512, 7168, 16),
                                        (5, 130, 0, 456, 16), (33, 512, 8, 64, 1),
-                                       (64, 16, 100, 1032, 16), (2, 1, 0, 8, 1)])
+                                       (64, 16, 100, 1032, 16), (2, 1, 0, 8, 1),
+                                       # clusters of 4 and 8 CTAs: more than 4 tokens per CTA
+                                       (17, 40, 24, 256, 4), (40, 100, 20, 512, 8),
+                                       (64, 384, 512, 512, 8), (3, 40, 24, 256, 4)])
 def test_moe_front_one_launch_and_two_launch_paths(env, monkeypatch, B, E, L, K, k):
     """The one-launch front end (clusters reduce the split-K partials on chip, per-tile
     top-k candidates merged by the last router CTA) and the two-launch path both match
