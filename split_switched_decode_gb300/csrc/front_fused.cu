@@ -337,16 +337,14 @@ __global__ void __launch_bounds__(FF_THREADS, 2)
   int32_t *sidx = reinterpret_cast<int32_t *>(ring);                      // [B*topk]
   unsigned long long *smask =
       reinterpret_cast<unsigned long long *>(sidx + MAX_B * MAX_TOPK);   // [E]
-  int *scnt = reinterpret_cast<int *>(smask + MAX_E);                     // [E]
-  int *soff = scnt + MAX_E;                                               // [E]
-  int *sused = soff + MAX_E;                                              // [E]
-  int *s_total = sused + MAX_E;                                           // [2]
+  int *soff = reinterpret_cast<int *>(smask + MAX_E);                     // [E]
+  int *swarp = soff + MAX_E;                                              // [16]
+  uint64_t *scand = reinterpret_cast<uint64_t *>(swarp + 16);             // [8][MAX_TOPK]
   const int topk = p.topk;
   if (single) {
     // up to 4 tokens, several warps share a token (a slice of the experts each, then one
     // merge); with the full softmax requested, or from 5 tokens, a warp per token
     const int nw = p.probs != nullptr ? 1 : (p.B == 1 ? 8 : (p.B == 2 ? 4 : (p.B <= 4 ? 2 : 1)));
-    uint64_t *scand = reinterpret_cast<uint64_t *>(sused + MAX_E + 2);  // [8][MAX_TOPK]
     const int b = warp / nw, wi = warp % nw;
     if (nw > 1 && b < p.B) {
       const float *lg = p.logits + static_cast<size_t>(b) * p.E;
@@ -370,12 +368,11 @@ __global__ void __launch_bounds__(FF_THREADS, 2)
     if (tid == 0) *cnt_all = 0;  // every arrival of this call is in: ready for the next
     __syncthreads();
     if (p.route_map != nullptr)
-      build_route_map_cta(sidx, p.B, topk, p.E, p.route_map, smask, scnt, soff, sused, s_total);
+      build_route_map_cta(sidx, p.B, topk, p.E, p.route_map, smask, soff, swarp);
   } else {
     // this group's tokens b = c + j*S: 8, 4 or 2 warps each for up to 4 tokens (16-CTA
     // clusters); one warp each for more (smaller clusters) or with the full softmax
     const int nw = p.probs != nullptr ? 1 : (nslc == 1 ? 8 : (nslc == 2 ? 4 : (nslc <= 4 ? 2 : 1)));
-    uint64_t *scand = reinterpret_cast<uint64_t *>(sused + MAX_E + 2);  // [8][MAX_TOPK]
     const int j = warp / nw, wi = warp % nw;
     if (nw > 1 && j < nslc) {
       const int b = c + (j << p.log2S);
@@ -409,7 +406,7 @@ __global__ void __launch_bounds__(FF_THREADS, 2)
       for (int q = tid; q < P; q += FF_THREADS) sidx[q] = __ldcg(p.topk_idx + q);
       __syncthreads();
       if (p.route_map != nullptr)
-        build_route_map_cta(sidx, p.B, topk, p.E, p.route_map, smask, scnt, soff, sused, s_total);
+        build_route_map_cta(sidx, p.B, topk, p.E, p.route_map, smask, soff, swarp);
     }
   }
   // every receiver has taken this CTA's rows (and nothing else targets it) before exit

@@ -39,9 +39,10 @@ __device__ __forceinline__ void empty_route_map(int B, int topk, int E, int32_t 
 }
 
 // Routed-expert gather for a caller without a route map, in one launch: every CTA
-// validates topk_idx and builds the whole route map in shared memory (a few KB, cheaper
-// than a second launch and its memory round trip), CTA 0 publishes it to rm for the
-// grouped launches and the combine, and every CTA copies its share of the rows
+// validates topk_idx and builds the whole route map in shared memory with all 256
+// threads (a few KB, cheaper than a second launch and its memory round trip), CTA 0
+// publishes it to rm for the grouped launches and the combine, and every CTA copies its
+// share of the rows
 // Xg[q, :] = X[pairs[q] / topk, :] with UNR independent 16-byte loads in flight per thread.
 __global__ void __launch_bounds__(256) gather_map_kernel(const uint16_t *X,
                                                          const int32_t *topk_idx, int B,
@@ -53,12 +54,13 @@ __global__ void __launch_bounds__(256) gather_map_kernel(const uint16_t *X,
   __shared__ unsigned long long smask[MAX_E];
   __shared__ int soff[MAX_E];
   __shared__ int32_t smap[3 * MAX_E + 2 + 2 * MAX_B * MAX_TOPK];
+  __shared__ int swarp[16];
   __shared__ int bad;
   if (!load_routing(topk_idx, B, topk, E, sidx, &bad)) {
     if (blockIdx.x == 0) empty_route_map(B, topk, E, rm, status);
     return;
   }
-  build_route_map(sidx, B, topk, E, smap, smask, soff, 256, 1, threadIdx.x);
+  build_route_map_cta(sidx, B, topk, E, smap, smask, soff, swarp);
   __syncthreads();
   const int P = B * topk;
   if (blockIdx.x == 0)

@@ -364,18 +364,19 @@ __device__ __forceinline__ void route_token_split(const float *logits, int E, in
   }
 }
 
-// The route map (layout of the public header) built by every thread of the CTA:
-// per-expert token masks by shared atomics; counts per expert in shared memory; one
-// warp turns them into offsets and the used-expert list (each lane scans a contiguous
-// run of experts); then every thread writes counts / offsets / used with coalesced
-// stores and places each (token, slot) entry by the rank of its token among the
-// expert's tokens. sidx: shared [B*topk] expert ids in [0, E). Scratch in shared memory:
-// smask uint64 [E], scnt / soff / sused int [E], s_total int [2]. Requires B <= 64.
+// The route map (layout of the public header) built by every thread of the CTA, each
+// thread owning two consecutive experts (E <= 2 * blockDim.x): per-expert token masks by
+// shared atomics; the counts scanned within each warp by shuffles and across warps from
+// the warp totals in shared memory; counts / offsets / used written by their owners;
+// every (token, slot) entry placed by the rank of its token among the expert's tokens.
+// Four CTA barriers, no serial loop. sidx: shared [B*topk] expert ids in [0, E);
+// scratch in shared memory: smask uint64 [E], soff int [E], swarp int [2 * warps].
+// Requires B <= 64.
 __device__ __noinline__ static void build_route_map_cta(const int32_t *sidx, int B, int topk,
                                                         int E, int32_t *rm,
-                                                        unsigned long long *smask, int *scnt,
-                                                        int *soff, int *sused, int *s_total) {
-  const int tid = threadIdx.x, nthr = blockDim.x;
+                                                        unsigned long long *smask, int *soff,
+                                                        int *swarp) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int P = B * topk;
   int32_t *counts = rm;
   int32_t *offsets = rm + E;
@@ -383,56 +384,53 @@ __device__ __noinline__ static void build_route_map_cta(const int32_t *sidx, int
   int32_t *pos = pairs + P;
   int32_t *num_used = pos + P;
   int32_t *used = num_used + 1;
-  for (int e = tid; e < E; e += nthr) smask[e] = 0ull;
+  const int e0 = 2 * tid, e1 = e0 + 1;
+  if (e0 < E) smask[e0] = 0ull;
+  if (e1 < E) smask[e1] = 0ull;
   __syncthreads();
-  for (int q = tid; q < P; q += nthr) atomicOr(&smask[sidx[q]], 1ull << (q / topk));
+  for (int q = tid; q < P; q += blockDim.x) atomicOr(&smask[sidx[q]], 1ull << (q / topk));
   __syncthreads();
-  for (int e = tid; e < E; e += nthr) scnt[e] = __popcll(smask[e]);
-  __syncthreads();
-  if (tid < 32) {
-    const int lane = tid;
-    const int per = (E + 31) / 32;
-    const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
-    int c = 0, u = 0;
-    for (int e = e0; e < e1; ++e) {
-      const int k = scnt[e];
-      c += k;
-      u += (k > 0);
-    }
-    int ic = c, iu = u;
+  const int c0 = e0 < E ? __popcll(smask[e0]) : 0, c1 = e1 < E ? __popcll(smask[e1]) : 0;
+  const int c = c0 + c1, u = (c0 > 0) + (c1 > 0);
+  int ic = c, iu = u;  // inclusive scans within the warp
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int a = __shfl_up_sync(0xFFFFFFFFu, ic, o);
-      const int b = __shfl_up_sync(0xFFFFFFFFu, iu, o);
-      if (lane >= o) {
-        ic += a;
-        iu += b;
-      }
+  for (int o = 1; o < 32; o <<= 1) {
+    const int a = __shfl_up_sync(0xFFFFFFFFu, ic, o);
+    const int b = __shfl_up_sync(0xFFFFFFFFu, iu, o);
+    if (lane >= o) {
+      ic += a;
+      iu += b;
     }
-    int run = ic - c, runu = iu - u;
-    for (int e = e0; e < e1; ++e) {
-      const int k = scnt[e];
-      soff[e] = run;
-      if (k > 0) sused[runu++] = e;
-      run += k;
-    }
-    if (lane == 31) {
-      s_total[0] = ic;
-      s_total[1] = iu;
-    }
+  }
+  if (lane == 31) {
+    swarp[2 * warp] = ic;
+    swarp[2 * warp + 1] = iu;
   }
   __syncthreads();
-  const int nu = s_total[1];
-  for (int e = tid; e < E; e += nthr) {
-    counts[e] = scnt[e];
-    offsets[e] = soff[e];
+  int bc = 0, bu = 0;  // totals of the warps before this one
+  for (int w = 0; w < warp; ++w) {
+    bc += swarp[2 * w];
+    bu += swarp[2 * w + 1];
   }
-  for (int u = tid; u < nu; u += nthr) used[u] = sused[u];
-  if (tid == 0) {
-    offsets[E] = s_total[0];
-    *num_used = nu;
+  const int o0 = bc + ic - c, u0 = bu + iu - u;
+  if (e0 < E) {
+    counts[e0] = c0;
+    offsets[e0] = o0;
+    soff[e0] = o0;
+    if (c0 > 0) used[u0] = e0;
   }
-  for (int q = tid; q < P; q += nthr) {
+  if (e1 < E) {
+    counts[e1] = c1;
+    offsets[e1] = o0 + c0;
+    soff[e1] = o0 + c0;
+    if (c1 > 0) used[u0 + (c0 > 0)] = e1;
+  }
+  if (tid == blockDim.x - 1) {
+    offsets[E] = o0 + c;
+    *num_used = u0 + u;
+  }
+  __syncthreads();
+  for (int q = tid; q < P; q += blockDim.x) {
     const int e = sidx[q];
     const int b = q / topk;
     const int at = soff[e] + __popcll(smask[e] & ((1ull << b) - 1ull));
