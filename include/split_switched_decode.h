@@ -232,11 +232,15 @@ DEC_API size_t moe_route_map_ints(int B, int E, int topk);
  * X [B,K]; latent [B,L] (NULL allowed when L == 0); topk_idx int32 [B,topk];
  * topk_w fp32 [B,topk]; probs_opt fp32 [B,E] or NULL; route_map_opt int32
  * [moe_route_map_ints(B,E,topk)] or NULL. E in 1..512, topk in 1..min(E,16), L >= 0.
- * Two launches on `s`: the product, then a finishing kernel that starts as the
- * product's CTAs retire (programmatic dependent launch): it adds the partial tiles,
- * routes each token with one warp and builds the route map -- for B <= 8 inside one
- * thread-block cluster of the routing CTAs, otherwise in the CTA that routes the last
- * token. Both ways give the same bits.
+ * One launch on `s` where the device can hold its thread-block clusters (the default):
+ * each 128-row tile of Wcat is one cluster of up to 16 CTAs that split K and add their
+ * partials through distributed shared memory; router CTAs publish the logits (fp32, in
+ * the workspace) and arrival counters elect the CTAs that route (a warp per token) and
+ * build the route map. Otherwise, or with the environment switch DEC_FRONT_FUSED=0, two
+ * launches: the product, then a finishing kernel that starts as the product's CTAs
+ * retire (programmatic dependent launch). Every way gives the same top-k ids, weights
+ * and route map. The workspace must be zeroed once before its first use (its arrival
+ * counters return to zero at the end of every call).
  */
 DEC_API size_t moe_front_workspace_bytes(int B, int E, int L, int K);
 DEC_API dec_status moe_front(const dec_bf16 *X, const dec_bf16 *Wcat, int B, int K, int E, int L,

@@ -432,7 +432,7 @@ dec_status run_splitk_rows(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 
 struct FrontPlan {
   SplitPlan sk;
   size_t done_off, logits_off;  // done_off: the route-map counter of the two-launch path
-  size_t cand_off, fcnt_off;    // one-launch path: per-tile top-k candidates, arrivals
+  size_t fcnt_off;              // one-launch path: arrival counters
   size_t total;
 };
 
@@ -452,9 +452,7 @@ bool plan_front(int B, int E, int L, int K, int num_sms, FrontPlan *fp, int spli
   if (!plan_splitk(B, E + L, K, splits, num_sms, &fp->sk)) return false;
   fp->done_off = fp->sk.total;
   fp->logits_off = fp->done_off + kAlign;
-  fp->cand_off = fp->logits_off + align_up(static_cast<size_t>(B) * E * sizeof(float));
-  const size_t router_tiles = static_cast<size_t>(ceil_div(E, TILE_N));
-  fp->fcnt_off = fp->cand_off + align_up(static_cast<size_t>(B) * router_tiles * MAX_TOPK * 8);
+  fp->fcnt_off = fp->logits_off + align_up(static_cast<size_t>(B) * E * sizeof(float));
   fp->total = fp->fcnt_off + kAlign;
   return true;
 }
@@ -482,6 +480,31 @@ int front_stages_override() {
     return v >= 2 && v <= 12 ? v : 0;
   }
   return 0;
+}
+
+// Largest batch whose tokens the one-launch front end routes in one CTA (a warp per
+// token, one arrival counter; DEC_FRONT_SINGLE_B, default 8). Larger batches route each
+// token group in its own CTA and elect the route-map builder with a second counter.
+int front_single_batch() {
+  if (const char *s = std::getenv("DEC_FRONT_SINGLE_B")) {
+    const int v = std::atoi(s);
+    if (v >= 0 && v <= MAX_B) return v;
+  }
+  return 8;
+}
+
+// Largest batch for which the one-launch front end's router CTAs hold back the trigger
+// of the next kernel until their routing has read the logits (DEC_FRONT_LATE_TRIGGER_B).
+// The next kernel's weight loads, issued before its dependency wait, otherwise flood L2
+// while the routing CTA reads the freshly published logits (measured at B = 1: 2.0 us
+// for those reads, 0.6 us without the burst). Default 8: a chain of front
+// ends measured 8.3-8.6 us per call at B = 1-8 with it, 8.8-9.9 us without.
+int front_late_trigger_batch() {
+  if (const char *s = std::getenv("DEC_FRONT_LATE_TRIGGER_B")) {
+    const int v = std::atoi(s);
+    if (v >= 0 && v <= MAX_B) return v;
+  }
+  return 8;
 }
 
 struct FusedFrontPlan {
@@ -820,12 +843,13 @@ dec_status run_front(const dec_bf16 *X, const dec_bf16 *Wcat, int B, int K, int 
     f.topk = topk;
     f.nst = ffp.nst;
     f.nsl = ffp.nsl;
+    f.single_b = front_single_batch();
+    f.trig_late = B <= front_late_trigger_batch() ? 1 : 0;
     f.latent = latent;
     f.topk_idx = topk_idx;
     f.topk_w = topk_w;
     f.probs = probs_opt;
     f.logits = reinterpret_cast<float *>(wsb + fp.logits_off);
-    f.cand = reinterpret_cast<uint32_t *>(wsb + fp.cand_off);
     f.route_map = route_map_opt;
     f.counter = reinterpret_cast<int *>(wsb + fp.fcnt_off);
     f.status = d->status;

@@ -1,6 +1,6 @@
 // front_fused.cu -- the MoE front end in one kernel: router + latent product on tensor
-// cores, split-K reduction on chip, per-tile top-k, one global merge of the candidates,
-// renormalisation and the routing inverse map.
+// cores, split-K reduction on chip, top-k routing, renormalisation and the routing
+// inverse map.
 //
 // "Hyper Optimizing Kimi K3 in vLLM", Part 1 / 3 "Improve MoE scheduling and overlap":
 // the router scores and the latent input projection are computed as one matrix product
@@ -27,13 +27,12 @@
 // Every CTA that owns tokens then adds the S partials of each of its tokens in CTA
 // order (fixed order: the bits do not depend on timing), tells each sender that its
 // rows have landed (remote mbarrier arrive: a CTA leaves only when all its receivers
-// have), writes the latent rows as bf16 and, for router rows, sorts the token's 128
-// candidate keys (logit, then lower expert index) with a warp bitonic sort and
-// publishes the best topk. An acquire-release arrival counter elects the last router
-// CTA, which sorts every token's TR x topk candidates again (a warp per token),
-// renormalises the chosen weights, writes topk_idx / topk_w and the optional full
-// softmax, and builds the route map with all its threads. No CTA ever waits for a CTA
-// outside its cluster; inside a cluster the hardware co-schedules all CTAs.
+// have), and writes the latent rows as bf16 and the router logits as fp32. Acquire-
+// release arrival counters then elect the router CTA(s) that route -- a warp per token:
+// a lower bound from the lanes' largest logits, the candidates above it, their exact
+// ranks -- renormalise the chosen weights, write topk_idx / topk_w and the optional full
+// softmax, and the CTA that builds the route map with all its threads. No CTA ever waits
+// for a CTA outside its cluster; inside a cluster the hardware co-schedules all CTAs.
 #include <atomic>
 
 #include "common.cuh"
@@ -173,7 +172,8 @@ __global__ void __launch_bounds__(FF_THREADS, 2)
                                 t * TILE_N, pol);
       }
       for (int kb = kb0 + pre; kb < kb1; ++kb) tma_prefetch_l2_2d(&wmap, kb * TILE_K, t * TILE_N);
-      griddep_launch_dependents();
+      // the next kernel may start loading (router CTAs with trig_late: once routed)
+      if (!(p.trig_late && t < p.TR)) griddep_launch_dependents();
       griddep_wait();
       bool ok = true;
       int q = 0;
@@ -317,12 +317,15 @@ __global__ void __launch_bounds__(FF_THREADS, 2)
   }
   __syncthreads();
   // ------------------------------------------------- routing: last router CTA(s)
-  // Up to 4 tokens one arrival counter elects the last router CTA, which routes every
-  // token (several warps per token) and builds the route map. Beyond, the three (TR) router
-  // CTAs owning a token group (the same cluster rank) elect their last one, which
+  // Up to p.single_b tokens one arrival counter elects the last router CTA, which routes
+  // every token (a warp per token) and builds the route map. Beyond, the three (TR)
+  // router CTAs owning a token group (the same cluster rank) elect their last one, which
   // routes that group; a second counter over the groups elects the CTA that builds the
   // route map from the published top-k ids.
-  const bool single = p.B <= 4;
+  // With trig_late the router CTAs let the next kernel start only here (a CTA that exits
+  // counts as triggered; a routing warp triggers once its logits are loaded): the next
+  // kernel's burst of weight loads would otherwise queue in front of these L2 reads.
+  const bool single = p.B <= p.single_b;
   int *cnt_all = p.counter;           // [0]: every router CTA (single) / every group
   int *cnt_grp = p.counter + 1 + c;   // [1 + c]: the TR router CTAs of group c
   if (router && nslc > 0 && tid == 0)
@@ -333,69 +336,36 @@ __global__ void __launch_bounds__(FF_THREADS, 2)
     if (tid == 0) (void)mbar_wait_bounded(sent_bar, 0u, p.status, flags, p.wait_limit_ns);
     return;
   }
-  // route-map scratch in the idle stage ring
+  // routing and route-map scratch in the idle stage ring
   int32_t *sidx = reinterpret_cast<int32_t *>(ring);                      // [B*topk]
   unsigned long long *smask =
       reinterpret_cast<unsigned long long *>(sidx + MAX_B * MAX_TOPK);   // [E]
   int *soff = reinterpret_cast<int *>(smask + MAX_E);                     // [E]
   int *swarp = soff + MAX_E;                                              // [16]
-  uint64_t *scand = reinterpret_cast<uint64_t *>(swarp + 16);             // [8][MAX_TOPK]
+  uint64_t *rscr = reinterpret_cast<uint64_t *>(swarp + 16) +
+                   warp * (RT_CMAX + MAX_TOPK);                           // [8][RT_CMAX+16]
   const int topk = p.topk;
-  if (single) {
-    // up to 4 tokens, several warps share a token (a slice of the experts each, then one
-    // merge); with the full softmax requested, or from 5 tokens, a warp per token
-    const int nw = p.probs != nullptr ? 1 : (p.B == 1 ? 8 : (p.B == 2 ? 4 : (p.B <= 4 ? 2 : 1)));
-    const int b = warp / nw, wi = warp % nw;
-    if (nw > 1 && b < p.B) {
-      const float *lg = p.logits + static_cast<size_t>(b) * p.E;
-      uint64_t *sc = scand + b * nw * MAX_TOPK;
-      if (nw == 8)
-        route_token_split<8>(lg, p.E, topk, wi, sc, 3 + b, p.topk_idx + b * topk,
-                             p.topk_w + b * topk, sidx + b * topk);
-      else if (nw == 4)
-        route_token_split<4>(lg, p.E, topk, wi, sc, 3 + b, p.topk_idx + b * topk,
-                             p.topk_w + b * topk, sidx + b * topk);
-      else
-        route_token_split<2>(lg, p.E, topk, wi, sc, 3 + b, p.topk_idx + b * topk,
-                             p.topk_w + b * topk, sidx + b * topk);
+  // this CTA's tokens: every token (single), else the group's b = c + j*S
+  const int ntok = single ? p.B : nslc;
+  for (int j = warp; j < ntok; j += FF_THREADS / 32) {
+    const int b = single ? j : c + (j << p.log2S);
+    const float *lg = p.logits + static_cast<size_t>(b) * p.E;
+    int32_t *si = single ? sidx + b * topk : nullptr;
+    if (p.probs != nullptr) {  // the full softmax as well
+      if (p.trig_late && lane == 0) griddep_launch_dependents();
+      route_token_sorted(lg, p.E, topk, p.topk_idx + b * topk, p.topk_w + b * topk,
+                         p.probs + static_cast<size_t>(b) * p.E, si);
+    } else {
+      route_token_filtered(lg, p.E, topk, p.topk_idx + b * topk, p.topk_w + b * topk, si,
+                           rscr, p.trig_late != 0);
     }
-    if (nw == 1)
-      for (int bb = warp; bb < p.B; bb += FF_THREADS / 32)  // a warp per token
-        route_token_sorted(p.logits + static_cast<size_t>(bb) * p.E, p.E, topk,
-                           p.topk_idx + bb * topk, p.topk_w + bb * topk,
-                           p.probs ? p.probs + static_cast<size_t>(bb) * p.E : nullptr,
-                           sidx + bb * topk);
+  }
+  if (single) {
     if (tid == 0) *cnt_all = 0;  // every arrival of this call is in: ready for the next
     __syncthreads();
     if (p.route_map != nullptr)
       build_route_map_cta(sidx, p.B, topk, p.E, p.route_map, smask, soff, swarp);
   } else {
-    // this group's tokens b = c + j*S: 8, 4 or 2 warps each for up to 4 tokens (16-CTA
-    // clusters); one warp each for more (smaller clusters) or with the full softmax
-    const int nw = p.probs != nullptr ? 1 : (nslc == 1 ? 8 : (nslc == 2 ? 4 : (nslc <= 4 ? 2 : 1)));
-    const int j = warp / nw, wi = warp % nw;
-    if (nw > 1 && j < nslc) {
-      const int b = c + (j << p.log2S);
-      const float *lg = p.logits + static_cast<size_t>(b) * p.E;
-      uint64_t *sc = scand + j * nw * MAX_TOPK;
-      if (nw == 8)
-        route_token_split<8>(lg, p.E, topk, wi, sc, 3 + j, p.topk_idx + b * topk,
-                             p.topk_w + b * topk, nullptr);
-      else if (nw == 4)
-        route_token_split<4>(lg, p.E, topk, wi, sc, 3 + j, p.topk_idx + b * topk,
-                             p.topk_w + b * topk, nullptr);
-      else
-        route_token_split<2>(lg, p.E, topk, wi, sc, 3 + j, p.topk_idx + b * topk,
-                             p.topk_w + b * topk, nullptr);
-    }
-    if (nw == 1)
-      for (int jj = warp; jj < nslc; jj += FF_THREADS / 32) {
-        const int b = c + (jj << p.log2S);
-        route_token_sorted(p.logits + static_cast<size_t>(b) * p.E, p.E, topk,
-                           p.topk_idx + b * topk, p.topk_w + b * topk,
-                           p.probs ? p.probs + static_cast<size_t>(b) * p.E : nullptr,
-                           nullptr);
-      }
     if (tid == 0) *cnt_grp = 0;
     __syncthreads();
     if (tid == 0) flags[1] = (atom_add_acq_rel_gpu(cnt_all, 1) == ndst - 1);

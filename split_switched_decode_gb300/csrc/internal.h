@@ -144,19 +144,20 @@ cudaError_t launch_front_finish(const FrontFinishParams &f, cudaStream_t s);
 // The whole front end in one launch (front_fused.cu): T tiles of 128 W_cat rows, one
 // thread-block cluster of S CTAs per tile, CTA c of a cluster multiplying k-blocks
 // [c*KB/S, (c+1)*KB/S); the partials are added in the token-owning CTA (token b -> CTA
-// b % S) after bulk copies through distributed shared memory; router tiles publish
-// per-token top-k candidates, and the last router CTA (arrival counter) merges them,
-// renormalises and builds the route map.
+// b % S) after transfers through distributed shared memory; router CTAs publish the
+// token's logits, and arrival counters elect the CTAs that route (a warp per token) and
+// build the route map.
 struct FrontFusedParams {
   int B, E, L, KB, T, S, log2S, TR, topk;
-  int nst;  // stage-ring depth (weight + activation boxes of one k-block per stage)
-  int nsl;  // token slots per CTA: ceil(B / S)
+  int nst;       // stage-ring depth (weight + activation boxes of one k-block per stage)
+  int nsl;       // token slots per CTA: ceil(B / S)
+  int single_b;  // up to this batch one CTA routes every token and builds the route map
+  int trig_late; // router CTAs trigger the next kernel once routed, not at their start
   uint16_t *latent;     // [B, L] bf16
   int32_t *topk_idx;    // [B, topk]
   float *topk_w;        // [B, topk]
   float *probs;         // [B, E] or nullptr
-  float *logits;        // [B, E] workspace, written only with probs
-  uint32_t *cand;       // [B][TR][topk] x {order key, expert}: per-tile candidates
+  float *logits;        // [B, E] workspace: router logits, fp32
   int32_t *route_map;   // or nullptr
   int *counter;         // arrivals of the router CTAs; zero between calls
   unsigned *status;

@@ -107,6 +107,16 @@ __device__ __forceinline__ void route_tokens_warp(const float *logits, int B, in
   }
 }
 
+// Token masks of the route-map builders: bit b of expert e's 64-bit mask lives in the
+// 32-bit word 2e + b/32 (set with 32-bit shared atomics, far cheaper than 64-bit ones);
+// every access goes through this 32-bit view.
+__device__ __forceinline__ uint64_t token_mask(const unsigned *m32, int e) {
+  return (static_cast<uint64_t>(m32[2 * e + 1]) << 32) | m32[2 * e];
+}
+__device__ __forceinline__ void token_mask_set(unsigned *m32, int e, int b) {
+  atomicOr(m32 + 2 * e + (b >> 5), 1u << (b & 31));
+}
+
 // Counting sort of the routing into the route-map layout of the public header, run by
 // `nthreads` threads of one CTA (a multiple of 32, >= 32; `tid` = 0..nthreads-1, whole
 // warps) that synchronise on named barrier `bar_id`. sidx: shared [B*topk] expert ids;
@@ -123,10 +133,10 @@ __device__ __noinline__ static void build_route_map(const int32_t *sidx, int B, 
   int32_t *num_used = pos + P;
   int32_t *used = num_used + 1;
 
-  for (int e = tid; e < E; e += nthreads) smask[e] = 0ull;
+  unsigned *m32 = reinterpret_cast<unsigned *>(smask);
+  for (int e = tid; e < E; e += nthreads) m32[2 * e] = m32[2 * e + 1] = 0u;
   named_bar_sync(bar_id, nthreads);
-  for (int q = tid; q < P; q += nthreads)
-    atomicOr(&smask[sidx[q]], 1ull << (q / topk));
+  for (int q = tid; q < P; q += nthreads) token_mask_set(m32, sidx[q], q / topk);
   named_bar_sync(bar_id, nthreads);
   if (tid < 32) {
     const int lane = tid;
@@ -134,7 +144,7 @@ __device__ __noinline__ static void build_route_map(const int32_t *sidx, int B, 
     const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
     int cnt = 0, nu = 0;
     for (int e = e0; e < e1; ++e) {
-      const int c = __popcll(smask[e]);
+      const int c = __popcll(token_mask(m32, e));
       cnt += c;
       nu += (c > 0);
     }
@@ -150,7 +160,7 @@ __device__ __noinline__ static void build_route_map(const int32_t *sidx, int B, 
     }
     int run = icnt - cnt, runu = inu - nu;
     for (int e = e0; e < e1; ++e) {
-      const int c = __popcll(smask[e]);
+      const int c = __popcll(token_mask(m32, e));
       counts[e] = c;
       offsets[e] = run;
       soff[e] = run;
@@ -166,7 +176,7 @@ __device__ __noinline__ static void build_route_map(const int32_t *sidx, int B, 
   for (int q = tid; q < P; q += nthreads) {
     const int e = sidx[q];
     const int b = q / topk;
-    const int rank = __popcll(smask[e] & ((1ull << b) - 1ull));
+    const int rank = __popcll(token_mask(m32, e) & ((1ull << b) - 1ull));
     const int at = soff[e] + rank;
     pairs[at] = q;
     pos[q] = at;
@@ -318,40 +328,89 @@ __device__ __forceinline__ void sort_desc_lane(uint64_t (&k)[V]) {
   }
 }
 
-// Routes one token with NW warps of the CTA (warps wbase .. wbase+NW-1, named barrier
-// bar_id over their NW*32 threads; E <= 512, NW in 2, 4, 8). Warp wi takes the experts
-// [wi*32*V, (wi+1)*32*V) (V = 16/NW keys per lane, loads coalesced), sorts each lane's
-// keys and picks its slice's topk by k warp rounds; the first warp of the group then
-// picks the token's topk among the NW*topk candidates (<= 4 per lane) the same way and
-// renormalises. Same choices and weights formula as route_token_sorted.
-template <int NW>
-__device__ __forceinline__ void route_token_split(const float *logits, int E, int topk, int wi,
-                                                  uint64_t *scand, int bar_id, int32_t *idx,
-                                                  float *w, int32_t *sidx) {
-  constexpr int V = 16 / NW;
+// Candidates a warp keeps for the exact ranking of route_token_filtered (more: the token
+// is routed by k warp rounds instead).
+constexpr int RT_CMAX = 64;
+
+// Routes one token with one warp: the topk largest logits (ties to the lower expert index,
+// listed by descending logit), weights renormalised over the chosen k -- the same choices
+// and the same weight arithmetic as route_token_sorted, without the full softmax. Lane l
+// holds experts l, l+32, ... (E <= 512), read from global memory at L2 (written by other
+// CTAs of the launch).
+//   1. Lower bound: every lane's largest key is one candidate per lane; the topk-th
+//      largest of those 32 heads (by logit) bounds the topk-th largest logit from below,
+//      since the topk lanes with the largest heads hold topk distinct keys at or above it.
+//   2. Filter: the keys whose logit reaches the bound (every chosen expert among them,
+//      typically 8-16 of 384) are appended to a shared list in lane order (ballots).
+//   3. Rank: each candidate counts the candidates above it; rank j < topk is choice j.
+// No step waits on another lane's choice, unlike k rounds of warp reductions. With more
+// than RT_CMAX candidates (many equal logits) the warp sorts its registers and takes k
+// rounds, as route_token_sorted does.
+// scratch: shared uint64 [RT_CMAX + MAX_TOPK] of this warp. Outputs: idx/w [topk]
+// (global), sidx [topk] (shared, optional). trigger: once the logits are in registers,
+// let the next kernel of the stream be scheduled (programmatic dependent launch).
+__device__ __forceinline__ void route_token_filtered(const float *logits, int E, int topk,
+                                                     int32_t *idx, float *w, int32_t *sidx,
+                                                     uint64_t *scratch, bool trigger = false) {
+  constexpr int V = MAX_E / 32;
   const int lane = threadIdx.x & 31;
   const unsigned FULL = 0xFFFFFFFFu;
   uint64_t k[V];
+  uint32_t head = 0u;  // this lane's largest logit key (0: no expert)
 #pragma unroll
   for (int i = 0; i < V; ++i) {
-    const int e = (wi * V + i) * 32 + lane;
+    const int e = lane + 32 * i;
     k[i] = e < E ? route_key(__ldcg(logits + e), static_cast<uint32_t>(e)) : 0ull;
+    head = max(head, static_cast<uint32_t>(k[i] >> 32));
   }
-  sort_desc_lane<V>(k);
-  uint32_t my_e;
-  float my_v;
-  warp_rounds<V>(k, topk, my_e, my_v);
-  if (lane < MAX_TOPK)
-    scand[wi * MAX_TOPK + lane] =
-        (lane < topk && my_e != 0xFFFFFFFFu) ? route_key(my_v, my_e) : 0ull;
-  named_bar_sync(bar_id, NW * 32);
-  if (wi != 0) return;
-  constexpr int C = NW * MAX_TOPK / 32;  // candidates per lane: 1, 2 or 4
-  uint64_t c[C];
+  if (trigger) {
+    asm volatile("" ::"r"(head));  // every load of this lane has returned
+    __syncwarp();
+    if (lane == 0) griddep_launch_dependents();
+  }
+  // 1. the topk-th largest head: the smallest head with fewer than topk heads above it
+  int above = 0;
 #pragma unroll
-  for (int i = 0; i < C; ++i) c[i] = scand[lane * C + i];
-  sort_desc_lane<C>(c);
-  warp_rounds<C>(c, topk, my_e, my_v);
+  for (int h = 0; h < 32; ++h) above += __shfl_sync(FULL, head, h) > head;
+  const uint32_t bound = __reduce_min_sync(FULL, above < topk ? head : 0xFFFFFFFFu);
+  // 2. candidates in lane order
+  uint64_t *cand = scratch, *slot = scratch + RT_CMAX;
+  const unsigned lower = (1u << lane) - 1u;
+  int C = 0;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const bool in = k[i] != 0ull && static_cast<uint32_t>(k[i] >> 32) >= bound;
+    const unsigned bal = __ballot_sync(FULL, in);
+    const int at = C + __popc(bal & lower);
+    if (in && at < RT_CMAX) cand[at] = k[i];
+    C += __popc(bal);
+  }
+  __syncwarp();
+  uint32_t my_e = 0xFFFFFFFFu;
+  float my_v = 0.f;
+  if (C <= RT_CMAX) {
+    // 3. exact ranks (keys of distinct experts differ)
+    const uint64_t a0 = lane < C ? cand[lane] : 0ull;
+    const uint64_t a1 = lane + 32 < C ? cand[lane + 32] : 0ull;
+    int r0 = 0, r1 = 0;
+    for (int j = 0; j < C; ++j) {
+      const uint64_t x = cand[j];
+      r0 += x > a0;
+      r1 += x > a1;
+    }
+    if (lane < C && r0 < topk) slot[r0] = a0;
+    if (lane + 32 < C && r1 < topk) slot[r1] = a1;
+    __syncwarp();
+    if (lane < topk) {
+      const uint64_t kk = slot[lane];
+      my_e = 0xFFFFFFFFu - static_cast<uint32_t>(kk);
+      my_v = order_key_to_f32(static_cast<uint32_t>(kk >> 32));
+    }
+    __syncwarp();  // slots read before the scratch is reused
+  } else {
+    sort_desc_lane<V>(k);
+    warp_rounds<V>(k, topk, my_e, my_v);
+  }
   const float m0 = __shfl_sync(FULL, my_v, 0);  // the largest logit
   const float ex = lane < topk ? expf(my_v - m0) : 0.f;
   float zs = ex;
@@ -385,12 +444,14 @@ __device__ __noinline__ static void build_route_map_cta(const int32_t *sidx, int
   int32_t *num_used = pos + P;
   int32_t *used = num_used + 1;
   const int e0 = 2 * tid, e1 = e0 + 1;
-  if (e0 < E) smask[e0] = 0ull;
-  if (e1 < E) smask[e1] = 0ull;
+  unsigned *m32 = reinterpret_cast<unsigned *>(smask);
+  if (e0 < E) m32[2 * e0] = m32[2 * e0 + 1] = 0u;
+  if (e1 < E) m32[2 * e1] = m32[2 * e1 + 1] = 0u;
   __syncthreads();
-  for (int q = tid; q < P; q += blockDim.x) atomicOr(&smask[sidx[q]], 1ull << (q / topk));
+  for (int q = tid; q < P; q += blockDim.x) token_mask_set(m32, sidx[q], q / topk);
   __syncthreads();
-  const int c0 = e0 < E ? __popcll(smask[e0]) : 0, c1 = e1 < E ? __popcll(smask[e1]) : 0;
+  const int c0 = e0 < E ? __popcll(token_mask(m32, e0)) : 0;
+  const int c1 = e1 < E ? __popcll(token_mask(m32, e1)) : 0;
   const int c = c0 + c1, u = (c0 > 0) + (c1 > 0);
   int ic = c, iu = u;  // inclusive scans within the warp
 #pragma unroll
@@ -433,7 +494,7 @@ __device__ __noinline__ static void build_route_map_cta(const int32_t *sidx, int
   for (int q = tid; q < P; q += blockDim.x) {
     const int e = sidx[q];
     const int b = q / topk;
-    const int at = soff[e] + __popcll(smask[e] & ((1ull << b) - 1ull));
+    const int at = soff[e] + __popcll(token_mask(m32, e) & ((1ull << b) - 1ull));
     pairs[at] = q;
     pos[q] = at;
   }

@@ -124,11 +124,13 @@ def test_moe_front_cluster_route_map_equals_counter_path(env, monkeypatch, B):
                                        (17, 40, 24, 256, 4), (40, 100, 20, 512, 8),
                                        (64, 384, 512, 512, 8), (3, 40, 24, 256, 4)])
 def test_moe_front_one_launch_and_two_launch_paths(env, monkeypatch, B, E, L, K, k):
-    """The one-launch front end (clusters reduce the split-K partials on chip, per-tile
-    top-k candidates merged by the last router CTA) and the two-launch path both match
-    the oracle: the same top-k ids and route map bit for bit, latent and weights within
-    tolerance. The one-launch path repeated on the same workspace gives the same bits
-    (fixed reduction order; its arrival counter is back at zero after each call)."""
+    """The one-launch front end (clusters reduce the split-K partials on chip, arrival
+    counters elect the routing CTAs) and the two-launch path both match the oracle: the
+    same top-k ids and route map bit for bit, latent and weights within tolerance. The
+    one-launch path repeated on the same workspace gives the same bits (fixed reduction
+    order; its arrival counters are back at zero after each call). Without the full
+    softmax the one-launch path routes by candidate filtering and ranking instead of k
+    warp rounds: the same ids, weights and route map, bit for bit."""
     torch, ssd, oracle, dev = env
     from split_switched_decode_gb300 import inputs
     X = inputs.activations(B, K, dev, 13, "pfx")
@@ -141,6 +143,10 @@ def test_moe_front_one_launch_and_two_launch_paths(env, monkeypatch, B, E, L, K,
     for x, y, name in zip(a, b, ["latent", "idx", "w", "probs", "route map"]):
         if x is not None:
             assert torch.equal(x, y), f"one-launch {name} not repeatable"
+    f = _run_front(env, X, Wc, E, L, k, probs=False)
+    for i, name in [(0, "latent"), (1, "idx"), (2, "w"), (4, "route map")]:
+        if a[i] is not None:
+            assert torch.equal(a[i], f[i]), f"filtered routing: {name} differs"
     monkeypatch.setenv("DEC_FRONT_FUSED", "0")
     _check_front(env, X, Wc, E, L, k, f"two-launch front B={B} E={E} L={L} K={K} k={k}")
     assert ssd.dec_last_variant() == ssd.VARIANT_SPLITK_TC
@@ -182,6 +188,88 @@ def test_moe_front_one_launch_chained_calls_are_deterministic(env, monkeypatch, 
     ref = oracle.moe_front(inputs.bits(X), inputs.bits(Wc), E, L, k)
     assert np.array_equal(outs[0][1].cpu().numpy(), ref["idx"])
     assert_close(outs[0][2].cpu().numpy(), ref["w"], f"chained B={B} weights")
+
+
+@pytest.mark.parametrize("B", [1, 4, 5, 8, 9, 17, 64])
+def test_moe_front_single_and_grouped_routing_agree(env, monkeypatch, B):
+    """The one-launch front end routes up to DEC_FRONT_SINGLE_B tokens in one CTA (a warp
+    per token, several tokens per warp beyond 8) and larger batches per token group with a
+    second counter electing the route-map builder. Forcing either way for every batch
+    gives bit-identical outputs, with and without the full softmax, matching the oracle."""
+    torch, ssd, oracle, dev = env
+    from split_switched_decode_gb300 import inputs
+    monkeypatch.setenv("DEC_FRONT_FUSED", "1")
+    E, L, K, k = 384, 512, 7168, 8
+    X = inputs.activations(B, K, dev, 15, "sgx")
+    Wc = inputs.weight(E + L, K, dev, 15, "sgw")
+    ref = oracle.moe_front(inputs.bits(X), inputs.bits(Wc), E, L, k)
+    m = oracle.route_map(ref["idx"], E)
+    outs = {}
+    for single in ["0", "8", "64"]:
+        monkeypatch.setenv("DEC_FRONT_SINGLE_B", single)
+        for probs in (False, True):
+            outs[(single, probs)] = _run_front(env, X, Wc, E, L, k, probs=probs)
+            assert ssd.dec_last_variant() == ssd.VARIANT_FRONT_ONE_LAUNCH
+    assert ssd.dec_sync_status() == ssd.DEC_OK
+    a = outs[("8", False)]
+    assert np.array_equal(a[1].cpu().numpy(), ref["idx"])
+    assert_close(a[2].cpu().numpy(), ref["w"], f"B={B} weights")
+    P = B * k
+    r = a[4].cpu().numpy()
+    assert np.array_equal(r[:2 * E + 1 + 2 * P + 1],
+                          np.concatenate([m["counts"], m["offsets"], m["pairs"], m["pos"],
+                                          [m["num_used"]]]))
+    for key, o in outs.items():
+        for i, name in [(0, "latent"), (1, "idx"), (2, "w"), (4, "route map")]:
+            assert torch.equal(a[i], o[i]), f"single_b={key[0]} probs={key[1]}: {name}"
+
+
+def test_moe_front_filtered_routing_ties_and_many_candidates(env, monkeypatch):
+    """Routing without the full softmax (candidates above a lower bound, exact ranks):
+    (a) 32 copies of each of 4 router rows: the 32 copies of the largest logit are the
+    candidates, the 8 lowest experts among them win, equal weights 1/8; (b) all router
+    rows zero: 128 equal logits, more candidates than the ranking keeps, so the warp
+    falls back to k rounds: experts 0..7, weights 1/8; (c) planted duplicate rows as in
+    the softmax-path tie test. Every case matches the oracle bit for bit on the ids."""
+    torch, ssd, oracle, dev = env
+    from split_switched_decode_gb300 import inputs
+    monkeypatch.setenv("DEC_FRONT_FUSED", "1")
+    B, E, L, K, k = 16, 128, 16, 512, 8
+    X = inputs.activations(B, K, dev, 16, "ftx")
+    Wc = inputs.weight(E + L, K, dev, 16, "ftw")
+    base = [inputs.randn_bf16((K,), 0.5, dev, 16, f"fb{i}") for i in range(4)]
+    Wa = Wc.clone()
+    for r in range(E):  # one 128-row tile: copies accumulate in the same order
+        Wa[r] = base[r % 4]
+    for name, W in [("copies", Wa), ("zeros", None), ("pairs", None)]:
+        if name == "zeros":
+            W = Wc.clone()
+            W[:E] = 0
+        elif name == "pairs":
+            W = Wc.clone()
+            big = inputs.randn_bf16((K,), 0.5, dev, 16, "fbig")
+            W[9] = big
+            W[40] = big
+            W[20] = -big
+            W[33] = -big
+        lat, idx, w, pr, rm = _run_front(env, X, W, E, L, k, probs=False)
+        assert ssd.dec_last_variant() == ssd.VARIANT_FRONT_ONE_LAUNCH
+        ref = oracle.moe_front(inputs.bits(X), inputs.bits(W), E, L, k)
+        assert np.array_equal(idx.cpu().numpy(), ref["idx"]), name
+        assert_close(w.cpu().numpy(), ref["w"], f"{name} weights")
+        if name == "zeros":
+            assert np.array_equal(idx.cpu().numpy(), np.tile(np.arange(k), (B, 1)))
+            assert torch.all(w == 1.0 / k)
+        if name == "copies":
+            # the winning row group: 8 lowest of its 16 copies, equal weights
+            for b in range(B):
+                g = int(ref["idx"][b, 0]) % 4
+                assert idx[b].tolist() == [g + 4 * i for i in range(k)], idx[b].tolist()
+                assert torch.all(w[b] == 1.0 / k)
+        m = oracle.route_map(ref["idx"], E)
+        r = rm.cpu().numpy()
+        assert np.array_equal(r[:E], m["counts"]) and np.array_equal(r[E:2 * E + 1], m["offsets"])
+    assert ssd.dec_sync_status() == ssd.DEC_OK
 
 
 def test_moe_front_ties_go_to_lower_index(env):
