@@ -80,6 +80,8 @@ def parse_args():
                          "moe_front + moe_experts")
     ap.add_argument("--prefetch", action="store_true",
                     help="step: L2 prefetch of the shared expert's weights during the front end")
+    ap.add_argument("--row-major", action="store_true",
+                    help="projection weights row-major [N,K] instead of tile-packed")
     return ap.parse_args()
 
 
@@ -170,8 +172,13 @@ class ClockSampler:
 class Workload:
     """All tensors of the step on one GPU, plus the per-call launch counts."""
 
-    def __init__(self, torch, ssd, inputs, dev, batches, seed=0, num_experts=E, experts=True):
+    def __init__(self, torch, ssd, inputs, dev, batches, seed=0, num_experts=E, experts=True,
+                 packed=True):
         self.torch, self.ssd, self.dev, self.batches = torch, ssd, dev, batches
+        # projection weights tile-packed once here, at load time (dec_pack_weight), and
+        # read by the packed projections; row-major [N,K] with packed=False
+        self.packed = packed
+        self.lin = ssd.dec_linear_packed if packed else ssd.dec_linear
         self.E = num_experts
         l2 = torch.cuda.get_device_properties(dev).L2_cache_size
         self.l2 = l2
@@ -183,6 +190,8 @@ class Workload:
         def pool(w):
             n = max(1, math.ceil(3 * l2 / (w.numel() * 2)))
             return [w] + [w.clone() for _ in range(n - 1)]
+        if packed:
+            W_in, W_o = ssd.dec_pack_weight(W_in), ssd.dec_pack_weight(W_o)
         self.W_in, self.W_o, self.W_cat = pool(W_in), pool(W_o), pool(W_cat)
         if experts:
             self.Wgu, self.Wd = inputs.expert_bank(num_experts, H, I, dev, seed, "bank")
@@ -221,12 +230,12 @@ class Workload:
     # -- operations (each adds the kernels it launches to self.launches) --
     def op_in(self, B, rot=0):
         d = self.t[B]
-        self.ssd.dec_linear(d["x_in"], self.W_in[rot % len(self.W_in)], None, d["y_in"], d["ws_in"])
+        self.lin(d["x_in"], self.W_in[rot % len(self.W_in)], None, d["y_in"], d["ws_in"])
         self.launches += 1
 
     def op_o(self, B, rot=0):
         d = self.t[B]
-        self.ssd.dec_linear(d["x_o"], self.W_o[rot % len(self.W_o)], d["r_o"], d["y_o"], d["ws_o"])
+        self.lin(d["x_o"], self.W_o[rot % len(self.W_o)], d["r_o"], d["y_o"], d["ws_o"])
         self.launches += 1
 
     def op_front(self, B, rot=0, v=0, prefetch=True, with_map=True):
@@ -347,7 +356,7 @@ def prefetch_scenario(torch, ssd, wl, batches, reps):
             if mode == "prefetch":
                 main.wait_event(wl.join)
             if mode != "wait":
-                ssd.dec_linear(d["x_o"], W, d["r_o"], d["y_o"], d["ws_o"])
+                wl.lin(d["x_o"], W, d["r_o"], d["y_o"], d["ws_o"])
 
     for B in batches:
         t = {}
@@ -384,7 +393,7 @@ def spec_sweep(torch, ssd, inputs, wl, dev, reps):
             Rr = inputs.residual(M, N, dev, 0, "spec_r") if res else None
             Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
             ws = ssd.workspace(ssd.dec_linear_workspace_bytes(M, N, K), dev)
-            g = capture(torch, lambda: [ssd.dec_linear(X, pool[r % len(pool)], Rr, Y, ws)
+            g = capture(torch, lambda: [wl.lin(X, pool[r % len(pool)], Rr, Y, ws)
                                         for r in range(R)])
             us = statistics.median(time_graph(torch, g, reps)) / R
             del g
@@ -398,19 +407,22 @@ def spec_sweep(torch, ssd, inputs, wl, dev, reps):
 
 # --------------------------------------------------------- single skinny GEMM ----
 
-def skinny_sweep(torch, ssd, inputs, dev, l2, reps):
+def skinny_sweep(torch, ssd, inputs, dev, l2, reps, packed=False):
     """The single skinny GEMM Y = X . W^T at B = 1, K = 1024, N = 2048 through the batch
     switch (the tiny-matrix kernel: "Part 1 / 1. Tune shapes for the workload", small
     matrices at batch 1-2). Its 4.2 MB of weights fit in L2, so the graph makes one call
     per copy of a pool >= 3x L2: every copy is read again only after the whole pool."""
     B = 1
     W0 = inputs.weight(N_SK, K_SK, dev, 0, "w_skinny")
+    if packed:
+        W0 = ssd.dec_pack_weight(W0)
+    lin = ssd.dec_linear_packed if packed else ssd.dec_linear
     n = max(2, math.ceil(3 * l2 / (W0.numel() * 2)))
     pool = [W0] + [W0.clone() for _ in range(n - 1)]
     X = inputs.activations(B, K_SK, dev, 0, "x_skinny")
     Y = torch.empty(B, N_SK, dtype=torch.bfloat16, device=dev)
     ws = ssd.workspace(ssd.dec_linear_workspace_bytes(B, N_SK, K_SK), dev)
-    g = capture(torch, lambda: [ssd.dec_linear(X, w, None, Y, ws) for w in pool])
+    g = capture(torch, lambda: [lin(X, w, None, Y, ws) for w in pool])
     us = statistics.median(time_graph(torch, g, reps)) / len(pool)
     del g
     nb = bytes_linear(B, N_SK, K_SK, False)
@@ -589,7 +601,7 @@ def main():
     if not args.sweep_only:
         ops = {"in", "o", "front", "experts", "pfscen", "spec", "skinny"}
     wl = Workload(torch, ssd, inputs, dev, batches, num_experts=args.num_experts,
-                  experts="experts" in ops)
+                  experts="experts" in ops, packed=not args.row_major)
     # Measured (graphs of 3 layers, B = 1/4/16/64): front end + experts as separate calls
     # 147.0 / 441.3 / 1437.7 / 3615.5 us; with the L2 prefetch of the shared expert's
     # weights during the front end 152.1 / 443.1 / 1440.6 / 3623.9; as moe_layer 149.2 /
@@ -641,7 +653,8 @@ def main():
     torch.cuda.synchronize()
     skinny = None
     if "skinny" in ops and not args.step_only:
-        skinny = skinny_sweep(torch, ssd, inputs, dev, wl.l2, args.reps)
+        # config 1 is the tiny kernel's own case: its row-major weights as given
+        skinny = skinny_sweep(torch, ssd, inputs, dev, wl.l2, args.reps, packed=False)
     spec = None
     if "spec" in ops and not args.step_only:
         spec = spec_sweep(torch, ssd, inputs, wl, dev, args.reps)
@@ -780,6 +793,9 @@ def main():
                                         else "moe_front + moe_experts"),
                            "l2_prefetch_in_step": wl.prefetch and not wl.layer,
                            "parallelism": f"replicas x{world}",
+                           "projection_weights": ("row-major [N,K]" if not wl.packed else
+                                                  "tile-packed once at load (dec_pack_weight): "
+                                                  "16 KB blocks of 128 rows x 64 k"),
                            **compact_table(sweep, skinny, batches)},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": per_step_launches * args.steps, "clocks": clocks,

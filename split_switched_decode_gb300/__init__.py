@@ -39,6 +39,7 @@ EXPORTS = [
     "moe_front_workspace_bytes", "moe_front", "moe_experts_workspace_bytes", "moe_experts",
     "moe_layer_workspace_bytes", "moe_layer",
     "l2_prefetch", "dec_sim_comm_wait", "dec_splitk_gemm_noalloc",
+    "dec_pack_weight", "dec_gemv_packed", "dec_splitk_gemm_packed", "dec_linear_packed",
 ]
 
 _lib = None
@@ -82,6 +83,10 @@ def _load():
         "dec_splitk_gemm": (I, [P, P, P, P, I, I, I, I, I, P, S, P]),
         "dec_linear_workspace_bytes": (S, [I, I, I]),
         "dec_linear": (I, [P, P, P, P, I, I, I, P, S, P]),
+        "dec_pack_weight": (I, [P, I, I, P, P]),
+        "dec_gemv_packed": (I, [P, P, P, P, I, I, I, P]),
+        "dec_splitk_gemm_packed": (I, [P, P, P, P, I, I, I, I, I, P, S, P]),
+        "dec_linear_packed": (I, [P, P, P, P, I, I, I, P, S, P]),
         "moe_route_map_ints": (S, [I, I, I]),
         "moe_front_workspace_bytes": (S, [I, I, I, I]),
         "moe_front": (I, [P, P, I, I, I, I, I, P, P, P, P, P, P, S, P]),
@@ -216,6 +221,49 @@ def dec_linear(X, W, R, Y, ws, stream=None):
     nb = 0 if ws is None else ws.numel() * ws.element_size()
     _check(_load().dec_linear(_ptr(X), _ptr(W), _ptr(R), _ptr(Y), B, N, K, _ptr(ws), nb,
                               _stream(stream)), "dec_linear")
+
+
+def dec_pack_weight(W, Wp=None, stream=None):
+    """The tile-packed copy of a row-major W [N,K] (N % 128 == 0, K % 64 == 0): a tensor
+    of the same shape and dtype whose storage is 16 KB blocks of 128 rows x 64 k. Pass it
+    to the *_packed projections only."""
+    import torch
+    _bf16(W, "W")
+    N, K = W.shape
+    if Wp is None:
+        Wp = torch.empty_like(W)
+    _bf16(Wp, "Wp")
+    _check(_load().dec_pack_weight(_ptr(W), N, K, _ptr(Wp), _stream(stream)), "dec_pack_weight")
+    return Wp
+
+
+def dec_gemv_packed(X, Wp, R, Y, stream=None):
+    for t, n in ((X, "X"), (Wp, "Wp"), (R, "R"), (Y, "Y")):
+        _bf16(t, n)
+    B, K = X.shape
+    N = Wp.shape[0]
+    _check(_load().dec_gemv_packed(_ptr(X), _ptr(Wp), _ptr(R), _ptr(Y), B, N, K,
+                                   _stream(stream)), "dec_gemv_packed")
+
+
+def dec_splitk_gemm_packed(X, Wp, R, Y, ws, split_k=0, use_tc=0, stream=None):
+    for t, n in ((X, "X"), (Wp, "Wp"), (R, "R"), (Y, "Y")):
+        _bf16(t, n)
+    B, K = X.shape
+    N = Wp.shape[0]
+    _check(_load().dec_splitk_gemm_packed(_ptr(X), _ptr(Wp), _ptr(R), _ptr(Y), B, N, K, split_k,
+                                          use_tc, _ptr(ws), ws.numel() * ws.element_size(),
+                                          _stream(stream)), "dec_splitk_gemm_packed")
+
+
+def dec_linear_packed(X, Wp, R, Y, ws, stream=None):
+    for t, n in ((X, "X"), (Wp, "Wp"), (R, "R"), (Y, "Y")):
+        _bf16(t, n)
+    B, K = X.shape
+    N = Wp.shape[0]
+    nb = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(_load().dec_linear_packed(_ptr(X), _ptr(Wp), _ptr(R), _ptr(Y), B, N, K, _ptr(ws), nb,
+                                     _stream(stream)), "dec_linear_packed")
 
 
 # ---------------------------------------------------------------------- MoE ----

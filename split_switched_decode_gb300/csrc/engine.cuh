@@ -100,10 +100,15 @@ __device__ __forceinline__ uint32_t stage_tx_bytes(const EngineParams &p, const 
 }
 
 // Weight boxes of one k-block: one 128-row box, or the 64 gate rows and the 64 matching
-// up rows (two boxes) in gate/up mode.
+// up rows (two boxes) in gate/up mode. A tile-packed W is mapped as rows of 128 bytes
+// (64 k): the box of tile t, k-block kb is the contiguous 16 KB block t*KB + kb.
 __device__ __forceinline__ void load_weights(const EngineParams &p, const SegInfo &s,
                                              const CUtensorMap *wmap, uint8_t *dst,
                                              uint64_t *bar, int kb, uint64_t pol) {
+  if (p.packed) {
+    tma_load_2d_hint(dst, wmap, bar, 0, ((s.wrow0 >> 7) * p.KB + kb) * TILE_N, pol);
+    return;
+  }
   tma_load_2d_hint(dst, wmap, bar, kb * TILE_K, s.wrow0, pol);
   if (p.wbox_rows == 64)
     tma_load_2d_hint(dst + 8192, wmap, bar, kb * TILE_K, s.wrow1, pol);

@@ -18,6 +18,11 @@
 // dependent launch the first weight loads are issued before griddepcontrol.wait and
 // every activation load after it (asm volatile loads with a memory clobber, so the
 // compiler cannot hoist them above the wait).
+//
+// A tile-packed W (dec_pack_weight: 16 KB blocks of 128 rows x 64 k, block (n/128, k/64)
+// at index (n/128)*(K/64) + k/64, rows of 128 bytes inside) has its own kernel below: a
+// warp's load covers 4 adjacent rows x 128 bytes of one block (512 contiguous bytes)
+// instead of 512 bytes along one row.
 #include "common.cuh"
 #include "internal.h"
 
@@ -141,6 +146,102 @@ __global__ void __launch_bounds__(TINY_THREADS, 2)
   }
 }
 
+// Tile-packed W. The CTA owns whole quads of rows (4 consecutive rows, never across a
+// 128-row tile); lane l handles row 4q + l/8 of a quad and the 16-byte chunk l%8 of a
+// 64-wide k-block, so one load instruction of a warp reads 4 rows x 128 bytes, contiguous
+// in the packed block. Warp (piece, slot) covers k-blocks [KB*piece/P, KB*(piece+1)/P)
+// of RG quads per iteration, quads slot, slot + S, ... interleaved over the S slots as
+// the row-major kernel interleaves rows (RG x JU = 16 loads in flight per lane); the
+// eight lanes of a row are added with three shuffles, the P pieces in piece order.
+template <int NB>
+__global__ void __launch_bounds__(TINY_THREADS, 2)
+    gemv_tiny_packed_kernel(const uint16_t *X, const uint16_t *__restrict__ W, const uint16_t *R,
+                            uint16_t *Y, int N, int K, int P, int early_trigger) {
+  extern __shared__ float red[];  // [rows of this CTA][P][NB]
+  const int KB = K >> 6;
+  const int Q = N >> 2;  // quads
+  const int G = gridDim.x;
+  const int q0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * Q / G);
+  const int q1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * Q / G);
+  const int nq = q1 - q0, r0 = 4 * q0, nrows = 4 * nq;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r4 = lane >> 3, c8 = lane & 7;
+  const int S = TINY_WARPS / P;
+  const int piece = warp % P, slot = warp / P;
+  const int kbb = static_cast<int>(static_cast<int64_t>(piece) * KB / P);
+  const int kbe = static_cast<int>(static_cast<int64_t>(piece + 1) * KB / P);
+  const uint8_t *Wb = reinterpret_cast<const uint8_t *>(W);
+  const uint8_t *Xb = reinterpret_cast<const uint8_t *>(X);
+  const size_t row_bytes = static_cast<size_t>(K) * 2;
+  bool waited = false;
+
+  for (int qq = slot; qq < nq; qq += S * TINY_RG) {
+    float acc[TINY_RG][NB];
+#pragma unroll
+    for (int g = 0; g < TINY_RG; ++g)
+#pragma unroll
+      for (int b = 0; b < NB; ++b) acc[g][b] = 0.f;
+
+    for (int kb = kbb; kb < kbe; kb += TINY_JU) {
+      uint4 wv[TINY_RG][TINY_JU];
+#pragma unroll
+      for (int g = 0; g < TINY_RG; ++g) {
+        const int n = r0 + 4 * (qq + g * S) + r4;  // global row
+#pragma unroll
+        for (int u = 0; u < TINY_JU; ++u) {
+          if (kb + u < kbe && qq + g * S < nq) {
+            const size_t blk = static_cast<size_t>(n >> 7) * KB + static_cast<size_t>(kb + u);
+            wv[g][u] = ld_weight_stream(Wb + ((blk << 7) + static_cast<size_t>(n & 127)) * 128 +
+                                        static_cast<size_t>(c8) * 16);
+          } else {
+            wv[g][u] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+      }
+      if (!waited) {  // activations are written by the previous kernel of the stream
+        griddep_wait();
+        waited = true;
+        if (early_trigger) griddep_launch_dependents();
+      }
+#pragma unroll
+      for (int u = 0; u < TINY_JU; ++u) {
+        if (kb + u < kbe) {
+#pragma unroll
+          for (int b = 0; b < NB; ++b) {
+            const uint4 xv = ld_act_v4(Xb + static_cast<size_t>(b) * row_bytes +
+                                       static_cast<size_t>((kb + u) * 8 + c8) * 16);
+#pragma unroll
+            for (int g = 0; g < TINY_RG; ++g) acc[g][b] = dot8(wv[g][u], xv, acc[g][b]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < TINY_RG; ++g) {
+      const int row = 4 * (qq + g * S) + r4;  // local row
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        float v = acc[g][b];
+        v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+        v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+        v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
+        if (c8 == 0 && qq + g * S < nq) red[(row * P + piece) * NB + b] = v;
+      }
+    }
+  }
+  griddep_launch_dependents();
+  griddep_wait();
+  __syncthreads();
+  for (int i = threadIdx.x; i < nrows * NB; i += TINY_THREADS) {
+    const int row = i / NB, b = i - row * NB;
+    float s = 0.f;
+    for (int pc = 0; pc < P; ++pc) s += red[(row * P + pc) * NB + b];
+    const int n = r0 + row;
+    if (R != nullptr) s += bf16_to_f32(R[static_cast<size_t>(b) * N + n]);
+    Y[static_cast<size_t>(b) * N + n] = f32_to_bf16_rn(s);
+  }
+}
+
 int tiny_pieces(int K) {
   const int C = K / 8;
   int P = 1;
@@ -167,28 +268,32 @@ int gemv_tiny_grid(int N, int K, int num_sms) {
   return g;
 }
 
+template <int NB>
+cudaError_t launch_tiny_nb(const uint16_t *X, const uint16_t *W, const uint16_t *R, uint16_t *Y,
+                           int N, int K, int G, int P, int early, size_t smem, bool packed,
+                           cudaStream_t s) {
+  return packed ? launch_pdl(gemv_tiny_packed_kernel<NB>, dim3(G), dim3(TINY_THREADS), smem, s, X,
+                             W, R, Y, N, K, P, early)
+                : launch_pdl(gemv_tiny_kernel<NB>, dim3(G), dim3(TINY_THREADS), smem, s, X, W, R,
+                             Y, N, K, P, early);
+}
+
 cudaError_t launch_gemv_tiny(const uint16_t *X, const uint16_t *W, const uint16_t *R,
-                             uint16_t *Y, int B, int N, int K, int num_sms, cudaStream_t s) {
-  const int G = gemv_tiny_grid(N, K, num_sms);
+                             uint16_t *Y, int B, int N, int K, int num_sms, cudaStream_t s,
+                             bool packed) {
+  int G = gemv_tiny_grid(N, K, num_sms);
+  if (packed && G > N / 4) G = N / 4;  // whole quads of rows per CTA
   const int P = tiny_pieces(K);
   const int early = tiny_small(N, K) ? 1 : 0;
-  const int rows = (N + G - 1) / G;
+  // rows of the largest CTA: whole quads when packed
+  const int rows = packed ? 4 * ((N / 4 + G - 1) / G) : (N + G - 1) / G;
   const size_t smem = static_cast<size_t>(rows) * P * B * sizeof(float);
   switch (B) {
-    case 1:
-      return launch_pdl(gemv_tiny_kernel<1>, dim3(G), dim3(TINY_THREADS), smem, s, X, W, R, Y, N,
-                        K, P, early);
-    case 2:
-      return launch_pdl(gemv_tiny_kernel<2>, dim3(G), dim3(TINY_THREADS), smem, s, X, W, R, Y, N,
-                        K, P, early);
-    case 3:
-      return launch_pdl(gemv_tiny_kernel<3>, dim3(G), dim3(TINY_THREADS), smem, s, X, W, R, Y, N,
-                        K, P, early);
-    case 4:
-      return launch_pdl(gemv_tiny_kernel<4>, dim3(G), dim3(TINY_THREADS), smem, s, X, W, R, Y, N,
-                        K, P, early);
-    default:
-      return cudaErrorInvalidValue;
+    case 1: return launch_tiny_nb<1>(X, W, R, Y, N, K, G, P, early, smem, packed, s);
+    case 2: return launch_tiny_nb<2>(X, W, R, Y, N, K, G, P, early, smem, packed, s);
+    case 3: return launch_tiny_nb<3>(X, W, R, Y, N, K, G, P, early, smem, packed, s);
+    case 4: return launch_tiny_nb<4>(X, W, R, Y, N, K, G, P, early, smem, packed, s);
+    default: return cudaErrorInvalidValue;
   }
 }
 

@@ -25,6 +25,7 @@ struct EngineParams {
   int slot_cols;     // columns per partial slot (slot = 128 * slot_cols floats)
   int defer;         // 1: store every segment's partial tile and stop (MODE_FRONT)
   int vec_y;         // LINEAR: N % 8 == 0 and Y (and R) 16-byte aligned: 16-byte stores
+  int packed;        // LINEAR: W tile-packed (block (t, kb) = 128 rows x 64 k, contiguous)
   int pair;          // LINEAR, tensor cores: 2-CTA clusters, CTA pair (2t, 2t+1) holds the two
                      // k-halves of tile t and adds them through distributed shared memory
   int ngrp;          // LINEAR, tensor cores: groups of 64 batch columns sharing each weight
@@ -119,8 +120,13 @@ cudaError_t launch_engine_tc(int maxc, const CUtensorMap &wmap, const CUtensorMa
 // ------------------------------------------------------------- gemv_tiny.cu --
 constexpr int TINY_MAX_NB = 4;  // batch rows of the tiny kernel (1..4)
 int gemv_tiny_grid(int N, int K, int num_sms);
+// packed: W in the tile-packed layout of dec_pack_weight instead of row-major [N,K].
 cudaError_t launch_gemv_tiny(const uint16_t *X, const uint16_t *W, const uint16_t *R,
-                             uint16_t *Y, int B, int N, int K, int num_sms, cudaStream_t s);
+                             uint16_t *Y, int B, int N, int K, int num_sms, cudaStream_t s,
+                             bool packed = false);
+// Row-major W [N,K] -> tile-packed Wp (N % 128 == 0, K % 64 == 0): 16 KB blocks of 128
+// rows x 64 k, block (n/128, k/64) at index (n/128)*(K/64) + k/64 (moe_aux.cu).
+cudaError_t launch_pack_weight(const uint16_t *W, int N, int K, uint16_t *Wp, cudaStream_t s);
 
 // --------------------------------------------------------------- moe_aux.cu --
 // Second half of the front end: adds the product's partial tiles in worker order,

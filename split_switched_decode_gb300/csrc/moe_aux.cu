@@ -1,5 +1,6 @@
 // moe_aux.cu -- small kernels around the grouped expert GEMV, the L2 prefetch kernel,
-// the simulated communication phase and the bounded-wait self-test.
+// the weight packing kernel, the simulated communication phase and the bounded-wait
+// self-test.
 #include "common.cuh"
 #include "internal.h"
 #include "routing.cuh"
@@ -364,7 +365,33 @@ __global__ void comm_wait_kernel(uint64_t ns) {
   while (globaltimer_ns() - t0 < ns) __nanosleep(256);
 }
 
+// Row-major W [N,K] -> tile-packed Wp: 16 KB blocks of 128 rows x 64 k (rows of 128
+// bytes), block (n/128, k/64) at index (n/128)*KB + k/64, KB = K/64. One thread per
+// 16-byte chunk of Wp (stores coalesced; eight threads read one 128-byte row piece).
+// A plain copy: run once when the weights are loaded, not in the decode step.
+__global__ void __launch_bounds__(256) pack_weight_kernel(const uint4 *W, uint4 *Wp, int K,
+                                                          long long chunks) {
+  const int KB = K >> 6;
+  const long long row_chunks = K >> 3;
+  for (long long i = blockIdx.x * 256ll + threadIdx.x; i < chunks;
+       i += static_cast<long long>(gridDim.x) * 256) {
+    const long long block = i >> 10;          // 1024 chunks of 16 bytes per block
+    const int r = static_cast<int>((i >> 3) & 127), c = static_cast<int>(i & 7);
+    const long long t = block / KB, kb = block - t * KB;
+    Wp[i] = __ldg(W + (t * 128 + r) * row_chunks + kb * 8 + c);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_pack_weight(const uint16_t *W, int N, int K, uint16_t *Wp, cudaStream_t s) {
+  const long long chunks = static_cast<long long>(N) * K / 8;
+  long long blocks = (chunks + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  pack_weight_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+      reinterpret_cast<const uint4 *>(W), reinterpret_cast<uint4 *>(Wp), K, chunks);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_comm_wait(uint64_t ns, cudaStream_t s) {
   comm_wait_kernel<<<1, 32, 0, s>>>(ns);

@@ -98,4 +98,18 @@ def test_host_argument_checks_need_no_device(ssd):
     bad[0], bad[12] = A, N0  # latent missing with L > 0
     assert lib.moe_layer(*bad) == ssd.DEC_ERR_INVALID_ARG
     assert lib.dec_sim_comm_wait(1000000001, s) == ssd.DEC_ERR_INVALID_ARG
+    # tile-packed weights: whole 128-row tiles and 64-wide k-blocks only
+    assert lib.dec_pack_weight(A, 256, 128, A, s) == ssd.DEC_ERR_INVALID_ARG  # W and Wp overlap
+    assert lib.dec_pack_weight(A, 200, 128, ctypes.c_void_p(0x100000), s) == \
+        ssd.DEC_ERR_UNSUPPORTED_SHAPE
+    assert lib.dec_pack_weight(A, 256, 96, ctypes.c_void_p(0x100000), s) == \
+        ssd.DEC_ERR_UNSUPPORTED_SHAPE
+    assert lib.dec_pack_weight(U, 256, 128, ctypes.c_void_p(0x100000), s) == ssd.DEC_ERR_MISALIGNED
+    assert lib.dec_pack_weight(N0, 256, 128, A, s) == ssd.DEC_ERR_INVALID_ARG
+    assert lib.dec_gemv_packed(A, A, N0, A, 1, 200, 128, s) == ssd.DEC_ERR_UNSUPPORTED_SHAPE
+    assert lib.dec_gemv_packed(A, A, N0, A, 1, 256, 96, s) == ssd.DEC_ERR_UNSUPPORTED_SHAPE
+    assert lib.dec_splitk_gemm_packed(A, A, N0, A, 4, 8, 64, 0, 1, A, 0, s) == \
+        ssd.DEC_ERR_UNSUPPORTED_SHAPE
+    assert lib.dec_linear_packed(A, A, N0, A, 4, 128, 72, A, 0, s) == ssd.DEC_ERR_UNSUPPORTED_SHAPE
+    assert lib.dec_linear_packed(A, N0, N0, A, 4, 128, 64, A, 0, s) == ssd.DEC_ERR_INVALID_ARG
     assert lib.dec_set_fault_inject(-1) == ssd.DEC_ERR_INVALID_ARG
