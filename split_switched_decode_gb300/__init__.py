@@ -40,6 +40,7 @@ EXPORTS = [
     "moe_layer_workspace_bytes", "moe_layer",
     "l2_prefetch", "dec_sim_comm_wait", "dec_splitk_gemm_noalloc",
     "dec_pack_weight", "dec_gemv_packed", "dec_splitk_gemm_packed", "dec_linear_packed",
+    "dec_pack_expert_weights", "moe_experts_packed", "moe_layer_packed",
 ]
 
 _lib = None
@@ -94,6 +95,10 @@ def _load():
         "moe_experts": (I, [P, P, P, P, P, P, I, P, P, I, I, I, I, P, P, S, P, P, I]),
         "moe_layer_workspace_bytes": (S, [I, I, I, I, I, I]),
         "moe_layer": (I, [P, P, I, I, I, P, P, P, P, I, I, I, P, P, P, P, P, P, S, P, P, I]),
+        "dec_pack_expert_weights": (I, [P, P, I, I, I, P, P, P]),
+        "moe_experts_packed": (I, [P, P, P, P, P, P, I, P, P, I, I, I, I, P, P, S, P, P, I]),
+        "moe_layer_packed": (I, [P, P, I, I, I, P, P, P, P, I, I, I, P, P, P, P, P, P, S, P, P,
+                                 I]),
         "l2_prefetch": (I, [P, S, I, P]),
         "dec_sim_comm_wait": (I, [U64, P]),
         "dec_splitk_gemm_noalloc": (I, [P, P, P, P, I, I, I, I, P]),
@@ -293,7 +298,8 @@ def moe_experts_workspace_bytes(B, E, topk, H, I) -> int:
 
 
 def moe_experts(X, topk_idx, topk_w, route_map, Wgu, Wd, Wgu_shared, Wd_shared, Y, ws,
-                main_stream=None, side_stream=None, side_max_ctas=0):
+                main_stream=None, side_stream=None, side_max_ctas=0, packed=False):
+    """packed: Wgu/Wd (and the shared pair) from dec_pack_expert_weights."""
     for t, n in ((X, "X"), (Wgu, "Wgu"), (Wd, "Wd"), (Wgu_shared, "Wgu_shared"),
                  (Wd_shared, "Wd_shared"), (Y, "Y")):
         _bf16(t, n)
@@ -303,10 +309,24 @@ def moe_experts(X, topk_idx, topk_w, route_map, Wgu, Wd, Wgu_shared, Wd_shared, 
     topk = topk_idx.shape[1]
     ms = _stream(main_stream)
     ss = _stream(side_stream) if side_stream is not None else ms
-    _check(_load().moe_experts(_ptr(X), _ptr(topk_idx), _ptr(topk_w), _ptr(route_map),
-                               _ptr(Wgu), _ptr(Wd), E, _ptr(Wgu_shared), _ptr(Wd_shared), B, H,
-                               I, topk, _ptr(Y), _ptr(ws), ws.numel() * ws.element_size(), ms,
-                               ss, side_max_ctas), "moe_experts")
+    fn = _load().moe_experts_packed if packed else _load().moe_experts
+    _check(fn(_ptr(X), _ptr(topk_idx), _ptr(topk_w), _ptr(route_map), _ptr(Wgu), _ptr(Wd), E,
+              _ptr(Wgu_shared), _ptr(Wd_shared), B, H, I, topk, _ptr(Y), _ptr(ws),
+              ws.numel() * ws.element_size(), ms, ss, side_max_ctas), "moe_experts")
+
+
+def dec_pack_expert_weights(Wgu, Wd, stream=None):
+    """Tile-packed copies of an expert bank: Wgu [E, 2I, H] (gate rows, then up rows) and
+    Wd [E, H, I] -> tensors of the same shapes whose storage is 16 KB blocks (64 gate rows
+    + the 64 matching up rows, resp. 128 down rows, x 64 k). For moe_*(packed=True)."""
+    import torch
+    _bf16(Wgu, "Wgu")
+    _bf16(Wd, "Wd")
+    E, twoI, H = Wgu.shape
+    Wgu_p, Wd_p = torch.empty_like(Wgu), torch.empty_like(Wd)
+    _check(_load().dec_pack_expert_weights(_ptr(Wgu), _ptr(Wd), E, H, twoI // 2, _ptr(Wgu_p),
+                                           _ptr(Wd_p), _stream(stream)), "dec_pack_expert_weights")
+    return Wgu_p, Wd_p
 
 
 def l2_prefetch(t, nbytes=None, max_ctas=0, stream=None):
@@ -326,8 +346,10 @@ def moe_layer_workspace_bytes(B, E, L, H, I, topk) -> int:
 
 
 def moe_layer(X, Wcat, E, L, topk, Wgu, Wd, Wgu_shared, Wd_shared, latent, topk_idx, topk_w,
-              Y, ws, route_map=None, stream=None, side_stream=None, side_max_ctas=0):
-    """moe_front + moe_experts with the shared expert overlapping the routing."""
+              Y, ws, route_map=None, stream=None, side_stream=None, side_max_ctas=0,
+              packed=False):
+    """moe_front + moe_experts with the shared expert overlapping the routing (packed:
+    expert banks from dec_pack_expert_weights)."""
     for t, n in ((X, "X"), (Wcat, "Wcat"), (Wgu, "Wgu"), (Wd, "Wd"), (Wgu_shared, "Wgu_shared"),
                  (Wd_shared, "Wd_shared"), (latent, "latent"), (Y, "Y")):
         _bf16(t, n)
@@ -335,8 +357,8 @@ def moe_layer(X, Wcat, E, L, topk, Wgu, Wd, Wgu_shared, Wd_shared, latent, topk_
     I = Wgu.shape[1] // 2
     main = _stream(stream)
     side = _stream(side_stream) if side_stream is not None else main
-    _check(_load().moe_layer(_ptr(X), _ptr(Wcat), E, L, topk, _ptr(Wgu), _ptr(Wd),
-                             _ptr(Wgu_shared), _ptr(Wd_shared), B, H, I, _ptr(latent),
-                             _ptr(topk_idx), _ptr(topk_w), _ptr(route_map), _ptr(Y), _ptr(ws),
-                             ws.numel() * ws.element_size(), main, side, side_max_ctas),
-           "moe_layer")
+    fn = _load().moe_layer_packed if packed else _load().moe_layer
+    _check(fn(_ptr(X), _ptr(Wcat), E, L, topk, _ptr(Wgu), _ptr(Wd), _ptr(Wgu_shared),
+              _ptr(Wd_shared), B, H, I, _ptr(latent), _ptr(topk_idx), _ptr(topk_w),
+              _ptr(route_map), _ptr(Y), _ptr(ws), ws.numel() * ws.element_size(), main, side,
+              side_max_ctas), "moe_layer")

@@ -984,7 +984,7 @@ dec_status moe_experts_impl(const dec_bf16 *X, const int32_t *topk_idx, const fl
                             int E, const dec_bf16 *Wgu_shared, const dec_bf16 *Wd_shared, int B,
                             int H, int I, int topk, dec_bf16 *Y, void *ws, size_t ws_bytes,
                             dec_stream_t main_stream, dec_stream_t side_stream,
-                            int side_max_ctas, const FrontCall *fc);
+                            int side_max_ctas, const FrontCall *fc, bool packed);
 
 }  // namespace
 
@@ -1006,7 +1006,40 @@ dec_status moe_experts(const dec_bf16 *X, const int32_t *topk_idx, const float *
                        dec_stream_t main_stream, dec_stream_t side_stream, int side_max_ctas) {
   return moe_experts_impl(X, topk_idx, topk_w, route_map, Wgu, Wd, E, Wgu_shared, Wd_shared, B,
                           H, I, topk, Y, ws, ws_bytes, main_stream, side_stream, side_max_ctas,
-                          nullptr);
+                          nullptr, false);
+}
+
+dec_status moe_experts_packed(const dec_bf16 *X, const int32_t *topk_idx, const float *topk_w,
+                              const int32_t *route_map, const dec_bf16 *Wgu_p,
+                              const dec_bf16 *Wd_p, int E, const dec_bf16 *Wgu_shared_p,
+                              const dec_bf16 *Wd_shared_p, int B, int H, int I, int topk,
+                              dec_bf16 *Y, void *ws, size_t ws_bytes, dec_stream_t main_stream,
+                              dec_stream_t side_stream, int side_max_ctas) {
+  return moe_experts_impl(X, topk_idx, topk_w, route_map, Wgu_p, Wd_p, E, Wgu_shared_p,
+                          Wd_shared_p, B, H, I, topk, Y, ws, ws_bytes, main_stream, side_stream,
+                          side_max_ctas, nullptr, true);
+}
+
+dec_status dec_pack_expert_weights(const dec_bf16 *Wgu, const dec_bf16 *Wd, int E, int H, int I,
+                                   dec_bf16 *Wgu_p, dec_bf16 *Wd_p, dec_stream_t s) {
+  if (!Wgu || !Wd || !Wgu_p || !Wd_p || E < 1 || H < 1 || I < 1) return DEC_ERR_INVALID_ARG;
+  if (H % TILE_N != 0 || I % TILE_K != 0 || H % TILE_K != 0) return DEC_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(Wgu) || !aligned16(Wd) || !aligned16(Wgu_p) || !aligned16(Wd_p))
+    return DEC_ERR_MISALIGNED;
+  const size_t n = static_cast<size_t>(E) * H * I;  // elements of Wd; Wgu has 2n
+  if (n > (size_t(1) << 40)) return DEC_ERR_UNSUPPORTED_SHAPE;
+  auto overlap = [](const dec_bf16 *a, size_t na, const dec_bf16 *b, size_t nb) {
+    return a < b + nb && b < a + na;
+  };
+  if (overlap(Wgu, 2 * n, Wgu_p, 2 * n) || overlap(Wd, n, Wd_p, n) ||
+      overlap(Wgu_p, 2 * n, Wd_p, n))
+    return DEC_ERR_INVALID_ARG;
+  cudaError_t ce;
+  if (!device_info(&ce)) return DEC_ERR_CUDA;
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
+  ce = launch_pack_weight(Wgu, E * 2 * I, H, Wgu_p, cs, I);
+  if (ce == cudaSuccess) ce = launch_pack_weight(Wd, E * H, I, Wd_p, cs);
+  return cuda_status(ce);
 }
 
 size_t moe_layer_workspace_bytes(int B, int E, int L, int H, int I, int topk) {
@@ -1015,12 +1048,16 @@ size_t moe_layer_workspace_bytes(int B, int E, int L, int H, int I, int topk) {
   return (e == 0 || f == 0) ? 0 : align_up(e) + f;
 }
 
-dec_status moe_layer(const dec_bf16 *X, const dec_bf16 *Wcat, int E, int L, int topk,
-                     const dec_bf16 *Wgu, const dec_bf16 *Wd, const dec_bf16 *Wgu_shared,
-                     const dec_bf16 *Wd_shared, int B, int H, int I, dec_bf16 *latent,
-                     int32_t *topk_idx, float *topk_w, int32_t *route_map_opt, dec_bf16 *Y,
-                     void *ws, size_t ws_bytes, dec_stream_t main_stream,
-                     dec_stream_t side_stream, int side_max_ctas) {
+}  // extern "C"
+
+namespace {
+
+dec_status moe_layer_impl(const dec_bf16 *X, const dec_bf16 *Wcat, int E, int L, int topk,
+                          const dec_bf16 *Wgu, const dec_bf16 *Wd, const dec_bf16 *Wgu_shared,
+                          const dec_bf16 *Wd_shared, int B, int H, int I, dec_bf16 *latent,
+                          int32_t *topk_idx, float *topk_w, int32_t *route_map_opt, dec_bf16 *Y,
+                          void *ws, size_t ws_bytes, dec_stream_t main_stream,
+                          dec_stream_t side_stream, int side_max_ctas, bool packed) {
   if (!X || !Wcat || !ws) return DEC_ERR_INVALID_ARG;
   if (L < 0 || (L > 0 && !latent)) return DEC_ERR_INVALID_ARG;
   if (!aligned16(Wcat)) return DEC_ERR_MISALIGNED;
@@ -1040,7 +1077,34 @@ dec_status moe_layer(const dec_bf16 *X, const dec_bf16 *Wcat, int E, int L, int 
   fc.ws_bytes = f;
   return moe_experts_impl(X, topk_idx, topk_w, route_map_opt, Wgu, Wd, E, Wgu_shared, Wd_shared,
                           B, H, I, topk, Y, ws, align_up(e), main_stream, side_stream,
-                          side_max_ctas, &fc);
+                          side_max_ctas, &fc, packed);
+}
+
+}  // namespace
+
+extern "C" {
+
+dec_status moe_layer(const dec_bf16 *X, const dec_bf16 *Wcat, int E, int L, int topk,
+                     const dec_bf16 *Wgu, const dec_bf16 *Wd, const dec_bf16 *Wgu_shared,
+                     const dec_bf16 *Wd_shared, int B, int H, int I, dec_bf16 *latent,
+                     int32_t *topk_idx, float *topk_w, int32_t *route_map_opt, dec_bf16 *Y,
+                     void *ws, size_t ws_bytes, dec_stream_t main_stream,
+                     dec_stream_t side_stream, int side_max_ctas) {
+  return moe_layer_impl(X, Wcat, E, L, topk, Wgu, Wd, Wgu_shared, Wd_shared, B, H, I, latent,
+                        topk_idx, topk_w, route_map_opt, Y, ws, ws_bytes, main_stream,
+                        side_stream, side_max_ctas, false);
+}
+
+dec_status moe_layer_packed(const dec_bf16 *X, const dec_bf16 *Wcat, int E, int L, int topk,
+                            const dec_bf16 *Wgu_p, const dec_bf16 *Wd_p,
+                            const dec_bf16 *Wgu_shared_p, const dec_bf16 *Wd_shared_p, int B,
+                            int H, int I, dec_bf16 *latent, int32_t *topk_idx, float *topk_w,
+                            int32_t *route_map_opt, dec_bf16 *Y, void *ws, size_t ws_bytes,
+                            dec_stream_t main_stream, dec_stream_t side_stream,
+                            int side_max_ctas) {
+  return moe_layer_impl(X, Wcat, E, L, topk, Wgu_p, Wd_p, Wgu_shared_p, Wd_shared_p, B, H, I,
+                        latent, topk_idx, topk_w, route_map_opt, Y, ws, ws_bytes, main_stream,
+                        side_stream, side_max_ctas, true);
 }
 
 }  // extern "C"
@@ -1052,7 +1116,7 @@ dec_status moe_experts_impl(const dec_bf16 *X, const int32_t *topk_idx, const fl
                             int E, const dec_bf16 *Wgu_shared, const dec_bf16 *Wd_shared, int B,
                             int H, int I, int topk, dec_bf16 *Y, void *ws, size_t ws_bytes,
                             dec_stream_t main_stream, dec_stream_t side_stream,
-                            int side_max_ctas, const FrontCall *fc) {
+                            int side_max_ctas, const FrontCall *fc, bool packed) {
   if (!X || !topk_idx || !topk_w || !Wgu || !Wd || !Y || !ws) return DEC_ERR_INVALID_ARG;
   if ((Wgu_shared == nullptr) != (Wd_shared == nullptr)) return DEC_ERR_INVALID_ARG;
   if (B < 1 || E < 1 || H < 1 || I < 1 || topk < 1 || side_max_ctas < 0)
@@ -1113,14 +1177,22 @@ dec_status moe_experts_impl(const dec_bf16 *X, const int32_t *topk_idx, const fl
 
   CUtensorMap m_wgu, m_wd, m_xg, m_a;
   // grouped launches keep 16-row activation boxes: most experts have few tokens
-  if (!make_map(&m_wgu, Wgu, H, static_cast<uint64_t>(E) * 2 * I, 64) ||
-      !make_map(&m_wd, Wd, I, static_cast<uint64_t>(E) * H, 128) ||
+  // tile-packed banks are mapped as rows of 64 k (128 bytes): one box = one 16 KB block
+  const uint64_t gu_rows = static_cast<uint64_t>(E) * 2 * I, d_rows = static_cast<uint64_t>(E) * H;
+  if (!(packed ? make_map(&m_wgu, Wgu, TILE_K, gu_rows * (H / TILE_K), 128)
+               : make_map(&m_wgu, Wgu, H, gu_rows, 64)) ||
+      !(packed ? make_map(&m_wd, Wd, TILE_K, d_rows * (I / TILE_K), 128)
+               : make_map(&m_wd, Wd, I, d_rows, 128)) ||
       !make_map(&m_xg, Xg, H, P, XBOX_ROWS) || !make_map(&m_a, A, I, P, XBOX_ROWS))
     return DEC_ERR_CUDA;
   CUtensorMap m_wgus, m_wds, m_x, m_as;
   const int xb_shared = xbox_rows_for(ep.maxc);
-  if (shared && (!make_map(&m_wgus, Wgu_shared, H, 2 * I, 64) ||
-                 !make_map(&m_wds, Wd_shared, I, H, 128) ||
+  if (shared && (!(packed ? make_map(&m_wgus, Wgu_shared, TILE_K,
+                                    static_cast<uint64_t>(2) * I * (H / TILE_K), 128)
+                           : make_map(&m_wgus, Wgu_shared, H, 2 * I, 64)) ||
+                 !(packed ? make_map(&m_wds, Wd_shared, TILE_K,
+                                     static_cast<uint64_t>(H) * (I / TILE_K), 128)
+                          : make_map(&m_wds, Wd_shared, I, H, 128)) ||
                  !make_map(&m_x, X, H, B, xb_shared) || !make_map(&m_as, As, I, B, xb_shared)))
     return DEC_ERR_CUDA;
 
@@ -1137,6 +1209,7 @@ dec_status moe_experts_impl(const dec_bf16 *X, const int32_t *topk_idx, const fl
   auto base = [&](EngineParams &p, int mode, int N, int K, int T, int KB, int G, int grouped,
                   size_t part_off, size_t cnt_off) {
     std::memset(&p, 0, sizeof p);
+    p.packed = packed ? 1 : 0;
     p.mode = mode;
     p.N = N;
     p.K = K;
@@ -1182,7 +1255,7 @@ dec_status moe_experts_impl(const dec_bf16 *X, const int32_t *topk_idx, const fl
     p.w_group_rows = 2 * I;
     p.up_row_off = I;
     p.A = As;
-    p.w_base = reinterpret_cast<const uint8_t *>(Wgu_shared);
+    p.w_base = packed ? nullptr : reinterpret_cast<const uint8_t *>(Wgu_shared);
     p.w_rows = 2LL * I;
     p.l2pf_kb = l2_prefetch_kblocks();
     if ((ce = engine(m_wgus, m_x, p, sst)) != cudaSuccess) return DEC_ERR_CUDA;
@@ -1191,7 +1264,7 @@ dec_status moe_experts_impl(const dec_bf16 *X, const int32_t *topk_idx, const fl
     p.w_group_rows = H;
     p.Yp = S;
     if (fused) set_combine(p);
-    p.w_base = reinterpret_cast<const uint8_t *>(Wd_shared);
+    p.w_base = packed ? nullptr : reinterpret_cast<const uint8_t *>(Wd_shared);
     p.w_rows = H;
     p.l2pf_kb = l2_prefetch_kblocks();
     if ((ce = engine(m_wds, m_as, p, sst)) != cudaSuccess) return DEC_ERR_CUDA;

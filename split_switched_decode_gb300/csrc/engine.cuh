@@ -52,6 +52,7 @@ struct SegInfo {
   int wrow0;   // W row of tile rows 0..63
   int wrow1;   // W row of tile rows 64..127
   bool full;   // the segment covers the whole tile
+  int pblk;    // tile-packed W: block of this tile's k-block 0 ((expert * T + t) * KB)
 };
 
 __device__ __forceinline__ void seg_info(const EngineParams &p, int64_t it, int64_t end,
@@ -64,11 +65,12 @@ __device__ __forceinline__ void seg_info(const EngineParams &p, int64_t it, int6
   const int g = s.gt / p.T;
   s.t = s.gt - g * p.T;
   int wbase;
+  int e = 0;  // expert of a grouped launch
   if (p.grouped) {
     // the route map comes from moe_front or the validating rebuild kernel; the clamps
     // only keep a corrupted map from steering loads or stores out of their buffers
     const int32_t *rm = p.route_map;
-    const int e = min(max(rm[2 * p.E + 2 + 2 * p.P + g], 0), p.E - 1);
+    e = min(max(rm[2 * p.E + 2 + 2 * p.P + g], 0), p.E - 1);
     s.xrow0 = min(max(rm[p.E + e], 0), p.P);
     s.ncols = min(max(rm[e], 0), min(p.slot_cols, p.P - s.xrow0));
     wbase = e * p.w_group_rows;
@@ -85,6 +87,7 @@ __device__ __forceinline__ void seg_info(const EngineParams &p, int64_t it, int6
     s.wrow1 = s.wrow0 + 64;
   }
   s.full = (s.kb0 == 0 && s.kb1 == p.KB);
+  s.pblk = (e * p.T + s.t) * p.KB;
   s.cgrp = 0;
 }
 
@@ -101,12 +104,13 @@ __device__ __forceinline__ uint32_t stage_tx_bytes(const EngineParams &p, const 
 
 // Weight boxes of one k-block: one 128-row box, or the 64 gate rows and the 64 matching
 // up rows (two boxes) in gate/up mode. A tile-packed W is mapped as rows of 128 bytes
-// (64 k): the box of tile t, k-block kb is the contiguous 16 KB block t*KB + kb.
+// (64 k): the box of (expert, tile t, k-block kb) is the contiguous 16 KB block
+// (expert*T + t)*KB + kb, whose rows land where the two gate/up boxes would.
 __device__ __forceinline__ void load_weights(const EngineParams &p, const SegInfo &s,
                                              const CUtensorMap *wmap, uint8_t *dst,
                                              uint64_t *bar, int kb, uint64_t pol) {
   if (p.packed) {
-    tma_load_2d_hint(dst, wmap, bar, 0, ((s.wrow0 >> 7) * p.KB + kb) * TILE_N, pol);
+    tma_load_2d_hint(dst, wmap, bar, 0, (s.pblk + kb) * TILE_N, pol);
     return;
   }
   tma_load_2d_hint(dst, wmap, bar, kb * TILE_K, s.wrow0, pol);

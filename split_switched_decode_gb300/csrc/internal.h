@@ -25,7 +25,9 @@ struct EngineParams {
   int slot_cols;     // columns per partial slot (slot = 128 * slot_cols floats)
   int defer;         // 1: store every segment's partial tile and stop (MODE_FRONT)
   int vec_y;         // LINEAR: N % 8 == 0 and Y (and R) 16-byte aligned: 16-byte stores
-  int packed;        // LINEAR: W tile-packed (block (t, kb) = 128 rows x 64 k, contiguous)
+  int packed;        // W tile-packed: contiguous 16 KB blocks of 128 rows x 64 k, block
+                     // (expert, tile, k-block) at (expert * T + tile) * KB + k-block (gate/up:
+                     // 64 gate rows then the 64 matching up rows)
   int pair;          // LINEAR, tensor cores: 2-CTA clusters, CTA pair (2t, 2t+1) holds the two
                      // k-halves of tile t and adds them through distributed shared memory
   int ngrp;          // LINEAR, tensor cores: groups of 64 batch columns sharing each weight
@@ -126,7 +128,10 @@ cudaError_t launch_gemv_tiny(const uint16_t *X, const uint16_t *W, const uint16_
                              bool packed = false);
 // Row-major W [N,K] -> tile-packed Wp (N % 128 == 0, K % 64 == 0): 16 KB blocks of 128
 // rows x 64 k, block (n/128, k/64) at index (n/128)*(K/64) + k/64 (moe_aux.cu).
-cudaError_t launch_pack_weight(const uint16_t *W, int N, int K, uint16_t *Wp, cudaStream_t s);
+// gateup_I > 0: W is a gate/up bank [E, 2*gateup_I, K]; each block holds 64 gate rows
+// then the 64 matching up rows of one expert (N = E * 2 * gateup_I).
+cudaError_t launch_pack_weight(const uint16_t *W, int N, int K, uint16_t *Wp, cudaStream_t s,
+                               int gateup_I = 0);
 
 // --------------------------------------------------------------- moe_aux.cu --
 // Second half of the front end: adds the product's partial tiles in worker order,

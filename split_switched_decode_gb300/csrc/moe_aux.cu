@@ -366,11 +366,14 @@ __global__ void comm_wait_kernel(uint64_t ns) {
 }
 
 // Row-major W [N,K] -> tile-packed Wp: 16 KB blocks of 128 rows x 64 k (rows of 128
-// bytes), block (n/128, k/64) at index (n/128)*KB + k/64, KB = K/64. One thread per
-// 16-byte chunk of Wp (stores coalesced; eight threads read one 128-byte row piece).
-// A plain copy: run once when the weights are loaded, not in the decode step.
+// bytes), block (n/128, k/64) at index (n/128)*KB + k/64, KB = K/64. For a gate/up bank
+// (gate_I > 0: W = [E, 2 gate_I, K], gate rows then up rows per expert) block row r of
+// block-row t' = e * (gate_I/64) + t is gate row t*64 + r (r < 64) or up row
+// gate_I + t*64 + r - 64 of expert e. One thread per 16-byte chunk of Wp (stores
+// coalesced; eight threads read one 128-byte row piece). A plain copy: run once when the
+// weights are loaded, not in the decode step.
 __global__ void __launch_bounds__(256) pack_weight_kernel(const uint4 *W, uint4 *Wp, int K,
-                                                          long long chunks) {
+                                                          long long chunks, int gate_I) {
   const int KB = K >> 6;
   const long long row_chunks = K >> 3;
   for (long long i = blockIdx.x * 256ll + threadIdx.x; i < chunks;
@@ -378,18 +381,25 @@ __global__ void __launch_bounds__(256) pack_weight_kernel(const uint4 *W, uint4 
     const long long block = i >> 10;          // 1024 chunks of 16 bytes per block
     const int r = static_cast<int>((i >> 3) & 127), c = static_cast<int>(i & 7);
     const long long t = block / KB, kb = block - t * KB;
-    Wp[i] = __ldg(W + (t * 128 + r) * row_chunks + kb * 8 + c);
+    long long row = t * 128 + r;
+    if (gate_I > 0) {
+      const long long tpe = gate_I >> 6;  // 64-row gate tiles per expert
+      const long long e = t / tpe, te = t - e * tpe;
+      row = e * 2 * gate_I + (r < 64 ? te * 64 + r : gate_I + te * 64 + (r - 64));
+    }
+    Wp[i] = __ldg(W + row * row_chunks + kb * 8 + c);
   }
 }
 
 }  // namespace
 
-cudaError_t launch_pack_weight(const uint16_t *W, int N, int K, uint16_t *Wp, cudaStream_t s) {
+cudaError_t launch_pack_weight(const uint16_t *W, int N, int K, uint16_t *Wp, cudaStream_t s,
+                               int gateup_I) {
   const long long chunks = static_cast<long long>(N) * K / 8;
   long long blocks = (chunks + 255) / 256;
   if (blocks > 4096) blocks = 4096;
   pack_weight_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-      reinterpret_cast<const uint4 *>(W), reinterpret_cast<uint4 *>(Wp), K, chunks);
+      reinterpret_cast<const uint4 *>(W), reinterpret_cast<uint4 *>(Wp), K, chunks, gateup_I);
   return cudaGetLastError();
 }
 

@@ -112,4 +112,12 @@ def test_host_argument_checks_need_no_device(ssd):
         ssd.DEC_ERR_UNSUPPORTED_SHAPE
     assert lib.dec_linear_packed(A, A, N0, A, 4, 128, 72, A, 0, s) == ssd.DEC_ERR_UNSUPPORTED_SHAPE
     assert lib.dec_linear_packed(A, N0, N0, A, 4, 128, 64, A, 0, s) == ssd.DEC_ERR_INVALID_ARG
+    B1, B2, B3 = (ctypes.c_void_p(0x1000000 * i) for i in (2, 3, 4))
+    assert lib.dec_pack_expert_weights(A, B1, 2, 256, 128, A, B3, s) == ssd.DEC_ERR_INVALID_ARG
+    assert lib.dec_pack_expert_weights(A, B1, 2, 200, 128, B2, B3, s) == \
+        ssd.DEC_ERR_UNSUPPORTED_SHAPE
+    assert lib.dec_pack_expert_weights(A, B1, 2, 256, 96, B2, B3, s) == \
+        ssd.DEC_ERR_UNSUPPORTED_SHAPE
+    assert lib.dec_pack_expert_weights(U, B1, 2, 256, 128, B2, B3, s) == ssd.DEC_ERR_MISALIGNED
+    assert lib.dec_pack_expert_weights(N0, B1, 2, 256, 128, B2, B3, s) == ssd.DEC_ERR_INVALID_ARG
     assert lib.dec_set_fault_inject(-1) == ssd.DEC_ERR_INVALID_ARG

@@ -325,7 +325,8 @@ def _routing(B, E, k, seed):
     return idx, w.astype(np.float32)
 
 
-def _run_experts(env, X, idx, w, Wgu, Wd, Wgs, Wds, rm=None, side=True, side_ctas=0, ws=None):
+def _run_experts(env, X, idx, w, Wgu, Wd, Wgs, Wds, rm=None, side=True, side_ctas=0, ws=None,
+                 packed=False):
     torch, ssd, oracle, dev = env
     B, H = X.shape
     E, twoI, _ = Wgu.shape
@@ -334,7 +335,8 @@ def _run_experts(env, X, idx, w, Wgu, Wd, Wgs, Wds, rm=None, side=True, side_cta
     if ws is None:
         ws = ssd.workspace(ssd.moe_experts_workspace_bytes(B, E, k, H, twoI // 2), dev)
     ss = torch.cuda.Stream(device=dev) if side else None
-    ssd.moe_experts(X, idx, w, rm, Wgu, Wd, Wgs, Wds, Y, ws, side_stream=ss, side_max_ctas=side_ctas)
+    ssd.moe_experts(X, idx, w, rm, Wgu, Wd, Wgs, Wds, Y, ws, side_stream=ss, side_max_ctas=side_ctas,
+                    packed=packed)
     torch.cuda.synchronize()
     assert ssd.dec_sync_status() == ssd.DEC_OK
     return Y
@@ -358,6 +360,59 @@ def test_moe_experts_small_bank(env, B, k, shared, side):
                                   None if Wgs is None else inputs.bits(Wgs),
                                   None if Wds is None else inputs.bits(Wds))
     assert_close(to_f64(oracle, Y), y_ref, f"experts B={B} k={k} shared={shared} side={side}")
+
+
+def _packed_bank_reference(torch, Wgu, Wd):
+    """Tile-packed banks by their definition: gate/up blocks of 64 gate rows then the 64
+    matching up rows, down blocks of 128 rows, each block 64 k wide, blocks in (expert,
+    tile, k-block) order."""
+    E, twoI, H = Wgu.shape
+    I = twoI // 2
+    g = Wgu[:, :I].reshape(E, I // 64, 64, H)
+    u = Wgu[:, I:].reshape(E, I // 64, 64, H)
+    rows = torch.cat([g, u], dim=2).reshape(-1, 128, H // 64, 64)
+    gu = rows.permute(0, 2, 1, 3).contiguous().view(E, twoI, H)
+    d = Wd.reshape(-1, 128, I // 64, 64).permute(0, 2, 1, 3).contiguous().view(E, H, I)
+    return gu, d
+
+
+@pytest.mark.parametrize("E,H,I", [(3, 256, 128), (1, 384, 192), (2, 128, 64)])
+def test_pack_expert_weights_layout(env, E, H, I):
+    torch, ssd, oracle, dev = env
+    from split_switched_decode_gb300 import inputs
+    Wgu, Wd = inputs.expert_bank(E, H, I, dev, 30)
+    gu, d = ssd.dec_pack_expert_weights(Wgu, Wd)
+    torch.cuda.synchronize()
+    rgu, rd = _packed_bank_reference(torch, Wgu, Wd)
+    assert torch.equal(gu, rgu) and torch.equal(d, rd)
+    # one element of each by the block formula
+    e, t, r, k = E - 1, I // 64 - 1, 70, H - 1  # an up row of the last tile
+    blk = (e * (I // 64) + t) * (H // 64) + k // 64
+    assert gu.view(-1)[blk * 8192 + r * 64 + k % 64].item() == Wgu[e, I + t * 64 + r - 64, k].item()
+
+
+@pytest.mark.parametrize("B,k", [(1, 8), (4, 2), (17, 8), (64, 8), (64, 1)])
+@pytest.mark.parametrize("shared,side,with_map", [(True, True, False), (True, False, True),
+                                                  (False, False, False)])
+def test_moe_experts_packed_equals_row_major(env, B, k, shared, side, with_map):
+    """Packed expert banks run the same tiles in the same order: bit-identical outputs,
+    with and without the shared expert, side stream and a given route map."""
+    torch, ssd, oracle, dev = env
+    from split_switched_decode_gb300 import inputs
+    E, H, I = 16, 256, 128
+    Wgu, Wd = inputs.expert_bank(E, H, I, dev, 31)
+    Wgs, Wds = inputs.shared_expert(H, I, dev, 31) if shared else (None, None)
+    Pgu, Pd = ssd.dec_pack_expert_weights(Wgu, Wd)
+    Pgs, Pds = ssd.dec_pack_expert_weights(Wgs[None], Wds[None]) if shared else (None, None)
+    X = inputs.activations(B, H, dev, 31, "pex")
+    idx_np, w_np = _routing(B, E, k, 50 + B)
+    idx = torch.from_numpy(idx_np).to(dev)
+    w = torch.from_numpy(w_np).to(dev)
+    rm = _host_route_map(oracle, idx_np, E, dev) if with_map else None
+    Y0 = _run_experts(env, X, idx, w, Wgu, Wd, Wgs, Wds, rm=rm, side=side)
+    Y1 = _run_experts(env, X, idx, w, Pgu, Pd, None if Pgs is None else Pgs[0],
+                      None if Pds is None else Pds[0], rm=rm, side=side, packed=True)
+    assert torch.equal(Y0, Y1)
 
 
 @pytest.mark.parametrize("B,E,k", [(64, 512, 16), (3, 1, 1), (64, 2, 2)])
@@ -528,6 +583,39 @@ def test_moe_layer_full_size(env, big_layer, B, with_map):
         _, s = oracle.expert_mlp(xb[b], gs, ds)
         y_ref[t] = oracle.combine(ref["w"][b:b + 1], yp, s[None, :])[0][0]
     assert_close(Yf[tokens], y_ref, f"MoE layer B={B}")
+
+
+@pytest.mark.parametrize("B", [1, 8, 64])
+def test_moe_layer_packed_full_size_equals_row_major(env, big_layer, B):
+    """The full-size layer on tile-packed expert banks (moe_layer_packed) against the
+    row-major layer, which test_moe_layer_full_size checks against the oracle: the same
+    top-k ids, route map, latent and output bits."""
+    torch, ssd, oracle, dev = env
+    from split_switched_decode_gb300 import inputs
+    g = big_layer
+    if "Pgu" not in g:
+        g["Pgu"], g["Pd"] = ssd.dec_pack_expert_weights(g["Wgu"], g["Wd"])
+        ps, pd = ssd.dec_pack_expert_weights(g["Wgs"][None], g["Wds"][None])
+        g["Pgs"], g["Pds"] = ps[0], pd[0]
+    E, H, I, L, k = g["E"], g["H"], g["I"], g["L"], 8
+    X = inputs.activations(B, H, dev, 32, "player_x")
+    outs = []
+    for packed in (False, True):
+        lat = torch.empty(B, L, dtype=torch.bfloat16, device=dev)
+        idx = torch.empty(B, k, dtype=torch.int32, device=dev)
+        w = torch.empty(B, k, dtype=torch.float32, device=dev)
+        rm = torch.full((ssd.moe_route_map_ints(B, E, k),), -7, dtype=torch.int32, device=dev)
+        Y = torch.empty(B, H, dtype=torch.bfloat16, device=dev)
+        ws = ssd.workspace(ssd.moe_layer_workspace_bytes(B, E, L, H, I, k), dev)
+        Wgu, Wd, Wgs, Wds = ((g["Pgu"], g["Pd"], g["Pgs"], g["Pds"]) if packed else
+                             (g["Wgu"], g["Wd"], g["Wgs"], g["Wds"]))
+        ssd.moe_layer(X, g["Wc"], E, L, k, Wgu, Wd, Wgs, Wds, lat, idx, w, Y, ws, route_map=rm,
+                      side_stream=torch.cuda.Stream(device=dev), packed=packed)
+        torch.cuda.synchronize()
+        assert ssd.dec_sync_status() == ssd.DEC_OK
+        outs.append((lat, idx, w, rm, Y))
+    for a, b, name in zip(outs[0], outs[1], ["latent", "idx", "w", "route map", "Y"]):
+        assert torch.equal(a, b), name
 
 
 def test_l2_prefetch_does_not_change_results(env):
