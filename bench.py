@@ -335,7 +335,9 @@ def time_graph(torch, g, reps):
 # ------------------------------------------------------- prefetch scenario ----
 
 PF_WAIT_US = 20.0
-EXPERTS_TRAFFIC_RATIO = 1.0125
+# DRAM bytes / algorithmic bytes of one expert-layer call (ncu, 32-expert bank, B = 64),
+# with tile-packed banks and with row-major ones
+EXPERTS_TRAFFIC_RATIO = {True: 1.0117, False: 1.0126}
 
 
 def prefetch_scenario(torch, ssd, wl, batches, reps):
@@ -769,7 +771,7 @@ def main():
     nb_dom = statistics.mean(bytes_experts(int(Bmax), u) for u in dom["distinct_experts"])
     roofline = {"bound": "hbm", "kernel": f"moe_experts grouped expert GEMV, B={Bmax}",
                 "achieved": dom["GBps"], "peak": peak, "peak_source": peak_src, "unit": "GB/s",
-                "frac": dom["GBps"] / peak, "traffic": EXPERTS_TRAFFIC_RATIO * nb_dom,
+                "frac": dom["GBps"] / peak, "traffic": EXPERTS_TRAFFIC_RATIO[wl.packed] * nb_dom,
                 "traffic_unit": "bytes per call"}
     for Bk, row in sweep.items():
         for op in row.values():
