@@ -104,9 +104,8 @@ __global__ void __launch_bounds__(FF_THREADS, 2)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int S = p.S, nsl = p.nsl, nst = p.nst;
   uint8_t *ring = smem;                                           // nst stages
-  float *recv = reinterpret_cast<float *>(smem + nst * STAGE);    // [S][128][nsl]
-  float *lg = recv + S * nsl * 128;                               // [nsl][128]
-  uint64_t *full = reinterpret_cast<uint64_t *>(lg + nsl * 128);  // [nst]
+  float *recv = reinterpret_cast<float *>(smem + nst * STAGE);      // [S][128][nsl]
+  uint64_t *full = reinterpret_cast<uint64_t *>(recv + S * nsl * 128);  // [nst]
   uint64_t *empty = full + nst;                                   // [nst]
   uint64_t *acc_full = empty + nst;   // both accumulators final (two commits)
   uint64_t *recv_bar = acc_full + 1;  // this CTA's tokens: every sender's rows landed
@@ -434,8 +433,7 @@ int max_clusters_nxb(int S, size_t smem) {
 
 size_t front_fused_smem(int S, int nxb, int nst, int nsl) {
   const size_t stage = 16384 + static_cast<size_t>(nxb) * 2048;
-  return 1024 + nst * stage + static_cast<size_t>(S) * nsl * 512 + static_cast<size_t>(nsl) * 512 +
-         (2 * nst + 5) * 8 + 64;
+  return 1024 + nst * stage + static_cast<size_t>(S) * nsl * 512 + (2 * nst + 5) * 8 + 64;
 }
 
 int front_fused_max_clusters(int S, int nxb, size_t smem) {
