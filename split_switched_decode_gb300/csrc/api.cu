@@ -288,6 +288,16 @@ int defer_min_k() {
   return 12288;
 }
 
+// Slack on the shared expert's share of the SMs next to the routed experts
+// (DEC_SIDE_SLACK, 1.0 .. 2.0; default 1.25): its fair share is num_sms / (U + 1).
+double side_slack() {
+  if (const char *s = std::getenv("DEC_SIDE_SLACK")) {
+    const double v = std::atof(s);
+    if (v >= 1.0 && v <= 2.0) return v;
+  }
+  return 1.25;
+}
+
 // Whether grouped launches whose route map is already complete read it, and issue their
 // first weight loads, before the dependency wait (DEC_EARLY_ROUTE_MAP=0 turns it off).
 bool early_route_map() {
@@ -1165,9 +1175,9 @@ dec_status moe_experts_impl(const dec_bf16 *X, const int32_t *topk_idx, const fl
       double miss = 1.0;
       for (int b = 0; b < B; ++b) miss *= 1.0 - static_cast<double>(topk) / E;
       const double u_exp = E * (1.0 - miss);
-      // a fair bandwidth share is num_sms/(U+1) SMs; round up with 25% slack so the
+      // a fair bandwidth share is num_sms/(U+1) SMs; round up with some slack so the
       // shared expert (88 MB at the Kimi shape) never becomes the critical path
-      g_side = static_cast<int>(std::ceil(1.25 * d->num_sms / (1.0 + u_exp)));
+      g_side = static_cast<int>(std::ceil(side_slack() * d->num_sms / (1.0 + u_exp)));
       if (g_side < 2) g_side = 2;
     }
     if (g_side < 1) g_side = 1;
