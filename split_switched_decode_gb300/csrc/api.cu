@@ -1041,8 +1041,10 @@ dec_status dec_pack_expert_weights(const dec_bf16 *Wgu, const dec_bf16 *Wd, int 
   auto overlap = [](const dec_bf16 *a, size_t na, const dec_bf16 *b, size_t nb) {
     return a < b + nb && b < a + na;
   };
+  // no destination may overlap a source or the other destination
   if (overlap(Wgu, 2 * n, Wgu_p, 2 * n) || overlap(Wd, n, Wd_p, n) ||
-      overlap(Wgu_p, 2 * n, Wd_p, n))
+      overlap(Wgu_p, 2 * n, Wd_p, n) || overlap(Wgu, 2 * n, Wd_p, n) ||
+      overlap(Wd, n, Wgu_p, 2 * n))
     return DEC_ERR_INVALID_ARG;
   cudaError_t ce;
   if (!device_info(&ce)) return DEC_ERR_CUDA;

@@ -120,4 +120,7 @@ def test_host_argument_checks_need_no_device(ssd):
         ssd.DEC_ERR_UNSUPPORTED_SHAPE
     assert lib.dec_pack_expert_weights(U, B1, 2, 256, 128, B2, B3, s) == ssd.DEC_ERR_MISALIGNED
     assert lib.dec_pack_expert_weights(N0, B1, 2, 256, 128, B2, B3, s) == ssd.DEC_ERR_INVALID_ARG
+    # a source bank overlapping the other bank's destination
+    assert lib.dec_pack_expert_weights(A, B1, 2, 256, 128, B2, A, s) == ssd.DEC_ERR_INVALID_ARG
+    assert lib.dec_pack_expert_weights(A, B1, 2, 256, 128, B1, B3, s) == ssd.DEC_ERR_INVALID_ARG
     assert lib.dec_set_fault_inject(-1) == ssd.DEC_ERR_INVALID_ARG
