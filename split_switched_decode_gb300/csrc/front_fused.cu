@@ -355,8 +355,12 @@ __global__ void __launch_bounds__(FF_THREADS, 2)
       route_token_sorted(lg, p.E, topk, p.topk_idx + b * topk, p.topk_w + b * topk,
                          p.probs + static_cast<size_t>(b) * p.E, si);
     } else {
-      route_token_filtered(lg, p.E, topk, p.topk_idx + b * topk, p.topk_w + b * topk, si,
-                           rscr, p.trig_late != 0);
+      if (p.E <= 12 * 32)
+        route_token_filtered<12>(lg, p.E, topk, p.topk_idx + b * topk, p.topk_w + b * topk,
+                                 si, rscr, p.trig_late != 0);
+      else
+        route_token_filtered<16>(lg, p.E, topk, p.topk_idx + b * topk, p.topk_w + b * topk,
+                                 si, rscr, p.trig_late != 0);
     }
   }
   if (single) {

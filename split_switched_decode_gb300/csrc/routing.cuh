@@ -349,10 +349,12 @@ constexpr int RT_CMAX = 64;
 // scratch: shared uint64 [RT_CMAX + MAX_TOPK] of this warp. Outputs: idx/w [topk]
 // (global), sidx [topk] (shared, optional). trigger: once the logits are in registers,
 // let the next kernel of the stream be scheduled (programmatic dependent launch).
+// V: logits per lane, E <= 32 V (12 covers 384 experts; 16 the 512 maximum).
+template <int V>
 __device__ __forceinline__ void route_token_filtered(const float *logits, int E, int topk,
                                                      int32_t *idx, float *w, int32_t *sidx,
                                                      uint64_t *scratch, bool trigger = false) {
-  constexpr int V = MAX_E / 32;
+  static_assert(V >= 1 && V <= MAX_E / 32, "logits per lane");
   const int lane = threadIdx.x & 31;
   const unsigned FULL = 0xFFFFFFFFu;
   uint64_t k[V];
@@ -393,6 +395,7 @@ __device__ __forceinline__ void route_token_filtered(const float *logits, int E,
     const uint64_t a0 = lane < C ? cand[lane] : 0ull;
     const uint64_t a1 = lane + 32 < C ? cand[lane + 32] : 0ull;
     int r0 = 0, r1 = 0;
+#pragma unroll 4
     for (int j = 0; j < C; ++j) {
       const uint64_t x = cand[j];
       r0 += x > a0;
@@ -407,9 +410,12 @@ __device__ __forceinline__ void route_token_filtered(const float *logits, int E,
       my_v = order_key_to_f32(static_cast<uint32_t>(kk >> 32));
     }
     __syncwarp();  // slots read before the scratch is reused
-  } else {
-    sort_desc_lane<V>(k);
-    warp_rounds<V>(k, topk, my_e, my_v);
+  } else {  // the sorting network wants a power of two: pad with empty keys
+    uint64_t k16[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) k16[i] = i < V ? k[i] : 0ull;
+    sort_desc_lane<16>(k16);
+    warp_rounds<16>(k16, topk, my_e, my_v);
   }
   const float m0 = __shfl_sync(FULL, my_v, 0);  // the largest logit
   const float ex = lane < topk ? expf(my_v - m0) : 0.f;
