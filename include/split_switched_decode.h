@@ -13,7 +13,8 @@
  * ---------------------------------------
  *  - Types. dec_bf16 is the raw 16-bit pattern of an IEEE bfloat16. Matrices are
  *    row-major with the last dimension contiguous. Weights W[N,K] use the nn.Linear
- *    layout, so Y = X . W^T.
+ *    layout, so Y = X . W^T -- except for the *_packed entry points, which read the
+ *    tile-packed copy made once by dec_pack_weight / dec_pack_expert_weights.
  *  - Memory. Every pointer is DEVICE memory owned by the caller. The library never
  *    allocates or frees memory. Where a call needs scratch memory it takes a caller
  *    workspace whose size comes from the matching *_workspace_bytes() query; the
