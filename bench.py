@@ -773,6 +773,22 @@ def main():
                 "achieved": dom["GBps"], "peak": peak, "peak_source": peak_src, "unit": "GB/s",
                 "frac": dom["GBps"] / peak, "traffic": EXPERTS_TRAFFIC_RATIO[wl.packed] * nb_dom,
                 "traffic_unit": "bytes per call"}
+    # context for `frac`: the read-only HBM rate (every SM streaming a contiguous share
+    # of 4 GiB in 16 KB bulk copies; the copy peak above counts read and written bytes)
+    rs_buf = torch.empty(4 << 30, dtype=torch.uint8, device=dev)
+    ssd.dec_read_stream(rs_buf)
+    torch.cuda.synchronize()
+    rs_t = []
+    for _ in range(5):
+        ra, rb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ra.record()
+        rs_n = ssd.dec_read_stream(rs_buf)
+        rb.record()
+        torch.cuda.synchronize()
+        rs_t.append(ra.elapsed_time(rb))
+    del rs_buf
+    roofline["read_stream_gbs"] = rs_n / (min(rs_t) * 1e-3) / 1e9
+    roofline["frac_of_read_stream"] = dom["GBps"] / roofline["read_stream_gbs"]
     for Bk, row in sweep.items():
         for op in row.values():
             op["frac"] = op["GBps"] / peak

@@ -41,6 +41,7 @@ EXPORTS = [
     "l2_prefetch", "dec_sim_comm_wait", "dec_splitk_gemm_noalloc",
     "dec_pack_weight", "dec_gemv_packed", "dec_splitk_gemm_packed", "dec_linear_packed",
     "dec_pack_expert_weights", "moe_experts_packed", "moe_layer_packed",
+    "dec_read_stream_bytes", "dec_read_stream",
 ]
 
 _lib = None
@@ -96,6 +97,8 @@ def _load():
         "moe_layer_workspace_bytes": (S, [I, I, I, I, I, I]),
         "moe_layer": (I, [P, P, I, I, I, P, P, P, P, I, I, I, P, P, P, P, P, P, S, P, P, I]),
         "dec_pack_expert_weights": (I, [P, P, I, I, I, P, P, P]),
+        "dec_read_stream_bytes": (S, [S]),
+        "dec_read_stream": (I, [P, S, P]),
         "moe_experts_packed": (I, [P, P, P, P, P, P, I, P, P, I, I, I, I, P, P, S, P, P, I]),
         "moe_layer_packed": (I, [P, P, I, I, I, P, P, P, P, I, I, I, P, P, P, P, P, P, S, P, P,
                                  I]),
@@ -332,6 +335,14 @@ def dec_pack_expert_weights(Wgu, Wd, stream=None):
 def l2_prefetch(t, nbytes=None, max_ctas=0, stream=None):
     n = t.numel() * t.element_size() if nbytes is None else int(nbytes)
     _check(_load().l2_prefetch(_ptr(t), n, max_ctas, _stream(stream)), "l2_prefetch")
+
+
+def dec_read_stream(t, stream=None) -> int:
+    """Stream tensor t's bytes through every SM (bulk copies into shared memory; nothing
+    is written) -- a measurement helper. Returns the bytes the call reads."""
+    n = t.numel() * t.element_size()
+    _check(_load().dec_read_stream(_ptr(t), n, _stream(stream)), "dec_read_stream")
+    return int(_load().dec_read_stream_bytes(n))
 
 
 def dec_sim_comm_wait(ns: int, stream=None):

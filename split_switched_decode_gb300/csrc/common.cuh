@@ -190,6 +190,17 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void *addr, uint32_t byte
                : "memory");
 }
 
+// 1-D bulk copy global -> shared memory of `bytes` (a multiple of 16, both addresses
+// 16-byte aligned), completion counted in bytes on `bar`.
+__device__ __forceinline__ void bulk_load_1d(void *dst, const void *src, uint32_t bytes,
+                                             uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+
 // ---------------------------------------------------------------- atomics ----
 // GPU-scope acquire-release add. Issued by one thread after a CTA barrier, it publishes
 // every write the CTA made before the barrier (release is cumulative) and, for the

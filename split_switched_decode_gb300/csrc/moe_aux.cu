@@ -360,6 +360,46 @@ __global__ void wait_selftest_kernel(unsigned *status, uint64_t limit_ns) {
 
 // Occupies its stream for ns nanoseconds (globaltimer) while touching no memory: a
 // stand-in for a communication phase that leaves HBM idle.
+// HBM read-stream measurement (dec_read_stream): CTA c streams bytes
+// [c * per_cta, (c + 1) * per_cta) into RS_STAGES rotating 16 KB shared-memory stages
+// with 1-D bulk copies, one thread issuing and the stage's mbarrier counting the bytes;
+// nothing is written anywhere. Every wait is bounded; after a time-out the copies still
+// in flight land before the CTA exits.
+constexpr int RS_STAGES = 8;
+constexpr int RS_CHUNK = 16384;
+__global__ void __launch_bounds__(32) read_stream_kernel(const uint8_t *p, size_t per_cta,
+                                                         unsigned *status, uint64_t limit_ns) {
+  extern __shared__ __align__(1024) uint8_t rs_stage[];
+  __shared__ __align__(8) uint64_t bar[RS_STAGES];
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  abort_flag = 0;
+  for (int s = 0; s < RS_STAGES; ++s) mbar_init(&bar[s], 1);
+  fence_mbar_init();
+  const uint8_t *b = p + per_cta * blockIdx.x;
+  const long long n = static_cast<long long>(per_cta / RS_CHUNK);
+  long long issued = 0;
+  for (long long c = 0; c < n + RS_STAGES; ++c) {
+    if (c >= RS_STAGES) {
+      const long long d = c - RS_STAGES;
+      if (!mbar_wait_bounded(&bar[d % RS_STAGES], static_cast<uint32_t>((d / RS_STAGES) & 1),
+                             status, &abort_flag, limit_ns))
+        break;
+    }
+    if (c < n) {
+      const int s = static_cast<int>(c % RS_STAGES);
+      mbar_arrive_expect_tx(&bar[s], RS_CHUNK);
+      bulk_load_1d(rs_stage + s * RS_CHUNK, b + c * RS_CHUNK, RS_CHUNK, &bar[s]);
+      ++issued;
+    }
+  }
+  if (abort_flag) {
+    for (long long d = issued > RS_STAGES ? issued - RS_STAGES : 0; d < issued; ++d)
+      (void)mbar_wait_drain(&bar[d % RS_STAGES], static_cast<uint32_t>((d / RS_STAGES) & 1),
+                            10000000ull);
+  }
+}
+
 __global__ void comm_wait_kernel(uint64_t ns) {
   const uint64_t t0 = globaltimer_ns();
   while (globaltimer_ns() - t0 < ns) __nanosleep(256);
@@ -400,6 +440,18 @@ cudaError_t launch_pack_weight(const uint16_t *W, int N, int K, uint16_t *Wp, cu
   if (blocks > 4096) blocks = 4096;
   pack_weight_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
       reinterpret_cast<const uint4 *>(W), reinterpret_cast<uint4 *>(Wp), K, chunks, gateup_I);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_read_stream(const void *p, size_t per_cta, int ctas, unsigned *status,
+                               uint64_t limit_ns, cudaStream_t s) {
+  const size_t smem = static_cast<size_t>(RS_STAGES) * RS_CHUNK;
+  cudaError_t e = cudaFuncSetAttribute(read_stream_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  read_stream_kernel<<<ctas, 32, smem, s>>>(static_cast<const uint8_t *>(p), per_cta, status,
+                                            limit_ns);
   return cudaGetLastError();
 }
 

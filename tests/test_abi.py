@@ -98,6 +98,8 @@ def test_host_argument_checks_need_no_device(ssd):
     bad[0], bad[12] = A, N0  # latent missing with L > 0
     assert lib.moe_layer(*bad) == ssd.DEC_ERR_INVALID_ARG
     assert lib.dec_sim_comm_wait(1000000001, s) == ssd.DEC_ERR_INVALID_ARG
+    assert lib.dec_read_stream(N0, 1 << 20, s) == ssd.DEC_ERR_INVALID_ARG
+    assert lib.dec_read_stream(U, 1 << 20, s) == ssd.DEC_ERR_MISALIGNED
     # tile-packed weights: whole 128-row tiles and 64-wide k-blocks only
     assert lib.dec_pack_weight(A, 256, 128, A, s) == ssd.DEC_ERR_INVALID_ARG  # W and Wp overlap
     assert lib.dec_pack_weight(A, 200, 128, ctypes.c_void_p(0x100000), s) == \
