@@ -307,6 +307,12 @@ DEC_API dec_status moe_front(const dec_bf16 *X, const dec_bf16 *Wcat, int B, int
  * The combine is its own launch; with a route map and the environment switch
  * DEC_FUSED_COMBINE=1 it runs instead inside the down launches (the tile that completes
  * a token's 128-row block adds it up, in the same order: the same bits).
+ * Schedule of the routed launches: below about 6.5 expected tiles per CTA, equal
+ * stream-K ranges of (expert, tile, k-block) with a fixed-order reduction of split
+ * tiles; above it, whole tiles (a static share per CTA, the rest claimed one by one from
+ * a counter in the workspace, cleared by the call's gather launch), each accumulated
+ * over all of its k-blocks by one CTA, so the bits do not depend on which CTA computes
+ * a tile. Both are deterministic; they differ from each other by fp32 summation order.
  * H % 128 == 0, I % 64 == 0, topk <= 16, E <= 512.
  */
 DEC_API size_t moe_experts_workspace_bytes(int B, int E, int topk, int H, int I);

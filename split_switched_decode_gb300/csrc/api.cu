@@ -298,6 +298,24 @@ double side_slack() {
   return 1.25;
 }
 
+// Whole-tile schedule of the routed-expert launches (tensor cores): the static share of
+// the tiles, in 1/256 (DEC_EXPERT_DYN, 0 = stream-K ranges), and the expected tiles per
+// CTA from which a launch uses it (DEC_EXPERT_DYN_MIN_TILES).
+int expert_dyn() {
+  if (const char *s = std::getenv("DEC_EXPERT_DYN")) {
+    const int v = std::atoi(s);
+    if (v >= 0 && v <= 256) return v;
+  }
+  return 230;
+}
+double expert_dyn_min_tiles() {
+  if (const char *s = std::getenv("DEC_EXPERT_DYN_MIN_TILES")) {
+    const double v = std::atof(s);
+    if (v >= 0.0) return v;
+  }
+  return 6.5;
+}
+
 // Whether grouped launches whose route map is already complete read it, and issue their
 // first weight loads, before the dependency wait (DEC_EARLY_ROUTE_MAP=0 turns it off).
 bool early_route_map() {
@@ -586,7 +604,7 @@ bool plan_front_fused(int B, int K, FusedFrontPlan *f) {
 struct ExpertsPlan {
   int maxc, Tg, Td, KBg, KBd;
   size_t rm_off, xg_off, a_off, yp_off, as_off, s_off;
-  size_t main_part_off, main_cnt_off, side_part_off, side_cnt_off, cmb_off, total;
+  size_t main_part_off, main_cnt_off, side_part_off, side_cnt_off, cmb_off, dyn_off, total;
 };
 
 bool plan_experts(int B, int E, int topk, int H, int I, int num_sms, ExpertsPlan *ep) {
@@ -621,6 +639,8 @@ bool plan_experts(int B, int E, int topk, int H, int I, int num_sms, ExpertsPlan
   o += align_up(static_cast<size_t>(tmax) * sizeof(int));
   ep->cmb_off = o;  // fused combine: one arrival counter per (token, 128-row block of H)
   o += align_up(static_cast<size_t>(B) * ep->Td * sizeof(int));
+  ep->dyn_off = o;  // whole-tile schedule: claim counters of routed gate/up and down
+  o += align_up(4 * sizeof(int));
   ep->total = o;
   return true;
 }
@@ -1169,14 +1189,14 @@ dec_status moe_experts_impl(const dec_bf16 *X, const int32_t *topk_idx, const fl
   // CTA split between the routed experts (main) and the shared expert (side): in
   // proportion to the weight bytes each reads, using the expected number of distinct
   // experts for this batch, unless the caller caps the side.
+  double miss = 1.0;
+  for (int b = 0; b < B; ++b) miss *= 1.0 - static_cast<double>(topk) / E;
+  const double u_exp = E * (1.0 - miss);  // expected distinct experts of the batch
   int g_side = 0;
   if (overlap) {
     if (side_max_ctas > 0) {
       g_side = side_max_ctas;
     } else {
-      double miss = 1.0;
-      for (int b = 0; b < B; ++b) miss *= 1.0 - static_cast<double>(topk) / E;
-      const double u_exp = E * (1.0 - miss);
       // a fair bandwidth share is num_sms/(U+1) SMs; round up with some slack so the
       // shared expert (88 MB at the Kimi shape) never becomes the critical path
       g_side = static_cast<int>(std::ceil(side_slack() * d->num_sms / (1.0 + u_exp)));
@@ -1295,9 +1315,10 @@ dec_status moe_experts_impl(const dec_bf16 *X, const int32_t *topk_idx, const fl
 
   // ---- routed experts, main stream
   // without a route map the gather launch validates topk_idx and builds it
-  ce = have_map ? launch_gather_rows(X, rm, B, topk, E, H, Xg, ms)
+  int *dyn_ctr = reinterpret_cast<int *>(wsb + ep.dyn_off);
+  ce = have_map ? launch_gather_rows(X, rm, B, topk, E, H, Xg, dyn_ctr, ms)
                 : launch_gather_map(X, topk_idx, B, topk, E, H, Xg, rm, d->status,
-                                    2 * d->num_sms, ms);
+                                    2 * d->num_sms, dyn_ctr, ms);
   if (ce != cudaSuccess) return DEC_ERR_CUDA;
   {
     EngineParams p;
@@ -1308,17 +1329,30 @@ dec_status moe_experts_impl(const dec_bf16 *X, const int32_t *topk_idx, const fl
     // gate/up launch start; so when the map is not the gather's own output, it is
     // complete before gate/up starts, and likewise before down starts: both may then
     // read it, and issue their first weight loads, before their dependency wait.
+    // Whole-tile schedule once the CTAs expect enough tiles each that the last claims
+    // even out the SMs' different read rates (tiles per CTA from the expected number of
+    // distinct experts; with fewer, whole tiles are too coarse and stream-K ranges win).
+    const int dyn = tc ? expert_dyn() : 0;
+    const double dyn_min = expert_dyn_min_tiles();
     base(p, MODE_GATEUP, I, H, ep.Tg, ep.KBg, gg, 1, ep.main_part_off, ep.main_cnt_off);
     p.w_group_rows = 2 * I;
     p.up_row_off = I;
     p.A = A;
     p.rm_ready = (have_map && early_route_map()) ? 1 : 0;
+    if (dyn > 0 && u_exp * ep.Tg >= dyn_min * gg) {
+      p.dyn = dyn;
+      p.dyn_ctr = dyn_ctr;
+    }
     if ((ce = engine(m_wgu, m_xg, p, ms)) != cudaSuccess) return DEC_ERR_CUDA;
     base(p, MODE_DOWN, H, I, ep.Td, ep.KBd, gd, 1, ep.main_part_off, ep.main_cnt_off);
     p.w_group_rows = H;
     p.Yp = Yp;
     if (fused) set_combine(p);
     p.rm_ready = early_route_map() ? 1 : 0;
+    if (dyn > 0 && u_exp * ep.Td >= dyn_min * gd) {
+      p.dyn = dyn;
+      p.dyn_ctr = dyn_ctr + 1;
+    }
     if ((ce = engine(m_wd, m_a, p, ms)) != cudaSuccess) return DEC_ERR_CUDA;
   }
   // Y is complete once both streams are done: the main stream waits for the side one

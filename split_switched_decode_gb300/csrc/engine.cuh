@@ -212,6 +212,106 @@ __device__ __forceinline__ void engine_produce(const EngineParams &p, const CUte
   }
 }
 
+// Whole-tile schedule (p.dyn; grouped tensor-core launches). The launch's tiles are
+// numbered in (group, tile) order. CTA w streams its static tiles [w*S, (w+1)*S) and then
+// claims tiles G*S, G*S+1, ... one at a time from *p.dyn_ctr until none is left, so the
+// CTAs on SMs that stream faster take more of the remainder (the SMs of a GB300 do not
+// all read HBM at the same rate). Every tile is one segment over all of its k-blocks:
+// no partial tiles, no reduction, and each output is accumulated in the same k order
+// whichever CTA computes it.
+__device__ __forceinline__ int dyn_static_tiles(const EngineParams &p, int ntiles) {
+  return static_cast<int>((static_cast<int64_t>(ntiles) * p.dyn) / (256ll * p.G));
+}
+
+// Producer of the whole-tile schedule (one thread). Segment seg's tile, or -1 after the
+// last one, goes to slot seg % 4 of `tslot` for the MMA and epilogue warps: tready[slot]
+// completes a phase when the slot is written, tfree[slot] when both readers have taken
+// it. As in engine_produce, the weight boxes of the first STAGES k-blocks (of static
+// tiles) may be issued before griddep_wait; claims are made only after it (the counter
+// is cleared by the launch before this one). The next claim is issued STAGES k-blocks
+// before the current tile's last one, so its round trip overlaps the loads.
+template <int STAGES, int STAGE_BYTES>
+__device__ __forceinline__ void engine_produce_dyn(const EngineParams &p, const CUtensorMap *wmap,
+                                                   const CUtensorMap *xmap, uint8_t *stage_mem,
+                                                   uint64_t *full, uint64_t *empty,
+                                                   volatile int *tslot, uint64_t *tready,
+                                                   uint64_t *tfree, volatile int *flags,
+                                                   int ntiles) {
+  prefetch_tensormap(wmap);
+  prefetch_tensormap(xmap);
+  const uint64_t pol = policy_evict_first();
+  const int S = dyn_static_tiles(p, ntiles);
+  const int t0 = static_cast<int>(blockIdx.x) * S;
+  uint32_t pre = 0;
+  if (p.rm_ready) {
+    for (int i = 0; i < S && pre < STAGES; ++i) {
+      SegInfo s;
+      const int64_t it = static_cast<int64_t>(t0 + i) * p.KB;
+      seg_info(p, it, it + p.KB, s);
+      const uint32_t bytes = stage_tx_bytes(p, s);
+      for (int kb = 0; kb < p.KB && pre < STAGES; ++kb, ++pre) {
+        mbar_arrive_expect_tx(&full[pre], bytes);  // first use of the stage: it is empty
+        load_weights(p, s, wmap, stage_mem + pre * STAGE_BYTES, &full[pre], kb, pol);
+      }
+    }
+  }
+  griddep_wait();
+  const int base = p.G * S;
+  const int claim_kb = p.KB > STAGES ? p.KB - STAGES : 0;
+  uint32_t q = 0;
+  bool ok = true;
+  int ahead = -1;  // the next dynamic tile, once claimed
+  for (uint32_t seg = 0;; ++seg) {
+    int tile;
+    if (static_cast<int>(seg) < S) {
+      tile = t0 + static_cast<int>(seg);
+    } else {
+      if (ahead < 0 && ok) ahead = base + atomicAdd(p.dyn_ctr, 1);
+      tile = (ok && ahead < ntiles) ? ahead : -1;
+      ahead = -1;
+    }
+    const int sl = static_cast<int>(seg & 3u);
+    if (ok && !mbar_wait_bounded(&tfree[sl], ((seg >> 2) & 1u) ^ 1u, p.status, flags,
+                                 p.wait_limit_ns)) {
+      ok = false;
+      tile = -1;
+    }
+    tslot[sl] = tile;
+    mbar_arrive(&tready[sl]);
+    if (tile < 0) break;
+    SegInfo s;
+    const int64_t it = static_cast<int64_t>(tile) * p.KB;
+    seg_info(p, it, it + p.KB, s);
+    const int nxb = (16 * seg_xboxes(s) + p.xbox_rows - 1) / p.xbox_rows;
+    const uint32_t bytes = stage_tx_bytes(p, s);
+    const bool next_dyn = static_cast<int>(seg) + 1 >= S;
+    for (int kb = 0; kb < p.KB; ++kb, ++q) {
+      if (kb == claim_kb && next_dyn) ahead = base + atomicAdd(p.dyn_ctr, 1);
+      const int st = static_cast<int>(q % STAGES);
+      uint8_t *dst = stage_mem + st * STAGE_BYTES;
+      if (q >= pre) {
+        const uint32_t par = ((q / STAGES) & 1u) ^ 1u;
+        if (!mbar_wait_bounded(&empty[st], par, p.status, flags, p.wait_limit_ns)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[st], bytes);
+        load_weights(p, s, wmap, dst, &full[st], kb, pol);
+      }
+      for (int i = 0; i < nxb; ++i)
+        tma_load_2d(dst + 16384 + i * p.xbox_rows * 128, xmap, &full[st], kb * TILE_K,
+                    s.xrow0 + p.xbox_rows * i);
+    }
+  }
+  griddep_launch_dependents();
+  if (flags[0]) {
+    // after a time-out: let this CTA's copies still in flight land before it exits
+    const uint32_t q0 = q > STAGES ? q - STAGES : 0u;
+    for (uint32_t qq = q0; qq < q; ++qq)
+      (void)mbar_wait_drain(&full[qq % STAGES], (qq / STAGES) & 1u, 10000000ull);
+  }
+}
+
 // Y rows n0 .. n0+7 of batch column j: y (+ R) rounded once to bf16, one 16-byte store
 // (or element by element for a ragged tail). Requires N % 8 == 0 and 16-byte aligned Y
 // and R (p.vec_y).

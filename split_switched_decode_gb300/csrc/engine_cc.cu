@@ -188,6 +188,7 @@ int engine_maxc_for(int ncols) {
 cudaError_t launch_engine_cc(int maxc, const CUtensorMap &wmap, const CUtensorMap &xmap,
                              const EngineParams &p, cudaStream_t s) {
   if (p.ngrp != 1) return cudaErrorInvalidValue;  // wide projections: tensor cores only
+  if (p.dyn) return cudaErrorInvalidValue;        // whole-tile schedule: tensor cores only
   switch (maxc) {
     case 2: return launch_t<2>(wmap, xmap, p, s);
     case 4: return launch_t<4>(wmap, xmap, p, s);

@@ -48,7 +48,7 @@ struct TCConfig {
   static constexpr int NXB = NC / 16 * NG;          // 16-row activation boxes per stage
   static constexpr int STAGE_BYTES = 16384 + NXB * 2048;
   static constexpr int SCRATCH_BYTES = 64 * MAXC * 4;  // gate/up pairing
-  static constexpr int TAIL = 256;
+  static constexpr int TAIL = 512;
   static constexpr int BUDGET = TC_SMEM_LIMIT - 1024 - TAIL;
   static constexpr int FIT = (BUDGET - SCRATCH_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = FIT > 8 ? 8 : FIT;
@@ -72,8 +72,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   uint64_t *acc_full = empty + C::STAGES;   // [2]
   uint64_t *acc_empty = acc_full + 2;       // [2]
   uint64_t *drain = acc_empty + 2;          // [1]
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  uint64_t *tready = drain + 1;             // [4] whole-tile schedule: slot written
+  uint64_t *tfree = tready + 4;             // [4] whole-tile schedule: slot read
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tfree + 4);
   volatile int *flags = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  volatile int *tslot = flags + 3;          // [4] tile of segment seg in slot seg % 4
+  volatile int *etile = tslot + 4;          // [2] the epilogue's copy, by segment parity
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int w = blockIdx.x;
@@ -99,6 +103,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       mbar_init(&acc_empty[b], 4);
     }
     mbar_init(drain, 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&tready[i], 1);
+      mbar_init(&tfree[i], 2);  // the MMA issuer and epilogue thread 0
+    }
     flags[0] = 0;
     flags[1] = 0;
     flags[2] = 0;
@@ -120,7 +128,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
     if (!p.grouped) prefetch_weights_l2(p, begin, end, C::STAGES, lane);
-    if (lane == 0)
+    if (lane == 0 && p.dyn)
+      engine_produce_dyn<C::STAGES, C::STAGE_BYTES>(p, &wmap, &xmap, stage_mem, full, empty,
+                                                    tslot, tready, tfree, flags,
+                                                    ngroups * p.T);
+    else if (lane == 0)
       engine_produce<C::STAGES, C::STAGE_BYTES>(p, &wmap, &xmap, stage_mem, full, empty, flags,
                                                 begin, end);
     else
@@ -129,27 +141,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // ------------------------------------------------------------- MMA issuer
     griddep_wait();
     if (lane == 0) {
-      uint32_t q = 0, seg = 0;
+      uint32_t q = 0;
       bool ok = true;
-      for (int64_t it = begin; it < end && ok; ++seg) {
-        SegInfo s;
-        seg_info(p, it, end, s);
+      // one segment's k-blocks into accumulator buffer seg % 2; false after a time-out
+      auto mma_segment = [&](const SegInfo &s, uint32_t seg) -> bool {
         const uint32_t idesc = idesc_bf16(16 * seg_xboxes(s));
         const uint32_t buf = seg & 1u;
         if (!mbar_wait_bounded(&acc_empty[buf], ((seg >> 1) & 1u) ^ 1u, p.status, flags,
-                               p.wait_limit_ns)) {
-          ok = false;
-          break;
-        }
+                               p.wait_limit_ns))
+          return false;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * 64u * NG;
         for (int kb = s.kb0; kb < s.kb1; ++kb, ++q) {
           const int st = static_cast<int>(q % C::STAGES);
           if (!mbar_wait_bounded(&full[st], (q / C::STAGES) & 1u, p.status, flags,
-                                 p.wait_limit_ns)) {
-            ok = false;
-            break;
-          }
+                                 p.wait_limit_ns))
+            return false;
           tc_fence_after();
           const uint32_t a_addr = smem_u32(stage_mem + st * C::STAGE_BYTES);
           const uint64_t adesc = sw128_desc(a_addr);
@@ -160,9 +167,30 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                    (kb > s.kb0 || kk > 0) ? 1u : 0u);
           tc_commit(&empty[st]);  // the stage is free once these MMAs have read it
         }
-        if (!ok) break;
         tc_commit(&acc_full[buf]);  // accumulator ready for the epilogue
-        it += s.kb1 - s.kb0;
+        return true;
+      };
+      if (p.dyn) {
+        for (uint32_t seg = 0; ok; ++seg) {
+          const int sl = static_cast<int>(seg & 3u);
+          if (!mbar_wait_bounded(&tready[sl], (seg >> 2) & 1u, p.status, flags, p.wait_limit_ns))
+            break;
+          const int tile = tslot[sl];
+          mbar_arrive(&tfree[sl]);
+          if (tile < 0) break;
+          SegInfo s;
+          const int64_t it = static_cast<int64_t>(tile) * p.KB;
+          seg_info(p, it, it + p.KB, s);
+          ok = mma_segment(s, seg);
+        }
+      } else {
+        uint32_t seg = 0;
+        for (int64_t it = begin; it < end && ok; ++seg) {
+          SegInfo s;
+          seg_info(p, it, end, s);
+          ok = mma_segment(s, seg);
+          it += s.kb1 - s.kb0;
+        }
       }
       if (flags[0]) {  // let every MMA issued so far finish before the memory is freed
         tc_commit(drain);
@@ -175,7 +203,44 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (p.pair) cluster_wait();
     const int r = 32 * (warp & 3) + lane;  // tile row == tensor-memory lane
     uint32_t seg = 0;
-    for (int64_t it = begin; it < end; ++seg) {
+    // whole-tile schedule (grouped launches: one column group, no pair): thread 0 takes
+    // each segment's tile from the producer's slot and hands it to the other 127 threads
+    // through etile across the barrier; every segment is a whole tile, so there is no
+    // reduction
+    for (; p.dyn; ++seg) {
+      const int sl = static_cast<int>(seg & 3u);
+      if (r == 0) {
+        const bool got =
+            mbar_wait_bounded(&tready[sl], (seg >> 2) & 1u, p.status, flags, p.wait_limit_ns);
+        etile[seg & 1u] = (got && !flags[0]) ? tslot[sl] : -1;
+        mbar_arrive(&tfree[sl]);
+      }
+      named_bar_sync(2, 128);
+      const int tile = etile[seg & 1u];
+      if (tile < 0) break;
+      SegInfo s;
+      const int64_t it = static_cast<int64_t>(tile) * p.KB;
+      seg_info(p, it, it + p.KB, s);
+      const uint32_t buf = seg & 1u;
+      (void)mbar_wait_bounded(&acc_full[buf], (seg >> 1) & 1u, p.status, flags, p.wait_limit_ns);
+      named_bar_sync(2, 128);
+      if (flags[0]) break;
+      tc_fence_after();
+      float v[C::NC];
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + buf * 64u * NG;
+#pragma unroll
+      for (int c = 0; c < C::NC / 16; ++c) tmem_ld16(taddr + 16u * c, v + 16 * c);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      float acc[MAXC];
+#pragma unroll
+      for (int j = 0; j < MAXC; ++j) acc[j] = v[j];
+      epilogue_rows<MAXC>(p, s, r, acc, scratch, 2, flags);
+    }
+    for (int64_t it = begin; !p.dyn && it < end; ++seg) {
       SegInfo s;
       seg_info(p, it, end, s);
       const uint32_t buf = seg & 1u;
@@ -378,6 +443,9 @@ cudaError_t launch_t(const CUtensorMap &wmap, const CUtensorMap &xmap, const Eng
 
 cudaError_t launch_engine_tc(int maxc, const CUtensorMap &wmap, const CUtensorMap &xmap,
                              const EngineParams &p, cudaStream_t s) {
+  if (p.dyn && (p.dyn < 0 || p.dyn > 256 || !p.grouped || p.ngrp != 1 || p.defer || p.pair ||
+                p.dyn_ctr == nullptr))
+    return cudaErrorInvalidValue;
   if (p.pair && ((p.ngrp > 1 && maxc != 64) || p.grouped || p.defer || p.mode != MODE_LINEAR ||
                  p.G != 2 * p.T || p.KB % 2 != 0))
     return cudaErrorInvalidValue;

@@ -32,6 +32,11 @@ struct EngineParams {
                      // k-halves of tile t and adds them through distributed shared memory
   int ngrp;          // LINEAR, tensor cores: groups of 64 batch columns sharing each weight
                      // tile (B > 64: up to 4); 1 everywhere else
+  int dyn;           // grouped, tensor cores: whole-tile schedule. Of the launch's tiles,
+                     // CTA w first takes [w*S, (w+1)*S), S = floor(dyn * tiles / (256 * G)),
+                     // then claims the rest one tile at a time from *dyn_ctr. 0: stream-K
+  int *dyn_ctr;      // this launch's claim counter, zero when the launch starts (the gather
+                     // launch before the routed launches clears it)
   int wbox_rows;     // rows per weight TMA box: 128 (one box per tile) or 64 (gate/up)
   const uint8_t *w_base;  // weight matrix (raw pointer, for L2 prefetch)
   long long w_rows;       // rows of the weight matrix (all groups)
@@ -196,17 +201,18 @@ struct LinearFinishParams {
 };
 cudaError_t launch_linear_finish(const LinearFinishParams &f, cudaStream_t s);
 // Validates topk_idx, builds the route map (written to route_map) and gathers in one
-// launch of at most max_ctas CTAs.
+// launch of at most max_ctas CTAs. Both gather launches also zero dyn_reset[0..3] (the
+// whole-tile claim counters of the routed launches after them), unless it is nullptr.
 cudaError_t launch_gather_map(const uint16_t *X, const int32_t *topk_idx, int B, int topk, int E,
                               int K, uint16_t *Xg, int32_t *route_map, unsigned *status,
-                              int max_ctas, cudaStream_t s);
+                              int max_ctas, int *dyn_reset, cudaStream_t s);
 cudaError_t launch_comm_wait(uint64_t ns, cudaStream_t s);
 // Read-stream measurement: `ctas` CTAs, each reading per_cta bytes (a multiple of 16 KB)
 // of p into shared memory (moe_aux.cu).
 cudaError_t launch_read_stream(const void *p, size_t per_cta, int ctas, unsigned *status,
                                uint64_t limit_ns, cudaStream_t s);
 cudaError_t launch_gather_rows(const uint16_t *X, const int32_t *route_map, int B, int topk,
-                               int E, int K, uint16_t *Xg, cudaStream_t s);
+                               int E, int K, uint16_t *Xg, int *dyn_reset, cudaStream_t s);
 cudaError_t launch_combine(const float *topk_w, const int32_t *route_map, const float *Yp,
                            const float *S, int B, int topk, int E, int H, uint16_t *Y,
                            cudaStream_t s);
