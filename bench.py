@@ -335,9 +335,9 @@ def time_graph(torch, g, reps):
 # ------------------------------------------------------- prefetch scenario ----
 
 PF_WAIT_US = 20.0
-# DRAM bytes / algorithmic bytes of one expert-layer call (ncu, 32-expert bank, B = 64),
-# with tile-packed banks and with row-major ones
-EXPERTS_TRAFFIC_RATIO = {True: 1.0117, False: 1.0126}
+# DRAM bytes / algorithmic bytes of one expert-layer call (ncu, 32-expert bank, B = 64,
+# whole-tile schedule of the routed launches), with tile-packed banks and with row-major ones
+EXPERTS_TRAFFIC_RATIO = {True: 1.0115, False: 1.0115}
 
 
 def prefetch_scenario(torch, ssd, wl, batches, reps):
