@@ -266,7 +266,9 @@ class Workload:
         self.ssd.moe_experts(d["x_moe"][v], d["idx"][v], d["w"][v], d["rm"][v], self.Wgu, self.Wd,
                              self.Wgs, self.Wds, d["y_moe"], d["ws_e"], side_stream=self.side,
                              packed=self.packed)
-        self.launches += 6  # gather, shared gate/up + down, routed gate/up + down, combine
+        # gather, shared gate/up + down, routed gate/up + down in one launch (two with
+        # DEC_EXPERT_ONE_LAUNCH=0), combine
+        self.launches += 5 if os.environ.get("DEC_EXPERT_ONE_LAUNCH", "1") != "0" else 6
 
     def op_layer(self, B, v=0):
         """moe_layer: the front end runs while the shared expert streams its weights on the
@@ -277,7 +279,8 @@ class Workload:
                            self.Wgs, self.Wds, d["lat"][v], d["idx"][v], d["w"][v], d["y_moe"],
                            d["ws_l"], route_map=d["rm"][v], side_stream=self.side,
                            packed=self.packed)
-        self.launches += 7  # one-launch front end, gather, 4 expert GEMVs, combine
+        # one-launch front end, gather, shared gate/up + down, routed experts, combine
+        self.launches += 6 if os.environ.get("DEC_EXPERT_ONE_LAUNCH", "1") != "0" else 7
 
     def op_moe(self, B):
         if self.layer:

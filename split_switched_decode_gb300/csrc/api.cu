@@ -316,6 +316,13 @@ double expert_dyn_min_tiles() {
   return 6.5;
 }
 
+// Routed gate/up and down in one launch (tensor cores; DEC_EXPERT_ONE_LAUNCH=0: two
+// launches, whole-tile or stream-K as above).
+bool expert_one_launch() {
+  if (const char *s = std::getenv("DEC_EXPERT_ONE_LAUNCH")) return std::atoi(s) != 0;
+  return true;
+}
+
 // Whether grouped launches whose route map is already complete read it, and issue their
 // first weight loads, before the dependency wait (DEC_EARLY_ROUTE_MAP=0 turns it off).
 bool early_route_map() {
@@ -414,8 +421,8 @@ dec_status run_splitk_rows(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 
   p.R = R;
   p.vec_y = (N % 8 == 0 && aligned16(Y) && (R == nullptr || aligned16(R))) ? 1 : 0;
   p.packed = packed ? 1 : 0;
-  // the optional L2 prefetch of later k-blocks walks row-major rows
-  p.w_base = packed ? nullptr : reinterpret_cast<const uint8_t *>(W);
+  // the optional L2 prefetch of later k-blocks (row-major rows or packed blocks)
+  p.w_base = reinterpret_cast<const uint8_t *>(W);
   p.w_rows = N;
   // Every tile split into exactly two k-halves (G = 2 T, KB even): on tensor cores the
   // two workers of a tile run as a 2-CTA cluster and add their halves through
@@ -639,8 +646,8 @@ bool plan_experts(int B, int E, int topk, int H, int I, int num_sms, ExpertsPlan
   o += align_up(static_cast<size_t>(tmax) * sizeof(int));
   ep->cmb_off = o;  // fused combine: one arrival counter per (token, 128-row block of H)
   o += align_up(static_cast<size_t>(B) * ep->Td * sizeof(int));
-  ep->dyn_off = o;  // whole-tile schedule: claim counters of routed gate/up and down
-  o += align_up(4 * sizeof(int));
+  ep->dyn_off = o;  // routed launches: claim counters [4], then one ready count per expert
+  o += align_up((4 + static_cast<size_t>(E)) * sizeof(int));
   ep->total = o;
   return true;
 }
@@ -1316,9 +1323,9 @@ dec_status moe_experts_impl(const dec_bf16 *X, const int32_t *topk_idx, const fl
   // ---- routed experts, main stream
   // without a route map the gather launch validates topk_idx and builds it
   int *dyn_ctr = reinterpret_cast<int *>(wsb + ep.dyn_off);
-  ce = have_map ? launch_gather_rows(X, rm, B, topk, E, H, Xg, dyn_ctr, ms)
+  ce = have_map ? launch_gather_rows(X, rm, B, topk, E, H, Xg, dyn_ctr, 4 + E, ms)
                 : launch_gather_map(X, topk_idx, B, topk, E, H, Xg, rm, d->status,
-                                    2 * d->num_sms, dyn_ctr, ms);
+                                    2 * d->num_sms, dyn_ctr, 4 + E, ms);
   if (ce != cudaSuccess) return DEC_ERR_CUDA;
   {
     EngineParams p;
@@ -1329,6 +1336,28 @@ dec_status moe_experts_impl(const dec_bf16 *X, const int32_t *topk_idx, const fl
     // gate/up launch start; so when the map is not the gather's own output, it is
     // complete before gate/up starts, and likewise before down starts: both may then
     // read it, and issue their first weight loads, before their dependency wait.
+    if (tc && expert_one_launch()) {
+      // gate/up and down in one launch: whole tiles claimed at run time, each down tile
+      // after its expert's gate/up tiles have stored A
+      EngineParams p2;
+      base(p, MODE_GATEUP, I, H, ep.Tg, ep.KBg, g_main, 1, ep.main_part_off, ep.main_cnt_off);
+      p.w_group_rows = 2 * I;
+      p.up_row_off = I;
+      p.A = A;
+      p.rm_ready = (have_map && early_route_map()) ? 1 : 0;
+      p.dyn_ctr = dyn_ctr;
+      p.ready = dyn_ctr + 4;
+      p.w_base = packed ? reinterpret_cast<const uint8_t *>(Wgu) : nullptr;
+      base(p2, MODE_DOWN, H, I, ep.Td, ep.KBd, g_main, 1, ep.main_part_off, ep.main_cnt_off);
+      p2.w_group_rows = H;
+      p2.Yp = Yp;
+      if (fused) set_combine(p2);
+      p2.rm_ready = p.rm_ready;
+      p2.w_base = packed ? reinterpret_cast<const uint8_t *>(Wd) : nullptr;
+      if ((ce = launch_engine_tc_moe(ep.maxc, m_wgu, m_xg, m_wd, m_a, p, p2, ms)) !=
+          cudaSuccess)
+        return DEC_ERR_CUDA;
+    } else {
     // Whole-tile schedule once the CTAs expect enough tiles each that the last claims
     // even out the SMs' different read rates (tiles per CTA from the expected number of
     // distinct experts; with fewer, whole tiles are too coarse and stream-K ranges win).
@@ -1354,6 +1383,7 @@ dec_status moe_experts_impl(const dec_bf16 *X, const int32_t *topk_idx, const fl
       p.dyn_ctr = dyn_ctr + 1;
     }
     if ((ce = engine(m_wd, m_a, p, ms)) != cudaSuccess) return DEC_ERR_CUDA;
+    }
   }
   // Y is complete once both streams are done: the main stream waits for the side one
   if (overlap && (ce = cudaStreamWaitEvent(ms, ev->join, 0)) != cudaSuccess) return DEC_ERR_CUDA;

@@ -213,6 +213,46 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int *p, int v) {
   return old;
 }
 
+// GPU-scope release add without a return value: issued by one thread after a CTA
+// barrier, it publishes every write the CTA made before the barrier.
+__device__ __forceinline__ void red_add_release_gpu(int *p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Orders this thread's generic-proxy accesses to global memory with its async-proxy
+// ones (TMA): data written by ordinary stores and then read by cp.async.bulk.tensor.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Wait until *cnt >= target (GPU-scope acquire), for at most limit_ns; on time-out the
+// same as mbar_wait_bounded.
+__device__ __forceinline__ bool wait_count_bounded(const int *cnt, int target, unsigned *status,
+                                                   volatile int *abort_flag,
+                                                   uint64_t limit_ns) {
+  if (ld_acquire_gpu(cnt) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 8; ++i) {
+      __nanosleep(64);
+      if (ld_acquire_gpu(cnt) >= target) return true;
+    }
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      atomicOr(status, ST_TIMEOUT);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
 // ------------------------------------------------ programmatic dependent launch ----
 // griddep_wait: block until the previous kernel of the stream has completed and its
 // writes are visible (a no-op when the launch was not programmatic). Everything that

@@ -130,6 +130,14 @@ __device__ __forceinline__ void prefetch_weights_l2(const EngineParams &p, int64
   int64_t it = begin + skip;
   int64_t stop = it + p.l2pf_kb;
   if (stop > end) stop = end;
+  if (p.packed) {  // tile-packed W: each k-block of a segment is one contiguous 16 KB block
+    for (int64_t i = it + lane; i < stop; i += 32) {
+      SegInfo s;
+      seg_info(p, i, i + 1, s);
+      prefetch_l2_bulk(p.w_base + static_cast<long long>(s.pblk + s.kb0) * 16384, 16384u);
+    }
+    return;
+  }
   while (it < stop) {
     SegInfo s;
     seg_info(p, it, stop, s);

@@ -56,6 +56,40 @@ struct TCConfig {
   static_assert(STAGES >= 4, "pipeline too shallow");
 };
 
+// MMA issuer (one thread): one segment's k-blocks into accumulator buffer seg % 2,
+// 4 x tcgen05.mma (M128 x N x K16) per k-block; each stage is released by a commit once
+// its MMAs have read it, and the accumulator by a commit after the last. False after a
+// time-out.
+template <int STAGES, int STAGE_BYTES, int NG>
+__device__ __forceinline__ bool mma_segment(const SegInfo &s, uint32_t seg, uint32_t &q,
+                                            uint32_t tmem_base, uint8_t *stage_mem,
+                                            uint64_t *full, uint64_t *empty, uint64_t *acc_full,
+                                            uint64_t *acc_empty, const EngineParams &p,
+                                            volatile int *flags) {
+  const uint32_t idesc = idesc_bf16(16 * seg_xboxes(s));
+  const uint32_t buf = seg & 1u;
+  if (!mbar_wait_bounded(&acc_empty[buf], ((seg >> 1) & 1u) ^ 1u, p.status, flags,
+                         p.wait_limit_ns))
+    return false;
+  tc_fence_after();
+  const uint32_t d_tmem = tmem_base + buf * 64u * NG;
+  for (int kb = s.kb0; kb < s.kb1; ++kb, ++q) {
+    const int st = static_cast<int>(q % STAGES);
+    if (!mbar_wait_bounded(&full[st], (q / STAGES) & 1u, p.status, flags, p.wait_limit_ns))
+      return false;
+    tc_fence_after();
+    const uint32_t a_addr = smem_u32(stage_mem + st * STAGE_BYTES);
+    const uint64_t adesc = sw128_desc(a_addr);
+    const uint64_t bdesc = sw128_desc(a_addr + 16384u);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)  // K = 16 per MMA: +32 bytes along the swizzled row
+      tc_mma(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc, (kb > s.kb0 || kk > 0) ? 1u : 0u);
+    tc_commit(&empty[st]);  // the stage is free once these MMAs have read it
+  }
+  tc_commit(&acc_full[buf]);  // accumulator ready for the epilogue
+  return true;
+}
+
 template <int MAXC, int NG>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     engine_tc_kernel(const __grid_constant__ CUtensorMap wmap,
@@ -143,33 +177,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (lane == 0) {
       uint32_t q = 0;
       bool ok = true;
-      // one segment's k-blocks into accumulator buffer seg % 2; false after a time-out
-      auto mma_segment = [&](const SegInfo &s, uint32_t seg) -> bool {
-        const uint32_t idesc = idesc_bf16(16 * seg_xboxes(s));
-        const uint32_t buf = seg & 1u;
-        if (!mbar_wait_bounded(&acc_empty[buf], ((seg >> 1) & 1u) ^ 1u, p.status, flags,
-                               p.wait_limit_ns))
-          return false;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + buf * 64u * NG;
-        for (int kb = s.kb0; kb < s.kb1; ++kb, ++q) {
-          const int st = static_cast<int>(q % C::STAGES);
-          if (!mbar_wait_bounded(&full[st], (q / C::STAGES) & 1u, p.status, flags,
-                                 p.wait_limit_ns))
-            return false;
-          tc_fence_after();
-          const uint32_t a_addr = smem_u32(stage_mem + st * C::STAGE_BYTES);
-          const uint64_t adesc = sw128_desc(a_addr);
-          const uint64_t bdesc = sw128_desc(a_addr + 16384u);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)  // K = 16 per MMA: +32 bytes along the swizzled row
-            tc_mma(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc,
-                   (kb > s.kb0 || kk > 0) ? 1u : 0u);
-          tc_commit(&empty[st]);  // the stage is free once these MMAs have read it
-        }
-        tc_commit(&acc_full[buf]);  // accumulator ready for the epilogue
-        return true;
-      };
       if (p.dyn) {
         for (uint32_t seg = 0; ok; ++seg) {
           const int sl = static_cast<int>(seg & 3u);
@@ -181,14 +188,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           SegInfo s;
           const int64_t it = static_cast<int64_t>(tile) * p.KB;
           seg_info(p, it, it + p.KB, s);
-          ok = mma_segment(s, seg);
+          ok = mma_segment<C::STAGES, C::STAGE_BYTES, NG>(s, seg, q, tmem_base, stage_mem, full,
+                                                       empty, acc_full, acc_empty, p, flags);
         }
       } else {
         uint32_t seg = 0;
         for (int64_t it = begin; it < end && ok; ++seg) {
           SegInfo s;
           seg_info(p, it, end, s);
-          ok = mma_segment(s, seg);
+          ok = mma_segment<C::STAGES, C::STAGE_BYTES, NG>(s, seg, q, tmem_base, stage_mem, full,
+                                                       empty, acc_full, acc_empty, p, flags);
           it += s.kb1 - s.kb0;
         }
       }
@@ -204,16 +213,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int r = 32 * (warp & 3) + lane;  // tile row == tensor-memory lane
     uint32_t seg = 0;
     // whole-tile schedule (grouped launches: one column group, no pair): thread 0 takes
-    // each segment's tile from the producer's slot and hands it to the other 127 threads
-    // through etile across the barrier; every segment is a whole tile, so there is no
-    // reduction
+    // each segment's tile from the producer's slot, waits for its accumulator and hands
+    // the tile to the other 127 threads through etile across the barrier (so all take
+    // the same branches); every segment is a whole tile, so there is no reduction
     for (; p.dyn; ++seg) {
       const int sl = static_cast<int>(seg & 3u);
+      const uint32_t buf = seg & 1u;
       if (r == 0) {
         const bool got =
             mbar_wait_bounded(&tready[sl], (seg >> 2) & 1u, p.status, flags, p.wait_limit_ns);
-        etile[seg & 1u] = (got && !flags[0]) ? tslot[sl] : -1;
+        int t = (got && !flags[0]) ? tslot[sl] : -1;
         mbar_arrive(&tfree[sl]);
+        if (t >= 0 && (!mbar_wait_bounded(&acc_full[buf], (seg >> 1) & 1u, p.status, flags,
+                                          p.wait_limit_ns) ||
+                       flags[0]))
+          t = -1;
+        etile[seg & 1u] = t;
       }
       named_bar_sync(2, 128);
       const int tile = etile[seg & 1u];
@@ -221,10 +236,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       SegInfo s;
       const int64_t it = static_cast<int64_t>(tile) * p.KB;
       seg_info(p, it, it + p.KB, s);
-      const uint32_t buf = seg & 1u;
-      (void)mbar_wait_bounded(&acc_full[buf], (seg >> 1) & 1u, p.status, flags, p.wait_limit_ns);
-      named_bar_sync(2, 128);
-      if (flags[0]) break;
       tc_fence_after();
       float v[C::NC];
       const uint32_t taddr =
@@ -439,6 +450,309 @@ cudaError_t launch_t(const CUtensorMap &wmap, const CUtensorMap &xmap, const Eng
                     xmap, p);
 }
 
+// ---------------------------------------------------------------------------
+// Routed experts in one launch. Tiles are numbered gate/up first (used expert g, tile
+// t: g*T1 + t), then down (n1 + g*T2 + t), and every CTA claims them one at a time from
+// one counter, each a whole tile over all of its k-blocks (no partial tiles, no
+// reduction). A down tile reads its expert's A, which the expert's T1 gate/up tiles
+// write: each gate/up tile, once its rows of A are stored, adds one to the expert's
+// ready count (release), and the producer loads a down tile's A only after an acquire
+// read sees all T1 (then a proxy fence, since TMA reads what ordinary stores wrote); once
+// it sees every gate/up tile of the launch done (a second count), one fence covers all of
+// its later down tiles. No down tile is claimed before the last gate/up tile, and every
+// claimed tile is held by a running CTA, so a wait only ever depends on CTAs that are
+// running. While it waits, the producer has the down tile's first weight blocks pulled
+// into L2.
+// Weight and activation loads of one whole tile (local index t of its phase) into the
+// stage ring; claims the next tile STAGES k-blocks before the end. False after a time-out.
+template <int STAGES, int STAGE_BYTES>
+__device__ __forceinline__ bool moe_tile_loads(const EngineParams &p, const CUtensorMap *wmap,
+                                               const CUtensorMap *xmap, int t, uint8_t *stage_mem,
+                                               uint64_t *full, uint64_t *empty,
+                                               volatile int *flags, uint32_t &q, int &ahead,
+                                               int *ctr, uint64_t pol) {
+  SegInfo s;
+  const int64_t it = static_cast<int64_t>(t) * p.KB;
+  seg_info(p, it, it + p.KB, s);
+  const int nxb = (16 * seg_xboxes(s) + p.xbox_rows - 1) / p.xbox_rows;
+  const uint32_t bytes = stage_tx_bytes(p, s);
+  const int claim_kb = p.KB > STAGES ? p.KB - STAGES : 0;
+  for (int kb = 0; kb < p.KB; ++kb, ++q) {
+    if (kb == claim_kb) ahead = atomicAdd(ctr, 1);
+    const int st = static_cast<int>(q % STAGES);
+    uint8_t *dst = stage_mem + st * STAGE_BYTES;
+    const uint32_t par = ((q / STAGES) & 1u) ^ 1u;
+    if (!mbar_wait_bounded(&empty[st], par, p.status, flags, p.wait_limit_ns)) return false;
+    mbar_arrive_expect_tx(&full[st], bytes);
+    load_weights(p, s, wmap, dst, &full[st], kb, pol);
+    for (int i = 0; i < nxb; ++i)
+      tma_load_2d(dst + 16384 + i * p.xbox_rows * 128, xmap, &full[st], kb * TILE_K,
+                  s.xrow0 + p.xbox_rows * i);
+  }
+  return true;
+}
+
+template <int STAGES, int STAGE_BYTES>
+__device__ __forceinline__ void moe_produce(const EngineParams &p1, const EngineParams &p2,
+                                            const CUtensorMap *wmap1, const CUtensorMap *xmap1,
+                                            const CUtensorMap *wmap2, const CUtensorMap *xmap2,
+                                            uint8_t *stage_mem, uint64_t *full, uint64_t *empty,
+                                            volatile int *tslot, uint64_t *tready,
+                                            uint64_t *tfree, volatile int *flags, int n1,
+                                            int ntot) {
+  prefetch_tensormap(wmap1);
+  prefetch_tensormap(xmap1);
+  prefetch_tensormap(wmap2);
+  prefetch_tensormap(xmap2);
+  const uint64_t pol = policy_evict_first();
+  // Before the dependency wait: the first claims go to about the first G gate/up tiles,
+  // so pull the first weight blocks of tile blockIdx.x into L2 (writes nothing; packed
+  // banks: one bulk prefetch per 16 KB block).
+  if (p1.rm_ready && p1.packed && p1.w_base != nullptr && static_cast<int>(blockIdx.x) < n1) {
+    SegInfo s;
+    const int64_t it = static_cast<int64_t>(blockIdx.x) * p1.KB;
+    seg_info(p1, it, it + p1.KB, s);
+    for (int kb = 0; kb < STAGES && kb < p1.KB; ++kb)
+      prefetch_l2_bulk(p1.w_base + static_cast<long long>(s.pblk + kb) * 16384, 16384u);
+  }
+  griddep_wait();
+  const int *gu_done = p1.dyn_ctr + 1;  // gate/up tiles whose rows of A are stored
+  uint32_t q = 0;
+  bool ok = true;
+  bool all_ready = false;  // every expert's A seen complete (and fenced) by this thread
+  int ahead = -1;  // the next tile, claimed STAGES k-blocks before the current one ends
+  for (uint32_t seg = 0;; ++seg) {
+    int t = ahead;
+    if (t < 0) t = ok ? atomicAdd(p1.dyn_ctr, 1) : ntot;
+    ahead = -1;
+    int tile = (ok && t < ntot) ? t : -1;
+    const int sl = static_cast<int>(seg & 3u);
+    if (tile >= n1 && !all_ready) {  // a down tile: its expert's A must be complete
+      const int g = (tile - n1) / p2.T;
+      if (ld_acquire_gpu(gu_done) >= n1)
+        all_ready = true;  // then one proxy fence covers every later down tile
+      else if (ld_acquire_gpu(p1.ready + g) < p1.T) {
+        if (p2.packed && p2.w_base != nullptr) {
+          SegInfo s;
+          const int64_t it = static_cast<int64_t>(tile - n1) * p2.KB;
+          seg_info(p2, it, it + p2.KB, s);
+          for (int kb = 0; kb < STAGES && kb < p2.KB; ++kb)
+            prefetch_l2_bulk(p2.w_base + static_cast<long long>(s.pblk + kb) * 16384, 16384u);
+        }
+        if (!wait_count_bounded(p1.ready + g, p1.T, p1.status, flags, p1.wait_limit_ns)) {
+          ok = false;
+          tile = -1;
+        }
+      }
+      fence_proxy_async_global();
+    }
+    if (ok && !mbar_wait_bounded(&tfree[sl], ((seg >> 2) & 1u) ^ 1u, p1.status, flags,
+                                 p1.wait_limit_ns)) {
+      ok = false;
+      tile = -1;
+    }
+    tslot[sl] = tile;
+    mbar_arrive(&tready[sl]);
+    if (tile < 0) break;
+    // the phases' parameters and tensor maps stay compile-time operands in each branch
+    ok = tile >= n1
+             ? moe_tile_loads<STAGES, STAGE_BYTES>(p2, wmap2, xmap2, tile - n1, stage_mem, full,
+                                                   empty, flags, q, ahead, p1.dyn_ctr, pol)
+             : moe_tile_loads<STAGES, STAGE_BYTES>(p1, wmap1, xmap1, tile, stage_mem, full,
+                                                   empty, flags, q, ahead, p1.dyn_ctr, pol);
+  }
+  griddep_launch_dependents();
+  if (flags[0]) {
+    // after a time-out: let this CTA's copies still in flight land before it exits
+    const uint32_t q0 = q > STAGES ? q - STAGES : 0u;
+    for (uint32_t qq = q0; qq < q; ++qq)
+      (void)mbar_wait_drain(&full[qq % STAGES], (qq / STAGES) & 1u, 10000000ull);
+  }
+}
+
+template <int MAXC>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    engine_tc_moe_kernel(const __grid_constant__ CUtensorMap wmap1,
+                         const __grid_constant__ CUtensorMap xmap1,
+                         const __grid_constant__ CUtensorMap wmap2,
+                         const __grid_constant__ CUtensorMap xmap2, const EngineParams p1,
+                         const EngineParams p2) {
+  using C = TCConfig<MAXC, 1>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t *stage_mem = smem;
+  float *scratch = reinterpret_cast<float *>(smem + C::STAGES * C::STAGE_BYTES);
+  uint8_t *tail = smem + C::STAGES * C::STAGE_BYTES + C::SCRATCH_BYTES;
+  uint64_t *full = reinterpret_cast<uint64_t *>(tail);
+  uint64_t *empty = full + C::STAGES;
+  uint64_t *acc_full = empty + C::STAGES;   // [2]
+  uint64_t *acc_empty = acc_full + 2;       // [2]
+  uint64_t *drain = acc_empty + 2;          // [1]
+  uint64_t *tready = drain + 1;             // [4]
+  uint64_t *tfree = tready + 4;             // [4]
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tfree + 4);
+  volatile int *flags = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  volatile int *tslot = flags + 3;          // [4]
+  volatile int *etile = tslot + 4;          // [2]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // the route map picks the experts: read it now only if it was complete before the
+  // previous kernel of the stream started
+  if (!p1.rm_ready) griddep_wait();
+  const int U = rm_num_used(p1);
+  const int n1 = U * p1.T;
+  const int ntot = n1 + U * p2.T;
+
+  if (tid == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    mbar_init(drain, 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&tready[i], 1);
+      mbar_init(&tfree[i], 2);  // the MMA issuer and epilogue thread 0
+    }
+    flags[0] = 0;
+    flags[1] = 0;
+    flags[2] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0)
+      moe_produce<C::STAGES, C::STAGE_BYTES>(p1, p2, &wmap1, &xmap1, &wmap2, &xmap2, stage_mem,
+                                             full, empty, tslot, tready, tfree, flags, n1, ntot);
+    else
+      griddep_wait();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA issuer
+    griddep_wait();
+    if (lane == 0) {
+      uint32_t q = 0;
+      bool ok = true;
+      for (uint32_t seg = 0; ok; ++seg) {
+        const int sl = static_cast<int>(seg & 3u);
+        if (!mbar_wait_bounded(&tready[sl], (seg >> 2) & 1u, p1.status, flags, p1.wait_limit_ns))
+          break;
+        const int tile = tslot[sl];
+        mbar_arrive(&tfree[sl]);
+        if (tile < 0) break;
+        SegInfo s;
+        if (tile >= n1) {
+          const int64_t it = static_cast<int64_t>(tile - n1) * p2.KB;
+          seg_info(p2, it, it + p2.KB, s);
+        } else {
+          const int64_t it = static_cast<int64_t>(tile) * p1.KB;
+          seg_info(p1, it, it + p1.KB, s);
+        }
+        ok = mma_segment<C::STAGES, C::STAGE_BYTES, 1>(s, seg, q, tmem_base, stage_mem, full,
+                                                      empty, acc_full, acc_empty, p1, flags);
+      }
+      if (flags[0]) {  // let every MMA issued so far finish before the memory is freed
+        tc_commit(drain);
+        (void)mbar_wait_drain(drain, 0u, 10000000ull);
+      }
+    }
+  } else {
+    // --------------------------------------------------------------- epilogue
+    griddep_wait();
+    const int r = 32 * (warp & 3) + lane;  // tile row == tensor-memory lane
+    for (uint32_t seg = 0;; ++seg) {
+      const int sl = static_cast<int>(seg & 3u);
+      const uint32_t buf = seg & 1u;
+      // thread 0 takes the segment's tile from the producer's slot and waits for its
+      // accumulator; the other 127 threads learn both through etile across the barrier,
+      // so every thread takes the same branches around the named barriers below
+      if (r == 0) {
+        const bool got =
+            mbar_wait_bounded(&tready[sl], (seg >> 2) & 1u, p1.status, flags, p1.wait_limit_ns);
+        int t = (got && !flags[0]) ? tslot[sl] : -1;
+        mbar_arrive(&tfree[sl]);
+        if (t >= 0 && (!mbar_wait_bounded(&acc_full[buf], (seg >> 1) & 1u, p1.status, flags,
+                                          p1.wait_limit_ns) ||
+                       flags[0]))
+          t = -1;
+        etile[seg & 1u] = t;
+      }
+      named_bar_sync(2, 128);
+      const int tile = etile[seg & 1u];
+      if (tile < 0) break;
+      const bool down = tile >= n1;
+      SegInfo s;
+      if (down) {
+        const int64_t it = static_cast<int64_t>(tile - n1) * p2.KB;
+        seg_info(p2, it, it + p2.KB, s);
+      } else {
+        const int64_t it = static_cast<int64_t>(tile) * p1.KB;
+        seg_info(p1, it, it + p1.KB, s);
+      }
+      tc_fence_after();
+      float v[C::NC];
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + buf * 64u;
+#pragma unroll
+      for (int c = 0; c < C::NC / 16; ++c) tmem_ld16(taddr + 16u * c, v + 16 * c);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      float acc[MAXC];
+#pragma unroll
+      for (int j = 0; j < MAXC; ++j) acc[j] = v[j];
+      if (down) {
+        epilogue_rows<MAXC>(p2, s, r, acc, scratch, 2, flags);
+      } else {
+        epilogue_rows<MAXC>(p1, s, r, acc, scratch, 2, flags);
+        // this tile's rows of A are stored: count them for the expert's down tiles
+        fence_proxy_async_global();
+        named_bar_sync(2, 128);
+        if (r == 0) {
+          red_add_release_gpu(p1.ready + s.gt / p1.T, 1);
+          red_add_release_gpu(p1.dyn_ctr + 1, 1);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+}
+
+template <int MAXC>
+cudaError_t launch_moe_t(const CUtensorMap &wmap1, const CUtensorMap &xmap1,
+                         const CUtensorMap &wmap2, const CUtensorMap &xmap2,
+                         const EngineParams &p1, const EngineParams &p2, cudaStream_t s) {
+  using C = TCConfig<MAXC, 1>;
+  static std::atomic<uint64_t> attr_set{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(attr_set.load() & bit)) {
+    e = cudaFuncSetAttribute(engine_tc_moe_kernel<MAXC>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set.fetch_or(bit);
+  }
+  return launch_pdl(engine_tc_moe_kernel<MAXC>, dim3(p1.G), dim3(TC_THREADS), C::SMEM, s, wmap1,
+                    xmap1, wmap2, xmap2, p1, p2);
+}
+
 }  // namespace
 
 cudaError_t launch_engine_tc(int maxc, const CUtensorMap &wmap, const CUtensorMap &xmap,
@@ -461,6 +775,30 @@ cudaError_t launch_engine_tc(int maxc, const CUtensorMap &wmap, const CUtensorMa
     case 16: return launch_t<16>(wmap, xmap, p, s);
     case 32: return launch_t<32>(wmap, xmap, p, s);
     case 64: return launch_t<64>(wmap, xmap, p, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace ssd
+
+namespace ssd {
+
+cudaError_t launch_engine_tc_moe(int maxc, const CUtensorMap &wmap1, const CUtensorMap &xmap1,
+                                 const CUtensorMap &wmap2, const CUtensorMap &xmap2,
+                                 const EngineParams &p1, const EngineParams &p2,
+                                 cudaStream_t s) {
+  if (!p1.grouped || !p2.grouped || p1.mode != MODE_GATEUP || p2.mode != MODE_DOWN ||
+      p1.dyn_ctr == nullptr || p1.ready == nullptr || p1.ngrp != 1 || p2.ngrp != 1 ||
+      p1.defer || p2.defer || p1.pair || p2.pair || p1.slot_cols != p2.slot_cols ||
+      p1.route_map != p2.route_map || p1.G < 1)
+    return cudaErrorInvalidValue;
+  switch (maxc) {
+    case 2: return launch_moe_t<2>(wmap1, xmap1, wmap2, xmap2, p1, p2, s);
+    case 4: return launch_moe_t<4>(wmap1, xmap1, wmap2, xmap2, p1, p2, s);
+    case 8: return launch_moe_t<8>(wmap1, xmap1, wmap2, xmap2, p1, p2, s);
+    case 16: return launch_moe_t<16>(wmap1, xmap1, wmap2, xmap2, p1, p2, s);
+    case 32: return launch_moe_t<32>(wmap1, xmap1, wmap2, xmap2, p1, p2, s);
+    case 64: return launch_moe_t<64>(wmap1, xmap1, wmap2, xmap2, p1, p2, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -49,11 +49,12 @@ __global__ void __launch_bounds__(256) gather_map_kernel(const uint16_t *X,
                                                          const int32_t *topk_idx, int B,
                                                          int topk, int E, int K, uint16_t *Xg,
                                                          int32_t *rm, unsigned *status,
-                                                         int *dyn_reset) {
+                                                         int *dyn_reset, int nreset) {
   griddep_wait();
   griddep_launch_dependents();
-  // the claim counters of the routed launches that follow (whole-tile schedule)
-  if (dyn_reset != nullptr && blockIdx.x == 0 && threadIdx.x < 4) dyn_reset[threadIdx.x] = 0;
+  // the claim and ready counters of the routed launches that follow
+  if (dyn_reset != nullptr && blockIdx.x == 0)
+    for (int i = threadIdx.x; i < nreset; i += 256) dyn_reset[i] = 0;
   __shared__ int32_t sidx[MAX_B * MAX_TOPK];
   __shared__ unsigned long long smask[MAX_E];
   __shared__ int soff[MAX_E];
@@ -279,11 +280,13 @@ __global__ void __launch_bounds__(128) linear_finish_kernel(const LinearFinishPa
 // in expert order, so each expert's rows are contiguous for the TMA tile loads.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t *X, const int32_t *rm,
                                                           int B, int topk, int E, int K,
-                                                          uint16_t *Xg, int *dyn_reset) {
+                                                          uint16_t *Xg, int *dyn_reset,
+                                                          int nreset) {
   griddep_wait();
   griddep_launch_dependents();
-  // the claim counters of the routed launches that follow (whole-tile schedule)
-  if (dyn_reset != nullptr && blockIdx.x == 0 && threadIdx.x < 4) dyn_reset[threadIdx.x] = 0;
+  // the claim and ready counters of the routed launches that follow
+  if (dyn_reset != nullptr && blockIdx.x == 0)
+    for (int i = threadIdx.x; i < nreset; i += 256) dyn_reset[i] = 0;
   const int P = B * topk;
   const int32_t *pairs = rm + 2 * E + 1;
   const int chunks = K / 8;  // 16-byte chunks per row
@@ -477,22 +480,23 @@ cudaError_t launch_linear_finish(const LinearFinishParams &f, cudaStream_t s) {
 
 cudaError_t launch_gather_map(const uint16_t *X, const int32_t *topk_idx, int B, int topk, int E,
                               int K, uint16_t *Xg, int32_t *route_map, unsigned *status,
-                              int max_ctas, int *dyn_reset, cudaStream_t s) {
+                              int max_ctas, int *dyn_reset, int nreset, cudaStream_t s) {
   const int64_t n = static_cast<int64_t>(B) * topk * (K / 8);
   int64_t need = (n + 1023) / 1024;  // 256 threads x 4 chunks per CTA and sweep
   int grid = static_cast<int>(need < max_ctas ? need : max_ctas);
   if (grid < 1) grid = 1;
   return launch_pdl(gather_map_kernel, dim3(grid), dim3(256), 0, s, X, topk_idx, B, topk, E, K,
-                    Xg, route_map, status, dyn_reset);
+                    Xg, route_map, status, dyn_reset, nreset);
 }
 
 cudaError_t launch_gather_rows(const uint16_t *X, const int32_t *route_map, int B, int topk,
-                               int E, int K, uint16_t *Xg, int *dyn_reset, cudaStream_t s) {
+                               int E, int K, uint16_t *Xg, int *dyn_reset, int nreset,
+                               cudaStream_t s) {
   const int64_t n = static_cast<int64_t>(B) * topk * (K / 8);
   int grid = static_cast<int>((n + 255) / 256);
   if (grid > 1024) grid = 1024;
   return launch_pdl(gather_rows_kernel, dim3(grid), dim3(256), 0, s, X, route_map, B, topk, E, K,
-                    Xg, dyn_reset);
+                    Xg, dyn_reset, nreset);
 }
 
 cudaError_t launch_combine(const float *topk_w, const int32_t *route_map, const float *Yp,

@@ -1,13 +1,15 @@
-"""GPU parity of the whole-tile schedule of the routed-expert launches, through the C ABI.
+"""GPU parity of the schedules of the routed-expert launches, through the C ABI.
 
-In this schedule every tile of the grouped gate/up and down launches is computed by one
-CTA over all of its k-blocks: each CTA first streams a static share of the tiles, then
-claims the remaining tiles one at a time from a counter that the gather launch clears
-before every call. Checked here: agreement with the fp64 oracle; bit-identical outputs
-whatever the static share, the number of CTAs (side-stream cap), the layout of the banks
-and the route-map source, since every output is accumulated in the same k order
-whichever CTA computes it; the counters starting from zero on every call that reuses a
-workspace; the fused combine; an invalid routing reported, not faulted.
+One launch (the default on tensor cores): every gate/up and down tile claimed at run
+time from one counter, whole tiles only, each down tile loading its expert's A once that
+expert's gate/up tiles have published it. Two launches with the whole-tile schedule: each
+CTA streams a static share of the tiles, then claims the rest one at a time. Both
+compute every tile over all of its k-blocks in one CTA, so they give the same bits as
+each other whatever the claims, the static share, the number of CTAs (side-stream cap),
+the layout of the banks or the route-map source. Checked here: agreement with the fp64
+oracle; those equalities; the counters (cleared by the gather launch) starting from zero
+on every call that reuses a workspace; the fused combine; an invalid routing reported,
+not faulted.
 """
 import numpy as np
 import pytest
@@ -32,12 +34,20 @@ def env():
     return torch, ssd, oracle, dev
 
 
-@pytest.fixture
-def whole_tiles(monkeypatch):
-    """The whole-tile schedule at every batch size (by default only from about 12
-    expected tiles per CTA)."""
-    monkeypatch.setenv("DEC_EXPERT_DYN_MIN_TILES", "0")
+SCHEDULES = {
+    # gate/up and down in one launch (the default)
+    "one_launch": {"DEC_EXPERT_ONE_LAUNCH": "1"},
+    # two launches, whole tiles at every batch size (by default from 6.5 tiles per CTA)
+    "two_launch_whole_tiles": {"DEC_EXPERT_ONE_LAUNCH": "0", "DEC_EXPERT_DYN_MIN_TILES": "0"},
+}
+
+
+@pytest.fixture(params=sorted(SCHEDULES))
+def whole_tiles(request, monkeypatch):
     monkeypatch.delenv("DEC_EXPERT_DYN", raising=False)
+    for k, v in SCHEDULES[request.param].items():
+        monkeypatch.setenv(k, v)
+    monkeypatch.schedule = request.param
     return monkeypatch
 
 
@@ -113,18 +123,22 @@ def test_whole_tile_schedule_matches_oracle(env, whole_tiles, B, k, shared, side
 
 @pytest.mark.parametrize("B,k", [(5, 3), (33, 8), (64, 8)])
 def test_whole_tile_result_does_not_depend_on_the_schedule(env, whole_tiles, B, k):
-    """Static shares from none (every tile claimed) to all, and different CTA counts for
-    the routed launches (side-stream caps): the same bits every time."""
+    """One launch, and two launches with static shares from none (every tile claimed) to
+    all, each with different CTA counts for the routed launches (side-stream caps): the
+    same bits every time."""
     torch, ssd, oracle, dev = env
     E, H, I = 32, 256, 192
     pb = _problem(env, B, E, H, I, k, 2)
     rm = _host_route_map(oracle, pb["idx_np"], E, dev)
     outs = []
-    for share in ("1", "128", "230", "256"):
-        whole_tiles.setenv("DEC_EXPERT_DYN", share)
-        for cap in (0, 7, 60):
-            outs.append(_run(env, pb["X"], pb["idx"], pb["w"], pb["Wgu"], pb["Wd"], pb["Wgs"],
-                             pb["Wds"], rm=rm, side=True, side_ctas=cap))
+    for one in ("1", "0"):
+        whole_tiles.setenv("DEC_EXPERT_ONE_LAUNCH", one)
+        whole_tiles.setenv("DEC_EXPERT_DYN_MIN_TILES", "0")
+        for share in (("230",) if one == "1" else ("1", "128", "230", "256")):
+            whole_tiles.setenv("DEC_EXPERT_DYN", share)
+            for cap in (0, 7, 60):
+                outs.append(_run(env, pb["X"], pb["idx"], pb["w"], pb["Wgu"], pb["Wd"],
+                                 pb["Wgs"], pb["Wds"], rm=rm, side=True, side_ctas=cap))
     for Y in outs[1:]:
         assert torch.equal(outs[0], Y)
     assert_close(to_f64(oracle, outs[0]), _oracle_y(env, pb), f"schedule-independent B={B}")
@@ -162,6 +176,7 @@ def test_whole_tile_equals_packed_and_stream_k_within_tolerance(env, whole_tiles
     Y0 = _run(env, pb["X"], pb["idx"], pb["w"], pb["Wgu"], pb["Wd"], pb["Wgs"], pb["Wds"])
     Y1 = _run(env, pb["X"], pb["idx"], pb["w"], Pgu, Pd, Pgs[0], Pds[0], packed=True)
     assert torch.equal(Y0, Y1)
+    whole_tiles.setenv("DEC_EXPERT_ONE_LAUNCH", "0")
     whole_tiles.setenv("DEC_EXPERT_DYN", "0")
     Y2 = _run(env, pb["X"], pb["idx"], pb["w"], pb["Wgu"], pb["Wd"], pb["Wgs"], pb["Wds"])
     y = _oracle_y(env, pb)

@@ -675,6 +675,26 @@ def test_prefetch_during_communication_phase_keeps_results(env, B):
     assert 1.9 <= a.elapsed_time(b) <= 50.0  # ms: the 2 ms phase ends on time
 
 
+@pytest.mark.parametrize("B", [1, 8, 64])
+def test_moe_experts_one_launch_equals_two_launches_full_size(env, big_layer, monkeypatch, B):
+    """The full-size routed experts in one launch (down tiles waiting for their expert's
+    gate/up tiles) and in two launches on whole tiles compute every tile in the same k
+    order in one CTA: the same bits."""
+    torch, ssd, oracle, dev = env
+    from split_switched_decode_gb300 import inputs
+    g = big_layer
+    E, H, I, L, k = g["E"], g["H"], g["I"], g["L"], 8
+    X = inputs.activations(B, H, dev, 33, "one_launch_x")
+    _, idx, w, _, rm = _run_front(env, X, g["Wc"], E, L, k)
+    outs = []
+    for one in ("1", "0"):
+        monkeypatch.setenv("DEC_EXPERT_ONE_LAUNCH", one)
+        monkeypatch.setenv("DEC_EXPERT_DYN_MIN_TILES", "0")
+        outs.append(_run_experts(env, X, idx, w, g["Wgu"], g["Wd"], g["Wgs"], g["Wds"], rm=rm,
+                                 side=True))
+    assert torch.equal(outs[0], outs[1])
+
+
 def test_invalid_routing_is_reported_not_faulted(env):
     """An out-of-range or repeated expert index passed without a route map is caught by
     the rebuild kernel: empty map, DEC_ERR_INVALID_ARG from dec_sync_status."""

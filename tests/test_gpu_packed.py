@@ -163,3 +163,25 @@ def test_packed_chained_calls_are_deterministic(env):
         for Y in outs[1:]:
             assert torch.equal(outs[0], Y)
     assert ssd.dec_sync_status() == ssd.DEC_OK
+
+
+@pytest.mark.parametrize("B", [1, 4, 64])
+@pytest.mark.parametrize("N,K", [(8192, 7168), (7168, 16384)])
+def test_packed_l2_prefetch_keeps_bits(env, monkeypatch, B, N, K):
+    """The optional L2 prefetch of each worker's next k-blocks before its dependency wait
+    (DEC_L2PF_KB; one 16 KB bulk prefetch per packed block) writes nothing: the same bits."""
+    torch, ssd, oracle, dev = env
+    from split_switched_decode_gb300 import inputs
+    X = inputs.activations(B, K, dev, 27)
+    W = inputs.weight(N, K, dev, 27)
+    Wp = ssd.dec_pack_weight(W)
+    ws = ssd.workspace(ssd.dec_linear_workspace_bytes(B, N, K), dev)
+    outs = []
+    for kb in ("0", "24"):
+        monkeypatch.setenv("DEC_L2PF_KB", kb)
+        Y = torch.empty(B, N, dtype=torch.bfloat16, device=dev)
+        ssd.dec_splitk_gemm_packed(X, Wp, None, Y, ws, split_k=0, use_tc=1)
+        torch.cuda.synchronize()
+        assert ssd.dec_sync_status() == ssd.DEC_OK
+        outs.append(Y)
+    assert torch.equal(outs[0], outs[1])
