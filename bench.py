@@ -339,8 +339,8 @@ def time_graph(torch, g, reps):
 
 PF_WAIT_US = 20.0
 # DRAM bytes / algorithmic bytes of one expert-layer call (ncu, 32-expert bank, B = 64,
-# whole-tile schedule of the routed launches), with tile-packed banks and with row-major ones
-EXPERTS_TRAFFIC_RATIO = {True: 1.0115, False: 1.0115}
+# routed gate/up and down in one launch), with tile-packed banks and with row-major ones
+EXPERTS_TRAFFIC_RATIO = {True: 1.0097, False: 1.0097}
 
 
 def prefetch_scenario(torch, ssd, wl, batches, reps):
