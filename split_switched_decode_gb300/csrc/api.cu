@@ -323,6 +323,14 @@ bool expert_one_launch() {
   return true;
 }
 
+// With the routed experts in one launch: the shared expert's tiles join that launch as
+// one more group, claimed by every SM, instead of running on the side stream
+// (DEC_SHARED_IN_ROUTED=0 keeps the side stream; a caller's side_max_ctas > 0 does too).
+bool shared_in_routed() {
+  if (const char *s = std::getenv("DEC_SHARED_IN_ROUTED")) return std::atoi(s) != 0;
+  return true;
+}
+
 // Whether grouped launches whose route map is already complete read it, and issue their
 // first weight loads, before the dependency wait (DEC_EARLY_ROUTE_MAP=0 turns it off).
 bool early_route_map() {
@@ -624,12 +632,14 @@ bool plan_experts(int B, int E, int topk, int H, int I, int num_sms, ExpertsPlan
   size_t o = 0;
   ep->rm_off = o;
   o += align_up(moe_route_map_ints(B, E, topk) * sizeof(int32_t));
+  // P gathered rows, then B more for the shared expert when it runs in the routed launch
+  const size_t PB = P + static_cast<size_t>(B);
   ep->xg_off = o;
-  o += align_up(P * H * 2);
+  o += align_up(PB * H * 2);
   ep->a_off = o;
-  o += align_up(P * I * 2);
+  o += align_up(PB * I * 2);
   ep->yp_off = o;
-  o += align_up(P * H * sizeof(float));
+  o += align_up(PB * H * sizeof(float));
   ep->as_off = o;
   o += align_up(static_cast<size_t>(B) * I * 2);
   ep->s_off = o;
@@ -646,8 +656,8 @@ bool plan_experts(int B, int E, int topk, int H, int I, int num_sms, ExpertsPlan
   o += align_up(static_cast<size_t>(tmax) * sizeof(int));
   ep->cmb_off = o;  // fused combine: one arrival counter per (token, 128-row block of H)
   o += align_up(static_cast<size_t>(B) * ep->Td * sizeof(int));
-  ep->dyn_off = o;  // routed launches: claim counters [4], then one ready count per expert
-  o += align_up((4 + static_cast<size_t>(E)) * sizeof(int));
+  ep->dyn_off = o;  // routed launches: counters [4], then a ready count per group (E + 1)
+  o += align_up((5 + static_cast<size_t>(E)) * sizeof(int));
   ep->total = o;
   return true;
 }
@@ -1182,7 +1192,14 @@ dec_status moe_experts_impl(const dec_bf16 *X, const int32_t *topk_idx, const fl
   // The fused combine counts every (token, block)'s contributions, so it needs a routing
   // that is valid by construction: a route map from the caller (moe_front) or moe_layer.
   const bool fused = (route_map != nullptr || fc != nullptr) && fused_combine();
-  const bool overlap = shared && (ss != ms);
+  // tensor-core tiles for the expert GEMVs from the same batch threshold as dec_linear
+  const int fv = force_variant();
+  const bool tc = (fv == DEC_VARIANT_SPLITK_TC) || (fv == DEC_VARIANT_NONE && B >= tc_min_batch());
+  // the shared expert as one more group of the one-launch routed experts (every SM claims
+  // its tiles too), unless the caller capped its CTAs or the combine is fused
+  const bool merged = shared && tc && expert_one_launch() && shared_in_routed() && !fused &&
+                      side_max_ctas == 0;
+  const bool overlap = shared && !merged && (ss != ms);
   const int P = B * topk;
   char *wsb = static_cast<char *>(ws);
   int32_t *rm = route_map ? const_cast<int32_t *>(route_map)
@@ -1222,7 +1239,8 @@ dec_status moe_experts_impl(const dec_bf16 *X, const int32_t *topk_idx, const fl
                : make_map(&m_wgu, Wgu, H, gu_rows, 64)) ||
       !(packed ? make_map(&m_wd, Wd, TILE_K, d_rows * (I / TILE_K), 128)
                : make_map(&m_wd, Wd, I, d_rows, 128)) ||
-      !make_map(&m_xg, Xg, H, P, XBOX_ROWS) || !make_map(&m_a, A, I, P, XBOX_ROWS))
+      !make_map(&m_xg, Xg, H, P + (merged ? B : 0), XBOX_ROWS) ||
+      !make_map(&m_a, A, I, P + (merged ? B : 0), XBOX_ROWS))
     return DEC_ERR_CUDA;
   CUtensorMap m_wgus, m_wds, m_x, m_as;
   const int xb_shared = xbox_rows_for(ep.maxc);
@@ -1237,9 +1255,6 @@ dec_status moe_experts_impl(const dec_bf16 *X, const int32_t *topk_idx, const fl
 
   if (consume_fault()) return DEC_ERR_CUDA;
 
-  // tensor-core tiles for the expert GEMVs from the same batch threshold as dec_linear
-  const int fv = force_variant();
-  const bool tc = (fv == DEC_VARIANT_SPLITK_TC) || (fv == DEC_VARIANT_NONE && B >= tc_min_batch());
   auto engine = [&](const CUtensorMap &wm, const CUtensorMap &xm, EngineParams &p,
                     cudaStream_t st_) -> cudaError_t {
     return tc ? launch_engine_tc(p.slot_cols, wm, xm, p, st_)
@@ -1280,8 +1295,9 @@ dec_status moe_experts_impl(const dec_bf16 *X, const int32_t *topk_idx, const fl
     p.cmb_y = reinterpret_cast<uint16_t *>(Y);
   };
 
-  // ---- shared expert, side stream (or main when no second stream was given)
-  if (shared) {
+  // ---- shared expert, side stream (or main when no second stream was given), unless
+  // it runs inside the routed launch
+  if (shared && !merged) {
     cudaStream_t sst = overlap ? ss : ms;
     const int gs = overlap ? g_side : d->num_sms;
     if (overlap) {
@@ -1323,9 +1339,10 @@ dec_status moe_experts_impl(const dec_bf16 *X, const int32_t *topk_idx, const fl
   // ---- routed experts, main stream
   // without a route map the gather launch validates topk_idx and builds it
   int *dyn_ctr = reinterpret_cast<int *>(wsb + ep.dyn_off);
-  ce = have_map ? launch_gather_rows(X, rm, B, topk, E, H, Xg, dyn_ctr, 4 + E, ms)
+  const int xrows = merged ? B : 0;  // X's rows after the gathered ones: the shared expert's
+  ce = have_map ? launch_gather_rows(X, rm, B, topk, E, H, Xg, dyn_ctr, 5 + E, xrows, ms)
                 : launch_gather_map(X, topk_idx, B, topk, E, H, Xg, rm, d->status,
-                                    2 * d->num_sms, dyn_ctr, 4 + E, ms);
+                                    2 * d->num_sms, dyn_ctr, 5 + E, xrows, ms);
   if (ce != cudaSuccess) return DEC_ERR_CUDA;
   {
     EngineParams p;
@@ -1347,15 +1364,17 @@ dec_status moe_experts_impl(const dec_bf16 *X, const int32_t *topk_idx, const fl
       p.rm_ready = (have_map && early_route_map()) ? 1 : 0;
       p.dyn_ctr = dyn_ctr;
       p.ready = dyn_ctr + 4;
+      p.with_shared = merged ? 1 : 0;
       p.w_base = packed ? reinterpret_cast<const uint8_t *>(Wgu) : nullptr;
       base(p2, MODE_DOWN, H, I, ep.Td, ep.KBd, g_main, 1, ep.main_part_off, ep.main_cnt_off);
       p2.w_group_rows = H;
       p2.Yp = Yp;
       if (fused) set_combine(p2);
       p2.rm_ready = p.rm_ready;
+      p2.with_shared = p.with_shared;
       p2.w_base = packed ? reinterpret_cast<const uint8_t *>(Wd) : nullptr;
-      if ((ce = launch_engine_tc_moe(ep.maxc, m_wgu, m_xg, m_wd, m_a, p, p2, ms)) !=
-          cudaSuccess)
+      if ((ce = launch_engine_tc_moe(ep.maxc, m_wgu, m_xg, m_wd, m_a, merged ? m_wgus : m_wgu,
+                                     merged ? m_wds : m_wd, p, p2, ms)) != cudaSuccess)
         return DEC_ERR_CUDA;
     } else {
     // Whole-tile schedule once the CTAs expect enough tiles each that the last claims
@@ -1388,7 +1407,9 @@ dec_status moe_experts_impl(const dec_bf16 *X, const int32_t *topk_idx, const fl
   // Y is complete once both streams are done: the main stream waits for the side one
   if (overlap && (ce = cudaStreamWaitEvent(ms, ev->join, 0)) != cudaSuccess) return DEC_ERR_CUDA;
   if (!fused &&
-      (ce = launch_combine(topk_w, rm, Yp, shared ? S : nullptr, B, topk, E, H, Y, ms)) !=
+      (ce = launch_combine(topk_w, rm, Yp,
+                           shared ? (merged ? Yp + static_cast<size_t>(P) * H : S) : nullptr, B,
+                           topk, E, H, Y, ms)) !=
           cudaSuccess)
     return DEC_ERR_CUDA;
   return DEC_OK;

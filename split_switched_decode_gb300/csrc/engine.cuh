@@ -55,8 +55,11 @@ struct SegInfo {
   int pblk;    // tile-packed W: block of this tile's k-block 0 ((expert * T + t) * KB)
 };
 
+// shared_g: the group index of the shared expert inside a grouped launch (after the used
+// experts), or -1: its weights come from their own tensor map (expert 0 of it) and its
+// activation rows are P .. P+B-1.
 __device__ __forceinline__ void seg_info(const EngineParams &p, int64_t it, int64_t end,
-                                         SegInfo &s) {
+                                         SegInfo &s, int shared_g = -1) {
   s.gt = static_cast<int>(it / p.KB);
   s.kb0 = static_cast<int>(it - static_cast<int64_t>(s.gt) * p.KB);
   const int64_t tend = static_cast<int64_t>(s.gt + 1) * p.KB;
@@ -66,7 +69,11 @@ __device__ __forceinline__ void seg_info(const EngineParams &p, int64_t it, int6
   s.t = s.gt - g * p.T;
   int wbase;
   int e = 0;  // expert of a grouped launch
-  if (p.grouped) {
+  if (p.grouped && g == shared_g) {
+    s.xrow0 = p.P;
+    s.ncols = min(p.B, p.slot_cols);
+    wbase = 0;
+  } else if (p.grouped) {
     // the route map comes from moe_front or the validating rebuild kernel; the clamps
     // only keep a corrupted map from steering loads or stores out of their buffers
     const int32_t *rm = p.route_map;

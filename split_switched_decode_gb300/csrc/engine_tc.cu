@@ -467,13 +467,13 @@ cudaError_t launch_t(const CUtensorMap &wmap, const CUtensorMap &xmap, const Eng
 // stage ring; claims the next tile STAGES k-blocks before the end. False after a time-out.
 template <int STAGES, int STAGE_BYTES>
 __device__ __forceinline__ bool moe_tile_loads(const EngineParams &p, const CUtensorMap *wmap,
-                                               const CUtensorMap *xmap, int t, uint8_t *stage_mem,
-                                               uint64_t *full, uint64_t *empty,
-                                               volatile int *flags, uint32_t &q, int &ahead,
-                                               int *ctr, uint64_t pol) {
+                                               const CUtensorMap *xmap, int t, int shared_g,
+                                               uint8_t *stage_mem, uint64_t *full,
+                                               uint64_t *empty, volatile int *flags, uint32_t &q,
+                                               int &ahead, int *ctr, uint64_t pol) {
   SegInfo s;
   const int64_t it = static_cast<int64_t>(t) * p.KB;
-  seg_info(p, it, it + p.KB, s);
+  seg_info(p, it, it + p.KB, s, shared_g);
   const int nxb = (16 * seg_xboxes(s) + p.xbox_rows - 1) / p.xbox_rows;
   const uint32_t bytes = stage_tx_bytes(p, s);
   const int claim_kb = p.KB > STAGES ? p.KB - STAGES : 0;
@@ -496,19 +496,25 @@ template <int STAGES, int STAGE_BYTES>
 __device__ __forceinline__ void moe_produce(const EngineParams &p1, const EngineParams &p2,
                                             const CUtensorMap *wmap1, const CUtensorMap *xmap1,
                                             const CUtensorMap *wmap2, const CUtensorMap *xmap2,
+                                            const CUtensorMap *wmap1s, const CUtensorMap *wmap2s,
                                             uint8_t *stage_mem, uint64_t *full, uint64_t *empty,
                                             volatile int *tslot, uint64_t *tready,
                                             uint64_t *tfree, volatile int *flags, int n1,
-                                            int ntot) {
+                                            int ntot, int shared_g) {
   prefetch_tensormap(wmap1);
   prefetch_tensormap(xmap1);
   prefetch_tensormap(wmap2);
   prefetch_tensormap(xmap2);
+  if (shared_g >= 0) {
+    prefetch_tensormap(wmap1s);
+    prefetch_tensormap(wmap2s);
+  }
   const uint64_t pol = policy_evict_first();
   // Before the dependency wait: the first claims go to about the first G gate/up tiles,
   // so pull the first weight blocks of tile blockIdx.x into L2 (writes nothing; packed
   // banks: one bulk prefetch per 16 KB block).
-  if (p1.rm_ready && p1.packed && p1.w_base != nullptr && static_cast<int>(blockIdx.x) < n1) {
+  if (p1.rm_ready && p1.packed && p1.w_base != nullptr &&
+      static_cast<int>(blockIdx.x) / p1.T != shared_g && static_cast<int>(blockIdx.x) < n1) {
     SegInfo s;
     const int64_t it = static_cast<int64_t>(blockIdx.x) * p1.KB;
     seg_info(p1, it, it + p1.KB, s);
@@ -532,7 +538,7 @@ __device__ __forceinline__ void moe_produce(const EngineParams &p1, const Engine
       if (ld_acquire_gpu(gu_done) >= n1)
         all_ready = true;  // then one proxy fence covers every later down tile
       else if (ld_acquire_gpu(p1.ready + g) < p1.T) {
-        if (p2.packed && p2.w_base != nullptr) {
+        if (p2.packed && p2.w_base != nullptr && g != shared_g) {
           SegInfo s;
           const int64_t it = static_cast<int64_t>(tile - n1) * p2.KB;
           seg_info(p2, it, it + p2.KB, s);
@@ -555,11 +561,14 @@ __device__ __forceinline__ void moe_produce(const EngineParams &p1, const Engine
     mbar_arrive(&tready[sl]);
     if (tile < 0) break;
     // the phases' parameters and tensor maps stay compile-time operands in each branch
-    ok = tile >= n1
-             ? moe_tile_loads<STAGES, STAGE_BYTES>(p2, wmap2, xmap2, tile - n1, stage_mem, full,
-                                                   empty, flags, q, ahead, p1.dyn_ctr, pol)
-             : moe_tile_loads<STAGES, STAGE_BYTES>(p1, wmap1, xmap1, tile, stage_mem, full,
-                                                   empty, flags, q, ahead, p1.dyn_ctr, pol);
+    if (tile >= n1)
+      ok = moe_tile_loads<STAGES, STAGE_BYTES>(p2, (tile - n1) / p2.T == shared_g ? wmap2s : wmap2,
+                                               xmap2, tile - n1, shared_g, stage_mem, full, empty,
+                                               flags, q, ahead, p1.dyn_ctr, pol);
+    else
+      ok = moe_tile_loads<STAGES, STAGE_BYTES>(p1, tile / p1.T == shared_g ? wmap1s : wmap1, xmap1,
+                                               tile, shared_g, stage_mem, full, empty, flags, q,
+                                               ahead, p1.dyn_ctr, pol);
   }
   griddep_launch_dependents();
   if (flags[0]) {
@@ -575,7 +584,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     engine_tc_moe_kernel(const __grid_constant__ CUtensorMap wmap1,
                          const __grid_constant__ CUtensorMap xmap1,
                          const __grid_constant__ CUtensorMap wmap2,
-                         const __grid_constant__ CUtensorMap xmap2, const EngineParams p1,
+                         const __grid_constant__ CUtensorMap xmap2,
+                         const __grid_constant__ CUtensorMap wmap1s,
+                         const __grid_constant__ CUtensorMap wmap2s, const EngineParams p1,
                          const EngineParams p2) {
   using C = TCConfig<MAXC, 1>;
   extern __shared__ uint8_t smem_raw[];
@@ -601,8 +612,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   // previous kernel of the stream started
   if (!p1.rm_ready) griddep_wait();
   const int U = rm_num_used(p1);
-  const int n1 = U * p1.T;
-  const int ntot = n1 + U * p2.T;
+  // groups: the used experts, then (with_shared) the shared expert
+  const int shared_g = p1.with_shared ? U : -1;
+  const int ng = U + (p1.with_shared ? 1 : 0);
+  const int n1 = ng * p1.T;
+  const int ntot = n1 + ng * p2.T;
 
   if (tid == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -635,8 +649,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
     if (lane == 0)
-      moe_produce<C::STAGES, C::STAGE_BYTES>(p1, p2, &wmap1, &xmap1, &wmap2, &xmap2, stage_mem,
-                                             full, empty, tslot, tready, tfree, flags, n1, ntot);
+      moe_produce<C::STAGES, C::STAGE_BYTES>(p1, p2, &wmap1, &xmap1, &wmap2, &xmap2, &wmap1s,
+                                             &wmap2s, stage_mem, full, empty, tslot, tready,
+                                             tfree, flags, n1, ntot, shared_g);
     else
       griddep_wait();
   } else if (warp == 1) {
@@ -655,10 +670,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         SegInfo s;
         if (tile >= n1) {
           const int64_t it = static_cast<int64_t>(tile - n1) * p2.KB;
-          seg_info(p2, it, it + p2.KB, s);
+          seg_info(p2, it, it + p2.KB, s, shared_g);
         } else {
           const int64_t it = static_cast<int64_t>(tile) * p1.KB;
-          seg_info(p1, it, it + p1.KB, s);
+          seg_info(p1, it, it + p1.KB, s, shared_g);
         }
         ok = mma_segment<C::STAGES, C::STAGE_BYTES, 1>(s, seg, q, tmem_base, stage_mem, full,
                                                       empty, acc_full, acc_empty, p1, flags);
@@ -696,10 +711,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       SegInfo s;
       if (down) {
         const int64_t it = static_cast<int64_t>(tile - n1) * p2.KB;
-        seg_info(p2, it, it + p2.KB, s);
+        seg_info(p2, it, it + p2.KB, s, shared_g);
       } else {
         const int64_t it = static_cast<int64_t>(tile) * p1.KB;
-        seg_info(p1, it, it + p1.KB, s);
+        seg_info(p1, it, it + p1.KB, s, shared_g);
       }
       tc_fence_after();
       float v[C::NC];
@@ -736,6 +751,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 template <int MAXC>
 cudaError_t launch_moe_t(const CUtensorMap &wmap1, const CUtensorMap &xmap1,
                          const CUtensorMap &wmap2, const CUtensorMap &xmap2,
+                         const CUtensorMap &wmap1s, const CUtensorMap &wmap2s,
                          const EngineParams &p1, const EngineParams &p2, cudaStream_t s) {
   using C = TCConfig<MAXC, 1>;
   static std::atomic<uint64_t> attr_set{0};
@@ -750,7 +766,7 @@ cudaError_t launch_moe_t(const CUtensorMap &wmap1, const CUtensorMap &xmap1,
     attr_set.fetch_or(bit);
   }
   return launch_pdl(engine_tc_moe_kernel<MAXC>, dim3(p1.G), dim3(TC_THREADS), C::SMEM, s, wmap1,
-                    xmap1, wmap2, xmap2, p1, p2);
+                    xmap1, wmap2, xmap2, wmap1s, wmap2s, p1, p2);
 }
 
 }  // namespace
@@ -785,20 +801,21 @@ namespace ssd {
 
 cudaError_t launch_engine_tc_moe(int maxc, const CUtensorMap &wmap1, const CUtensorMap &xmap1,
                                  const CUtensorMap &wmap2, const CUtensorMap &xmap2,
+                                 const CUtensorMap &wmap1s, const CUtensorMap &wmap2s,
                                  const EngineParams &p1, const EngineParams &p2,
                                  cudaStream_t s) {
   if (!p1.grouped || !p2.grouped || p1.mode != MODE_GATEUP || p2.mode != MODE_DOWN ||
       p1.dyn_ctr == nullptr || p1.ready == nullptr || p1.ngrp != 1 || p2.ngrp != 1 ||
       p1.defer || p2.defer || p1.pair || p2.pair || p1.slot_cols != p2.slot_cols ||
-      p1.route_map != p2.route_map || p1.G < 1)
+      p1.route_map != p2.route_map || p1.G < 1 || p1.with_shared != p2.with_shared)
     return cudaErrorInvalidValue;
   switch (maxc) {
-    case 2: return launch_moe_t<2>(wmap1, xmap1, wmap2, xmap2, p1, p2, s);
-    case 4: return launch_moe_t<4>(wmap1, xmap1, wmap2, xmap2, p1, p2, s);
-    case 8: return launch_moe_t<8>(wmap1, xmap1, wmap2, xmap2, p1, p2, s);
-    case 16: return launch_moe_t<16>(wmap1, xmap1, wmap2, xmap2, p1, p2, s);
-    case 32: return launch_moe_t<32>(wmap1, xmap1, wmap2, xmap2, p1, p2, s);
-    case 64: return launch_moe_t<64>(wmap1, xmap1, wmap2, xmap2, p1, p2, s);
+    case 2: return launch_moe_t<2>(wmap1, xmap1, wmap2, xmap2, wmap1s, wmap2s, p1, p2, s);
+    case 4: return launch_moe_t<4>(wmap1, xmap1, wmap2, xmap2, wmap1s, wmap2s, p1, p2, s);
+    case 8: return launch_moe_t<8>(wmap1, xmap1, wmap2, xmap2, wmap1s, wmap2s, p1, p2, s);
+    case 16: return launch_moe_t<16>(wmap1, xmap1, wmap2, xmap2, wmap1s, wmap2s, p1, p2, s);
+    case 32: return launch_moe_t<32>(wmap1, xmap1, wmap2, xmap2, wmap1s, wmap2s, p1, p2, s);
+    case 64: return launch_moe_t<64>(wmap1, xmap1, wmap2, xmap2, wmap1s, wmap2s, p1, p2, s);
     default: return cudaErrorInvalidValue;
   }
 }

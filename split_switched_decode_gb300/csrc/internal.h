@@ -37,6 +37,9 @@ struct EngineParams {
                      // then claims the rest one tile at a time from *dyn_ctr. 0: stream-K
   int *dyn_ctr;      // this launch's claim counter, zero when the launch starts (the gather
                      // launch before the routed launches clears it)
+  int with_shared;   // one launch for gate/up and down: one more group after the used
+                     // experts, the shared expert (its own tensor maps; activation rows
+                     // P .. P+B-1, all B tokens)
   int *ready;        // one launch for gate/up and down: per used expert, the gate/up tiles
                      // whose rows of A are stored (zero at the start, cleared with dyn_ctr;
                      // dyn_ctr[1] counts them over all experts)
@@ -129,8 +132,11 @@ cudaError_t launch_engine_tc(int maxc, const CUtensorMap &wmap, const CUtensorMa
 // The routed gate/up (p1: wmap1, xmap1) and down (p2: wmap2, xmap2) GEMVs of a grouped
 // expert layer in one launch of p1.G CTAs: every tile claimed from p1.dyn_ctr, down tiles
 // after their expert's gate/up tiles have published A (p1.ready).
+// With p1.with_shared, the shared expert is one more group, its weights read through
+// wmap1s (gate/up) and wmap2s (down).
 cudaError_t launch_engine_tc_moe(int maxc, const CUtensorMap &wmap1, const CUtensorMap &xmap1,
                                  const CUtensorMap &wmap2, const CUtensorMap &xmap2,
+                                 const CUtensorMap &wmap1s, const CUtensorMap &wmap2s,
                                  const EngineParams &p1, const EngineParams &p2,
                                  cudaStream_t s);
 
@@ -212,10 +218,13 @@ struct LinearFinishParams {
 cudaError_t launch_linear_finish(const LinearFinishParams &f, cudaStream_t s);
 // Validates topk_idx, builds the route map (written to route_map) and gathers in one
 // launch of at most max_ctas CTAs. Both gather launches also zero dyn_reset[0..nreset)
-// (the claim and ready counters of the routed launches after them), unless it is nullptr.
+// (the claim and ready counters of the routed launches after them), unless it is nullptr,
+// and with shared_rows = B append X's B rows after the P gathered ones (the shared
+// expert's activation rows when it runs inside the routed launch).
 cudaError_t launch_gather_map(const uint16_t *X, const int32_t *topk_idx, int B, int topk, int E,
                               int K, uint16_t *Xg, int32_t *route_map, unsigned *status,
-                              int max_ctas, int *dyn_reset, int nreset, cudaStream_t s);
+                              int max_ctas, int *dyn_reset, int nreset, int shared_rows,
+                              cudaStream_t s);
 cudaError_t launch_comm_wait(uint64_t ns, cudaStream_t s);
 // Read-stream measurement: `ctas` CTAs, each reading per_cta bytes (a multiple of 16 KB)
 // of p into shared memory (moe_aux.cu).
@@ -223,7 +232,7 @@ cudaError_t launch_read_stream(const void *p, size_t per_cta, int ctas, unsigned
                                uint64_t limit_ns, cudaStream_t s);
 cudaError_t launch_gather_rows(const uint16_t *X, const int32_t *route_map, int B, int topk,
                                int E, int K, uint16_t *Xg, int *dyn_reset, int nreset,
-                               cudaStream_t s);
+                               int shared_rows, cudaStream_t s);
 cudaError_t launch_combine(const float *topk_w, const int32_t *route_map, const float *Yp,
                            const float *S, int B, int topk, int E, int H, uint16_t *Y,
                            cudaStream_t s);

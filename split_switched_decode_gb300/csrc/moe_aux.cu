@@ -49,7 +49,8 @@ __global__ void __launch_bounds__(256) gather_map_kernel(const uint16_t *X,
                                                          const int32_t *topk_idx, int B,
                                                          int topk, int E, int K, uint16_t *Xg,
                                                          int32_t *rm, unsigned *status,
-                                                         int *dyn_reset, int nreset) {
+                                                         int *dyn_reset, int nreset,
+                                                         int shared_rows) {
   griddep_wait();
   griddep_launch_dependents();
   // the claim and ready counters of the routed launches that follow
@@ -72,7 +73,7 @@ __global__ void __launch_bounds__(256) gather_map_kernel(const uint16_t *X,
     for (int i = threadIdx.x; i < 3 * E + 2 + 2 * P; i += 256) rm[i] = smap[i];
   const int32_t *pairs = smap + 2 * E + 1;
   const int chunks = K / 8;  // 16-byte chunks per row
-  const int64_t n = static_cast<int64_t>(P) * chunks;
+  const int64_t n = static_cast<int64_t>(P + shared_rows) * chunks;
   constexpr int UNR = 4;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * 256;
   for (int64_t i0 = blockIdx.x * 256ll + threadIdx.x; i0 < n; i0 += stride * UNR) {
@@ -83,7 +84,7 @@ __global__ void __launch_bounds__(256) gather_map_kernel(const uint16_t *X,
       if (i < n) {
         const int q = static_cast<int>(i / chunks);
         const int c = static_cast<int>(i - static_cast<int64_t>(q) * chunks);
-        const int b = pairs[q] / topk;  // a valid map: 0 <= b < B
+        const int b = q < P ? pairs[q] / topk : q - P;  // a valid map: 0 <= b < B
         v[u] = reinterpret_cast<const uint4 *>(X + static_cast<size_t>(b) * K)[c];
       }
     }
@@ -281,7 +282,7 @@ __global__ void __launch_bounds__(128) linear_finish_kernel(const LinearFinishPa
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t *X, const int32_t *rm,
                                                           int B, int topk, int E, int K,
                                                           uint16_t *Xg, int *dyn_reset,
-                                                          int nreset) {
+                                                          int nreset, int shared_rows) {
   griddep_wait();
   griddep_launch_dependents();
   // the claim and ready counters of the routed launches that follow
@@ -290,11 +291,11 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t *X, con
   const int P = B * topk;
   const int32_t *pairs = rm + 2 * E + 1;
   const int chunks = K / 8;  // 16-byte chunks per row
-  const int64_t n = static_cast<int64_t>(P) * chunks;
+  const int64_t n = static_cast<int64_t>(P + shared_rows) * chunks;
   for (int64_t i = blockIdx.x * 256ll + threadIdx.x; i < n; i += gridDim.x * 256ll) {
     const int q = static_cast<int>(i / chunks);
     const int c = static_cast<int>(i - static_cast<int64_t>(q) * chunks);
-    const int b = min(max(pairs[q] / topk, 0), B - 1);
+    const int b = q < P ? min(max(pairs[q] / topk, 0), B - 1) : q - P;
     const uint4 v = reinterpret_cast<const uint4 *>(X + static_cast<size_t>(b) * K)[c];
     reinterpret_cast<uint4 *>(Xg + static_cast<size_t>(q) * K)[c] = v;
   }
@@ -480,23 +481,24 @@ cudaError_t launch_linear_finish(const LinearFinishParams &f, cudaStream_t s) {
 
 cudaError_t launch_gather_map(const uint16_t *X, const int32_t *topk_idx, int B, int topk, int E,
                               int K, uint16_t *Xg, int32_t *route_map, unsigned *status,
-                              int max_ctas, int *dyn_reset, int nreset, cudaStream_t s) {
-  const int64_t n = static_cast<int64_t>(B) * topk * (K / 8);
+                              int max_ctas, int *dyn_reset, int nreset, int shared_rows,
+                              cudaStream_t s) {
+  const int64_t n = static_cast<int64_t>(B * topk + shared_rows) * (K / 8);
   int64_t need = (n + 1023) / 1024;  // 256 threads x 4 chunks per CTA and sweep
   int grid = static_cast<int>(need < max_ctas ? need : max_ctas);
   if (grid < 1) grid = 1;
   return launch_pdl(gather_map_kernel, dim3(grid), dim3(256), 0, s, X, topk_idx, B, topk, E, K,
-                    Xg, route_map, status, dyn_reset, nreset);
+                    Xg, route_map, status, dyn_reset, nreset, shared_rows);
 }
 
 cudaError_t launch_gather_rows(const uint16_t *X, const int32_t *route_map, int B, int topk,
                                int E, int K, uint16_t *Xg, int *dyn_reset, int nreset,
-                               cudaStream_t s) {
-  const int64_t n = static_cast<int64_t>(B) * topk * (K / 8);
+                               int shared_rows, cudaStream_t s) {
+  const int64_t n = static_cast<int64_t>(B * topk + shared_rows) * (K / 8);
   int grid = static_cast<int>((n + 255) / 256);
   if (grid > 1024) grid = 1024;
   return launch_pdl(gather_rows_kernel, dim3(grid), dim3(256), 0, s, X, route_map, B, topk, E, K,
-                    Xg, dyn_reset, nreset);
+                    Xg, dyn_reset, nreset, shared_rows);
 }
 
 cudaError_t launch_combine(const float *topk_w, const int32_t *route_map, const float *Yp,

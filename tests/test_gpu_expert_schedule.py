@@ -130,6 +130,7 @@ def test_whole_tile_result_does_not_depend_on_the_schedule(env, whole_tiles, B, 
     E, H, I = 32, 256, 192
     pb = _problem(env, B, E, H, I, k, 2)
     rm = _host_route_map(oracle, pb["idx_np"], E, dev)
+    whole_tiles.setenv("DEC_SHARED_IN_ROUTED", "0")  # routed schedules only; shared on its own
     outs = []
     for one in ("1", "0"):
         whole_tiles.setenv("DEC_EXPERT_ONE_LAUNCH", one)
@@ -192,6 +193,7 @@ def test_whole_tile_fused_combine_equals_combine_launch(env, whole_tiles, B, k, 
     pb = _problem(env, B, E, H, I, k, 6, shared)
     rm = _host_route_map(oracle, pb["idx_np"], E, dev)
     ws = ssd.workspace(ssd.moe_experts_workspace_bytes(B, E, k, H, I), dev)
+    whole_tiles.setenv("DEC_SHARED_IN_ROUTED", "0")  # the fused combine keeps it on its own
     whole_tiles.setenv("DEC_FUSED_COMBINE", "1")
     Y1 = _run(env, pb["X"], pb["idx"], pb["w"], pb["Wgu"], pb["Wd"], pb["Wgs"], pb["Wds"], rm=rm,
               ws=ws)
@@ -224,3 +226,34 @@ def test_whole_tile_invalid_routing_is_reported_not_faulted(env, whole_tiles):
     y_ref, _ = oracle.moe_experts(inputs.bits(X), idx_np, w.cpu().numpy().astype(np.float64),
                                   inputs.bits(Wgu), inputs.bits(Wd))
     assert_close(to_f64(oracle, Y), y_ref, "valid routing after invalid ones")
+
+
+@pytest.mark.parametrize("B,k", [(1, 8), (4, 2), (17, 8), (64, 8), (64, 1)])
+@pytest.mark.parametrize("with_map,packed", [(True, False), (False, True)])
+def test_shared_expert_inside_the_routed_launch(env, monkeypatch, B, k, with_map, packed):
+    """The shared expert as one more group of the one-launch routed experts (the default):
+    its gate/up and down tiles claimed with the routed ones, its activation rows appended
+    to the gathered ones, its output read by the combine. Against the oracle, and within
+    the same tolerance of the shared expert on its own launches (another summation split)."""
+    torch, ssd, oracle, dev = env
+    E, H, I = 24, 384, 256
+    pb = _problem(env, B, E, H, I, k, 8)
+    rm = _host_route_map(oracle, pb["idx_np"], E, dev) if with_map else None
+    Wgu, Wd, Wgs, Wds = pb["Wgu"], pb["Wd"], pb["Wgs"], pb["Wds"]
+    if packed:
+        Wgu, Wd = ssd.dec_pack_expert_weights(Wgu, Wd)
+        gs, ds = ssd.dec_pack_expert_weights(Wgs[None], Wds[None])
+        Wgs, Wds = gs[0], ds[0]
+    monkeypatch.setenv("DEC_EXPERT_ONE_LAUNCH", "1")
+    monkeypatch.setenv("DEC_SHARED_IN_ROUTED", "1")
+    Y1 = _run(env, pb["X"], pb["idx"], pb["w"], Wgu, Wd, Wgs, Wds, rm=rm, side=True,
+              packed=packed)
+    Y1b = _run(env, pb["X"], pb["idx"], pb["w"], Wgu, Wd, Wgs, Wds, rm=rm, side=False,
+               packed=packed)
+    assert torch.equal(Y1, Y1b)  # the side stream is not used: the same launches
+    monkeypatch.setenv("DEC_SHARED_IN_ROUTED", "0")
+    Y0 = _run(env, pb["X"], pb["idx"], pb["w"], Wgu, Wd, Wgs, Wds, rm=rm, side=True,
+              packed=packed)
+    y = _oracle_y(env, pb)
+    assert_close(to_f64(oracle, Y1), y, f"shared in routed B={B} k={k}")
+    assert_close(to_f64(oracle, Y0), y, f"shared on the side B={B} k={k}")

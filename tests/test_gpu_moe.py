@@ -466,6 +466,8 @@ def test_fused_combine_equals_combine_launch(env, monkeypatch, B, k, shared, sid
     w = torch.from_numpy(w_np).to(dev)
     rm = _host_route_map(oracle, idx_np, E, dev)
     ws = ssd.workspace(ssd.moe_experts_workspace_bytes(B, E, k, H, I), dev)
+    # the fused combine keeps the shared expert on its own launches: compare like with like
+    monkeypatch.setenv("DEC_SHARED_IN_ROUTED", "0")
     monkeypatch.setenv("DEC_FUSED_COMBINE", "1")
     Y1 = _run_experts(env, X, idx, w, Wgu, Wd, Wgs, Wds, rm=rm, side=side, ws=ws)
     Y1b = _run_experts(env, X, idx, w, Wgu, Wd, Wgs, Wds, rm=rm, side=side, ws=ws)
@@ -687,6 +689,7 @@ def test_moe_experts_one_launch_equals_two_launches_full_size(env, big_layer, mo
     X = inputs.activations(B, H, dev, 33, "one_launch_x")
     _, idx, w, _, rm = _run_front(env, X, g["Wc"], E, L, k)
     outs = []
+    monkeypatch.setenv("DEC_SHARED_IN_ROUTED", "0")  # the shared expert on its own launches
     for one in ("1", "0"):
         monkeypatch.setenv("DEC_EXPERT_ONE_LAUNCH", one)
         monkeypatch.setenv("DEC_EXPERT_DYN_MIN_TILES", "0")
