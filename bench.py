@@ -266,9 +266,7 @@ class Workload:
         self.ssd.moe_experts(d["x_moe"][v], d["idx"][v], d["w"][v], d["rm"][v], self.Wgu, self.Wd,
                              self.Wgs, self.Wds, d["y_moe"], d["ws_e"], side_stream=self.side,
                              packed=self.packed)
-        # gather, shared gate/up + down, routed gate/up + down in one launch (two with
-        # DEC_EXPERT_ONE_LAUNCH=0), combine
-        self.launches += 5 if os.environ.get("DEC_EXPERT_ONE_LAUNCH", "1") != "0" else 6
+        self.launches += expert_launches()
 
     def op_layer(self, B, v=0):
         """moe_layer: the front end runs while the shared expert streams its weights on the
@@ -279,8 +277,7 @@ class Workload:
                            self.Wgs, self.Wds, d["lat"][v], d["idx"][v], d["w"][v], d["y_moe"],
                            d["ws_l"], route_map=d["rm"][v], side_stream=self.side,
                            packed=self.packed)
-        # one-launch front end, gather, shared gate/up + down, routed experts, combine
-        self.launches += 6 if os.environ.get("DEC_EXPERT_ONE_LAUNCH", "1") != "0" else 7
+        self.launches += 1 + expert_launches()  # the one-launch front end, then the experts
 
     def op_moe(self, B):
         if self.layer:
@@ -335,12 +332,24 @@ def time_graph(torch, g, reps):
     return ts
 
 
+def expert_launches():
+    """Kernel launches of one moe_experts call with a route map, as the library's switches
+    pick them: the gather, the routed gate/up and down (one launch, or two), the shared
+    expert's gate/up and down (inside the routed launch, or two launches on the side
+    stream), the combine."""
+    one = os.environ.get("DEC_EXPERT_ONE_LAUNCH", "1") != "0"
+    inside = (one and os.environ.get("DEC_SHARED_IN_ROUTED", "1") != "0"
+              and os.environ.get("DEC_FUSED_COMBINE", "0") == "0")
+    fused = os.environ.get("DEC_FUSED_COMBINE", "0") != "0"
+    return 1 + (1 if one else 2) + (0 if inside else 2) + (0 if fused else 1)
+
+
 # ------------------------------------------------------- prefetch scenario ----
 
 PF_WAIT_US = 20.0
 # DRAM bytes / algorithmic bytes of one expert-layer call (ncu, 32-expert bank, B = 64,
-# routed gate/up and down in one launch), with tile-packed banks and with row-major ones
-EXPERTS_TRAFFIC_RATIO = {True: 1.0097, False: 1.0097}
+# routed and shared experts in one launch), with tile-packed banks and with row-major ones
+EXPERTS_TRAFFIC_RATIO = {True: 1.0096, False: 1.0093}
 
 
 def prefetch_scenario(torch, ssd, wl, batches, reps):
