@@ -2,8 +2,8 @@
  * split_switched_decode.h -- C ABI of the small-batch decode hot path for one NVIDIA
  * GB300 (sm_103a): the decode projection with a batch-size kernel switch, the MoE
  * front end (router scores + latent projection as one product, then softmax/top-k),
- * the routed-expert grouped GEMV with the shared expert on a side stream, and an L2
- * prefetch kernel.
+ * the routed-expert grouped GEMV with the shared expert overlapping it (inside the same
+ * launch, or on a side stream), and an L2 prefetch kernel.
  *
  * The method is the one described in "Hyper Optimizing Kimi K3 in vLLM: Moving Fast
  * and Responsibly" (vLLM blog), Part 1, sections 1-4. Each entry point below cites
@@ -300,19 +300,27 @@ DEC_API dec_status moe_front(const dec_bf16 *X, const dec_bf16 *Wcat, int B, int
  * NULL (then rebuilt on `main`); Wgu [E,2I,H]; Wd [E,H,I]; Wgu_shared [2I,H] and
  * Wd_shared [H,I], both NULL for no shared expert; Y [B,H].
  * Each used expert's weights are read once for all of its tokens.
- * The shared expert runs on `side` with at most side_max_ctas CTAs (0 = chosen from
- * the expected weight bytes); the routed experts use the remaining SMs on `main`.
- * `side` may equal `main` (then no overlap). The call records events so that `main`
- * waits for `side` before the combine; on return all work is ordered after `main`.
+ * On tensor cores (the default from B = 1) the routed experts' gate/up and down run as
+ * one launch on `main`, and the shared expert's tiles join it as one more group, claimed
+ * by every SM like the routed ones (the pages' overlap of the shared and routed experts,
+ * inside one launch; `side` is then unused). With side_max_ctas > 0, the environment
+ * switch DEC_SHARED_IN_ROUTED=0 or the fused combine, the shared expert runs instead on
+ * `side` with at most side_max_ctas CTAs (0 = chosen from the expected weight bytes)
+ * while the routed experts use the remaining SMs on `main`; `side` may equal `main`
+ * (then no overlap), and the call records events so that `main` waits for `side` before
+ * the combine. On return all work is ordered after `main`.
  * The combine is its own launch; with a route map and the environment switch
  * DEC_FUSED_COMBINE=1 it runs instead inside the down launches (the tile that completes
  * a token's 128-row block adds it up, in the same order: the same bits).
- * Schedule of the routed launches: below about 6.5 expected tiles per CTA, equal
- * stream-K ranges of (expert, tile, k-block) with a fixed-order reduction of split
- * tiles; above it, whole tiles (a static share per CTA, the rest claimed one by one from
- * a counter in the workspace, cleared by the call's gather launch), each accumulated
- * over all of its k-blocks by one CTA, so the bits do not depend on which CTA computes
- * a tile. Both are deterministic; they differ from each other by fp32 summation order.
+ * Schedule: in the one launch, whole tiles claimed one by one from a counter in the
+ * workspace (cleared by the call's gather launch), each accumulated over all of its
+ * k-blocks by one CTA, down tiles after their expert's gate/up tiles; so the bits do not
+ * depend on which CTA computes a tile. With DEC_EXPERT_ONE_LAUNCH=0, gate/up and down
+ * are two launches: whole tiles (a static share per CTA, the rest claimed) from about
+ * 6.5 expected tiles per CTA, equal stream-K ranges of (expert, tile, k-block) with a
+ * fixed-order reduction of split tiles below. All are deterministic; the whole-tile
+ * schedules give the same bits as each other, the stream-K ranges differ from them by
+ * fp32 summation order.
  * H % 128 == 0, I % 64 == 0, topk <= 16, E <= 512.
  */
 DEC_API size_t moe_experts_workspace_bytes(int B, int E, int topk, int H, int I);
