@@ -257,3 +257,31 @@ def test_shared_expert_inside_the_routed_launch(env, monkeypatch, B, k, with_map
     y = _oracle_y(env, pb)
     assert_close(to_f64(oracle, Y1), y, f"shared in routed B={B} k={k}")
     assert_close(to_f64(oracle, Y0), y, f"shared on the side B={B} k={k}")
+
+
+def test_shared_expert_inside_with_invalid_routing_is_reported(env, monkeypatch):
+    """An invalid routing leaves an empty route map; with the shared expert inside the
+    routed launch, that launch then holds the shared expert's tiles only. The call ends
+    with DEC_ERR_INVALID_ARG and faults nothing; a valid call on the same workspace
+    afterwards is correct."""
+    torch, ssd, oracle, dev = env
+    from split_switched_decode_gb300 import inputs
+    monkeypatch.setenv("DEC_EXPERT_ONE_LAUNCH", "1")
+    monkeypatch.setenv("DEC_SHARED_IN_ROUTED", "1")
+    E, H, I, B = 8, 256, 64, 3
+    Wgu, Wd = inputs.expert_bank(E, H, I, dev, 10)
+    Wgs, Wds = inputs.shared_expert(H, I, dev, 10)
+    X = inputs.activations(B, H, dev, 10, "bad_shared")
+    w = torch.full((B, 2), 0.5, dtype=torch.float32, device=dev)
+    Y = torch.empty(B, H, dtype=torch.bfloat16, device=dev)
+    ws = ssd.workspace(ssd.moe_experts_workspace_bytes(B, E, 2, H, I), dev)
+    bad = torch.tensor([[0, 1], [2, 9], [3, 4]], dtype=torch.int32, device=dev)
+    ssd.moe_experts(X, bad, w, None, Wgu, Wd, Wgs, Wds, Y, ws)
+    assert ssd.dec_sync_status() == ssd.DEC_ERR_INVALID_ARG
+    idx_np = np.array([[0, 1], [2, 7], [3, 4]], dtype=np.int32)
+    ssd.moe_experts(X, torch.from_numpy(idx_np).to(dev), w, None, Wgu, Wd, Wgs, Wds, Y, ws)
+    assert ssd.dec_sync_status() == ssd.DEC_OK
+    y_ref, _ = oracle.moe_experts(inputs.bits(X), idx_np, w.cpu().numpy().astype(np.float64),
+                                  inputs.bits(Wgu), inputs.bits(Wd), inputs.bits(Wgs),
+                                  inputs.bits(Wds))
+    assert_close(to_f64(oracle, Y), y_ref, "valid routing after an invalid one")
