@@ -451,18 +451,6 @@ cudaError_t launch_t(const CUtensorMap &wmap, const CUtensorMap &xmap, const Eng
 }
 
 // ---------------------------------------------------------------------------
-// Routed experts in one launch. Tiles are numbered gate/up first (used expert g, tile
-// t: g*T1 + t), then down (n1 + g*T2 + t), and every CTA claims them one at a time from
-// one counter, each a whole tile over all of its k-blocks (no partial tiles, no
-// reduction). A down tile reads its expert's A, which the expert's T1 gate/up tiles
-// write: each gate/up tile, once its rows of A are stored, adds one to the expert's
-// ready count (release), and the producer loads a down tile's A only after an acquire
-// read sees all T1 (then a proxy fence, since TMA reads what ordinary stores wrote); once
-// it sees every gate/up tile of the launch done (a second count), one fence covers all of
-// its later down tiles. No down tile is claimed before the last gate/up tile, and every
-// claimed tile is held by a running CTA, so a wait only ever depends on CTAs that are
-// running. While it waits, the producer has the down tile's first weight blocks pulled
-// into L2.
 // Weight and activation loads of one whole tile (local index t of its phase) into the
 // stage ring; claims the next tile STAGES k-blocks before the end. False after a time-out.
 template <int STAGES, int STAGE_BYTES>
@@ -492,6 +480,18 @@ __device__ __forceinline__ bool moe_tile_loads(const EngineParams &p, const CUte
   return true;
 }
 
+// Routed experts in one launch. Tiles are numbered gate/up first (used expert g, tile
+// t: g*T1 + t), then down (n1 + g*T2 + t), and every CTA claims them one at a time from
+// one counter, each a whole tile over all of its k-blocks (no partial tiles, no
+// reduction). A down tile reads its expert's A, which the expert's T1 gate/up tiles
+// write: each gate/up tile, once its rows of A are stored, adds one to the expert's
+// ready count (release), and the producer loads a down tile's A only after an acquire
+// read sees all T1 (then a proxy fence, since TMA reads what ordinary stores wrote); once
+// it sees every gate/up tile of the launch done (a second count), one fence covers all of
+// its later down tiles. No down tile is claimed before the last gate/up tile, and every
+// claimed tile is held by a running CTA, so a wait only ever depends on CTAs that are
+// running. While it waits, the producer has the down tile's first weight blocks pulled
+// into L2.
 template <int STAGES, int STAGE_BYTES>
 __device__ __forceinline__ void moe_produce(const EngineParams &p1, const EngineParams &p2,
                                             const CUtensorMap *wmap1, const CUtensorMap *xmap1,
