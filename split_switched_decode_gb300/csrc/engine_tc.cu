@@ -23,6 +23,11 @@
 // NG = 4) -- and the epilogue reduces and stores the column groups one after another,
 // each with its own partial slots and arrival counter.
 //
+// Whole-tile schedule (p.dyn, grouped launches): each CTA streams a static share of whole
+// tiles and claims the rest one at a time from a counter. engine_tc_moe_kernel (below)
+// runs the routed experts' gate/up and down, and by default the shared expert's, as one
+// launch of claimed whole tiles.
+//
 // Pair schedule (p.pair): every tile is split into exactly two k-halves and the two
 // workers of a tile run as a 2-CTA cluster. Instead of partial tiles in global memory
 // and an arrival counter, each CTA hands the partner the accumulator columns the
