@@ -387,14 +387,15 @@ DEC_API dec_status moe_layer_packed(const dec_bf16 *X, const dec_bf16 *Wcat, int
 
 /*
  * A measurement helper, not part of the decode path (like dec_sim_comm_wait): reads
- * dec_read_stream_bytes(bytes) bytes from the start of p into shared memory and writes
- * nothing. Every SM of the device streams a contiguous share of the buffer with 1-D bulk
- * copies of 16 KB, 8 in flight, the way the split-K tiles stream packed weights; the
- * rate it reaches is the read-only HBM ceiling the weight streams are measured against
- * (a copy benchmark counts read and written bytes). p: device memory, 16-byte aligned
- * (DEC_ERR_MISALIGNED), not NULL (DEC_ERR_INVALID_ARG). Less than 16 KB per SM reads
- * nothing (DEC_OK, no launch). Bounded waits as everywhere (DEC_ERR_TIMEOUT through
- * dec_sync_status).
+ * dec_read_stream_bytes(bytes) bytes (whole 256 KB chunks) from the start of p into
+ * shared memory and writes nothing. One CTA per SM claims chunks from a counter until
+ * none is left and streams each with 1-D bulk copies of 16 KB, 8 in flight, the way the
+ * expert tiles stream packed weights; the rate it reaches is the read-only HBM ceiling
+ * the weight streams are measured against (a copy benchmark counts read and written
+ * bytes). The counter is a library variable zeroed on `s` before each launch: calls on
+ * one device must not overlap. p: device memory, 16-byte aligned (DEC_ERR_MISALIGNED),
+ * not NULL (DEC_ERR_INVALID_ARG). Less than one chunk reads nothing (DEC_OK, no launch).
+ * Bounded waits as everywhere (DEC_ERR_TIMEOUT through dec_sync_status).
  */
 DEC_API size_t dec_read_stream_bytes(size_t bytes);
 DEC_API dec_status dec_read_stream(const void *p, size_t bytes, dec_stream_t s);

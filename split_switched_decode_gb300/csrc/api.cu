@@ -1438,9 +1438,8 @@ dec_status dec_sim_comm_wait(uint64_t ns, dec_stream_t s) {
 }
 
 size_t dec_read_stream_bytes(size_t bytes) {
-  const int sms = current_num_sms();
-  if (sms <= 0) return 0;
-  return (bytes / static_cast<size_t>(sms) / 16384u) * 16384u * static_cast<size_t>(sms);
+  const size_t c = read_stream_claim_bytes();
+  return (bytes / c) * c;
 }
 
 dec_status dec_read_stream(const void *p, size_t bytes, dec_stream_t s) {
@@ -1449,9 +1448,8 @@ dec_status dec_read_stream(const void *p, size_t bytes, dec_stream_t s) {
   cudaError_t ce;
   DeviceInfo *d = device_info(&ce);
   if (!d) return DEC_ERR_CUDA;
-  const size_t per_cta = (bytes / static_cast<size_t>(d->num_sms) / 16384u) * 16384u;
-  if (per_cta == 0) return DEC_OK;  // less than 16 KB per SM: nothing to read
-  return cuda_status(launch_read_stream(p, per_cta, d->num_sms, d->status,
+  if (bytes < read_stream_claim_bytes()) return DEC_OK;  // less than one chunk: nothing
+  return cuda_status(launch_read_stream(p, bytes, d->num_sms, d->status,
                                         g_wait_limit_ns.load(),
                                         reinterpret_cast<cudaStream_t>(s)));
 }

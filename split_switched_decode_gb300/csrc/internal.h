@@ -226,9 +226,10 @@ cudaError_t launch_gather_map(const uint16_t *X, const int32_t *topk_idx, int B,
                               int max_ctas, int *dyn_reset, int nreset, int shared_rows,
                               cudaStream_t s);
 cudaError_t launch_comm_wait(uint64_t ns, cudaStream_t s);
-// Read-stream measurement: `ctas` CTAs, each reading per_cta bytes (a multiple of 16 KB)
-// of p into shared memory (moe_aux.cu).
-cudaError_t launch_read_stream(const void *p, size_t per_cta, int ctas, unsigned *status,
+// Read-stream measurement: `ctas` CTAs claim 256 KB chunks (read_stream_claim_bytes) of
+// the first `bytes` of p and read them into shared memory (moe_aux.cu).
+size_t read_stream_claim_bytes();
+cudaError_t launch_read_stream(const void *p, size_t bytes, int ctas, unsigned *status,
                                uint64_t limit_ns, cudaStream_t s);
 cudaError_t launch_gather_rows(const uint16_t *X, const int32_t *route_map, int B, int topk,
                                int E, int K, uint16_t *Xg, int *dyn_reset, int nreset,

@@ -369,14 +369,19 @@ __global__ void wait_selftest_kernel(unsigned *status, uint64_t limit_ns) {
 
 // Occupies its stream for ns nanoseconds (globaltimer) while touching no memory: a
 // stand-in for a communication phase that leaves HBM idle.
-// HBM read-stream measurement (dec_read_stream): CTA c streams bytes
-// [c * per_cta, (c + 1) * per_cta) into RS_STAGES rotating 16 KB shared-memory stages
-// with 1-D bulk copies, one thread issuing and the stage's mbarrier counting the bytes;
-// nothing is written anywhere. Every wait is bounded; after a time-out the copies still
-// in flight land before the CTA exits.
+// HBM read-stream measurement (dec_read_stream): every CTA claims 256 KB chunks of the
+// buffer from a counter (*next, zeroed before the launch) until none is left and streams
+// each into RS_STAGES rotating 16 KB shared-memory stages with 1-D bulk copies, one
+// thread issuing and the stage's mbarrier counting the bytes; nothing is written
+// anywhere. Claiming, rather than a fixed share per CTA, keeps SMs that happen to stream
+// slower in a given call from setting its end. Every wait is bounded; after a time-out
+// the copies still in flight land before the CTA exits.
 constexpr int RS_STAGES = 8;
 constexpr int RS_CHUNK = 16384;
-__global__ void __launch_bounds__(32) read_stream_kernel(const uint8_t *p, size_t per_cta,
+constexpr int RS_CLAIM = 16;  // 16 KB pieces per claimed chunk
+__device__ unsigned long long g_rs_next;  // the current call's next chunk (one per device)
+__global__ void __launch_bounds__(32) read_stream_kernel(const uint8_t *p, long long nchunks,
+                                                         unsigned long long *next,
                                                          unsigned *status, uint64_t limit_ns) {
   extern __shared__ __align__(1024) uint8_t rs_stage[];
   __shared__ __align__(8) uint64_t bar[RS_STAGES];
@@ -385,27 +390,34 @@ __global__ void __launch_bounds__(32) read_stream_kernel(const uint8_t *p, size_
   abort_flag = 0;
   for (int s = 0; s < RS_STAGES; ++s) mbar_init(&bar[s], 1);
   fence_mbar_init();
-  const uint8_t *b = p + per_cta * blockIdx.x;
-  const long long n = static_cast<long long>(per_cta / RS_CHUNK);
-  long long issued = 0;
-  for (long long c = 0; c < n + RS_STAGES; ++c) {
-    if (c >= RS_STAGES) {
-      const long long d = c - RS_STAGES;
-      if (!mbar_wait_bounded(&bar[d % RS_STAGES], static_cast<uint32_t>((d / RS_STAGES) & 1),
-                             status, &abort_flag, limit_ns))
-        break;
+  long long chunk = 0, k = 0;  // k: pieces issued by this CTA
+  int sub = RS_CLAIM;          // pieces of the current chunk already issued
+  for (;;) {
+    if (sub == RS_CLAIM) {
+      chunk = static_cast<long long>(atomicAdd(next, 1ull));
+      sub = 0;
     }
-    if (c < n) {
-      const int s = static_cast<int>(c % RS_STAGES);
-      mbar_arrive_expect_tx(&bar[s], RS_CHUNK);
-      bulk_load_1d(rs_stage + s * RS_CHUNK, b + c * RS_CHUNK, RS_CHUNK, &bar[s]);
-      ++issued;
-    }
+    if (chunk >= nchunks) break;
+    const int s = static_cast<int>(k % RS_STAGES);
+    // the stage's previous piece must have landed before it is reused
+    if (k >= RS_STAGES &&
+        !mbar_wait_bounded(&bar[s], static_cast<uint32_t>(((k / RS_STAGES) - 1) & 1), status,
+                           &abort_flag, limit_ns))
+      break;
+    mbar_arrive_expect_tx(&bar[s], RS_CHUNK);
+    bulk_load_1d(rs_stage + s * RS_CHUNK, p + (chunk * RS_CLAIM + sub) * RS_CHUNK, RS_CHUNK,
+                 &bar[s]);
+    ++sub;
+    ++k;
   }
-  if (abort_flag) {
-    for (long long d = issued > RS_STAGES ? issued - RS_STAGES : 0; d < issued; ++d)
+  // the last pieces in flight (bounded; without a status update after a time-out)
+  for (long long d = k > RS_STAGES ? k - RS_STAGES : 0; d < k; ++d) {
+    if (abort_flag)
       (void)mbar_wait_drain(&bar[d % RS_STAGES], static_cast<uint32_t>((d / RS_STAGES) & 1),
                             10000000ull);
+    else if (!mbar_wait_bounded(&bar[d % RS_STAGES], static_cast<uint32_t>((d / RS_STAGES) & 1),
+                                status, &abort_flag, limit_ns))
+      continue;
   }
 }
 
@@ -452,15 +464,21 @@ cudaError_t launch_pack_weight(const uint16_t *W, int N, int K, uint16_t *Wp, cu
   return cudaGetLastError();
 }
 
-cudaError_t launch_read_stream(const void *p, size_t per_cta, int ctas, unsigned *status,
+size_t read_stream_claim_bytes() { return static_cast<size_t>(RS_CLAIM) * RS_CHUNK; }
+
+cudaError_t launch_read_stream(const void *p, size_t bytes, int ctas, unsigned *status,
                                uint64_t limit_ns, cudaStream_t s) {
   const size_t smem = static_cast<size_t>(RS_STAGES) * RS_CHUNK;
   cudaError_t e = cudaFuncSetAttribute(read_stream_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  read_stream_kernel<<<ctas, 32, smem, s>>>(static_cast<const uint8_t *>(p), per_cta, status,
-                                            limit_ns);
+  void *next = nullptr;
+  if ((e = cudaGetSymbolAddress(&next, g_rs_next)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(next, 0, sizeof(unsigned long long), s)) != cudaSuccess) return e;
+  read_stream_kernel<<<ctas, 32, smem, s>>>(
+      static_cast<const uint8_t *>(p), static_cast<long long>(bytes / read_stream_claim_bytes()),
+      static_cast<unsigned long long *>(next), status, limit_ns);
   return cudaGetLastError();
 }
 
