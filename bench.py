@@ -6,10 +6,10 @@ at every decode batch B in {1,2,4,8,16,32,64}, on synthetic bf16 inputs:
 
     input projection   Y = X . W^T            K=7168  -> N=8192       (batch switch)
     output projection  Y = X . W^T + R        K=16384 -> N=7168       (split-K + residual)
-    L2 prefetch        shared-expert gate/up weights, side stream, during the front end
     MoE front end      router 384 + latent 512 rows in one product, softmax, top-8
     MoE experts        384 routed experts (gate/up 2x2048x7168, down 7168x2048) grouped
-                       GEMV + shared expert of the same shape on a side stream + combine
+                       GEMV + the shared expert of the same shape, one launch, + combine
+    (--prefetch adds an L2 prefetch of the shared expert's weights during the front end)
 
 `value` is the whole step's algorithmic HBM bytes (weights read once + activations in
 and out, using the actual number of distinct experts each batch routes to) divided by
@@ -48,8 +48,8 @@ PREFETCH_BYTES = 24 << 20
 WORKLOAD = ("Kimi-K3-shaped decode layer hot path, B in {1,2,4,8,16,32,64}: input projection "
             "7168->8192 (batch-size kernel switch), output projection 16384->7168 + residual, "
             "MoE front end 7168->384 router + 512 latent with softmax/top-8, 384 routed experts "
-            "(gate/up 2x2048x7168, down 7168x2048) + shared expert on a side stream "
-            "overlapping the routed experts")
+            "(gate/up 2x2048x7168, down 7168x2048) + shared expert overlapping them (its "
+            "tiles in the routed experts' launch)")
 
 
 def parse_args():
@@ -269,9 +269,8 @@ class Workload:
         self.launches += expert_launches()
 
     def op_layer(self, B, v=0):
-        """moe_layer: the front end runs while the shared expert streams its weights on the
-        side stream, then the routed experts (no separate L2 prefetch: the shared expert's
-        own reads fill the front end's idle HBM time)."""
+        """moe_layer: the front end and the experts in one call (on the side-stream path the
+        shared expert streams its weights during the front end)."""
         d = self.t[B]
         self.ssd.moe_layer(d["x_moe"][v], self.W_cat[0], self.E, L, TOPK, self.Wgu, self.Wd,
                            self.Wgs, self.Wds, d["lat"][v], d["idx"][v], d["w"][v], d["y_moe"],
