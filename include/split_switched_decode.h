@@ -77,15 +77,18 @@ typedef enum {
     DEC_VARIANT_TINY = 0,        /* tiny-matrix GEMV, B <= 2, CUDA cores              */
     DEC_VARIANT_SPLITK = 1,      /* split-K, TMA-staged weight tiles, CUDA cores     */
     DEC_VARIANT_SPLITK_TC = 2,   /* split-K, TMA-staged tiles, tcgen05 tensor cores  */
-    DEC_VARIANT_FRONT_ONE_LAUNCH = 3 /* moe_front as one launch: tensor-core product,
-                                        on-chip split-K reduction, routing, route map */
+    DEC_VARIANT_FRONT_ONE_LAUNCH = 3, /* moe_front as one launch: tensor-core product,
+                                         on-chip split-K reduction, routing, route map */
+    DEC_VARIANT_SPLITK_TC_PAIR = 4   /* 129..512 rows: CTA-pair tensor-core tiles (M = 256
+                                        weight rows per MMA over two SMs), one launch */
 } dec_variant;
 
 /* ------------------------------------------------------------ diagnostics ---- */
 
 /* Static English text for a status code (never NULL). */
 DEC_API const char *dec_status_string(int status);
-/* Static name of a variant ("tiny", "splitk", "splitk_tc", "front_one_launch", "none"). */
+/* Static name of a variant ("tiny", "splitk", "splitk_tc", "front_one_launch",
+ * "splitk_tc_pair", "none"). */
 DEC_API const char *dec_variant_name(int variant);
 /* Variant launched by the most recent successful projection call on this host
  * thread (dec_gemv, dec_splitk_gemm, dec_linear, moe_front), or DEC_VARIANT_NONE. */

@@ -29,6 +29,7 @@ VARIANT_TINY = 0
 VARIANT_SPLITK = 1
 VARIANT_SPLITK_TC = 2
 VARIANT_FRONT_ONE_LAUNCH = 3
+VARIANT_SPLITK_TC_PAIR = 4
 
 # every symbol the public header declares
 EXPORTS = [

@@ -20,7 +20,7 @@ LIB_NAME = "libsplit_switched_decode.so"
 LIB_PATH = os.path.join(OUT_DIR, LIB_NAME)
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["api.cu", "gemv_tiny.cu", "engine_cc.cu", "engine_tc.cu", "moe_aux.cu",
-           "front_fused.cu"]
+           "front_fused.cu", "engine_pair.cu"]
 HEADERS = ["common.cuh", "engine.cuh", "routing.cuh", "tcgen05.cuh", "internal.h"]
 
 

@@ -385,6 +385,96 @@ dec_status run_splitk_rows(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 
                            int B, int N, int K, int split_k, int use_tc, void *ws,
                            size_t ws_bytes, cudaStream_t s, bool packed = false);
 
+// Wide projections from DEC_WIDE_PAIR_MIN_B rows (default 129) up to 512 on CTA-pair
+// tensor-core tiles, one launch per call (DEC_WIDE_PAIR_MMA=0: launches of at most 256
+// rows on one-CTA tiles, each reading W).
+bool wide_pair_mma() {
+  if (const char *s = std::getenv("DEC_WIDE_PAIR_MMA")) return std::atoi(s) != 0;
+  return true;
+}
+int wide_pair_min_batch() {
+  if (const char *s = std::getenv("DEC_WIDE_PAIR_MIN_B")) {
+    const int v = std::atoi(s);
+    if (v >= MAX_B + 1) return v;
+  }
+  return 2 * MAX_B + 1;
+}
+
+// 4-CTA clusters of the pair kernel the device holds at once, per device and MMA count.
+std::atomic<int> g_pair_clusters[kMaxDevices][2];
+std::once_flag g_pair_init_once;
+
+int pair_clusters(int nmma) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  std::call_once(g_pair_init_once, []() {
+    for (auto &d : g_pair_clusters)
+      for (auto &v : d) v.store(-1);
+  });
+  std::atomic<int> &slot = g_pair_clusters[dev][nmma - 1];
+  int n = slot.load();
+  if (n < 0) {
+    if (engine_pair_max_clusters(nmma, &n) != cudaSuccess) {
+      (void)cudaGetLastError();
+      n = 0;
+    }
+    slot.store(n);
+  }
+  return n;
+}
+
+// Whether a call of B rows takes the CTA-pair kernel: every 256-row slice of W needs one
+// resident cluster (a second wave would double the time).
+bool use_pair_kernel(int B, int N, int K, int split_k, int use_tc) {
+  if (!use_tc || split_k != 0 || !wide_pair_mma() || B < wide_pair_min_batch() || B > MAX_ROWS)
+    return false;
+  if (ceil_div(K, TILE_K) < 2) return false;
+  const int slices = (ceil_div(N, TILE_N) + 1) / 2;
+  return pair_clusters(pair_mma_count(B)) >= slices;
+}
+
+// The CTA-pair launch. The workspace is checked as for the one-CTA launches (the same
+// size contract whichever kernel runs); the pair kernel itself uses none of it.
+dec_status run_pair_projection(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 *R,
+                               dec_bf16 *Y, int B, int N, int K, void *ws, size_t ws_bytes,
+                               cudaStream_t s, bool packed) {
+  cudaError_t ce;
+  DeviceInfo *d = device_info(&ce);
+  if (!d) return DEC_ERR_CUDA;
+  SplitPlan pl;
+  if (!plan_splitk(rows_per_launch(B), N, K, 0, d->num_sms, &pl))
+    return DEC_ERR_UNSUPPORTED_SHAPE;
+  if (!ws) return DEC_ERR_INVALID_ARG;
+  if (!aligned16(ws)) return DEC_ERR_MISALIGNED;
+  if (ws_bytes < pl.total) return DEC_ERR_WORKSPACE_TOO_SMALL;
+  CUtensorMap wmap, xmap;
+  const bool wmap_ok = packed ? make_map(&wmap, W, TILE_K, static_cast<uint64_t>(N) * pl.KB, 128)
+                              : make_map(&wmap, W, K, N, 128);
+  if (!wmap_ok || !make_map(&xmap, X, K, B, 128)) return DEC_ERR_CUDA;
+  EngineParams p;
+  std::memset(&p, 0, sizeof p);
+  p.mode = MODE_LINEAR;
+  p.N = N;
+  p.K = K;
+  p.T = pl.T;
+  p.KB = pl.KB;
+  p.G = 4 * ((pl.T + 1) / 2);
+  p.B = B;
+  p.ngrp = 1;
+  p.Y = Y;
+  p.R = R;
+  p.vec_y = (N % 8 == 0 && aligned16(Y) && (R == nullptr || aligned16(R))) ? 1 : 0;
+  p.packed = packed ? 1 : 0;
+  p.status = d->status;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  if (consume_fault()) return DEC_ERR_CUDA;
+  ce = launch_engine_pair(pair_mma_count(B), wmap, xmap, p, s);
+  if (ce == cudaErrorNotSupported) return DEC_ERR_UNSUPPORTED_SHAPE;
+  if (ce != cudaSuccess) return DEC_ERR_CUDA;
+  t_last_variant = DEC_VARIANT_SPLITK_TC_PAIR;
+  return DEC_OK;
+}
+
 // A projection of more than 256 rows (speculative verification of up to 64 sequences x
 // 8 tokens) runs as consecutive launches over row blocks, each reading W; on one
 // stream, each launch's workspace use begins after the previous launch has finished
@@ -392,6 +482,8 @@ dec_status run_splitk_rows(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 
 dec_status run_splitk(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 *R, dec_bf16 *Y,
                       int B, int N, int K, int split_k, int use_tc, void *ws, size_t ws_bytes,
                       cudaStream_t s, bool packed = false) {
+  if (use_pair_kernel(B, N, K, split_k, use_tc))
+    return run_pair_projection(X, W, R, Y, B, N, K, ws, ws_bytes, s, packed);
   if (B <= MAX_B_WIDE)
     return run_splitk_rows(X, W, R, Y, B, N, K, split_k, use_tc, ws, ws_bytes, s, packed);
   if (!use_tc) return DEC_ERR_UNSUPPORTED_SHAPE;
@@ -712,6 +804,7 @@ const char *dec_variant_name(int variant) {
     case DEC_VARIANT_SPLITK: return "splitk";
     case DEC_VARIANT_SPLITK_TC: return "splitk_tc";
     case DEC_VARIANT_FRONT_ONE_LAUNCH: return "front_one_launch";
+    case DEC_VARIANT_SPLITK_TC_PAIR: return "splitk_tc_pair";
     default: return "none";
   }
 }

@@ -1,0 +1,326 @@
+// engine_pair.cu -- wide projections (129-512 rows per call) on CTA-pair tensor-core
+// tiles.
+//
+// Speculative-decode verification multiplies one weight matrix by many activation rows
+// (sequences x (draft length + 1) tokens). With one CTA per 128-row weight tile, every
+// tile re-reads all M activation rows from L2 (M x 128 bytes per 16 KB of weights per
+// k-block), and from M = 256 on those bytes, not the weights, bound each SM. Here two CTAs
+// share one MMA (tcgen05 .cta_group::2, M = 256 weight rows): each CTA stages its own 128
+// weight rows and half of the activation rows of every k-block, so each SM receives half
+// the activation bytes per weight byte, and a 512-row call is one launch that reads W
+// once.
+//
+// One cluster of 4 CTAs per 256-row slice of W (weight tiles 2c and 2c+1):
+//   rank 0: tile 2c,   k-half 0  -- issues the pair MMA of ranks 0 and 1
+//   rank 1: tile 2c+1, k-half 0
+//   rank 2: tile 2c,   k-half 1  -- issues the pair MMA of ranks 2 and 3
+//   rank 3: tile 2c+1, k-half 1
+// Per k-block each CTA loads its 16 KB weight box and NMMA activation boxes of 128 rows
+// (rows 256m + 128h .. +127 for MMA m, h = rank & 1), so MMA m covers batch columns
+// 256m .. 256m+255 with N = 256 (rows beyond the batch read as zeros). Batch column j
+// accumulates in tensor-memory column j (NMMA x 256 columns; all 512 at NMMA = 2).
+//
+// Ring: the even CTA's full barrier of a stage counts both CTAs' bytes (the odd CTA's
+// copies signal it through the CTA-pair form of the TMA load); the MMA thread arms each
+// stage's next fill when it consumes the current one, so every copy either CTA issues
+// lands on an armed phase; the commit that frees a stage arrives on the empty barriers of
+// both CTAs (multicast), and after the last k-block a multicast commit tells both CTAs
+// that their accumulators are final.
+//
+// Tail: the two k-halves of a weight tile are ranks r and r ^ 2. k-half 0 finishes batch
+// columns [0, 128 NMMA), k-half 1 the rest. Once every CTA of the cluster is past its
+// MMAs (cluster barrier 1: every ring is idle), each CTA writes the partner's columns of
+// its accumulator into the partner's ring; after cluster barrier 2 each adds the two
+// halves for its columns, adds R, rounds once to bf16 and stores Y. No partial tile goes
+// through global memory and no counter is used.
+#include <atomic>
+
+#include "engine.cuh"
+#include "tcgen05.cuh"
+
+namespace ssd {
+
+namespace {
+
+constexpr int PAIR_THREADS = 192;  // warp 0 TMA, warp 1 MMA + tensor memory, warps 2-5 tail
+constexpr int PAIR_SMEM_LIMIT = 232448;
+
+template <int NMMA>
+struct PairConfig {
+  static constexpr int STAGE_BYTES = 16384 + NMMA * 16384;
+  static constexpr int TAIL = 256;
+  static constexpr int FIT = (PAIR_SMEM_LIMIT - 1024 - TAIL) / STAGE_BYTES;
+  static constexpr int STAGES = FIT > 8 ? 8 : FIT;
+  static constexpr int HALF = 128 * NMMA;            // batch columns one k-half finishes
+  static constexpr uint32_t TMEM_COLS = 256u * NMMA;
+  static constexpr int RECV_BYTES = HALF * 128 * 4;  // the partner's partial of them
+  static constexpr int OUT_BYTES = 64 * 128 * 4;     // one 64-column group of sums
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + TAIL;
+  static_assert(STAGES >= 4, "pipeline too shallow");
+  static_assert(RECV_BYTES + OUT_BYTES <= STAGES * STAGE_BYTES, "tail does not fit the ring");
+};
+
+// The weight box of tile t, k-block kb (row-major W, or the tile-packed 16 KB block).
+__device__ __forceinline__ void pair_load_w(const EngineParams &p, const CUtensorMap *wmap,
+                                            uint8_t *dst, uint32_t bar, int t, int kb,
+                                            uint64_t pol) {
+  if (p.packed)
+    tma_load_2d_pair_hint(dst, wmap, bar, 0, (t * p.KB + kb) * TILE_N, pol);
+  else
+    tma_load_2d_pair_hint(dst, wmap, bar, kb * TILE_K, t * TILE_N, pol);
+}
+
+template <int NMMA>
+__global__ void __launch_bounds__(PAIR_THREADS, 1)
+    engine_pair_kernel(const __grid_constant__ CUtensorMap wmap,
+                       const __grid_constant__ CUtensorMap xmap, const EngineParams p) {
+  using C = PairConfig<NMMA>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t *ring = smem;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t *empty = full + C::STAGES;
+  uint64_t *acc_full = empty + C::STAGES;
+  uint64_t *drain = acc_full + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *flags = reinterpret_cast<volatile int *>(tmem_slot + 1);  // [0] abort
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_ctarank();
+  const uint32_t h = rank & 1u;      // weight tile of the slice
+  const uint32_t kh = rank >> 1;     // k-half
+  const uint32_t lead = rank & ~1u;  // the pair's MMA-issuing CTA
+  const bool leader = h == 0;
+  const int t = 2 * static_cast<int>(blockIdx.x >> 2) + static_cast<int>(h);
+  const int kb0 = (static_cast<int>(kh) * p.KB) >> 1;
+  const int nkb = (((static_cast<int>(kh) + 1) * p.KB) >> 1) - kb0;  // >= 1: KB >= 2
+
+  if (tid == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(drain, 1);
+    flags[0] = 0;
+    // the even CTA arms the first fill of every stage for both CTAs' bytes
+    if (leader)
+      for (int s = 0; s < C::STAGES && s < nkb; ++s)
+        mbar_arrive_expect_tx(&full[s], 2u * C::STAGE_BYTES);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  // every CTA of the cluster has initialised and armed its barriers before a copy or a
+  // commit of another CTA can signal one
+  cluster_sync_all();
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      prefetch_tensormap(&wmap);
+      prefetch_tensormap(&xmap);
+      const uint64_t pol = policy_evict_first();  // weights are read once per launch
+      const uint32_t bar0 = cluster_map(full, lead);  // the pair's full barriers
+      const int pre = nkb < C::STAGES ? nkb : C::STAGES;
+      for (int q = 0; q < pre; ++q)  // weights only: they do not depend on earlier kernels
+        pair_load_w(p, &wmap, ring + q * C::STAGE_BYTES, bar0 + 8u * q, t, kb0 + q, pol);
+      griddep_wait();
+      for (int q = 0; q < nkb; ++q) {
+        const int st = q % C::STAGES;
+        uint8_t *dst = ring + st * C::STAGE_BYTES;
+        const uint32_t bar = bar0 + 8u * static_cast<uint32_t>(st);
+        if (q >= pre) {
+          if (!mbar_wait_bounded(&empty[st], ((q / C::STAGES) & 1) ^ 1, p.status, flags,
+                                 p.wait_limit_ns))
+            break;
+          pair_load_w(p, &wmap, dst, bar, t, kb0 + q, pol);
+        }
+#pragma unroll
+        for (int m = 0; m < NMMA; ++m)
+          tma_load_2d_pair(dst + 16384 * (1 + m), &xmap, bar, (kb0 + q) * TILE_K,
+                           256 * m + 128 * static_cast<int>(h));
+      }
+      // every load of this CTA is issued: the next kernel may be scheduled as SMs free up
+      griddep_launch_dependents();
+    } else {
+      griddep_wait();
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA issuer
+    griddep_wait();
+    if (leader && lane == 0) {
+      const uint32_t idesc = idesc_bf16_pair(256);
+      const uint16_t mask = static_cast<uint16_t>(3u << lead);
+      bool ok = true;
+      int q = 0;
+      for (; q < nkb; ++q) {
+        const int st = q % C::STAGES;
+        if (!mbar_wait_bounded(&full[st], (q / C::STAGES) & 1, p.status, flags,
+                               p.wait_limit_ns)) {
+          ok = false;
+          break;
+        }
+        // arm the stage's next fill (both CTAs issue it only after this stage is freed)
+        if (q + C::STAGES < nkb) mbar_arrive_expect_tx(&full[st], 2u * C::STAGE_BYTES);
+        tc_fence_after();
+        const uint32_t a_addr = smem_u32(ring + st * C::STAGE_BYTES);
+        const uint64_t adesc = sw128_desc(a_addr);
+#pragma unroll
+        for (int m = 0; m < NMMA; ++m) {
+          const uint64_t bdesc = sw128_desc(a_addr + 16384u * (1 + m));
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)  // K = 16 per MMA: +32 bytes along the swizzled row
+            tc_mma_pair(tmem_base + 256u * m, adesc + 2u * kk, bdesc + 2u * kk, idesc,
+                        (q > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit_pair_mc(&empty[st], mask);  // both CTAs' stage is free once read
+      }
+      if (ok) {
+        tc_commit_pair_mc(acc_full, mask);  // both accumulators final
+      } else {
+        // after a time-out: let the MMAs issued so far finish, then the copies of both
+        // CTAs into the stages armed but not consumed, before any memory is released
+        tc_commit_pair(drain);
+        (void)mbar_wait_drain(drain, 0u, 10000000ull);
+        const int qe = q + C::STAGES < nkb ? q + C::STAGES : nkb;
+        for (int qq = q; qq < qe; ++qq)
+          (void)mbar_wait_drain(&full[qq % C::STAGES], (qq / C::STAGES) & 1u, 10000000ull);
+      }
+    }
+  } else {
+    griddep_wait();
+    (void)mbar_wait_bounded(acc_full, 0u, p.status, flags, p.wait_limit_ns);
+  }
+
+  // ---------------------------------------------------------------------- tail
+  tc_fence_before();
+  __syncthreads();
+  const bool go = !flags[0];  // uniform across the CTA after the barrier
+  // 1: every CTA of the cluster is past its MMAs (or gave up): every ring is idle
+  cluster_sync_all();
+  tc_fence_after();
+  float *recv = reinterpret_cast<float *>(ring);                  // [HALF][128]
+  float *out = reinterpret_cast<float *>(ring + C::RECV_BYTES);   // [64][128]
+  const int own0 = static_cast<int>(kh) * C::HALF;  // first batch column this CTA finishes
+  const int oth0 = C::HALF - own0;                  // the partner's
+  const int r = 32 * (warp & 3) + lane;             // tile row == tensor-memory lane
+  const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+  if (go && warp >= 2) {
+    const uint32_t dst = cluster_map(recv, rank ^ 2u) + 4u * static_cast<uint32_t>(r);
+    for (int c = 0; c < C::HALF && oth0 + c < p.B; c += 16) {
+      float v[16];
+      tmem_ld16(taddr + static_cast<uint32_t>(oth0 + c), v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) st_cluster_f32(dst + 512u * static_cast<uint32_t>(c + j), v[j]);
+    }
+  }
+  tc_fence_before();
+  // 2: the partner's columns have landed in this CTA's ring
+  cluster_sync_all();
+  tc_fence_after();
+  if (go && warp >= 2) {
+    for (int g = 0; g < C::HALF / 64 && own0 + 64 * g < p.B; ++g) {
+      const int col0 = own0 + 64 * g;
+      float v[64];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        tmem_ld16(taddr + static_cast<uint32_t>(col0 + 16 * c), v + 16 * c);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 64; ++j) out[j * 128 + r] = v[j] + recv[(64 * g + j) * 128 + r];
+      named_bar_sync(2, 128);
+      for (int c = r; c < 64 * 16; c += 128) {
+        const int j = c >> 4, row8 = (c & 15) * 8;
+        const int col = col0 + j, n0 = t * TILE_N + row8;
+        if (col >= p.B || n0 >= p.N) continue;
+        const float *src = out + j * 128 + row8;
+        if (p.vec_y) {
+          store_y8(p, col, n0, *reinterpret_cast<const float4 *>(src),
+                   *reinterpret_cast<const float4 *>(src + 4));
+        } else {
+          for (int e = 0; e < 8 && n0 + e < p.N; ++e) {
+            float y = src[e];
+            const size_t off = static_cast<size_t>(col) * p.N + n0 + e;
+            if (p.R != nullptr) y += bf16_to_f32(p.R[off]);
+            p.Y[off] = f32_to_bf16_rn(y);
+          }
+        }
+      }
+      named_bar_sync(2, 128);  // `out` is rewritten by the next group
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+}
+
+template <int NMMA>
+cudaError_t set_pair_attrs() {
+  static std::atomic<uint64_t> attr_set{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(attr_set.load() & bit)) {
+    e = cudaFuncSetAttribute(engine_pair_kernel<NMMA>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, PairConfig<NMMA>::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set.fetch_or(bit);
+  }
+  return cudaSuccess;
+}
+
+template <int NMMA>
+cudaError_t launch_pair_t(const CUtensorMap &wmap, const CUtensorMap &xmap, const EngineParams &p,
+                          cudaStream_t s) {
+  cudaError_t e = set_pair_attrs<NMMA>();
+  if (e != cudaSuccess) return e;
+  const int slices = (p.T + 1) / 2;
+  return launch_pdl_cluster(engine_pair_kernel<NMMA>, dim3(4 * slices), dim3(PAIR_THREADS),
+                            PairConfig<NMMA>::SMEM, s, 4, wmap, xmap, p);
+}
+
+template <int NMMA>
+cudaError_t max_clusters_t(int *n) {
+  cudaError_t e = set_pair_attrs<NMMA>();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(4 * 64);
+  cfg.blockDim = dim3(PAIR_THREADS);
+  cfg.dynamicSmemBytes = PairConfig<NMMA>::SMEM;
+  cudaLaunchAttribute a[1];
+  a[0].id = cudaLaunchAttributeClusterDimension;
+  a[0].val.clusterDim.x = 4;
+  a[0].val.clusterDim.y = 1;
+  a[0].val.clusterDim.z = 1;
+  cfg.attrs = a;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(n, engine_pair_kernel<NMMA>, &cfg);
+}
+
+}  // namespace
+
+int pair_mma_count(int B) { return B <= 256 ? 1 : 2; }
+
+cudaError_t engine_pair_max_clusters(int nmma, int *n) {
+  return nmma == 1 ? max_clusters_t<1>(n) : max_clusters_t<2>(n);
+}
+
+cudaError_t launch_engine_pair(int nmma, const CUtensorMap &wmap, const CUtensorMap &xmap,
+                               const EngineParams &p, cudaStream_t s) {
+  if (p.mode != MODE_LINEAR || p.grouped || p.KB < 2 || p.T < 1 || p.B < 1 ||
+      p.B > 256 * nmma || (nmma != 1 && nmma != 2))
+    return cudaErrorNotSupported;
+  return nmma == 1 ? launch_pair_t<1>(wmap, xmap, p, s) : launch_pair_t<2>(wmap, xmap, p, s);
+}
+
+}  // namespace ssd

@@ -126,6 +126,16 @@ int engine_maxc_for(int ncols);                 // 2, 4, 8, 16, 32 or 64
 cudaError_t launch_engine_cc(int maxc, const CUtensorMap &wmap, const CUtensorMap &xmap,
                              const EngineParams &p, cudaStream_t s);
 
+// ----------------------------------------------------------- engine_pair.cu --
+// Wide projections (MODE_LINEAR, one group of p.B <= 256 * nmma columns, p.KB >= 2) on
+// CTA-pair tensor-core tiles: clusters of 4 CTAs per 256 rows of W ((p.T + 1) / 2
+// clusters), the two k-halves added inside the cluster; xmap has 128-row boxes, wmap
+// 128-row boxes (or tile-packed blocks). No workspace.
+int pair_mma_count(int B);  // MMAs of N = 256 per K step: 1 up to 256 rows, else 2
+cudaError_t engine_pair_max_clusters(int nmma, int *n);
+cudaError_t launch_engine_pair(int nmma, const CUtensorMap &wmap, const CUtensorMap &xmap,
+                               const EngineParams &p, cudaStream_t s);
+
 // ------------------------------------------------------------- engine_tc.cu --
 cudaError_t launch_engine_tc(int maxc, const CUtensorMap &wmap, const CUtensorMap &xmap,
                              const EngineParams &p, cudaStream_t s);

@@ -61,6 +61,51 @@ __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// CTA-pair forms (.cta_group::2): the two CTAs of a cluster whose ranks differ only in
+// bit 0 share one MMA. Allocation and release are collective: one warp of each CTA of
+// the pair executes them. The MMA is issued by one thread of the even-ranked CTA; A is
+// M = 256 rows, rows 0-127 from that CTA's shared memory and rows 128-255 from the same
+// offset in the odd-ranked CTA; B's N columns are split the same way (first N/2 in the
+// even CTA); each CTA's tensor memory receives its own 128 rows x N columns of D. Every
+// tcgen05 instruction of a kernel that uses these takes the same .cta_group.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_mma_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on the mbarrier at `bar`'s offset in every CTA of `cta_mask` (bit = rank)
+// when every pair MMA this thread issued so far has completed.
+__device__ __forceinline__ void tc_commit_pair_mc(uint64_t *bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit_pair(uint64_t *bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
 // Shared-memory matrix descriptor of a K-major operand stored with the 128-byte
 // swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart (stride byte offset),
 // leading byte offset unused for this layout, descriptor version 1, layout 2 (128B).
@@ -78,6 +123,13 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 __device__ __forceinline__ uint32_t idesc_bf16(int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
          (static_cast<uint32_t>(128 >> 4) << 24);
+}
+
+// Instruction descriptor of a CTA-pair MMA (kind::f16, fp32 accumulator, bf16 A and B,
+// both K-major): M = 256 over the pair, N = n (multiple of 32, 32..256).
+__device__ __forceinline__ uint32_t idesc_bf16_pair(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(256 >> 4) << 24);
 }
 
 }  // namespace ssd

@@ -49,6 +49,7 @@ def test_static_strings(ssd):
     assert lib.dec_variant_name(0) == b"tiny"
     assert lib.dec_variant_name(2) == b"splitk_tc"
     assert lib.dec_variant_name(3) == b"front_one_launch"
+    assert lib.dec_variant_name(4) == b"splitk_tc_pair"
     assert lib.dec_version() == 100
     assert lib.dec_last_variant() == -1
     assert lib.moe_route_map_ints(64, 384, 8) == 3 * 384 + 2 + 2 * 64 * 8

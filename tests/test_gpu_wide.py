@@ -2,7 +2,8 @@
 speculative-decoding verification (B sequences x (draft length + 1) tokens; "Hyper
 Optimizing Kimi K3 in vLLM", Part 3: Performance Deep Dive, decode with DSpark), where
 groups of 64 batch columns share each weight tile and are reduced separately (launches
-of at most 256 rows)."""
+of at most 256 rows), and from 129 rows the CTA-pair tiles (one launch up to 512 rows;
+tests/test_gpu_pair_projection.py covers that kernel on its own)."""
 import numpy as np
 import pytest
 
@@ -60,7 +61,10 @@ def test_wide_projection_matches_oracle(env, B, N, K, split_k):
     ws = ssd.workspace(ssd.dec_splitk_workspace_bytes(B, N, K, split_k), dev)
     ssd.dec_splitk_gemm(X, W, R, Y, ws, split_k=split_k, use_tc=1)
     torch.cuda.synchronize()
-    assert ssd.dec_last_variant() == ssd.VARIANT_SPLITK_TC
+    # from 129 rows the one-range-per-SM plan runs on CTA-pair tiles, one launch (two
+    # k-halves: at least two k-blocks)
+    pair = split_k == 0 and B > 128 and K > 64
+    assert ssd.dec_last_variant() == (ssd.VARIANT_SPLITK_TC_PAIR if pair else ssd.VARIANT_SPLITK_TC)
     assert ssd.dec_sync_status() == ssd.DEC_OK
     Y1 = Y.clone()
     ssd.dec_splitk_gemm(X, W, R, Y, ws, split_k=split_k, use_tc=1)
@@ -81,7 +85,8 @@ def test_wide_full_size_projections(env, B, which):
     ws = ssd.workspace(ssd.dec_linear_workspace_bytes(B, N, K), dev)
     ssd.dec_linear(X, W, R, Y, ws)
     torch.cuda.synchronize()
-    assert ssd.dec_last_variant() == ssd.VARIANT_SPLITK_TC
+    assert ssd.dec_last_variant() == (ssd.VARIANT_SPLITK_TC_PAIR if B > 128 else
+                                      ssd.VARIANT_SPLITK_TC)
     rng = np.random.default_rng(B)
     rows = np.unique(np.concatenate([rng.choice(N, 96, replace=False), [0, 127, 128, N - 1]]))
     assert_close(to_f64(oracle, Y)[:, rows], _ref(X, W, R, rows), f"{which} B={B}")
@@ -123,6 +128,7 @@ def test_wide_last_arriver_reduction(env, monkeypatch, B, N, K):
     """Wide projections with the reduction in each tile's last arriver (DEC_WIDE_DEFER=0)
     instead of the finishing kernel: same results within tolerance, deterministic."""
     torch, ssd, oracle, dev = env
+    monkeypatch.setenv("DEC_WIDE_PAIR_MMA", "0")  # the one-CTA tiles' reductions
     monkeypatch.setenv("DEC_WIDE_DEFER", "0")
     X, W, R, Y = _case(env, B, N, K, 24)
     ws = ssd.workspace(ssd.dec_splitk_workspace_bytes(B, N, K, 0), dev)
@@ -143,6 +149,7 @@ def test_wide_cluster_pair_matches_finishing_kernel(env, monkeypatch, B):
     column group by column group, give the same bits as the finishing kernel adding the
     same two partial tiles, and match the oracle."""
     torch, ssd, oracle, dev = env
+    monkeypatch.setenv("DEC_WIDE_PAIR_MMA", "0")  # one-CTA tiles, launches of <= 256 rows
     N, K = 8192, 1024
     X, W, R, Y = _case(env, B, N, K, 26)
     ws = ssd.workspace(ssd.dec_linear_workspace_bytes(B, N, K), dev)
