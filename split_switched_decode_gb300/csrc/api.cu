@@ -111,6 +111,22 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows,
   return r == CUDA_SUCCESS;
 }
 
+// A plain (unswizzled) 2-D map of a bf16 [rows, inner] tensor with boxes of box_inner x
+// box_rows elements, for whole-tile TMA loads and stores of outputs.
+bool make_map_plain(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows,
+                    uint32_t box_inner, uint32_t box_rows) {
+  if (!encoder_ready()) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int force_variant() {
   int v = g_force_variant.load();
   if (v == -2) {
@@ -467,8 +483,17 @@ dec_status run_pair_projection(const dec_bf16 *X, const dec_bf16 *W, const dec_b
   p.packed = packed ? 1 : 0;
   p.status = d->status;
   p.wait_limit_ns = g_wait_limit_ns.load();
+  // Y (and R) as whole tiles by TMA when their rows are 16-byte aligned (p.vec_y)
+  const int nmma = pair_mma_count(B);
+  CUtensorMap ymap, rmap;
+  std::memset(&ymap, 0, sizeof ymap);
+  std::memset(&rmap, 0, sizeof rmap);
+  if (p.vec_y) {
+    if (!make_map_plain(&ymap, Y, N, B, 128, 128 * nmma)) return DEC_ERR_CUDA;
+    if (R && !make_map_plain(&rmap, R, N, B, 128, 128 * nmma)) return DEC_ERR_CUDA;
+  }
   if (consume_fault()) return DEC_ERR_CUDA;
-  ce = launch_engine_pair(pair_mma_count(B), wmap, xmap, p, s);
+  ce = launch_engine_pair(nmma, wmap, xmap, ymap, rmap, p, s);
   if (ce == cudaErrorNotSupported) return DEC_ERR_UNSUPPORTED_SHAPE;
   if (ce != cudaSuccess) return DEC_ERR_CUDA;
   t_last_variant = DEC_VARIANT_SPLITK_TC_PAIR;

@@ -30,9 +30,11 @@
 // Tail: the two k-halves of a weight tile are ranks r and r ^ 2. k-half 0 finishes batch
 // columns [0, 128 NMMA), k-half 1 the rest. Once every CTA of the cluster is past its
 // MMAs (cluster barrier 1: every ring is idle), each CTA writes the partner's columns of
-// its accumulator into the partner's ring; after cluster barrier 2 each adds the two
-// halves for its columns, adds R, rounds once to bf16 and stores Y. No partial tile goes
-// through global memory and no counter is used.
+// its accumulator into the partner's ring; after cluster barrier 2 each adds its own half
+// to the received one (+ R, loaded as one TMA tile meanwhile), rounds once to bf16 into a
+// tile in its ring, releases tensor memory and writes the tile to Y with one TMA store
+// (rows of Y not 16-byte aligned: per-thread stores). No partial tile goes through
+// global memory and no counter is used.
 #include <atomic>
 
 #include "engine.cuh"
@@ -54,10 +56,10 @@ struct PairConfig {
   static constexpr int HALF = 128 * NMMA;            // batch columns one k-half finishes
   static constexpr uint32_t TMEM_COLS = 256u * NMMA;
   static constexpr int RECV_BYTES = HALF * 128 * 4;  // the partner's partial of them
-  static constexpr int OUT_BYTES = 64 * 128 * 4;     // one 64-column group of sums
+  static constexpr int TILE_BYTES = HALF * 128 * 2;  // R in, Y out: bf16 [HALF][128]
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + TAIL;
   static_assert(STAGES >= 4, "pipeline too shallow");
-  static_assert(RECV_BYTES + OUT_BYTES <= STAGES * STAGE_BYTES, "tail does not fit the ring");
+  static_assert(RECV_BYTES + TILE_BYTES <= STAGES * STAGE_BYTES, "tail does not fit the ring");
 };
 
 // The weight box of tile t, k-block kb (row-major W, or the tile-packed 16 KB block).
@@ -73,7 +75,9 @@ __device__ __forceinline__ void pair_load_w(const EngineParams &p, const CUtenso
 template <int NMMA>
 __global__ void __launch_bounds__(PAIR_THREADS, 1)
     engine_pair_kernel(const __grid_constant__ CUtensorMap wmap,
-                       const __grid_constant__ CUtensorMap xmap, const EngineParams p) {
+                       const __grid_constant__ CUtensorMap xmap,
+                       const __grid_constant__ CUtensorMap ymap,
+                       const __grid_constant__ CUtensorMap rmap, const EngineParams p) {
   using C = PairConfig<NMMA>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -83,7 +87,8 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
   uint64_t *empty = full + C::STAGES;
   uint64_t *acc_full = empty + C::STAGES;
   uint64_t *drain = acc_full + 1;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  uint64_t *rbar = drain + 1;  // the residual tile has landed
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(rbar + 1);
   volatile int *flags = reinterpret_cast<volatile int *>(tmem_slot + 1);  // [0] abort
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -103,6 +108,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
     }
     mbar_init(acc_full, 1);
     mbar_init(drain, 1);
+    mbar_init(rbar, 1);
     flags[0] = 0;
     // the even CTA arms the first fill of every stage for both CTAs' bytes
     if (leader)
@@ -207,20 +213,29 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
   // 1: every CTA of the cluster is past its MMAs (or gave up): every ring is idle
   cluster_sync_all();
   tc_fence_after();
-  float *recv = reinterpret_cast<float *>(ring);                  // [HALF][128]
-  float *out = reinterpret_cast<float *>(ring + C::RECV_BYTES);   // [64][128]
+  float *recv = reinterpret_cast<float *>(ring);                        // [HALF][128] fp32
+  uint16_t *tile = reinterpret_cast<uint16_t *>(ring + C::RECV_BYTES);  // [HALF][128] bf16
   const int own0 = static_cast<int>(kh) * C::HALF;  // first batch column this CTA finishes
   const int oth0 = C::HALF - own0;                  // the partner's
   const int r = 32 * (warp & 3) + lane;             // tile row == tensor-memory lane
   const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+  // Y (and R) as whole tiles by TMA when their rows are 16-byte aligned: per-thread
+  // stores from every SM at once are limited by the stores each SM keeps in flight
+  const bool tma_out = p.vec_y != 0;
+  if (go && tma_out && p.R != nullptr && tid == 64) {
+    mbar_arrive_expect_tx(rbar, static_cast<uint32_t>(C::HALF * 128 * 2));
+    tma_load_2d(tile, &rmap, rbar, t * TILE_N, own0);
+  }
   if (go && warp >= 2) {
     const uint32_t dst = cluster_map(recv, rank ^ 2u) + 4u * static_cast<uint32_t>(r);
-    for (int c = 0; c < C::HALF && oth0 + c < p.B; c += 16) {
-      float v[16];
-      tmem_ld16(taddr + static_cast<uint32_t>(oth0 + c), v);
+    // 64 columns per tensor-memory wait: the loads' latency is paid once per group
+    for (int c = 0; c < C::HALF && oth0 + c < p.B; c += 64) {
+      float v[64];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tmem_ld16(taddr + static_cast<uint32_t>(oth0 + c + 16 * q), v + 16 * q);
       tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < 16; ++j) st_cluster_f32(dst + 512u * static_cast<uint32_t>(c + j), v[j]);
+      for (int j = 0; j < 64; ++j) st_cluster_f32(dst + 512u * static_cast<uint32_t>(c + j), v[j]);
     }
   }
   tc_fence_before();
@@ -228,39 +243,64 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
   cluster_sync_all();
   tc_fence_after();
   if (go && warp >= 2) {
-    for (int g = 0; g < C::HALF / 64 && own0 + 64 * g < p.B; ++g) {
-      const int col0 = own0 + 64 * g;
-      float v[64];
+    // this CTA's columns: its own k-half plus the received one (+ R), rounded once
+    const bool res = tma_out && p.R != nullptr;
+    if (res && !mbar_wait_bounded(rbar, 0u, p.status, flags, p.wait_limit_ns))
+      (void)mbar_wait_drain(rbar, 0u, 10000000ull);  // the copy lands before the CTA exits
+    // 32 columns at a time, every shared-memory read of the group before its writes (the
+    // compiler cannot tell the areas apart, so interleaved they would run one by one)
+    for (int c = 0; c < C::HALF && own0 + c < p.B; c += 32) {
+      float v[32], o[32];
+      tmem_ld16(taddr + static_cast<uint32_t>(own0 + c), v);
+      tmem_ld16(taddr + static_cast<uint32_t>(own0 + c + 16), v + 16);
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        tmem_ld16(taddr + static_cast<uint32_t>(col0 + 16 * c), v + 16 * c);
-      tmem_wait_ld();
+      for (int j = 0; j < 32; ++j) o[j] = recv[(c + j) * 128 + r];
+      if (res) {
+        uint16_t rb[32];
 #pragma unroll
-      for (int j = 0; j < 64; ++j) out[j * 128 + r] = v[j] + recv[(64 * g + j) * 128 + r];
-      named_bar_sync(2, 128);
-      for (int c = r; c < 64 * 16; c += 128) {
-        const int j = c >> 4, row8 = (c & 15) * 8;
-        const int col = col0 + j, n0 = t * TILE_N + row8;
-        if (col >= p.B || n0 >= p.N) continue;
-        const float *src = out + j * 128 + row8;
-        if (p.vec_y) {
-          store_y8(p, col, n0, *reinterpret_cast<const float4 *>(src),
-                   *reinterpret_cast<const float4 *>(src + 4));
+        for (int j = 0; j < 32; ++j) rb[j] = tile[(c + j) * 128 + r];
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          tile[(c + j) * 128 + r] = f32_to_bf16_rn((v[j] + o[j]) + bf16_to_f32(rb[j]));
+      } else {
+        tmem_wait_ld();
+        if (tma_out) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) tile[(c + j) * 128 + r] = f32_to_bf16_rn(v[j] + o[j]);
         } else {
-          for (int e = 0; e < 8 && n0 + e < p.N; ++e) {
-            float y = src[e];
-            const size_t off = static_cast<size_t>(col) * p.N + n0 + e;
-            if (p.R != nullptr) y += bf16_to_f32(p.R[off]);
-            p.Y[off] = f32_to_bf16_rn(y);
-          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) recv[(c + j) * 128 + r] = v[j] + o[j];
         }
       }
-      named_bar_sync(2, 128);  // `out` is rewritten by the next group
     }
+    if (tma_out) fence_proxy_async_smem();  // the tile is read by the TMA store next
   }
+  // the accumulator is read: release tensor memory before the stores
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+  if (go && tma_out && !flags[0]) {
+    if (tid == 64) {
+      tma_store_2d(&ymap, tile, t * TILE_N, own0);  // rows >= B, columns >= N clipped
+      bulk_commit_group();
+      bulk_wait_all();
+    }
+  } else if (go && warp >= 2) {
+    const int ncol = min(C::HALF, p.B - own0);  // columns of the batch this CTA stores
+    for (int c = r; c < ncol * 16; c += 128) {
+      const int j = c >> 4, row8 = (c & 15) * 8;
+      const int col = own0 + j, n0 = t * TILE_N + row8;
+      if (n0 >= p.N) continue;
+      const float *src = recv + j * 128 + row8;
+      for (int e = 0; e < 8 && n0 + e < p.N; ++e) {
+        float y = src[e];
+        const size_t off = static_cast<size_t>(col) * p.N + n0 + e;
+        if (p.R != nullptr) y += bf16_to_f32(p.R[off]);
+        p.Y[off] = f32_to_bf16_rn(y);
+      }
+    }
+  }
 }
 
 template <int NMMA>
@@ -280,13 +320,14 @@ cudaError_t set_pair_attrs() {
 }
 
 template <int NMMA>
-cudaError_t launch_pair_t(const CUtensorMap &wmap, const CUtensorMap &xmap, const EngineParams &p,
+cudaError_t launch_pair_t(const CUtensorMap &wmap, const CUtensorMap &xmap,
+                          const CUtensorMap &ymap, const CUtensorMap &rmap, const EngineParams &p,
                           cudaStream_t s) {
   cudaError_t e = set_pair_attrs<NMMA>();
   if (e != cudaSuccess) return e;
   const int slices = (p.T + 1) / 2;
   return launch_pdl_cluster(engine_pair_kernel<NMMA>, dim3(4 * slices), dim3(PAIR_THREADS),
-                            PairConfig<NMMA>::SMEM, s, 4, wmap, xmap, p);
+                            PairConfig<NMMA>::SMEM, s, 4, wmap, xmap, ymap, rmap, p);
 }
 
 template <int NMMA>
@@ -316,11 +357,13 @@ cudaError_t engine_pair_max_clusters(int nmma, int *n) {
 }
 
 cudaError_t launch_engine_pair(int nmma, const CUtensorMap &wmap, const CUtensorMap &xmap,
+                               const CUtensorMap &ymap, const CUtensorMap &rmap,
                                const EngineParams &p, cudaStream_t s) {
   if (p.mode != MODE_LINEAR || p.grouped || p.KB < 2 || p.T < 1 || p.B < 1 ||
       p.B > 256 * nmma || (nmma != 1 && nmma != 2))
     return cudaErrorNotSupported;
-  return nmma == 1 ? launch_pair_t<1>(wmap, xmap, p, s) : launch_pair_t<2>(wmap, xmap, p, s);
+  return nmma == 1 ? launch_pair_t<1>(wmap, xmap, ymap, rmap, p, s)
+                   : launch_pair_t<2>(wmap, xmap, ymap, rmap, p, s);
 }
 
 }  // namespace ssd
