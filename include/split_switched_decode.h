@@ -37,8 +37,10 @@
  *    use_tc = 1, dec_linear) also take B = 65..512 rows: speculative-decoding
  *    verification scores B sequences x (draft length + 1) tokens in one projection
  *    ("Part 3: Performance Deep Dive", decode with DSpark, seven draft tokens: 8 rows
- *    per sequence, so up to 64 sequences). Up to 256 rows run as one launch; more run
- *    as consecutive launches over row blocks of at most 256, each reading W again.
+ *    per sequence, so up to 64 sequences). From 129 rows (split_k = 0) a call is one
+ *    launch on CTA-pair tensor-core tiles (two SMs share each MMA of 256 weight rows,
+ *    each SM staging half of the activation rows), reading W once; 65..128 rows, or
+ *    an explicit split_k, run on one-CTA tiles, at most 256 rows per launch.
  */
 #ifndef SPLIT_SWITCHED_DECODE_H
 #define SPLIT_SWITCHED_DECODE_H
@@ -167,8 +169,15 @@ DEC_API dec_status dec_gemv(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16
  * the MMA M dimension, the batch is the MMA N dimension, accumulator in tensor
  * memory). With use_tc = 1, B may be 65..512 (speculative verification rows): groups
  * of 64 batch columns share every weight tile, each group reduced separately, at most
- * 256 rows per launch; use_tc = 0 then returns DEC_ERR_UNSUPPORTED_SHAPE.
- * dec_splitk_workspace_bytes() covers every launch of the call (they reuse it in turn).
+ * 256 rows per launch; use_tc = 0 then returns DEC_ERR_UNSUPPORTED_SHAPE. With
+ * use_tc = 1, split_k = 0, 129 <= B <= 512 and at least two k-blocks, the call is
+ * instead one launch of 4-CTA clusters, one per 256 rows of W: two CTA pairs (tcgen05
+ * .cta_group::2, M = 256) hold the two k-halves, added inside the cluster through
+ * distributed shared memory in a fixed order (deterministic; the summation order
+ * differs from the one-CTA tiles, so bits may differ from them within the tolerance);
+ * DEC_WIDE_PAIR_MMA=0 turns it off, DEC_WIDE_PAIR_MIN_B moves its lower bound.
+ * dec_splitk_workspace_bytes() covers every launch of the call (they reuse it in turn;
+ * the CTA-pair launch checks the same size and uses none of it).
  */
 DEC_API size_t dec_splitk_workspace_bytes(int B, int N, int K, int split_k);
 DEC_API dec_status dec_splitk_gemm(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 *R,
