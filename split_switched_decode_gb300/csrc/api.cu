@@ -1627,6 +1627,9 @@ extern "C" dec_status dec_splitk_gemm_noalloc(const dec_bf16 *X, const dec_bf16 
   if (!plan_splitk(B, N, K, 0, d->num_sms, &pl)) return DEC_ERR_UNSUPPORTED_SHAPE;
   if (pl.total > kNoAllocScratchBytes) return DEC_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
+  // 129..256 rows: the CTA-pair launch, as dec_splitk_gemm takes it (it uses no scratch)
+  if (use_pair_kernel(B, N, K, 0, use_tc))
+    return run_pair_projection(X, W, R, Y, B, N, K, scratch, kNoAllocScratchBytes, cs, false);
   // The arrival counters must start at zero. Every call that completes leaves them at
   // zero, and the array starts zeroed, but a call whose kernel gave up on a bounded
   // wait can leave some set; clearing them here makes the next call correct anyway.

@@ -89,6 +89,28 @@ def test_noalloc_wide_rows_that_fit(env):
         assert_close(to_f64(oracle, Y), y_ref, f"no-alloc wide call {call}")
 
 
+def test_noalloc_cta_pair_rows_equal_workspace_entry_point(env):
+    """200 rows: like dec_splitk_gemm with split_k = 0, the no-alloc call runs on CTA-pair
+    tiles (same kernel, same bits), and matches the oracle."""
+    torch, ssd, oracle, dev = env
+    from split_switched_decode_gb300 import inputs
+    B, N, K = 200, 520, 776
+    X = inputs.activations(B, K, dev, 85)
+    W = inputs.weight(N, K, dev, 85)
+    R = inputs.residual(B, N, dev, 85)
+    Y = torch.empty(B, N, dtype=torch.bfloat16, device=dev)
+    assert _noalloc(env, X, W, R, Y, 1) == ssd.DEC_OK
+    torch.cuda.synchronize()
+    assert ssd.dec_last_variant() == ssd.VARIANT_SPLITK_TC_PAIR
+    Y_ws = torch.empty_like(Y)
+    ws = ssd.workspace(ssd.dec_splitk_workspace_bytes(B, N, K, 0), dev)
+    ssd.dec_splitk_gemm(X, W, R, Y_ws, ws, split_k=0, use_tc=1)
+    torch.cuda.synchronize()
+    assert torch.equal(Y, Y_ws)
+    y_ref, _ = oracle.linear(inputs.bits(X), inputs.bits(W), inputs.bits(R))
+    assert_close(to_f64(oracle, Y), y_ref, "no-alloc CTA-pair rows")
+
+
 @pytest.mark.parametrize("B,N,K,use_tc,status", [
     (256, 8192, 7168, 1, "DEC_ERR_WORKSPACE_TOO_SMALL"),  # ~34 MB of partial tiles
     (257, 512, 512, 1, "DEC_ERR_UNSUPPORTED_SHAPE"),       # more than one launch of rows
