@@ -37,10 +37,11 @@
  *    use_tc = 1, dec_linear) also take B = 65..512 rows: speculative-decoding
  *    verification scores B sequences x (draft length + 1) tokens in one projection
  *    ("Part 3: Performance Deep Dive", decode with DSpark, seven draft tokens: 8 rows
- *    per sequence, so up to 64 sequences). From 129 rows (split_k = 0) a call is one
+ *    per sequence, so up to 64 sequences). From 129 rows (split_k = 0), and from 65
+ *    rows where W has enough 256-row slices to cover 80 % of the SMs, a call is one
  *    launch on CTA-pair tensor-core tiles (two SMs share each MMA of 256 weight rows,
- *    each SM staging half of the activation rows), reading W once; 65..128 rows, or
- *    an explicit split_k, run on one-CTA tiles, at most 256 rows per launch.
+ *    each SM staging half of the activation rows), reading W once; other calls run on
+ *    one-CTA tiles, at most 256 rows per launch.
  */
 #ifndef SPLIT_SWITCHED_DECODE_H
 #define SPLIT_SWITCHED_DECODE_H
@@ -81,7 +82,7 @@ typedef enum {
     DEC_VARIANT_SPLITK_TC = 2,   /* split-K, TMA-staged tiles, tcgen05 tensor cores  */
     DEC_VARIANT_FRONT_ONE_LAUNCH = 3, /* moe_front as one launch: tensor-core product,
                                          on-chip split-K reduction, routing, route map */
-    DEC_VARIANT_SPLITK_TC_PAIR = 4   /* 129..512 rows: CTA-pair tensor-core tiles (M = 256
+    DEC_VARIANT_SPLITK_TC_PAIR = 4   /* 65..512 rows: CTA-pair tensor-core tiles (M = 256
                                         weight rows per MMA over two SMs), one launch */
 } dec_variant;
 
@@ -170,7 +171,8 @@ DEC_API dec_status dec_gemv(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16
  * memory). With use_tc = 1, B may be 65..512 (speculative verification rows): groups
  * of 64 batch columns share every weight tile, each group reduced separately, at most
  * 256 rows per launch; use_tc = 0 then returns DEC_ERR_UNSUPPORTED_SHAPE. With
- * use_tc = 1, split_k = 0, 129 <= B <= 512 and at least two k-blocks, the call is
+ * use_tc = 1, split_k = 0, at least two k-blocks and 129 <= B <= 512 (or 65 <= B <= 128
+ * with 4 x ceil(ceil(N / 128) / 2) >= 80 % of the SMs), the call is
  * instead one launch of 4-CTA clusters, one per 256 rows of W: two CTA pairs (tcgen05
  * .cta_group::2, M = 256) hold the two k-halves, added inside the cluster through
  * distributed shared memory in a fixed order (deterministic; the summation order

@@ -401,9 +401,13 @@ dec_status run_splitk_rows(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 
                            int B, int N, int K, int split_k, int use_tc, void *ws,
                            size_t ws_bytes, cudaStream_t s, bool packed = false);
 
-// Wide projections from DEC_WIDE_PAIR_MIN_B rows (default 129) up to 512 on CTA-pair
+// Wide projections from DEC_WIDE_PAIR_MIN_B rows (default 65) up to 512 on CTA-pair
 // tensor-core tiles, one launch per call (DEC_WIDE_PAIR_MMA=0: launches of at most 256
-// rows on one-CTA tiles, each reading W).
+// rows on one-CTA tiles, each reading W). Up to 128 rows only where the clusters (4 CTAs
+// per 256 rows of W) cover at least DEC_PAIR_SPLIT_MIN_SM_PCT of the SMs: measured on one
+// box (us, CTA pairs -> one-CTA tiles), the input projection (128 CTAs) 22.5 -> 24.6 at 65
+// rows and 23.0 -> 25.0 at 128, the output projection (112 CTAs) 43.4 -> 41.8 at 65 rows
+// and 43.6 -> 43.5 at 128; from 129 rows the pair tiles win on both.
 bool wide_pair_mma() {
   if (const char *s = std::getenv("DEC_WIDE_PAIR_MMA")) return std::atoi(s) != 0;
   return true;
@@ -413,24 +417,24 @@ int wide_pair_min_batch() {
     const int v = std::atoi(s);
     if (v >= MAX_B + 1) return v;
   }
-  return 2 * MAX_B + 1;
+  return MAX_B + 1;
 }
 
-// 4-CTA clusters of the pair kernel the device holds at once, per device and MMA count.
-std::atomic<int> g_pair_clusters[kMaxDevices][2];
+// 4-CTA clusters of the pair kernel the device holds at once, per device and column count.
+std::atomic<int> g_pair_clusters[kMaxDevices][3];
 std::once_flag g_pair_init_once;
 
-int pair_clusters(int nmma) {
+int pair_clusters(int ncol) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
   std::call_once(g_pair_init_once, []() {
     for (auto &d : g_pair_clusters)
       for (auto &v : d) v.store(-1);
   });
-  std::atomic<int> &slot = g_pair_clusters[dev][nmma - 1];
+  std::atomic<int> &slot = g_pair_clusters[dev][ncol == 128 ? 0 : (ncol == 256 ? 1 : 2)];
   int n = slot.load();
   if (n < 0) {
-    if (engine_pair_max_clusters(nmma, &n) != cudaSuccess) {
+    if (engine_pair_max_clusters(ncol, &n) != cudaSuccess) {
       (void)cudaGetLastError();
       n = 0;
     }
@@ -441,12 +445,13 @@ int pair_clusters(int nmma) {
 
 // Whether a call of B rows takes the CTA-pair kernel: every 256-row slice of W needs one
 // resident cluster (a second wave would double the time).
-bool use_pair_kernel(int B, int N, int K, int split_k, int use_tc) {
+bool use_pair_kernel(int B, int N, int K, int split_k, int use_tc, int num_sms) {
   if (!use_tc || split_k != 0 || !wide_pair_mma() || B < wide_pair_min_batch() || B > MAX_ROWS)
     return false;
   if (ceil_div(K, TILE_K) < 2) return false;
   const int slices = (ceil_div(N, TILE_N) + 1) / 2;
-  return pair_clusters(pair_mma_count(B)) >= slices;
+  if (B <= 2 * MAX_B && 400 * slices < pair_split_min_sm_pct() * num_sms) return false;
+  return pair_clusters(pair_cols(B)) >= slices;
 }
 
 // The CTA-pair launch. The workspace is checked as for the one-CTA launches (the same
@@ -466,7 +471,8 @@ dec_status run_pair_projection(const dec_bf16 *X, const dec_bf16 *W, const dec_b
   CUtensorMap wmap, xmap;
   const bool wmap_ok = packed ? make_map(&wmap, W, TILE_K, static_cast<uint64_t>(N) * pl.KB, 128)
                               : make_map(&wmap, W, K, N, 128);
-  if (!wmap_ok || !make_map(&xmap, X, K, B, 128)) return DEC_ERR_CUDA;
+  const int ncol = pair_cols(B);
+  if (!wmap_ok || !make_map(&xmap, X, K, B, pair_xbox_rows(ncol))) return DEC_ERR_CUDA;
   EngineParams p;
   std::memset(&p, 0, sizeof p);
   p.mode = MODE_LINEAR;
@@ -484,16 +490,15 @@ dec_status run_pair_projection(const dec_bf16 *X, const dec_bf16 *W, const dec_b
   p.status = d->status;
   p.wait_limit_ns = g_wait_limit_ns.load();
   // Y (and R) as whole tiles by TMA when their rows are 16-byte aligned (p.vec_y)
-  const int nmma = pair_mma_count(B);
   CUtensorMap ymap, rmap;
   std::memset(&ymap, 0, sizeof ymap);
   std::memset(&rmap, 0, sizeof rmap);
   if (p.vec_y) {
-    if (!make_map_plain(&ymap, Y, N, B, 128, 128 * nmma)) return DEC_ERR_CUDA;
-    if (R && !make_map_plain(&rmap, R, N, B, 128, 128 * nmma)) return DEC_ERR_CUDA;
+    if (!make_map_plain(&ymap, Y, N, B, 128, ncol / 2)) return DEC_ERR_CUDA;
+    if (R && !make_map_plain(&rmap, R, N, B, 128, ncol / 2)) return DEC_ERR_CUDA;
   }
   if (consume_fault()) return DEC_ERR_CUDA;
-  ce = launch_engine_pair(nmma, wmap, xmap, ymap, rmap, p, s);
+  ce = launch_engine_pair(ncol, wmap, xmap, ymap, rmap, p, s);
   if (ce == cudaErrorNotSupported) return DEC_ERR_UNSUPPORTED_SHAPE;
   if (ce != cudaSuccess) return DEC_ERR_CUDA;
   t_last_variant = DEC_VARIANT_SPLITK_TC_PAIR;
@@ -507,7 +512,10 @@ dec_status run_pair_projection(const dec_bf16 *X, const dec_bf16 *W, const dec_b
 dec_status run_splitk(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 *R, dec_bf16 *Y,
                       int B, int N, int K, int split_k, int use_tc, void *ws, size_t ws_bytes,
                       cudaStream_t s, bool packed = false) {
-  if (use_pair_kernel(B, N, K, split_k, use_tc))
+  cudaError_t ce;
+  DeviceInfo *d = device_info(&ce);
+  if (!d) return DEC_ERR_CUDA;
+  if (use_pair_kernel(B, N, K, split_k, use_tc, d->num_sms))
     return run_pair_projection(X, W, R, Y, B, N, K, ws, ws_bytes, s, packed);
   if (B <= MAX_B_WIDE)
     return run_splitk_rows(X, W, R, Y, B, N, K, split_k, use_tc, ws, ws_bytes, s, packed);
@@ -1628,7 +1636,7 @@ extern "C" dec_status dec_splitk_gemm_noalloc(const dec_bf16 *X, const dec_bf16 
   if (pl.total > kNoAllocScratchBytes) return DEC_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
   // 129..256 rows: the CTA-pair launch, as dec_splitk_gemm takes it (it uses no scratch)
-  if (use_pair_kernel(B, N, K, 0, use_tc))
+  if (use_pair_kernel(B, N, K, 0, use_tc, d->num_sms))
     return run_pair_projection(X, W, R, Y, B, N, K, scratch, kNoAllocScratchBytes, cs, false);
   // The arrival counters must start at zero. Every call that completes leaves them at
   // zero, and the array starts zeroed, but a call whose kernel gave up on a bounded

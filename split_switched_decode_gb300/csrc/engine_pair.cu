@@ -15,10 +15,11 @@
 //   rank 1: tile 2c+1, k-half 0
 //   rank 2: tile 2c,   k-half 1  -- issues the pair MMA of ranks 2 and 3
 //   rank 3: tile 2c+1, k-half 1
-// Per k-block each CTA loads its 16 KB weight box and NMMA activation boxes of 128 rows
-// (rows 256m + 128h .. +127 for MMA m, h = rank & 1), so MMA m covers batch columns
-// 256m .. 256m+255 with N = 256 (rows beyond the batch read as zeros). Batch column j
-// accumulates in tensor-memory column j (NMMA x 256 columns; all 512 at NMMA = 2).
+// A launch covers NCOL = 128, 256 or 512 batch columns as NMMA MMAs of N = NPER per K
+// step (one of 128 or 256, or two of 256). Per k-block each CTA loads its 16 KB weight box
+// and NMMA activation boxes of NPER / 2 rows (rows NPER m + (NPER / 2) h .. for MMA m,
+// h = rank & 1), so MMA m covers batch columns NPER m .. NPER m + NPER - 1 (rows beyond
+// the batch read as zeros). Batch column j accumulates in tensor-memory column j.
 //
 // Ring: the even CTA's full barrier of a stage counts both CTAs' bytes (the odd CTA's
 // copies signal it through the CTA-pair form of the TMA load); the MMA thread arms each
@@ -28,7 +29,7 @@
 // that their accumulators are final.
 //
 // Tail: the two k-halves of a weight tile are ranks r and r ^ 2. k-half 0 finishes batch
-// columns [0, 128 NMMA), k-half 1 the rest. Once every CTA of the cluster is past its
+// columns [0, NCOL / 2), k-half 1 the rest. Once every CTA of the cluster is past its
 // MMAs (cluster barrier 1: every ring is idle), each CTA writes the partner's columns of
 // its accumulator into the partner's ring; after cluster barrier 2 each adds its own half
 // to the received one (+ R, loaded as one TMA tile meanwhile), rounds once to bf16 into a
@@ -47,14 +48,20 @@ namespace {
 constexpr int PAIR_THREADS = 192;  // warp 0 TMA, warp 1 MMA + tensor memory, warps 2-5 tail
 constexpr int PAIR_SMEM_LIMIT = 232448;
 
-template <int NMMA>
+// NCOL batch columns per launch (128, 256 or 512): NMMA MMAs of N = NPER per K step, each
+// CTA of a pair staging XROWS = NPER / 2 activation rows per MMA.
+template <int NCOL>
 struct PairConfig {
-  static constexpr int STAGE_BYTES = 16384 + NMMA * 16384;
+  static constexpr int NPER = NCOL < 256 ? NCOL : 256;
+  static constexpr int NMMA = NCOL / NPER;
+  static constexpr int XROWS = NPER / 2;
+  static constexpr int XBYTES = XROWS * 128;
+  static constexpr int STAGE_BYTES = 16384 + NMMA * XBYTES;
   static constexpr int TAIL = 256;
   static constexpr int FIT = (PAIR_SMEM_LIMIT - 1024 - TAIL) / STAGE_BYTES;
   static constexpr int STAGES = FIT > 8 ? 8 : FIT;
-  static constexpr int HALF = 128 * NMMA;            // batch columns one k-half finishes
-  static constexpr uint32_t TMEM_COLS = 256u * NMMA;
+  static constexpr int HALF = NCOL / 2;              // batch columns one k-half finishes
+  static constexpr uint32_t TMEM_COLS = NCOL;
   static constexpr int RECV_BYTES = HALF * 128 * 4;  // the partner's partial of them
   static constexpr int TILE_BYTES = HALF * 128 * 2;  // R in, Y out: bf16 [HALF][128]
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + TAIL;
@@ -72,13 +79,13 @@ __device__ __forceinline__ void pair_load_w(const EngineParams &p, const CUtenso
     tma_load_2d_pair_hint(dst, wmap, bar, kb * TILE_K, t * TILE_N, pol);
 }
 
-template <int NMMA>
+template <int NCOL>
 __global__ void __launch_bounds__(PAIR_THREADS, 1)
     engine_pair_kernel(const __grid_constant__ CUtensorMap wmap,
                        const __grid_constant__ CUtensorMap xmap,
                        const __grid_constant__ CUtensorMap ymap,
                        const __grid_constant__ CUtensorMap rmap, const EngineParams p) {
-  using C = PairConfig<NMMA>;
+  using C = PairConfig<NCOL>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -150,9 +157,9 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
           pair_load_w(p, &wmap, dst, bar, t, kb0 + q, pol);
         }
 #pragma unroll
-        for (int m = 0; m < NMMA; ++m)
-          tma_load_2d_pair(dst + 16384 * (1 + m), &xmap, bar, (kb0 + q) * TILE_K,
-                           256 * m + 128 * static_cast<int>(h));
+        for (int m = 0; m < C::NMMA; ++m)
+          tma_load_2d_pair(dst + 16384 + m * C::XBYTES, &xmap, bar, (kb0 + q) * TILE_K,
+                           C::NPER * m + C::XROWS * static_cast<int>(h));
       }
       // every load of this CTA is issued: the next kernel may be scheduled as SMs free up
       griddep_launch_dependents();
@@ -163,7 +170,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
     // ------------------------------------------------------------- MMA issuer
     griddep_wait();
     if (leader && lane == 0) {
-      const uint32_t idesc = idesc_bf16_pair(256);
+      const uint32_t idesc = idesc_bf16_pair(C::NPER);
       const uint16_t mask = static_cast<uint16_t>(3u << lead);
       bool ok = true;
       int q = 0;
@@ -180,11 +187,12 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
         const uint32_t a_addr = smem_u32(ring + st * C::STAGE_BYTES);
         const uint64_t adesc = sw128_desc(a_addr);
 #pragma unroll
-        for (int m = 0; m < NMMA; ++m) {
-          const uint64_t bdesc = sw128_desc(a_addr + 16384u * (1 + m));
+        for (int m = 0; m < C::NMMA; ++m) {
+          const uint64_t bdesc = sw128_desc(a_addr + 16384u + static_cast<uint32_t>(m * C::XBYTES));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)  // K = 16 per MMA: +32 bytes along the swizzled row
-            tc_mma_pair(tmem_base + 256u * m, adesc + 2u * kk, bdesc + 2u * kk, idesc,
+            tc_mma_pair(tmem_base + static_cast<uint32_t>(C::NPER * m), adesc + 2u * kk,
+                        bdesc + 2u * kk, idesc,
                         (q > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit_pair_mc(&empty[st], mask);  // both CTAs' stage is free once read
@@ -303,7 +311,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
   }
 }
 
-template <int NMMA>
+template <int NCOL>
 cudaError_t set_pair_attrs() {
   static std::atomic<uint64_t> attr_set{0};
   int dev = 0;
@@ -311,33 +319,33 @@ cudaError_t set_pair_attrs() {
   if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
   if (!(attr_set.load() & bit)) {
-    e = cudaFuncSetAttribute(engine_pair_kernel<NMMA>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, PairConfig<NMMA>::SMEM);
+    e = cudaFuncSetAttribute(engine_pair_kernel<NCOL>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, PairConfig<NCOL>::SMEM);
     if (e != cudaSuccess) return e;
     attr_set.fetch_or(bit);
   }
   return cudaSuccess;
 }
 
-template <int NMMA>
+template <int NCOL>
 cudaError_t launch_pair_t(const CUtensorMap &wmap, const CUtensorMap &xmap,
                           const CUtensorMap &ymap, const CUtensorMap &rmap, const EngineParams &p,
                           cudaStream_t s) {
-  cudaError_t e = set_pair_attrs<NMMA>();
+  cudaError_t e = set_pair_attrs<NCOL>();
   if (e != cudaSuccess) return e;
   const int slices = (p.T + 1) / 2;
-  return launch_pdl_cluster(engine_pair_kernel<NMMA>, dim3(4 * slices), dim3(PAIR_THREADS),
-                            PairConfig<NMMA>::SMEM, s, 4, wmap, xmap, ymap, rmap, p);
+  return launch_pdl_cluster(engine_pair_kernel<NCOL>, dim3(4 * slices), dim3(PAIR_THREADS),
+                            PairConfig<NCOL>::SMEM, s, 4, wmap, xmap, ymap, rmap, p);
 }
 
-template <int NMMA>
+template <int NCOL>
 cudaError_t max_clusters_t(int *n) {
-  cudaError_t e = set_pair_attrs<NMMA>();
+  cudaError_t e = set_pair_attrs<NCOL>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(4 * 64);
   cfg.blockDim = dim3(PAIR_THREADS);
-  cfg.dynamicSmemBytes = PairConfig<NMMA>::SMEM;
+  cfg.dynamicSmemBytes = PairConfig<NCOL>::SMEM;
   cudaLaunchAttribute a[1];
   a[0].id = cudaLaunchAttributeClusterDimension;
   a[0].val.clusterDim.x = 4;
@@ -345,25 +353,27 @@ cudaError_t max_clusters_t(int *n) {
   a[0].val.clusterDim.z = 1;
   cfg.attrs = a;
   cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(n, engine_pair_kernel<NMMA>, &cfg);
+  return cudaOccupancyMaxActiveClusters(n, engine_pair_kernel<NCOL>, &cfg);
 }
 
 }  // namespace
 
-int pair_mma_count(int B) { return B <= 256 ? 1 : 2; }
+int pair_cols(int B) { return B <= 128 ? 128 : (B <= 256 ? 256 : 512); }
 
-cudaError_t engine_pair_max_clusters(int nmma, int *n) {
-  return nmma == 1 ? max_clusters_t<1>(n) : max_clusters_t<2>(n);
+cudaError_t engine_pair_max_clusters(int ncol, int *n) {
+  return ncol == 128 ? max_clusters_t<128>(n)
+                     : (ncol == 256 ? max_clusters_t<256>(n) : max_clusters_t<512>(n));
 }
 
-cudaError_t launch_engine_pair(int nmma, const CUtensorMap &wmap, const CUtensorMap &xmap,
+cudaError_t launch_engine_pair(int ncol, const CUtensorMap &wmap, const CUtensorMap &xmap,
                                const CUtensorMap &ymap, const CUtensorMap &rmap,
                                const EngineParams &p, cudaStream_t s) {
-  if (p.mode != MODE_LINEAR || p.grouped || p.KB < 2 || p.T < 1 || p.B < 1 ||
-      p.B > 256 * nmma || (nmma != 1 && nmma != 2))
+  if (p.mode != MODE_LINEAR || p.grouped || p.KB < 2 || p.T < 1 || p.B < 1 || p.B > ncol ||
+      (ncol != 128 && ncol != 256 && ncol != 512))
     return cudaErrorNotSupported;
-  return nmma == 1 ? launch_pair_t<1>(wmap, xmap, ymap, rmap, p, s)
-                   : launch_pair_t<2>(wmap, xmap, ymap, rmap, p, s);
+  if (ncol == 128) return launch_pair_t<128>(wmap, xmap, ymap, rmap, p, s);
+  if (ncol == 256) return launch_pair_t<256>(wmap, xmap, ymap, rmap, p, s);
+  return launch_pair_t<512>(wmap, xmap, ymap, rmap, p, s);
 }
 
 }  // namespace ssd

@@ -1,10 +1,11 @@
-"""GPU parity of the CTA-pair tensor-core projection (129..512 rows in one launch): the
+"""GPU parity of the CTA-pair tensor-core projection (65..512 rows in one launch): the
 speculative-verification shape (sequences x (draft length + 1) tokens; "Hyper Optimizing
 Kimi K3 in vLLM", Part 3: Performance Deep Dive, decode with DSpark) where two SMs share
 each MMA of 256 weight rows and the two k-halves of every weight tile are added inside a
 4-CTA cluster. Every case is compared with the fp64 oracle: ragged N and K, an odd number
-of 128-row tiles (a half-empty last slice), the smallest k-range (two k-blocks), one and
-two MMAs per K step (up to 256 / 512 rows), residual or not, vector and scalar stores."""
+of 128-row tiles (a half-empty last slice), the smallest k-range (two k-blocks), one MMA
+of N = 128 or 256 or two of 256 per K step (up to 128 / 256 / 512 rows), residual or not,
+vector and scalar stores."""
 import pytest
 
 from gpu_common import assert_close, to_f64
@@ -72,6 +73,38 @@ def test_pair_projection_matches_oracle(env, B, N, K, residual):
     torch.cuda.synchronize()
     assert torch.equal(Y, Y1), "repeated call changed bits"
     assert_close(to_f64(oracle, Y), _ref(X, W, R), f"pair B={B} N={N} K={K}")
+
+
+@pytest.mark.parametrize("B,N,K,residual", [
+    (65, 8192, 128, True),     # one MMA of N = 128 per K step, two k-blocks
+    (100, 8064, 456, False),   # ragged K
+    (128, 8100, 1000, True),   # ragged N: per-thread stores, a partly empty last tile
+    (128, 8192, 2048, False),
+])
+def test_pair_projection_128_columns_matches_oracle(env, B, N, K, residual):
+    """65..128 rows on CTA-pair tiles of N = 128 (each CTA stages 64 activation rows per
+    k-block), taken where the clusters cover >= 80 % of the SMs (about 8192 rows of W)."""
+    torch, ssd, oracle, dev = env
+    X, W, R, Y = _case(env, B, N, K, 45, residual)
+    ws = ssd.workspace(ssd.dec_linear_workspace_bytes(B, N, K), dev)
+    ssd.dec_linear(X, W, R, Y, ws)
+    torch.cuda.synchronize()
+    assert ssd.dec_last_variant() == ssd.VARIANT_SPLITK_TC_PAIR
+    assert ssd.dec_sync_status() == ssd.DEC_OK
+    assert_close(to_f64(oracle, Y), _ref(X, W, R), f"pair128 B={B} N={N} K={K}")
+
+
+def test_pair_tiles_below_129_rows_need_enough_clusters(env):
+    """Below 129 rows a shape whose clusters would cover too few SMs stays on one-CTA
+    tiles (the HBM-bound calls need the SMs more than the shared activation boxes)."""
+    torch, ssd, oracle, dev = env
+    B, N, K = 100, 1024, 1024
+    X, W, R, Y = _case(env, B, N, K, 46, True)
+    ws = ssd.workspace(ssd.dec_linear_workspace_bytes(B, N, K), dev)
+    ssd.dec_linear(X, W, R, Y, ws)
+    torch.cuda.synchronize()
+    assert ssd.dec_last_variant() == ssd.VARIANT_SPLITK_TC
+    assert_close(to_f64(oracle, Y), _ref(X, W, R), "one-CTA tiles B=100")
 
 
 @pytest.mark.parametrize("B,which", [(512, "input"), (300, "output"), (136, "input")])
