@@ -1,10 +1,10 @@
-// engine_pair.cu -- wide projections (129-512 rows per call) on CTA-pair tensor-core
+// engine_pair.cu -- wide projections (65-512 rows per call) on CTA-pair tensor-core
 // tiles.
 //
 // Speculative-decode verification multiplies one weight matrix by many activation rows
 // (sequences x (draft length + 1) tokens). With one CTA per 128-row weight tile, every
 // tile re-reads all M activation rows from L2 (M x 128 bytes per 16 KB of weights per
-// k-block), and from M = 256 on those bytes, not the weights, bound each SM. Here two CTAs
+// k-block), and from M = 128 on those bytes, not the weights, bound each SM. Here two CTAs
 // share one MMA (tcgen05 .cta_group::2, M = 256 weight rows): each CTA stages its own 128
 // weight rows and half of the activation rows of every k-block, so each SM receives half
 // the activation bytes per weight byte, and a 512-row call is one launch that reads W
