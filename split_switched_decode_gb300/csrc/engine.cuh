@@ -327,6 +327,29 @@ __device__ __forceinline__ void engine_produce_dyn(const EngineParams &p, const 
   }
 }
 
+// 8 consecutive rows a, b (plus the residual run rr when has_r), rounded once to bf16,
+// packed.
+__device__ __forceinline__ uint4 pack_y8r(const float4 &a, const float4 &b, const uint4 &rr,
+                                          bool has_r) {
+  float y[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  if (has_r) {
+    y[0] += bf16lo(rr.x);
+    y[1] += bf16hi(rr.x);
+    y[2] += bf16lo(rr.y);
+    y[3] += bf16hi(rr.y);
+    y[4] += bf16lo(rr.z);
+    y[5] += bf16hi(rr.z);
+    y[6] += bf16lo(rr.w);
+    y[7] += bf16hi(rr.w);
+  }
+  uint4 o;
+  o.x = f32_to_bf16_rn(y[0]) | (static_cast<uint32_t>(f32_to_bf16_rn(y[1])) << 16);
+  o.y = f32_to_bf16_rn(y[2]) | (static_cast<uint32_t>(f32_to_bf16_rn(y[3])) << 16);
+  o.z = f32_to_bf16_rn(y[4]) | (static_cast<uint32_t>(f32_to_bf16_rn(y[5])) << 16);
+  o.w = f32_to_bf16_rn(y[6]) | (static_cast<uint32_t>(f32_to_bf16_rn(y[7])) << 16);
+  return o;
+}
+
 // Y rows n0 .. n0+7 of batch column j: y (+ R) rounded once to bf16, one 16-byte store
 // (or element by element for a ragged tail). Requires N % 8 == 0 and 16-byte aligned Y
 // and R (p.vec_y).
@@ -482,22 +505,41 @@ __device__ __forceinline__ void epilogue_rows(const EngineParams &p, const SegIn
     // Through shared memory, half the columns at a time (scratch holds 128 x MAXC/2
     // fp32): thread r parks row r, then each thread adds R to and stores runs of 8 rows
     // of one column with 16-byte accesses. Per-lane 2-byte stores of 64 columns were
-    // the slow part of a wide tile's epilogue.
+    // the slow part of a wide tile's epilogue. Every R run this thread adds is loaded
+    // first: interleaved with the Y stores, each load would wait for the store before it
+    // (the compiler cannot tell R and Y apart).
     constexpr int CW = MAXC >= 2 ? MAXC / 2 : 1;
+    constexpr int NH = MAXC / CW;
+    constexpr int NI = (CW * 16 + 127) / 128;  // runs per thread and half
+    uint4 rr[NH][NI];
 #pragma unroll
-    for (int h = 0; h < MAXC / CW; ++h) {
+    for (int h = 0; h < NH; ++h)
+#pragma unroll
+      for (int i = 0; i < NI; ++i) {
+        const int c = r + 128 * i;
+        const int j = h * CW + (c >> 4), n0 = s.t * 128 + (c & 15) * 8;
+        rr[h][i] = make_uint4(0u, 0u, 0u, 0u);
+        if (p.R != nullptr && c < CW * 16 && j < s.ncols && n0 < p.N)
+          rr[h][i] = *reinterpret_cast<const uint4 *>(
+              p.R + static_cast<size_t>(s.xrow0 + j) * p.N + n0);
+      }
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
       named_bar_sync(bar_id, 128);
 #pragma unroll
       for (int jj = 0; jj < CW; ++jj)
         if (h * CW + jj < s.ncols) scratch[jj * 128 + r] = v[h * CW + jj];
       named_bar_sync(bar_id, 128);
-      for (int c = r; c < CW * 16; c += 128) {
+#pragma unroll
+      for (int i = 0; i < NI; ++i) {
+        const int c = r + 128 * i;
         const int jj = c >> 4, j = h * CW + jj;
         const int row8 = (c & 15) * 8, n0 = s.t * 128 + row8;
-        if (j >= s.ncols || n0 >= p.N) continue;
+        if (c >= CW * 16 || j >= s.ncols || n0 >= p.N) continue;
         const float4 a = *reinterpret_cast<const float4 *>(scratch + jj * 128 + row8);
         const float4 b = *reinterpret_cast<const float4 *>(scratch + jj * 128 + row8 + 4);
-        store_y8(p, s.xrow0 + j, n0, a, b);
+        *reinterpret_cast<uint4 *>(p.Y + static_cast<size_t>(s.xrow0 + j) * p.N + n0) =
+            pack_y8r(a, b, rr[h][i], p.R != nullptr);
       }
     }
   } else if (p.mode == MODE_LINEAR) {

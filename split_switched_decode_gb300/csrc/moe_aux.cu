@@ -237,6 +237,17 @@ __global__ void __launch_bounds__(128) linear_finish_kernel(const LinearFinishPa
 #pragma unroll
     for (int j = 0; j < 16; ++j) sz[j][r] = z[j];
     __syncthreads();
+    // both runs' residuals first: interleaved with the Y stores, the second load would
+    // wait for the first store (the compiler cannot tell R and Y apart)
+    uint4 rq[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int c = r + 128 * q;
+      const int j = c >> 4, n0 = t * 128 + (c & 15) * 8;
+      rq[q] = make_uint4(0u, 0u, 0u, 0u);
+      if (f.R != nullptr && j0 + j < f.B && n0 < f.N)
+        rq[q] = *reinterpret_cast<const uint4 *>(f.R + static_cast<size_t>(j0 + j) * f.N + n0);
+    }
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
       const int c = r + 128 * q;  // 16 columns x 16 runs of 8 rows
@@ -247,7 +258,7 @@ __global__ void __launch_bounds__(128) linear_finish_kernel(const LinearFinishPa
       for (int e = 0; e < 8; ++e) y[e] = sz[j][row8 + e];
       const size_t off = static_cast<size_t>(j0 + j) * f.N + n0;  // N % 8 == 0: whole run
       if (f.R != nullptr) {
-        const uint4 rr = *reinterpret_cast<const uint4 *>(f.R + off);
+        const uint4 rr = rq[q];
         y[0] += bf16lo(rr.x);
         y[1] += bf16hi(rr.x);
         y[2] += bf16lo(rr.y);
