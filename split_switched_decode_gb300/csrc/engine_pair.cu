@@ -15,8 +15,8 @@
 //   rank 1: tile 2c+1, k-half 0
 //   rank 2: tile 2c,   k-half 1  -- issues the pair MMA of ranks 2 and 3
 //   rank 3: tile 2c+1, k-half 1
-// A launch covers NCOL = 128, 256 or 512 batch columns as NMMA MMAs of N = NPER per K
-// step (one of 128 or 256, or two of 256). Per k-block each CTA loads its 16 KB weight box
+// A launch covers NCOL = 128, 256, 384 or 512 batch columns as NMMA MMAs of N = NPER per
+// K step (one of 128 or 256, or two of 192 or 256). Per k-block each CTA loads its 16 KB weight box
 // and NMMA activation boxes of NPER / 2 rows (rows NPER m + (NPER / 2) h .. for MMA m,
 // h = rank & 1), so MMA m covers batch columns NPER m .. NPER m + NPER - 1 (rows beyond
 // the batch read as zeros). Batch column j accumulates in tensor-memory column j.
@@ -48,12 +48,12 @@ namespace {
 constexpr int PAIR_THREADS = 192;  // warp 0 TMA, warp 1 MMA + tensor memory, warps 2-5 tail
 constexpr int PAIR_SMEM_LIMIT = 232448;
 
-// NCOL batch columns per launch (128, 256 or 512): NMMA MMAs of N = NPER per K step, each
-// CTA of a pair staging XROWS = NPER / 2 activation rows per MMA.
+// NCOL batch columns per launch (128, 256, 384 or 512): NMMA MMAs of N = NPER per K step,
+// each CTA of a pair staging XROWS = NPER / 2 activation rows per MMA.
 template <int NCOL>
 struct PairConfig {
-  static constexpr int NPER = NCOL < 256 ? NCOL : 256;
-  static constexpr int NMMA = NCOL / NPER;
+  static constexpr int NMMA = NCOL > 256 ? 2 : 1;
+  static constexpr int NPER = NCOL / NMMA;
   static constexpr int XROWS = NPER / 2;
   static constexpr int XBYTES = XROWS * 128;
   static constexpr int STAGE_BYTES = 16384 + NMMA * XBYTES;
@@ -61,7 +61,7 @@ struct PairConfig {
   static constexpr int FIT = (PAIR_SMEM_LIMIT - 1024 - TAIL) / STAGE_BYTES;
   static constexpr int STAGES = FIT > 8 ? 8 : FIT;
   static constexpr int HALF = NCOL / 2;              // batch columns one k-half finishes
-  static constexpr uint32_t TMEM_COLS = NCOL;
+  static constexpr uint32_t TMEM_COLS = NCOL <= 128 ? 128u : (NCOL <= 256 ? 256u : 512u);
   static constexpr int RECV_BYTES = HALF * 128 * 4;  // the partner's partial of them
   static constexpr int TILE_BYTES = HALF * 128 * 2;  // R in, Y out: bf16 [HALF][128]
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + TAIL;
@@ -358,22 +358,29 @@ cudaError_t max_clusters_t(int *n) {
 
 }  // namespace
 
-int pair_cols(int B) { return B <= 128 ? 128 : (B <= 256 ? 256 : 512); }
+int pair_cols(int B) { return B <= 128 ? 128 : (B <= 256 ? 256 : (B <= 384 ? 384 : 512)); }
 
 cudaError_t engine_pair_max_clusters(int ncol, int *n) {
-  return ncol == 128 ? max_clusters_t<128>(n)
-                     : (ncol == 256 ? max_clusters_t<256>(n) : max_clusters_t<512>(n));
+  switch (ncol) {
+    case 128: return max_clusters_t<128>(n);
+    case 256: return max_clusters_t<256>(n);
+    case 384: return max_clusters_t<384>(n);
+    default: return max_clusters_t<512>(n);
+  }
 }
 
 cudaError_t launch_engine_pair(int ncol, const CUtensorMap &wmap, const CUtensorMap &xmap,
                                const CUtensorMap &ymap, const CUtensorMap &rmap,
                                const EngineParams &p, cudaStream_t s) {
   if (p.mode != MODE_LINEAR || p.grouped || p.KB < 2 || p.T < 1 || p.B < 1 || p.B > ncol ||
-      (ncol != 128 && ncol != 256 && ncol != 512))
+      (ncol != 128 && ncol != 256 && ncol != 384 && ncol != 512))
     return cudaErrorNotSupported;
-  if (ncol == 128) return launch_pair_t<128>(wmap, xmap, ymap, rmap, p, s);
-  if (ncol == 256) return launch_pair_t<256>(wmap, xmap, ymap, rmap, p, s);
-  return launch_pair_t<512>(wmap, xmap, ymap, rmap, p, s);
+  switch (ncol) {
+    case 128: return launch_pair_t<128>(wmap, xmap, ymap, rmap, p, s);
+    case 256: return launch_pair_t<256>(wmap, xmap, ymap, rmap, p, s);
+    case 384: return launch_pair_t<384>(wmap, xmap, ymap, rmap, p, s);
+    default: return launch_pair_t<512>(wmap, xmap, ymap, rmap, p, s);
+  }
 }
 
 }  // namespace ssd
