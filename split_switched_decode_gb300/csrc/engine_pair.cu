@@ -66,6 +66,8 @@ struct PairConfig {
   static constexpr int TILE_BYTES = HALF * 128 * 2;  // R in, Y out: bf16 [HALF][128]
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + TAIL;
   static_assert(STAGES >= 4, "pipeline too shallow");
+  static_assert(HALF % 64 == 0, "the tail moves whole groups of 64 columns");
+  static_assert(NPER % 32 == 0 && NPER <= 256, "CTA-pair MMA: N a multiple of 32, <= 256");
   static_assert(RECV_BYTES + TILE_BYTES <= STAGES * STAGE_BYTES, "tail does not fit the ring");
 };
 
