@@ -398,7 +398,7 @@ def prefetch_scenario(torch, ssd, wl, batches, reps):
 
 # ------------------------------------------- speculative verification rows ----
 
-SPEC_ROWS = (64, 128, 256, 512)
+SPEC_ROWS = (64, 128, 256, 384, 512)
 
 
 def spec_sweep(torch, ssd, inputs, wl, dev, reps):
