@@ -56,7 +56,8 @@ def _ref(X, W, R, tokens=None):
     (256, 640, 2048, False),   # one MMA per K step, full
     (257, 256, 512, True),     # two MMAs per K step, one column in the second
     (300, 130, 136, False),    # odd k-block count: halves of 1 and 2 blocks
-    (384, 512, 1024, True),
+    (384, 512, 1024, True),    # two MMAs of N = 192 per K step, full
+    (385, 256, 512, False),    # two MMAs of N = 256, one column past 384
     (511, 1000, 520, False),
     (512, 256, 2048, True),    # two MMAs, full
 ])
@@ -123,6 +124,28 @@ def test_pair_full_size_projection_every_row(env, B, which):
     cand = [0, 1, 127, 128, 129, 255, 256, 257, 383, 384, 511, B // 2, B - 1]
     tokens = sorted({t for t in cand if t < B})
     assert_close(to_f64(oracle, Y)[tokens], _ref(X, W, R, tokens), f"pair full {which} B={B}")
+
+
+@pytest.mark.parametrize("B", [200, 300])
+def test_pair_unaligned_output_rows_use_per_thread_stores(env, B):
+    """Y and R views one element off a 16-byte boundary (N % 8 == 0): no TMA tiles for
+    them, the per-thread stores instead; same values as the aligned call."""
+    torch, ssd, oracle, dev = env
+    N, K = 512, 1024
+    X, W, R, Y = _case(env, B, N, K, 47, True)
+    ws = ssd.workspace(ssd.dec_linear_workspace_bytes(B, N, K), dev)
+    ssd.dec_linear(X, W, R, Y, ws)
+    Ybuf = torch.full((B * N + 8,), float("nan"), dtype=torch.bfloat16, device=dev)
+    Rbuf = torch.empty(B * N + 8, dtype=torch.bfloat16, device=dev)
+    Yu = Ybuf[1:1 + B * N].view(B, N)
+    Ru = Rbuf[1:1 + B * N].view(B, N)
+    Ru.copy_(R)
+    ssd.dec_linear(X, W, Ru, Yu, ws)
+    torch.cuda.synchronize()
+    assert ssd.dec_last_variant() == ssd.VARIANT_SPLITK_TC_PAIR
+    assert ssd.dec_sync_status() == ssd.DEC_OK
+    assert torch.equal(Yu, Y)
+    assert_close(to_f64(oracle, Yu), _ref(X, W, R), f"pair unaligned B={B}")
 
 
 def test_pair_packed_weights_equal_row_major(env):
