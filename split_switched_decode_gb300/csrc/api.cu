@@ -506,10 +506,11 @@ dec_status run_pair_projection(const dec_bf16 *X, const dec_bf16 *W, const dec_b
   return DEC_OK;
 }
 
-// A projection of more than 256 rows (speculative verification of up to 64 sequences x
-// 8 tokens) runs as consecutive launches over row blocks, each reading W; on one
-// stream, each launch's workspace use begins after the previous launch has finished
-// with it (the stream order, or the dependency wait of a programmatic launch).
+// A projection of 65..512 rows (speculative verification of up to 64 sequences x 8
+// tokens) is one CTA-pair launch where use_pair_kernel allows; otherwise more than 256
+// rows run as consecutive launches over row blocks, each reading W; on one stream, each
+// launch's workspace use begins after the previous launch has finished with it (the
+// stream order, or the dependency wait of a programmatic launch).
 dec_status run_splitk(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16 *R, dec_bf16 *Y,
                       int B, int N, int K, int split_k, int use_tc, void *ws, size_t ws_bytes,
                       cudaStream_t s, bool packed = false) {
