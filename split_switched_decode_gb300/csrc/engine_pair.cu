@@ -15,8 +15,8 @@
 //   rank 1: tile 2c+1, k-half 0
 //   rank 2: tile 2c,   k-half 1  -- issues the pair MMA of ranks 2 and 3
 //   rank 3: tile 2c+1, k-half 1
-// A launch covers NCOL = 128, 256, 384 or 512 batch columns as NMMA MMAs of N = NPER per
-// K step (one of 128 or 256, or two of 192 or 256). Per k-block each CTA loads its 16 KB weight box
+// A launch covers NCOL = 128, 192, 256, 384 or 512 batch columns as NMMA MMAs of N = NPER
+// per K step (one of 128, 192 or 256, or two of 192 or 256). Per k-block each CTA loads its 16 KB weight box
 // and NMMA activation boxes of NPER / 2 rows (rows NPER m + (NPER / 2) h .. for MMA m,
 // h = rank & 1), so MMA m covers batch columns NPER m .. NPER m + NPER - 1 (rows beyond
 // the batch read as zeros). Batch column j accumulates in tensor-memory column j.
@@ -48,7 +48,8 @@ namespace {
 constexpr int PAIR_THREADS = 192;  // warp 0 TMA, warp 1 MMA + tensor memory, warps 2-5 tail
 constexpr int PAIR_SMEM_LIMIT = 232448;
 
-// NCOL batch columns per launch (128, 256, 384 or 512): NMMA MMAs of N = NPER per K step,
+// NCOL batch columns per launch (128, 192, 256, 384 or 512): NMMA MMAs of N = NPER per K
+// step,
 // each CTA of a pair staging XROWS = NPER / 2 activation rows per MMA.
 template <int NCOL>
 struct PairConfig {
@@ -66,7 +67,7 @@ struct PairConfig {
   static constexpr int TILE_BYTES = HALF * 128 * 2;  // R in, Y out: bf16 [HALF][128]
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + TAIL;
   static_assert(STAGES >= 4, "pipeline too shallow");
-  static_assert(HALF % 64 == 0, "the tail moves whole groups of 64 columns");
+  static_assert(HALF % 32 == 0, "the tail moves whole groups of 32 columns");
   static_assert(NPER % 32 == 0 && NPER <= 256, "CTA-pair MMA: N a multiple of 32, <= 256");
   static_assert(RECV_BYTES + TILE_BYTES <= STAGES * STAGE_BYTES, "tail does not fit the ring");
 };
@@ -238,14 +239,16 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
   }
   if (go && warp >= 2) {
     const uint32_t dst = cluster_map(recv, rank ^ 2u) + 4u * static_cast<uint32_t>(r);
-    // 64 columns per tensor-memory wait: the loads' latency is paid once per group
-    for (int c = 0; c < C::HALF && oth0 + c < p.B; c += 64) {
-      float v[64];
+    // CG columns per tensor-memory wait: the loads' latency is paid once per group
+    constexpr int CG = C::HALF % 64 == 0 ? 64 : 32;
+    for (int c = 0; c < C::HALF && oth0 + c < p.B; c += CG) {
+      float v[CG];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) tmem_ld16(taddr + static_cast<uint32_t>(oth0 + c + 16 * q), v + 16 * q);
+      for (int q = 0; q < CG / 16; ++q)
+        tmem_ld16(taddr + static_cast<uint32_t>(oth0 + c + 16 * q), v + 16 * q);
       tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < 64; ++j) st_cluster_f32(dst + 512u * static_cast<uint32_t>(c + j), v[j]);
+      for (int j = 0; j < CG; ++j) st_cluster_f32(dst + 512u * static_cast<uint32_t>(c + j), v[j]);
     }
   }
   tc_fence_before();
@@ -360,11 +363,14 @@ cudaError_t max_clusters_t(int *n) {
 
 }  // namespace
 
-int pair_cols(int B) { return B <= 128 ? 128 : (B <= 256 ? 256 : (B <= 384 ? 384 : 512)); }
+int pair_cols(int B) {
+  return B <= 128 ? 128 : (B <= 192 ? 192 : (B <= 256 ? 256 : (B <= 384 ? 384 : 512)));
+}
 
 cudaError_t engine_pair_max_clusters(int ncol, int *n) {
   switch (ncol) {
     case 128: return max_clusters_t<128>(n);
+    case 192: return max_clusters_t<192>(n);
     case 256: return max_clusters_t<256>(n);
     case 384: return max_clusters_t<384>(n);
     default: return max_clusters_t<512>(n);
@@ -375,10 +381,11 @@ cudaError_t launch_engine_pair(int ncol, const CUtensorMap &wmap, const CUtensor
                                const CUtensorMap &ymap, const CUtensorMap &rmap,
                                const EngineParams &p, cudaStream_t s) {
   if (p.mode != MODE_LINEAR || p.grouped || p.KB < 2 || p.T < 1 || p.B < 1 || p.B > ncol ||
-      (ncol != 128 && ncol != 256 && ncol != 384 && ncol != 512))
+      (ncol != 128 && ncol != 192 && ncol != 256 && ncol != 384 && ncol != 512))
     return cudaErrorNotSupported;
   switch (ncol) {
     case 128: return launch_pair_t<128>(wmap, xmap, ymap, rmap, p, s);
+    case 192: return launch_pair_t<192>(wmap, xmap, ymap, rmap, p, s);
     case 256: return launch_pair_t<256>(wmap, xmap, ymap, rmap, p, s);
     case 384: return launch_pair_t<384>(wmap, xmap, ymap, rmap, p, s);
     default: return launch_pair_t<512>(wmap, xmap, ymap, rmap, p, s);

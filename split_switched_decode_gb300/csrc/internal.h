@@ -129,11 +129,11 @@ cudaError_t launch_engine_cc(int maxc, const CUtensorMap &wmap, const CUtensorMa
 // ----------------------------------------------------------- engine_pair.cu --
 // Wide projections (MODE_LINEAR, one group of p.B <= ncol columns, p.KB >= 2) on CTA-pair
 // tensor-core tiles: clusters of 4 CTAs per 256 rows of W ((p.T + 1) / 2 clusters), the
-// two k-halves added inside the cluster; ncol = pair_cols(p.B) is 128, 256, 384 or 512. wmap
+// two k-halves added inside the cluster; ncol = pair_cols(p.B) is 128..512. wmap
 // has 128-row boxes (or tile-packed blocks), xmap boxes of pair_xbox_rows(ncol) rows. With
 // p.vec_y, ymap and rmap (R, when given) map Y and R [B, N] without swizzle in boxes of
 // 128 x ncol / 2 elements; otherwise they are not read. No workspace.
-int pair_cols(int B);  // 128 up to 128 rows, 256 up to 256, 384 up to 384, else 512
+int pair_cols(int B);  // 128, 192, 256 or 384 columns up to that many rows, else 512
 inline int pair_xbox_rows(int ncol) { return (ncol > 256 ? ncol / 2 : ncol) / 2; }
 cudaError_t engine_pair_max_clusters(int ncol, int *n);
 cudaError_t launch_engine_pair(int ncol, const CUtensorMap &wmap, const CUtensorMap &xmap,
