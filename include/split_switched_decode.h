@@ -174,7 +174,9 @@ DEC_API dec_status dec_gemv(const dec_bf16 *X, const dec_bf16 *W, const dec_bf16
  * use_tc = 1, split_k = 0, at least two k-blocks and 129 <= B <= 512 (or 65 <= B <= 128
  * with 4 x ceil(ceil(N / 128) / 2) >= 80 % of the SMs), the call is
  * instead one launch of 4-CTA clusters, one per 256 rows of W: two CTA pairs (tcgen05
- * .cta_group::2, M = 256) hold the two k-halves, added inside the cluster through
+ * .cta_group::2, M = 256) hold the two k-halves, the batch taken as B rounded up to a
+ * multiple of 64 columns (at least 128; one MMA of that width up to 256, else two of
+ * half of it), the halves added inside the cluster through
  * distributed shared memory in a fixed order (deterministic; the summation order
  * differs from the one-CTA tiles, so bits may differ from them within the tolerance);
  * DEC_WIDE_PAIR_MMA=0 turns it off, DEC_WIDE_PAIR_MIN_B moves its lower bound.

@@ -421,7 +421,7 @@ int wide_pair_min_batch() {
 }
 
 // 4-CTA clusters of the pair kernel the device holds at once, per device and column count.
-std::atomic<int> g_pair_clusters[kMaxDevices][5];
+std::atomic<int> g_pair_clusters[kMaxDevices][7];
 std::once_flag g_pair_init_once;
 
 int pair_clusters(int ncol) {
@@ -431,8 +431,7 @@ int pair_clusters(int ncol) {
     for (auto &d : g_pair_clusters)
       for (auto &v : d) v.store(-1);
   });
-  const int ci = ncol == 128 ? 0 : ncol == 192 ? 1 : ncol == 256 ? 2 : ncol == 384 ? 3 : 4;
-  std::atomic<int> &slot = g_pair_clusters[dev][ci];
+  std::atomic<int> &slot = g_pair_clusters[dev][ncol / 64 - 2];  // ncol = 128, 192, .. 512
   int n = slot.load();
   if (n < 0) {
     if (engine_pair_max_clusters(ncol, &n) != cudaSuccess) {

@@ -15,8 +15,8 @@
 //   rank 1: tile 2c+1, k-half 0
 //   rank 2: tile 2c,   k-half 1  -- issues the pair MMA of ranks 2 and 3
 //   rank 3: tile 2c+1, k-half 1
-// A launch covers NCOL = 128, 192, 256, 384 or 512 batch columns as NMMA MMAs of N = NPER
-// per K step (one of 128, 192 or 256, or two of 192 or 256). Per k-block each CTA loads its 16 KB weight box
+// A launch covers NCOL = 128..512 batch columns (a multiple of 64) as NMMA MMAs of N = NPER
+// per K step (one of NCOL up to 256, else two of NCOL / 2). Per k-block each CTA loads its 16 KB weight box
 // and NMMA activation boxes of NPER / 2 rows (rows NPER m + (NPER / 2) h .. for MMA m,
 // h = rank & 1), so MMA m covers batch columns NPER m .. NPER m + NPER - 1 (rows beyond
 // the batch read as zeros). Batch column j accumulates in tensor-memory column j.
@@ -48,8 +48,8 @@ namespace {
 constexpr int PAIR_THREADS = 192;  // warp 0 TMA, warp 1 MMA + tensor memory, warps 2-5 tail
 constexpr int PAIR_SMEM_LIMIT = 232448;
 
-// NCOL batch columns per launch (128, 192, 256, 384 or 512): NMMA MMAs of N = NPER per K
-// step,
+// NCOL batch columns per launch (a multiple of 64 from 128 to 512): NMMA MMAs of N = NPER
+// per K step,
 // each CTA of a pair staging XROWS = NPER / 2 activation rows per MMA.
 template <int NCOL>
 struct PairConfig {
@@ -363,16 +363,16 @@ cudaError_t max_clusters_t(int *n) {
 
 }  // namespace
 
-int pair_cols(int B) {
-  return B <= 128 ? 128 : (B <= 192 ? 192 : (B <= 256 ? 256 : (B <= 384 ? 384 : 512)));
-}
+int pair_cols(int B) { return B <= 128 ? 128 : (B + 63) / 64 * 64; }
 
 cudaError_t engine_pair_max_clusters(int ncol, int *n) {
   switch (ncol) {
     case 128: return max_clusters_t<128>(n);
     case 192: return max_clusters_t<192>(n);
     case 256: return max_clusters_t<256>(n);
+    case 320: return max_clusters_t<320>(n);
     case 384: return max_clusters_t<384>(n);
+    case 448: return max_clusters_t<448>(n);
     default: return max_clusters_t<512>(n);
   }
 }
@@ -381,13 +381,15 @@ cudaError_t launch_engine_pair(int ncol, const CUtensorMap &wmap, const CUtensor
                                const CUtensorMap &ymap, const CUtensorMap &rmap,
                                const EngineParams &p, cudaStream_t s) {
   if (p.mode != MODE_LINEAR || p.grouped || p.KB < 2 || p.T < 1 || p.B < 1 || p.B > ncol ||
-      (ncol != 128 && ncol != 192 && ncol != 256 && ncol != 384 && ncol != 512))
+      ncol < 128 || ncol > 512 || ncol % 64 != 0)
     return cudaErrorNotSupported;
   switch (ncol) {
     case 128: return launch_pair_t<128>(wmap, xmap, ymap, rmap, p, s);
     case 192: return launch_pair_t<192>(wmap, xmap, ymap, rmap, p, s);
     case 256: return launch_pair_t<256>(wmap, xmap, ymap, rmap, p, s);
+    case 320: return launch_pair_t<320>(wmap, xmap, ymap, rmap, p, s);
     case 384: return launch_pair_t<384>(wmap, xmap, ymap, rmap, p, s);
+    case 448: return launch_pair_t<448>(wmap, xmap, ymap, rmap, p, s);
     default: return launch_pair_t<512>(wmap, xmap, ymap, rmap, p, s);
   }
 }

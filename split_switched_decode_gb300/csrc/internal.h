@@ -133,7 +133,7 @@ cudaError_t launch_engine_cc(int maxc, const CUtensorMap &wmap, const CUtensorMa
 // has 128-row boxes (or tile-packed blocks), xmap boxes of pair_xbox_rows(ncol) rows. With
 // p.vec_y, ymap and rmap (R, when given) map Y and R [B, N] without swizzle in boxes of
 // 128 x ncol / 2 elements; otherwise they are not read. No workspace.
-int pair_cols(int B);  // 128, 192, 256 or 384 columns up to that many rows, else 512
+int pair_cols(int B);  // 128 up to 128 rows, else B rounded up to a multiple of 64
 inline int pair_xbox_rows(int ncol) { return (ncol > 256 ? ncol / 2 : ncol) / 2; }
 cudaError_t engine_pair_max_clusters(int ncol, int *n);
 cudaError_t launch_engine_pair(int ncol, const CUtensorMap &wmap, const CUtensorMap &xmap,
