@@ -49,8 +49,9 @@ constexpr int PAIR_THREADS = 192;  // warp 0 TMA, warp 1 MMA + tensor memory, wa
 constexpr int PAIR_SMEM_LIMIT = 232448;
 
 // NCOL batch columns per launch (a multiple of 64 from 128 to 512): NMMA MMAs of N = NPER
-// per K step,
-// each CTA of a pair staging XROWS = NPER / 2 activation rows per MMA.
+// per K step, each CTA of a pair staging XROWS = NPER / 2 activation rows per MMA. Every
+// box and stage starts on a 1024-byte boundary (XBYTES is a multiple of 1024), as the
+// 128-byte swizzle of the TMA copies and of the MMA descriptors requires.
 template <int NCOL>
 struct PairConfig {
   static constexpr int NMMA = NCOL > 256 ? 2 : 1;
@@ -70,6 +71,7 @@ struct PairConfig {
   static_assert(HALF % 32 == 0, "the tail moves whole groups of 32 columns");
   static_assert(NPER % 32 == 0 && NPER <= 256, "CTA-pair MMA: N a multiple of 32, <= 256");
   static_assert(RECV_BYTES + TILE_BYTES <= STAGES * STAGE_BYTES, "tail does not fit the ring");
+  static_assert(XBYTES % 1024 == 0, "activation boxes on 1024-byte boundaries");
 };
 
 // The weight box of tile t, k-block kb (row-major W, or the tile-packed 16 KB block).
